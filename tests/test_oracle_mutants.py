@@ -1,0 +1,130 @@
+"""Plants plausible mistakes in the oracle and checks that the pins catch each.
+
+Every mutant replaces one oracle function (on the CPU, for the duration of the
+test) with a version carrying a typical slip: a wrong comparison, an off-by-one,
+a swapped operand, a dropped factor.  At least one of the named pin tests must
+then fail; if none does, that part of the oracle is not pinned.
+"""
+
+import numpy as np
+import pytest
+
+import oracle.philox as philox_mod
+import oracle.sampler as sampler_mod
+import oracle.verify as verify_mod
+from tests import test_oracle_philox as t_philox
+from tests import test_oracle_pins as t_pins
+from tests import test_oracle_properties as t_props
+from tests.conftest import load_golden
+
+
+def _softmax_times_t(z, temperature):
+    x = z * float(temperature)
+    w = np.exp(x - np.max(x))
+    return w / np.sum(w)
+
+
+def _top_k_plus_one(order, k):
+    keep = np.zeros(order.size, dtype=bool)
+    keep[order[: k + 1]] = True
+    return keep
+
+
+def _order_high_id_first(z):
+    ids = np.arange(z.size)
+    return np.lexsort((-ids, -z))
+
+
+def _nucleus_strict(p_sorted, top_p):
+    cum = np.cumsum(p_sorted)
+    reached = np.flatnonzero(cum > top_p)
+    return int(reached[0]) + 1 if reached.size else p_sorted.size
+
+
+def _nucleus_short_by_one(p_sorted, top_p):
+    cum = np.cumsum(p_sorted)
+    reached = np.flatnonzero(cum >= top_p)
+    return max(int(reached[0]), 1) if reached.size else p_sorted.size
+
+
+def _min_p_strict(p, min_p):
+    return p > float(min_p) * np.max(p)
+
+
+def _min_p_absolute(p, min_p):
+    return p >= float(min_p)
+
+
+def _walk_ge(weights, u):
+    running = np.cumsum(weights)
+    past = np.flatnonzero(running >= u)
+    return int(past[0]) if past.size else int(np.flatnonzero(weights > 0)[-1])
+
+
+def _accept_inverted(p, q, x, u):
+    return u < q[x] / max(p[x], 1e-300)
+
+
+def _residual_swapped(p, q):
+    r = np.maximum(q - p, 0.0)
+    return r / np.sum(r) if np.sum(r) > 0 else p
+
+
+def _uniform_second_word(seed, offset, row, draw):
+    w1 = philox_mod.philox4x64_10((offset, row, draw, 0), (seed, 0))[1]
+    return (w1 >> 11) * 2.0 ** -53
+
+
+def _fd_no_renorm(original):
+    def wrapped(row, temperature, top_k=0, top_p=1.0, min_p=0.0):
+        p, keep, _, diag = original(row, temperature, top_k, top_p, min_p)
+        return p, keep, np.where(keep, p, 0.0), diag
+    return wrapped
+
+
+MUTANTS = [
+    ("temperature multiplies", sampler_mod, "softmax_with_temperature", _softmax_times_t,
+     [lambda: t_pins.test_temperature_ratio_examples(load_golden),
+      t_props.test_temperature_ratio_identity_random]),
+    ("top-k keeps k+1", sampler_mod, "keep_top_k", _top_k_plus_one,
+     [lambda: t_pins.test_eight_word_example(load_golden), t_props.test_top_k_brute_force]),
+    ("ties favour the higher id", sampler_mod, "descending_order", _order_high_id_first,
+     [t_props.test_top_k_brute_force]),
+    ("top-p uses >", sampler_mod, "nucleus_length", _nucleus_strict,
+     [t_props.test_top_p_exact_boundary]),
+    ("top-p one short", sampler_mod, "nucleus_length", _nucleus_short_by_one,
+     [lambda: t_pins.test_eight_word_example(load_golden), t_props.test_top_p_brute_force_dyadic]),
+    ("min-p uses >", sampler_mod, "keep_min_p", _min_p_strict,
+     [lambda: t_pins.test_exercise_39_1(load_golden)]),
+    ("min-p ignores the maximum", sampler_mod, "keep_min_p", _min_p_absolute,
+     [lambda: t_pins.test_min_p_examples(load_golden)]),
+    ("walk uses >=", sampler_mod, "walk", _walk_ge,
+     [t_props.test_walk_boundaries]),
+    ("accept ratio inverted", verify_mod, "accept_draft", _accept_inverted,
+     [lambda: t_pins.test_spec_table(load_golden)]),
+    ("residual max(0, q - p)", verify_mod, "residual_distribution", _residual_swapped,
+     [lambda: t_pins.test_three_token_example(load_golden)]),
+    ("uniform from the wrong word", philox_mod, "uniform", _uniform_second_word,
+     [t_philox.test_uniform_layout]),
+    ("renormalisation dropped", sampler_mod, "filtered_distribution",
+     _fd_no_renorm(sampler_mod.filtered_distribution),
+     [lambda: t_pins.test_exercise_39_1(load_golden), t_props.test_renormalisation_invariants]),
+]
+
+
+@pytest.mark.parametrize("name,module,attr,mutant,pins", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pins_catch_mutant(monkeypatch, name, module, attr, mutant, pins):
+    monkeypatch.setattr(module, attr, mutant)
+    caught = 0
+    for pin in pins:
+        try:
+            pin()
+        except (AssertionError, IndexError, ValueError):
+            caught += 1
+    assert caught == len(pins), f"mutant '{name}' slipped past {len(pins) - caught} pin(s)"
+
+
+def test_wrong_philox_multiplier_is_caught(monkeypatch):
+    monkeypatch.setattr(philox_mod, "PHILOX_M0", philox_mod.PHILOX_M0 ^ 2)
+    with pytest.raises(AssertionError):
+        t_philox.test_random_blocks_match_numpy()

@@ -1,0 +1,406 @@
+"""Benchmark of the sampler and the speculative verifier on one GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl smp|reference]
+
+One step = one smp_sample call on the large-vocabulary batch (B=256,
+V=128256, bf16 Zipf-headed logits; half the rows min-p 0.1, a quarter greedy,
+a quarter T=0.7 with top-k 40) followed by one smp_spec_verify call on the
+verify batch (B=32, K=4, V=32000, fp32).  Inputs are resident in HBM and
+rotate over enough copies that every call reads logits that are not in L2.
+The K timed steps are replayed from a CUDA graph and timed with CUDA events.
+
+`value` is sampled rows per second of sampler time; the verifier's emitted
+tokens per second, the roofline of the sampler kernel, an end-to-end number
+through host buffers, the clocks seen during the timed region and the oracle's
+own rate on the host cores are reported beside it, on one JSON line.
+
+--impl reference times the fp64 oracle instead, on bounded samples of the
+same workload, on the host cores.
+"""
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "sampled rows/s and HBM GB/s (% of peak) at B=256,V=128256 bf16; verify tok/s"
+UNIT = "rows/s"
+WORKLOAD = "large_vocab"
+WORKLOAD_DESC = ("large_vocab: B=256, V=128256, bf16 logits log(Zipf s=1.1) over a seeded per-row "
+                 "permutation + N(0, 0.5^2); rows b%4 in {0,1}: min_p=0.1 T=1, b%4==2: greedy, "
+                 "b%4==3: T=0.7 top_k=40; Philox seed 0")
+VERIFY_DESC = "verify: B=32, K=4, V=32000, fp32; q = G[:, :4], p = G + N(0,1), G ~ N(0, 2^2)"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "sample_kernel_large_vocab.md")
+KERNEL_SOURCES = ["common.cuh", "row_ops.cuh", "sample.cu", "exp_table.h"]
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            data = json.load(fh)
+        return float(data["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_sha():
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "spec_verify_gb300", "csrc", name), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per launch from the committed ncu summary, if it matches the source."""
+    try:
+        with open(PROFILE_SUMMARY) as fh:
+            text = fh.read()
+    except OSError:
+        return None
+    fields = {}
+    for line in text.splitlines():
+        if line.startswith("- ") and ":" in line:
+            k, v = line[2:].split(":", 1)
+            fields[k.strip()] = v.strip().strip("`")
+    if fields.get("source_sha") != kernel_source_sha():
+        return None
+    try:
+        return float(fields["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi during a region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or self.path is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        with open(self.path) as fh:
+            for line in fh:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def oracle_rate(batch, seconds, start_row=0):
+    """Rows per second of the fp64 oracle on this process's host core."""
+    from oracle import sampler as osam
+    done = 0
+    t0 = time.perf_counter()
+    rows = []
+    b = start_row
+    while time.perf_counter() - t0 < seconds or done == 0:
+        osam.sample(batch.values, batch.params, batch.seed, batch.offset, rows=[b])
+        rows.append(b)
+        done += 1
+        b = (b + 1) % batch.data.shape[0]
+    elapsed = time.perf_counter() - t0
+    return done / elapsed, done, elapsed
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    from spec_verify_gb300 import workloads
+    batch = workloads.sampler_workload(WORKLOAD)
+    rows_per_step = 4
+    from oracle import sampler as osam
+
+    def step(i):
+        base = (i * rows_per_step) % batch.data.shape[0]
+        osam.sample(batch.values, batch.params, batch.seed, batch.offset,
+                    rows=list(range(base, base + rows_per_step)))
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(args.warmup + i)
+    elapsed = time.perf_counter() - t0
+    value = rows_per_step * args.steps / elapsed
+    sample = f"{rows_per_step} rows of the {WORKLOAD} batch per step, fp64 numpy oracle, one core"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1000.0 * elapsed / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD_DESC, "rows_per_step": rows_per_step},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    from spec_verify_gb300 import binding
+    from spec_verify_gb300 import build as smp_build
+    from spec_verify_gb300 import workloads
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    smp_build.build()
+    binding.load()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    # ---------------- inputs, resident in HBM, rotated past L2
+    batch = workloads.sampler_workload(WORKLOAD)
+    B, V = batch.data.shape
+    l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 129 * 2**20))
+    sample_bytes = batch.data.nbytes
+    n_copies = max(4, math.ceil(4 * l2 / sample_bytes))
+    host = torch.from_numpy(batch.data.view(np.int16)).view(torch.bfloat16)
+    logits = [host.to(dev) for _ in range(n_copies)]
+    params = binding.params_to_device(batch.params, dev)
+    out_ids = torch.empty(B, dtype=torch.int32, device=dev)
+    out_probs = torch.empty(B, dtype=torch.float32, device=dev)
+    status = torch.empty(1, dtype=torch.int32, device=dev)
+    seed = rank   # each rank samples its own rows (weak scaling, no collective)
+
+    vb = workloads.verify_workload()
+    vB, vK, vV = vb.shape
+    v_bytes = vb.p.nbytes + vb.q.nbytes
+    v_copies = max(4, math.ceil(4 * l2 / v_bytes))
+    p_dev = [torch.from_numpy(vb.p).to(dev) for _ in range(v_copies)]
+    q_dev = [torch.from_numpy(vb.q).to(dev) for _ in range(v_copies)]
+    d, _, _ = binding.sample(q_dev[0].view(vB * vK, vV), workloads.make_params(vB * vK), vb.draft_seed,
+                             vb.draft_offset)
+    drafts = d.view(vB, vK).contiguous()
+    ws = torch.empty(binding.spec_verify_workspace_bytes(vB, vK), dtype=torch.uint8, device=dev)
+    v_acc = torch.empty(vB, dtype=torch.int32, device=dev)
+    v_ids = torch.empty(vB, vK + 1, dtype=torch.int32, device=dev)
+    v_status = torch.empty(1, dtype=torch.int32, device=dev)
+
+    def sampler_call(i):
+        binding.sample(logits[i % n_copies], params, seed, i, out_ids, out_probs, status)
+
+    def verify_call(i):
+        binding.spec_verify(p_dev[i % v_copies], q_dev[i % v_copies], drafts, seed, i, ws, v_acc, v_ids,
+                            v_status)
+
+    # warm-up (also sets kernel attributes before any capture)
+    for i in range(max(args.warmup, 3)):
+        sampler_call(i)
+        verify_call(i)
+    torch.cuda.synchronize()
+    assert int(status.cpu()[0]) == 0 and int(v_status.cpu()[0]) == 0
+
+    def capture(fn):
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(g, stream=s):
+                for i in range(args.steps):
+                    fn(i)
+        torch.cuda.current_stream().wait_stream(s)
+        return g
+
+    g_step = capture(lambda i: (sampler_call(i), verify_call(i)))
+    g_samp = capture(sampler_call)
+    g_ver = capture(verify_call)
+
+    def timed(graph, reps):
+        for _ in range(reps):       # warm replays
+            graph.replay()
+        barrier()
+        stream = torch.cuda.current_stream()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        graph.replay()
+        e1.record(stream)
+        barrier()
+        ms = e0.elapsed_time(e1)
+        if world > 1:
+            t = torch.tensor([ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms = float(t.item())
+        return ms
+
+    with ClockSampler(local) as clocks:
+        step_ms = timed(g_step, max(1, args.warmup // max(1, args.steps)))
+        samp_ms = timed(g_samp, 1)
+        ver_ms = timed(g_ver, 1)
+    clock_info = clocks.summary()
+
+    gpu_launches = args.steps * 3     # sample_kernel + verify_pos_kernel + verify_resolve_kernel
+    samp_us = 1000.0 * samp_ms / args.steps
+    ver_us = 1000.0 * ver_ms / args.steps
+    rows_per_s = world * B / (samp_us * 1e-6)
+    acc_mean = float(v_acc.float().mean().item())
+    verify_tok_s = world * vB * (acc_mean + 1.0) / (ver_us * 1e-6)
+
+    # roofline of the sampler kernel: logits read once, ids + probs written, params read
+    alg_bytes = B * V * 2 + B * 8 + B * 20
+    achieved = alg_bytes / (samp_us * 1e-6) / 1e9
+    peak, peak_kind = measured_peaks()
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "traffic": profiled_traffic(),
+                "kernel": "sample_kernel", "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)",
+                "algorithmic_bytes_per_launch": alg_bytes}
+
+    # ---------------- end to end through the public API with host buffers
+    pinned = host.pin_memory()
+    params_host = torch.from_numpy(batch.params.view(np.uint8).copy()).pin_memory()
+    ids_host = torch.empty(B, dtype=torch.int32).pin_memory()
+    probs_host = torch.empty(B, dtype=torch.float32).pin_memory()
+    dev_in = torch.empty_like(logits[0])
+    dev_params = torch.empty_like(params)
+    e2e_steps = max(3, args.steps)
+
+    def e2e_step(i):
+        dev_in.copy_(pinned, non_blocking=True)
+        dev_params.copy_(params_host, non_blocking=True)
+        binding.sample(dev_in, dev_params, seed, i, out_ids, out_probs, status)
+        ids_host.copy_(out_ids, non_blocking=True)
+        probs_host.copy_(out_probs, non_blocking=True)
+
+    for i in range(3):
+        e2e_step(i)
+    barrier()
+    t0 = time.perf_counter()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(e2e_steps):
+        e2e_step(i)
+    e1.record()
+    barrier()
+    e2e_ms = e0.elapsed_time(e1)
+    e2e = {"value": world * B * e2e_steps / (e2e_ms * 1e-3), "unit": UNIT,
+           "h2d_bytes_per_step": sample_bytes + batch.params.nbytes, "d2h_bytes_per_step": B * 8,
+           "what": "pinned host logits+params -> device copy, smp_sample, ids+probs -> host, per step"}
+
+    # ---------------- oracle on the host cores (rank 0, N = 1 only)
+    cpu_baseline = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, rows_done, secs = oracle_rate(batch, args.cpu_seconds)
+        cpu_baseline = {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
+                        "sample": f"{rows_done} rows of the {WORKLOAD} batch in {secs:.1f} s, fp64 numpy oracle"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": rows_per_s, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "u64", "data": "synthetic",
+            "config": {"workload": WORKLOAD_DESC, "batch": B, "vocab": V, "logits_dtype": "bf16",
+                       "verify_workload": VERIFY_DESC,
+                       "l2": f"inputs rotate over {n_copies} sampler copies ({n_copies * sample_bytes / 1e6:.0f} MB) "
+                             f"and {v_copies} verify copies; L2 {l2 / 1e6:.0f} MB",
+                       "timing": "K steps captured in one CUDA graph, CUDA events on the launching stream",
+                       "parallelism": f"dp{world} (rows independent, no collective)"},
+            "sampler_us_per_call": samp_us,
+            "hbm_gbs": achieved,
+            "pct_of_measured_hbm": 100.0 * achieved / peak,
+            "pct_of_8tbs_nominal": 100.0 * achieved / NOMINAL_HBM_GBS,
+            "verify": {"tok_s": verify_tok_s, "us_per_call": ver_us, "mean_accepted": acc_mean,
+                       "bytes_per_call": v_bytes, "gbs": v_bytes / (ver_us * 1e-6) / 1e9},
+            "roofline": roofline,
+            "cpu_baseline": cpu_baseline,
+            "e2e": e2e,
+            "gpu_launches": gpu_launches,
+            "clocks": clock_info,
+        }
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["smp", "reference"], default="smp")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

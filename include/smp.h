@@ -1,0 +1,174 @@
+/*
+ * smp.h -- C ABI of libsmp: a batched next-token sampler and a
+ * speculative-decoding verifier for NVIDIA GB300 (sm_103a).
+ *
+ * Every entry point is asynchronous on the caller's CUDA stream, allocates
+ * nothing, and reads and writes only the caller-owned device buffers it is
+ * given.  Host-detectable errors (a NULL pointer, a size out of range, an
+ * unknown dtype) return a status code before anything is launched.  Problems
+ * that belong to one row (bad knobs, no finite logit, a draft id out of range,
+ * a wait that ran out of time) give that row the id -1 and OR a flag
+ * (SMP_ROW_*) into the optional device status word, which the call clears
+ * first.
+ *
+ * Random numbers: every draw uses Philox4x64-10 (Salmon et al., "Parallel
+ * Random Numbers: As Easy as 1, 2, 3", SC'11) with key (seed, 0) and counter
+ * (offset, row, draw, 0); the uniform is the top 53 bits of the first output
+ * word.  The same (seed, offset) reproduces a call bit for bit, whatever the
+ * launch shape.
+ *
+ * Probability masses: the device represents exp((z - max z) / T) of every
+ * token as a 64-bit fixed-point integer E = round(e * 2^44), computed with a
+ * double-float exponential (relative error below 2^-44), and sums them
+ * exactly in integers.  Masses below 2^-45 of the row maximum (more than
+ * about 31 T below the top logit) are zero.
+ */
+#ifndef SMP_H
+#define SMP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SMP_ABI_VERSION 1
+
+/* Largest vocabulary the kernels accept (rows are kept in on-chip memory). */
+#define SMP_MAX_VOCAB (1 << 19)
+/* Largest number of draft tokens per verify row. */
+#define SMP_MAX_DRAFT 16
+
+typedef enum smp_dtype {
+    SMP_F32 = 0,   /* IEEE binary32 logits */
+    SMP_BF16 = 1   /* bfloat16 logits (upper half of binary32) */
+} smp_dtype;
+
+/*
+ * Per-row sampling knobs, 20 bytes, little endian, laid out as written.
+ *   temperature  T: logits are divided by T before the softmax ("Decoding &
+ *                Speculative Sampling", section 39.2).  T == 0 means greedy;
+ *                T < 0, NaN or infinite makes the row invalid.
+ *   top_k        keep the k most likely tokens (ties: lower id first), active
+ *                for 0 < top_k < V; top_k < 0 is invalid.
+ *   top_p        keep the shortest most-likely prefix whose probability
+ *                reaches top_p (at least one token); off for top_p >= 1;
+ *                top_p < 0 or NaN is invalid.
+ *   min_p        keep p_i >= min_p * max_j p_j ("Inference: Sampling, the KV
+ *                Cache, Speculative Decoding and int8", section "Picking the
+ *                next token"); active for 0 < min_p < 1, off for 0 and >= 1;
+ *                min_p < 0 or NaN is invalid.
+ *   greedy       non-zero: take the arg-max (lowest id on ties), knobs ignored.
+ * The filters are applied to the same post-temperature distribution and their
+ * kept sets intersected, then renormalised (eq. 39.2).
+ */
+typedef struct smp_row_params {
+    float temperature;
+    int32_t top_k;
+    float top_p;
+    float min_p;
+    int32_t greedy;
+} smp_row_params;
+
+typedef enum smp_status {
+    SMP_OK = 0,
+    SMP_ERR_INVALID_ARG = 1,   /* NULL pointer, size or count out of range, misaligned base */
+    SMP_ERR_DTYPE = 2,         /* dtype is not SMP_F32 or SMP_BF16 */
+    SMP_ERR_CUDA = 3,          /* a CUDA runtime call failed (see smp_last_cuda_error) */
+    SMP_ERR_UNSUPPORTED = 4,   /* vocabulary too large for the on-chip row layout */
+    SMP_ERR_WORKSPACE = 5      /* workspace NULL or smaller than required */
+} smp_status;
+
+/* Flags OR-ed into the device status word, one or more per affected row. */
+#define SMP_ROW_BAD_PARAMS 1   /* invalid knobs on a sampling row */
+#define SMP_ROW_NONFINITE 2    /* the row's maximum logit is not finite (all -inf/NaN, or +inf) */
+#define SMP_ROW_TIMEOUT 4      /* a bounded wait between the CTAs of a row ran out of time */
+#define SMP_ROW_BAD_DRAFT 8    /* a draft id outside [0, V) */
+
+/*
+ * smp_sample -- draw one token per row from temperature / top-k / top-p /
+ * min-p filtered, renormalised distributions ("Decoding & Speculative
+ * Sampling", section 39.2 and eq. 39.2; the draw walks the kept tokens in id
+ * order and stops where the running total passes u: "Choosing the next word",
+ * section "Where the randomness comes from, and where it stops").
+ *
+ *   logits     device, [batch, vocab] row-major contiguous, dtype elements;
+ *              base aligned to the element size.  NaN counts as -inf.
+ *   batch      rows, 1 .. 2^31-1;  vocab: 1 .. SMP_MAX_VOCAB.
+ *   params     device, [batch] smp_row_params.
+ *   seed, offset  Philox key and per-step counter; row b uses draw 0.
+ *   out_ids    device, [batch] int32: the token, or -1 for an error row.
+ *   out_probs  device, [batch] float or NULL: p~ of the token (1 for greedy,
+ *              NaN for an error row).
+ *   status     device, one int32 or NULL: cleared, then OR of SMP_ROW_* flags.
+ *   stream     a cudaStream_t (NULL: the legacy default stream).
+ * Returns SMP_OK once the work is queued.
+ */
+smp_status smp_sample(const void* logits, int32_t batch, int32_t vocab, smp_dtype dtype,
+                      const smp_row_params* params, uint64_t seed, uint64_t offset,
+                      int32_t* out_ids, float* out_probs, int32_t* status, void* stream);
+
+/*
+ * smp_filter_debug -- as smp_sample, and also writes the renormalised
+ * distribution p~ of eq. 39.2 of every row and the size of its kept set.
+ *   out_probs_full  device, [batch, vocab] float: p~_i (0 outside the kept
+ *                   set; one-hot for greedy rows; NaN for error rows).
+ *   out_kept        device, [batch] int32: |S| (1 for greedy, 0 for errors).
+ * Meant for tests; it moves 4 bytes per logit more than smp_sample.
+ */
+smp_status smp_filter_debug(const void* logits, int32_t batch, int32_t vocab, smp_dtype dtype,
+                            const smp_row_params* params, uint64_t seed, uint64_t offset,
+                            int32_t* out_ids, float* out_probs, float* out_probs_full,
+                            int32_t* out_kept, int32_t* status, void* stream);
+
+/*
+ * smp_spec_verify_workspace_bytes -- device workspace smp_spec_verify needs
+ * for a batch of `batch` rows with `k` drafts (0 if the sizes are invalid).
+ */
+size_t smp_spec_verify_workspace_bytes(int32_t batch, int32_t k);
+
+/*
+ * smp_spec_verify -- speculative-decoding verification of a batch ("Decoding
+ * & Speculative Sampling", section 39.4, eqs. 39.3 and 39.4; "Speculative
+ * decoding -- Hinglish notes", section "The Algorithm (Step-by-Step)").
+ * For each row b and i = 0..K-1 in order, draft x = draft_ids[b, i] is kept
+ * when u_i < p_i(x) / max(q_i(x), 1e-300) with p_i = softmax(p_logits[b, i]),
+ * q_i = softmax(q_logits[b, i]) (temperature 1, no filters).  At the first
+ * rejection j the replacement is drawn from max(0, p_j - q_j) renormalised
+ * (from p_j if that mass is zero); if all K are kept a bonus token is drawn
+ * from softmax(p_logits[b, K]).  u_i is draw i of row b; the replacement or
+ * bonus uses draw K.
+ *
+ *   p_logits   device, [batch, k+1, vocab] contiguous, dtype elements.
+ *   q_logits   device, [batch, k, vocab] contiguous, same dtype.
+ *   draft_ids  device, [batch, k] int32.
+ *   batch 1 .. 2^20;  k 1 .. SMP_MAX_DRAFT;  vocab 1 .. SMP_MAX_VOCAB.
+ *   out_accepted_len  device, [batch] int32: accepted drafts 0..k (-1: error).
+ *   out_ids    device, [batch, k+1] int32: the accepted drafts, then the
+ *              replacement or bonus token, then -1 padding.
+ *   status     device int32 or NULL, as for smp_sample.
+ *   workspace  device buffer of at least smp_spec_verify_workspace_bytes(batch, k)
+ *              bytes, 8-byte aligned; owned by the caller, contents scratch.
+ *              Calls that overlap on the GPU must not share it.
+ */
+smp_status smp_spec_verify(const void* p_logits, const void* q_logits, const int32_t* draft_ids,
+                           int32_t batch, int32_t k, int32_t vocab, smp_dtype dtype,
+                           uint64_t seed, uint64_t offset, int32_t* out_accepted_len,
+                           int32_t* out_ids, int32_t* status, void* workspace,
+                           size_t workspace_bytes, void* stream);
+
+/* Human-readable name of a status code (static string). */
+const char* smp_status_string(smp_status s);
+
+/* cudaError_t value of the last SMP_ERR_CUDA returned on this thread. */
+int32_t smp_last_cuda_error(void);
+
+/* SMP_ABI_VERSION of the loaded library. */
+int32_t smp_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SMP_H */

@@ -1,0 +1,188 @@
+"""Thin Python binding of libsmp (include/smp.h): argument marshalling only.
+
+Every step of the sampler and the verifier runs in the library's CUDA kernels;
+PyTorch supplies device memory and the current stream.  If the library has not
+been built, loading fails loudly: there is no other implementation to fall
+back to.
+"""
+
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+SMP_F32 = 0
+SMP_BF16 = 1
+
+STATUS_NAMES = {0: "SMP_OK", 1: "SMP_ERR_INVALID_ARG", 2: "SMP_ERR_DTYPE", 3: "SMP_ERR_CUDA",
+                4: "SMP_ERR_UNSUPPORTED", 5: "SMP_ERR_WORKSPACE"}
+
+ROW_BAD_PARAMS = 1
+ROW_NONFINITE = 2
+ROW_TIMEOUT = 4
+ROW_BAD_DRAFT = 8
+
+# Symbols declared in include/smp.h.
+EXPORTS = ("smp_sample", "smp_filter_debug", "smp_spec_verify_workspace_bytes",
+           "smp_spec_verify", "smp_status_string", "smp_last_cuda_error", "smp_abi_version")
+
+_lib = None
+
+
+class SmpError(RuntimeError):
+    pass
+
+
+def library_path():
+    return _build.LIB
+
+
+def load():
+    """Load libsmp.so (built in-tree by spec_verify_gb300.build)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = library_path()
+    if not os.path.exists(path):
+        raise SmpError(f"libsmp.so is not built ({path}); run "
+                       "`python -m spec_verify_gb300.build` or __graft_entry__.build()")
+    lib = ctypes.CDLL(path)
+    vp, i32, u64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_uint64, ctypes.c_size_t
+    lib.smp_sample.argtypes = [vp, i32, i32, i32, vp, u64, u64, vp, vp, vp, vp]
+    lib.smp_sample.restype = i32
+    lib.smp_filter_debug.argtypes = [vp, i32, i32, i32, vp, u64, u64, vp, vp, vp, vp, vp, vp]
+    lib.smp_filter_debug.restype = i32
+    lib.smp_spec_verify_workspace_bytes.argtypes = [i32, i32]
+    lib.smp_spec_verify_workspace_bytes.restype = sz
+    lib.smp_spec_verify.argtypes = [vp, vp, vp, i32, i32, i32, i32, u64, u64, vp, vp, vp, vp, sz, vp]
+    lib.smp_spec_verify.restype = i32
+    lib.smp_status_string.argtypes = [i32]
+    lib.smp_status_string.restype = ctypes.c_char_p
+    lib.smp_last_cuda_error.argtypes = []
+    lib.smp_last_cuda_error.restype = i32
+    lib.smp_abi_version.argtypes = []
+    lib.smp_abi_version.restype = i32
+    _lib = lib
+    return lib
+
+
+def _check(code):
+    if code != 0:
+        lib = load()
+        msg = lib.smp_status_string(code).decode()
+        if code == 3:
+            msg += f" (cudaError {lib.smp_last_cuda_error()})"
+        raise SmpError(msg)
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _dtype_code(t):
+    torch = _torch()
+    if t.dtype == torch.float32:
+        return SMP_F32
+    if t.dtype == torch.bfloat16:
+        return SMP_BF16
+    raise SmpError(f"logits must be float32 or bfloat16, got {t.dtype}")
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _stream(stream):
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def params_to_device(params, device):
+    """A [B] record array of smp_row_params as a device byte tensor."""
+    torch = _torch()
+    if isinstance(params, torch.Tensor):
+        return params
+    arr = np.ascontiguousarray(params)
+    return torch.from_numpy(arr.view(np.uint8).copy()).to(device)
+
+
+def sample(logits, params, seed=0, offset=0, out_ids=None, out_probs=None, status=None, stream=None):
+    """smp_sample on a [B, V] float32/bfloat16 CUDA tensor.
+
+    params: record array (spec_verify_gb300.workloads.PARAMS_DTYPE) or a
+    device byte tensor holding it.  Returns (ids int32 [B], probs float32 [B],
+    status int32 [1]) on the logits' device.
+    """
+    torch = _torch()
+    lib = load()
+    if logits.dim() != 2 or not logits.is_cuda or not logits.is_contiguous():
+        raise SmpError("logits must be a contiguous [B, V] CUDA tensor")
+    batch, vocab = logits.shape
+    dev = logits.device
+    prm = params_to_device(params, dev)
+    out_ids = out_ids if out_ids is not None else torch.empty(batch, dtype=torch.int32, device=dev)
+    out_probs = out_probs if out_probs is not None else torch.empty(batch, dtype=torch.float32, device=dev)
+    status = status if status is not None else torch.empty(1, dtype=torch.int32, device=dev)
+    _check(lib.smp_sample(_ptr(logits), batch, vocab, _dtype_code(logits), _ptr(prm), seed, offset,
+                          _ptr(out_ids), _ptr(out_probs), _ptr(status), _stream(stream)))
+    return out_ids, out_probs, status
+
+
+def filter_debug(logits, params, seed=0, offset=0, stream=None):
+    """smp_filter_debug: (ids, probs, full p~ [B, V], kept [B], status)."""
+    torch = _torch()
+    lib = load()
+    if logits.dim() != 2 or not logits.is_cuda or not logits.is_contiguous():
+        raise SmpError("logits must be a contiguous [B, V] CUDA tensor")
+    batch, vocab = logits.shape
+    dev = logits.device
+    prm = params_to_device(params, dev)
+    ids = torch.empty(batch, dtype=torch.int32, device=dev)
+    probs = torch.empty(batch, dtype=torch.float32, device=dev)
+    full = torch.empty(batch, vocab, dtype=torch.float32, device=dev)
+    kept = torch.empty(batch, dtype=torch.int32, device=dev)
+    status = torch.empty(1, dtype=torch.int32, device=dev)
+    _check(lib.smp_filter_debug(_ptr(logits), batch, vocab, _dtype_code(logits), _ptr(prm), seed, offset,
+                                _ptr(ids), _ptr(probs), _ptr(full), _ptr(kept), _ptr(status),
+                                _stream(stream)))
+    return ids, probs, full, kept, status
+
+
+def spec_verify_workspace_bytes(batch, k):
+    return int(load().smp_spec_verify_workspace_bytes(batch, k))
+
+
+def spec_verify(p_logits, q_logits, draft_ids, seed=0, offset=0, workspace=None, out_accepted=None,
+                out_ids=None, status=None, stream=None):
+    """smp_spec_verify on p [B, K+1, V], q [B, K, V] and draft ids [B, K] (int32).
+
+    Returns (accepted_len int32 [B], ids int32 [B, K+1], status int32 [1]).
+    """
+    torch = _torch()
+    lib = load()
+    if p_logits.dim() != 3 or q_logits.dim() != 3 or draft_ids.dim() != 2:
+        raise SmpError("expected p [B, K+1, V], q [B, K, V], draft_ids [B, K]")
+    batch, k1, vocab = p_logits.shape
+    k = k1 - 1
+    if tuple(q_logits.shape) != (batch, k, vocab) or tuple(draft_ids.shape) != (batch, k):
+        raise SmpError("shape mismatch between p, q and draft_ids")
+    if p_logits.dtype != q_logits.dtype or draft_ids.dtype != torch.int32:
+        raise SmpError("p and q must share a dtype; draft_ids must be int32")
+    for t in (p_logits, q_logits, draft_ids):
+        if not t.is_cuda or not t.is_contiguous():
+            raise SmpError("inputs must be contiguous CUDA tensors")
+    dev = p_logits.device
+    need = spec_verify_workspace_bytes(batch, k)
+    if workspace is None:
+        workspace = torch.empty(max(need, 8), dtype=torch.uint8, device=dev)
+    out_accepted = out_accepted if out_accepted is not None else torch.empty(batch, dtype=torch.int32, device=dev)
+    out_ids = out_ids if out_ids is not None else torch.empty(batch, k + 1, dtype=torch.int32, device=dev)
+    status = status if status is not None else torch.empty(1, dtype=torch.int32, device=dev)
+    _check(lib.smp_spec_verify(_ptr(p_logits), _ptr(q_logits), _ptr(draft_ids), batch, k, vocab,
+                               _dtype_code(p_logits), seed, offset, _ptr(out_accepted), _ptr(out_ids),
+                               _ptr(status), _ptr(workspace), workspace.numel(), _stream(stream)))
+    return out_accepted, out_ids, status

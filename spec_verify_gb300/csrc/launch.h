@@ -1,0 +1,63 @@
+// Host-side launch helpers: device queries, per-kernel attributes and
+// cluster launches through cudaLaunchKernelEx.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "smp.h"
+
+namespace smp {
+
+constexpr size_t kSliceTargetBytes = 48 * 1024;   // preferred slice per CTA
+constexpr size_t kSliceMinBytes = 8 * 1024;       // smallest slice worth a CTA
+constexpr size_t kMaxDynamicSmem = 200 * 1024;
+
+struct LaunchShape {
+  int cluster = 1;   // CTAs per row
+  int slice = 0;     // elements per CTA
+  size_t smem = 0;   // dynamic shared memory per CTA
+};
+
+// Records `err` as the last CUDA error of this thread and returns SMP_ERR_CUDA.
+smp_status fail_cuda(cudaError_t err);
+
+// Current device, or -1 if it cannot be queried.
+int current_device();
+
+// Number of SMs of `dev` (cached).
+int device_sms(int dev);
+
+// Cluster size forced through the environment variable SMP_FORCE_CLUSTER
+// (1, 2, 4, 8 or 16; used by tests to show that results do not depend on the
+// launch shape), or 0.
+int forced_cluster();
+
+// Sets the dynamic shared memory limit and, for clusters above 8, the
+// non-portable cluster size attribute of `kernel` (once per device and size).
+cudaError_t prepare_kernel(const void* kernel, int dev, const LaunchShape& ls);
+
+// Launches `kernel(*args)` with a cluster of ls.cluster CTAs along x.
+template <typename Args>
+cudaError_t launch_cluster(const void* kernel, dim3 grid, dim3 block, const LaunchShape& ls,
+                           cudaStream_t stream, Args* args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = ls.smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = unsigned(ls.cluster);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  void* params[1] = {args};
+  return cudaLaunchKernelExC(&cfg, kernel, params);
+}
+
+}  // namespace smp

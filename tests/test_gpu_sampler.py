@@ -1,0 +1,213 @@
+"""CUDA sampler (through the C ABI) against the fp64 oracle."""
+
+import math
+import os
+
+import numpy as np
+import pytest
+
+from oracle import sampler as osam
+from spec_verify_gb300 import binding, workloads
+from tests.parity import PROB_RTOL, compare_sampler, device_logits
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    binding.load()
+
+
+def run(batch, seed=None, offset=None):
+    logits = device_logits(batch.data, batch.dtype)
+    ids, probs, status = binding.sample(logits, batch.params,
+                                        batch.seed if seed is None else seed,
+                                        batch.offset if offset is None else offset)
+    torch.cuda.synchronize()
+    return ids.cpu().numpy(), probs.cpu().numpy(), int(status.cpu()[0])
+
+
+def oracle(batch, rows=None, seed=None, offset=None):
+    return osam.sample(batch.values, batch.params, batch.seed if seed is None else seed,
+                       batch.offset if offset is None else offset, rows=rows)
+
+
+# ------------------------------------------------------------------ the named workloads at full size
+
+WORKLOAD_ROWS = {
+    "basic": None,
+    "mixed": None,
+    "large_vocab": list(range(0, 48)) + list(range(200, 256)),
+    "flat_nucleus": list(range(0, 1024, 23)) + [1023],
+}
+
+
+@pytest.mark.parametrize("name", list(WORKLOAD_ROWS))
+def test_workload_parity(name):
+    batch = workloads.sampler_workload(name)
+    ids, probs, status = run(batch)
+    assert status == 0
+    verdict = compare_sampler(oracle(batch, rows=WORKLOAD_ROWS[name]), ids, probs)
+    verdict.check()
+
+
+# ------------------------------------------------------------------ small seeded batches, ragged vocabularies
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("kinds", ["mixed", "greedy", "minp", "topk", "topp", "plain"])
+def test_random_parity(dtype, kinds):
+    batch = workloads.random_sampler_batch(24, 10007, dtype=dtype, seed=hash((dtype, kinds)) % 1000,
+                                           kinds=kinds)
+    ids, probs, status = run(batch, seed=11, offset=3)
+    assert status == 0
+    compare_sampler(oracle(batch, seed=11, offset=3), ids, probs).check()
+
+
+@pytest.mark.parametrize("vocab", [1, 2, 7, 33, 1000, 4099, 65537])
+def test_vocab_sizes(vocab):
+    batch = workloads.random_sampler_batch(9, vocab, dtype="bf16", seed=vocab, kinds="mixed")
+    ids, probs, status = run(batch)
+    assert status == 0
+    compare_sampler(oracle(batch), ids, probs).check()
+
+
+def test_filter_debug_matches_eq_39_2():
+    batch = workloads.random_sampler_batch(16, 5003, dtype="bf16", seed=5, kinds="mixed")
+    logits = device_logits(batch.data, batch.dtype)
+    ids, probs, full, kept, status = binding.filter_debug(logits, batch.params, 0, 0)
+    torch.cuda.synchronize()
+    full = full.cpu().numpy()
+    kept = kept.cpu().numpy()
+    want = osam.filtered_rows(batch.values, batch.params)
+    for b, (pt, size) in enumerate(want):
+        assert kept[b] == size, b
+        assert np.array_equal(full[b] > 0, pt > 0) or np.array_equal(full[b] != 0, pt != 0), b
+        nz = pt > 0
+        np.testing.assert_allclose(full[b][nz], pt[nz], rtol=PROB_RTOL, atol=0)
+
+
+# ------------------------------------------------------------------ edge cases
+
+def make_batch(rows, params, dtype="f32"):
+    data = np.asarray(rows, dtype=np.float32)
+    if dtype == "bf16":
+        data = workloads.f32_to_bf16_bits(data)
+    return workloads.Batch("edge", dtype, data, params)
+
+
+def test_ties_split_by_top_k_and_top_p():
+    # 4000 tokens on 5 distinct values: top-k and top-p boundaries fall inside
+    # tie buckets and must take the lower ids first.
+    rng = np.random.default_rng(1)
+    rows = rng.choice([0.0, -0.5, -1.0, -2.0, -3.0], size=(12, 4000)).astype(np.float32)
+    prm = workloads.make_params(12)
+    prm["top_k"][:6] = [1, 7, 100, 1000, 2500, 3999]
+    prm["top_p"][6:] = [0.01, 0.2, 0.5, 0.7, 0.9, 0.999]
+    for dtype in ("f32", "bf16"):
+        batch = make_batch(rows, prm, dtype)
+        ids, probs, _ = run(batch, seed=4)
+        compare_sampler(oracle(batch, seed=4), ids, probs).check()
+        logits = device_logits(batch.data, dtype)
+        _, _, full, kept, _ = binding.filter_debug(logits, prm, 4, 0)
+        kept = kept.cpu().numpy()
+        want = osam.filtered_rows(batch.values, prm)
+        assert [k for _, k in want] == list(kept)
+        full = full.cpu().numpy()
+        for b, (pt, _) in enumerate(want):
+            assert np.array_equal(full[b] > 0, pt > 0), b
+
+
+def test_error_rows_and_flags():
+    V = 64
+    rows = np.random.default_rng(2).normal(0, 1, size=(8, V)).astype(np.float32)
+    rows[0, :] = np.nan
+    rows[1, :] = -np.inf
+    rows[2, 5] = np.inf
+    rows[3, ::2] = np.nan                       # NaN counts as -inf, row still valid
+    prm = workloads.make_params(8)
+    prm["temperature"][4] = -1.0
+    prm["top_k"][5] = -2
+    prm["top_p"][6] = np.nan
+    prm["min_p"][7] = -0.5
+    batch = make_batch(rows, prm)
+    ids, probs, status = run(batch)
+    want = oracle(batch)
+    assert [r["token"] for r in want] == list(ids)
+    assert ids[3] >= 0 and ids[3] % 2 == 1
+    assert status == (binding.ROW_NONFINITE | binding.ROW_BAD_PARAMS)
+    assert all(math.isnan(p) for p in probs[[0, 1, 2, 4, 5, 6, 7]])
+
+
+def test_greedy_and_zero_temperature_lowest_id():
+    rows = np.zeros((3, 300), dtype=np.float32)
+    rows[:, [17, 120, 250]] = 5.0
+    prm = workloads.make_params(3, temperature=1.0)
+    prm["greedy"][0] = 1
+    prm["temperature"][1] = 0.0
+    prm["temperature"][2] = 1e-3                # sampling, but effectively the tied top tokens
+    ids, probs, _ = run(make_batch(rows, prm))
+    assert ids[0] == 17 and ids[1] == 17 and probs[0] == 1.0
+    assert ids[2] in (17, 120, 250)
+
+
+def test_signed_zero_and_min_p_one():
+    rows = np.array([[0.0, -0.0, -1.0, -0.0, 0.0]], dtype=np.float32)
+    prm = workloads.make_params(1, greedy=1)
+    ids, _, _ = run(make_batch(rows, prm))
+    assert ids[0] == 0
+    prm = workloads.make_params(1, min_p=1.0)   # min_p >= 1 is off
+    batch = make_batch(rows, prm)
+    ids, probs, _ = run(batch, seed=9)
+    compare_sampler(oracle(batch, seed=9), ids, probs).check()
+
+
+def test_misaligned_base_pointer():
+    batch = workloads.random_sampler_batch(6, 3001, dtype="bf16", seed=12, kinds="mixed")
+    big = np.zeros((6 * 3001 + 3,), dtype=np.uint16)
+    big[3:] = batch.data.reshape(-1)
+    t = torch.from_numpy(big.view(np.int16)).view(torch.bfloat16).cuda()
+    logits = t[3:].view(6, 3001)                 # base 6 bytes past a 16-byte boundary
+    ids, probs, status = binding.sample(logits, batch.params, 0, 0)
+    torch.cuda.synchronize()
+    compare_sampler(oracle(batch), ids.cpu().numpy(), probs.cpu().numpy()).check()
+
+
+def test_results_do_not_depend_on_cluster_size(monkeypatch):
+    batch = workloads.random_sampler_batch(16, 20011, dtype="bf16", seed=21, kinds="mixed")
+    outs = []
+    for cluster in ("1", "2", "4", "16"):
+        monkeypatch.setenv("SMP_FORCE_CLUSTER", cluster)
+        outs.append(run(batch, seed=2, offset=5)[:2])
+    monkeypatch.delenv("SMP_FORCE_CLUSTER")
+    for ids, probs in outs[1:]:
+        assert np.array_equal(ids, outs[0][0])
+        assert np.array_equal(probs, outs[0][1])
+
+
+def test_repeatable_and_offset_changes_draws():
+    batch = workloads.random_sampler_batch(32, 2000, dtype="f32", seed=3, kinds="plain")
+    a = run(batch, seed=1, offset=0)
+    b = run(batch, seed=1, offset=0)
+    c = run(batch, seed=1, offset=1)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+    assert not np.array_equal(a[0], c[0])
+
+
+def test_draw_histogram_chi_square():
+    z = np.array([2.0, 1.0, 0.5, 0.0, -1.0, -3.0, -7.0, 1.5], dtype=np.float32)
+    rows = 200_000
+    prm = workloads.make_params(rows, temperature=0.9, top_k=6, top_p=0.97)
+    logits = torch.from_numpy(np.tile(z, (rows, 1))).cuda()
+    ids, _, status = binding.sample(logits, prm, 8, 0)
+    counts = np.bincount(ids.cpu().numpy(), minlength=z.size)
+    _, _, pt, _ = osam.filtered_distribution(z, 0.9, top_k=6, top_p=0.97)
+    mask = pt > 0
+    assert np.all(counts[~mask] == 0)
+    expected = pt[mask] * rows
+    stat = float(np.sum((counts[mask] - expected) ** 2 / expected))
+    dof = int(mask.sum()) - 1
+    assert stat < {3: 16.27, 4: 18.47, 5: 20.52}[dof]

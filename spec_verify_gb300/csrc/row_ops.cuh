@@ -155,11 +155,13 @@ __device__ uint64_t cluster_max(RowCtx<T>& c, uint64_t local) {
   return best;
 }
 
-// Cluster-wide sums of up to 4 u64 values; also the exclusive prefix over
-// ranks of value 0 (for this CTA).
+// Cluster-wide sums of up to 4 per-thread u64 values; also this CTA's own sum
+// and the exclusive prefix over ranks of value 0.
 template <typename T>
-__device__ void cluster_sum4(RowCtx<T>& c, uint64_t v[4], int nv, uint64_t* prefix0) {
+__device__ void cluster_sum4(RowCtx<T>& c, uint64_t v[4], int nv, uint64_t* prefix0,
+                             uint64_t* local0 = nullptr) {
   for (int j = 0; j < nv; ++j) v[j] = block_sum<uint64_t>(v[j], c.sh->red64);
+  if (local0) *local0 = v[0];
   if (threadIdx.x == 0)
     for (int j = 0; j < nv; ++j) c.mine().w[j] = v[j];
   c.exchange();

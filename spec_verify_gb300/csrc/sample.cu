@@ -219,10 +219,9 @@ __global__ void __launch_bounds__(kThreads, 1) sample_kernel(SampleArgs a) {
     // Kept mass Z_S of this CTA, of the row, and the prefix over CTAs.
     uint64_t zs = 0;
     for (int i = threadIdx.x; i < n; i += kThreads) zs += weight(i);
-    const uint64_t z_local = block_sum<uint64_t>(zs, sh.red64);
-    uint64_t tot[4] = {z_local, 0, 0, 0};
-    uint64_t z_before = 0;
-    cluster_sum4(c, tot, 1, &z_before);
+    uint64_t tot[4] = {zs, 0, 0, 0};
+    uint64_t z_before = 0, z_local = 0;
+    cluster_sum4(c, tot, 1, &z_before, &z_local);
     const uint64_t z_kept = tot[0];
 
     // The draw: the first kept token (id order) whose running mass exceeds

@@ -158,6 +158,42 @@ smp_status smp_spec_verify(const void* p_logits, const void* q_logits, const int
                            int32_t* out_ids, int32_t* status, void* workspace,
                            size_t workspace_bytes, void* stream);
 
+/*
+ * Size of the device array that smp_spec_verify_static uses as its workspace
+ * (1 MiB: enough for batch * (2k+1) <= 43690, e.g. 1024 rows with k = 16).
+ */
+#define SMP_STATIC_VERIFY_SCRATCH_BYTES (1u << 20)
+
+/*
+ * smp_spec_verify_static -- smp_spec_verify for callers that cannot allocate
+ * device memory.  The pages have no counterpart to this call; it exists for
+ * the deployment, not for the method.
+ *
+ * Some callers cannot hand the verifier a workspace: code that runs inside an
+ * allocator or memory-pool callback, runtimes that forbid cudaMalloc once they
+ * have started serving, or loops that must not let cudaMalloc / cudaFree
+ * synchronise the device.  This entry point takes the same arguments as
+ * smp_spec_verify minus the workspace, and allocates nothing: its scratch is
+ * a fixed array of SMP_STATIC_VERIFY_SCRATCH_BYTES in device memory that the
+ * library holds on every GPU that loads it, until the process exits.
+ *
+ *   - Sizes whose workspace (smp_spec_verify_workspace_bytes(batch, k)) is
+ *     larger than SMP_STATIC_VERIFY_SCRATCH_BYTES return SMP_ERR_WORKSPACE
+ *     before anything is launched.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture on the device.
+ *   - Every call on a device uses the same array and leaves its contents
+ *     behind.  Each call writes every entry it reads before reading it, so
+ *     nothing needs to start at zero, but calls that can overlap on the GPU
+ *     (different streams without ordering between them) race on the array and
+ *     must not be issued.
+ */
+smp_status smp_spec_verify_static(const void* p_logits, const void* q_logits, const int32_t* draft_ids,
+                                  int32_t batch, int32_t k, int32_t vocab, smp_dtype dtype,
+                                  uint64_t seed, uint64_t offset, int32_t* out_accepted_len,
+                                  int32_t* out_ids, int32_t* status, void* stream);
+
 /* Human-readable name of a status code (static string). */
 const char* smp_status_string(smp_status s);
 

@@ -26,7 +26,10 @@ ROW_BAD_DRAFT = 8
 
 # Symbols declared in include/smp.h.
 EXPORTS = ("smp_sample", "smp_filter_debug", "smp_spec_verify_workspace_bytes",
-           "smp_spec_verify", "smp_status_string", "smp_last_cuda_error", "smp_abi_version")
+           "smp_spec_verify", "smp_spec_verify_static", "smp_status_string", "smp_last_cuda_error",
+           "smp_abi_version")
+
+STATIC_VERIFY_SCRATCH_BYTES = 1 << 20
 
 _lib = None
 
@@ -58,6 +61,8 @@ def load():
     lib.smp_spec_verify_workspace_bytes.restype = sz
     lib.smp_spec_verify.argtypes = [vp, vp, vp, i32, i32, i32, i32, u64, u64, vp, vp, vp, vp, sz, vp]
     lib.smp_spec_verify.restype = i32
+    lib.smp_spec_verify_static.argtypes = [vp, vp, vp, i32, i32, i32, i32, u64, u64, vp, vp, vp, vp]
+    lib.smp_spec_verify_static.restype = i32
     lib.smp_status_string.argtypes = [i32]
     lib.smp_status_string.restype = ctypes.c_char_p
     lib.smp_last_cuda_error.argtypes = []
@@ -185,4 +190,23 @@ def spec_verify(p_logits, q_logits, draft_ids, seed=0, offset=0, workspace=None,
     _check(lib.smp_spec_verify(_ptr(p_logits), _ptr(q_logits), _ptr(draft_ids), batch, k, vocab,
                                _dtype_code(p_logits), seed, offset, _ptr(out_accepted), _ptr(out_ids),
                                _ptr(status), _ptr(workspace), workspace.numel(), _stream(stream)))
+    return out_accepted, out_ids, status
+
+
+def spec_verify_static(p_logits, q_logits, draft_ids, seed=0, offset=0, out_accepted=None, out_ids=None,
+                       status=None, stream=None):
+    """smp_spec_verify_static: as spec_verify, with the library's own fixed
+    device scratch instead of a workspace (for callers that cannot allocate).
+    The outputs must be supplied by the caller if it cannot allocate either."""
+    torch = _torch()
+    lib = load()
+    batch, k1, vocab = p_logits.shape
+    k = k1 - 1
+    dev = p_logits.device
+    out_accepted = out_accepted if out_accepted is not None else torch.empty(batch, dtype=torch.int32, device=dev)
+    out_ids = out_ids if out_ids is not None else torch.empty(batch, k + 1, dtype=torch.int32, device=dev)
+    status = status if status is not None else torch.empty(1, dtype=torch.int32, device=dev)
+    _check(lib.smp_spec_verify_static(_ptr(p_logits), _ptr(q_logits), _ptr(draft_ids), batch, k, vocab,
+                                      _dtype_code(p_logits), seed, offset, _ptr(out_accepted),
+                                      _ptr(out_ids), _ptr(status), _stream(stream)))
     return out_accepted, out_ids, status

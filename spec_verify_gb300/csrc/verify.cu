@@ -14,6 +14,8 @@
 //                          bonus draw from p_K.
 #include <cuda_runtime.h>
 
+#include <mutex>
+
 #include "launch.h"
 #include "row_ops.cuh"
 #include "smp.h"
@@ -320,4 +322,61 @@ extern "C" smp_status smp_spec_verify(const void* p_logits, const void* q_logits
   a.ws = reinterpret_cast<PosStat*>(workspace);
   if (dtype == SMP_F32) return launch_verify<float>(a, st);
   return launch_verify<uint16_t>(a, st);
+}
+
+// ------------------------------------------------------------------ allocation-free variant
+//
+// For callers that cannot allocate device memory when they verify (allocator
+// or pool callbacks, runtimes that forbid cudaMalloc while serving, loops that
+// must not let cudaMalloc / cudaFree synchronise the device), the workspace of
+// smp_spec_verify can live in this fixed array instead.  Every GPU that loads
+// the library holds it until the process exits.  All calls on a device share
+// it: each call writes every entry before it reads it, and calls that overlap
+// on the GPU race.
+
+namespace smp {
+
+constexpr size_t kStaticVerifyScratchBytes = SMP_STATIC_VERIFY_SCRATCH_BYTES;
+constexpr int kMaxDevices = 64;
+
+static __device__ __align__(256) unsigned char g_verify_scratch[kStaticVerifyScratchBytes];
+
+// Device address of g_verify_scratch on `dev`, looked up once per device with
+// that device current (in host code the array's name is not a device address).
+static void* static_scratch_address(int dev, cudaError_t* err) {
+  static std::mutex mu;
+  static void* addr[kMaxDevices] = {};
+  std::lock_guard<std::mutex> lock(mu);
+  if (dev < 0 || dev >= kMaxDevices) {
+    *err = cudaErrorInvalidDevice;
+    return nullptr;
+  }
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    *err = cudaGetSymbolAddress(&p, g_verify_scratch);
+    if (*err != cudaSuccess) return nullptr;
+    addr[dev] = p;
+  }
+  *err = cudaSuccess;
+  return addr[dev];
+}
+
+}  // namespace smp
+
+extern "C" smp_status smp_spec_verify_static(const void* p_logits, const void* q_logits,
+                                             const int32_t* draft_ids, int32_t batch, int32_t k,
+                                             int32_t vocab, smp_dtype dtype, uint64_t seed,
+                                             uint64_t offset, int32_t* out_accepted_len,
+                                             int32_t* out_ids, int32_t* status, void* stream) {
+  using namespace smp;
+  const size_t need = smp_spec_verify_workspace_bytes(batch, k);
+  if (need == 0) return SMP_ERR_INVALID_ARG;
+  if (need > kStaticVerifyScratchBytes) return SMP_ERR_WORKSPACE;
+  const int dev = current_device();
+  if (dev < 0) return fail_cuda(cudaGetLastError());
+  cudaError_t err = cudaSuccess;
+  void* scratch = static_scratch_address(dev, &err);
+  if (scratch == nullptr) return fail_cuda(err);
+  return smp_spec_verify(p_logits, q_logits, draft_ids, batch, k, vocab, dtype, seed, offset,
+                         out_accepted_len, out_ids, status, scratch, kStaticVerifyScratchBytes, stream);
 }

@@ -4,6 +4,7 @@
 #include <stdlib.h>
 
 #include <map>
+#include <tuple>
 #include <mutex>
 #include <utility>
 
@@ -45,6 +46,8 @@ int forced_cluster() {
   return (c == 1 || c == 2 || c == 4 || c == 8 || c == 16) ? c : 0;
 }
 
+bool verbose() { return getenv("SMP_VERBOSE") != nullptr; }
+
 cudaError_t prepare_kernel(const void* kernel, int dev, const LaunchShape& ls) {
   static std::mutex mu;
   static std::map<std::pair<const void*, int>, std::pair<size_t, int>> done;
@@ -60,6 +63,35 @@ cudaError_t prepare_kernel(const void* kernel, int dev, const LaunchShape& ls) {
     if (err != cudaSuccess) return err;
     slot.second = 1;
   }
+  return cudaSuccess;
+}
+
+cudaError_t max_active_clusters(const void* kernel, int dev, const LaunchShape& ls, int* out) {
+  static std::mutex mu;
+  static std::map<std::tuple<const void*, int, int, size_t>, int> cache;
+  std::lock_guard<std::mutex> lock(mu);
+  const auto key = std::make_tuple(kernel, dev, ls.cluster, ls.smem);
+  auto it = cache.find(key);
+  if (it != cache.end()) {
+    *out = it->second;
+    return cudaSuccess;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(ls.cluster) * 64u);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = ls.smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = unsigned(ls.cluster);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  const cudaError_t err = cudaOccupancyMaxActiveClusters(&n, kernel, &cfg);
+  if (err != cudaSuccess) return err;
+  cache[key] = n;
+  *out = n;
   return cudaSuccess;
 }
 

@@ -131,12 +131,17 @@ __device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
   e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
 }
 
+// c = log2(e) / T as head + tail, in binary32 arithmetic: q = L_hi / T, then
+// the exact residual L_hi - q T (one fused multiply-add) plus L_lo, divided by T.
 __device__ __forceinline__ RowScale make_row_scale(float m, float temperature) {
+  constexpr float kLog2eHi = 0x1.715476p+0f;     // binary32 nearest log2(e)
+  constexpr float kLog2eLo = 0x1.4ae0cp-26f;     // log2(e) - kLog2eHi
   RowScale rs;
   rs.m = m;
-  const double c = 1.4426950408889634073599246810019 / double(temperature);
-  rs.c_hi = float(c);
-  rs.c_lo = float(c - double(rs.c_hi));
+  const float q = __fdiv_rn(kLog2eHi, temperature);
+  const float r = __fadd_rn(__fmaf_rn(-q, temperature, kLog2eHi), kLog2eLo);
+  rs.c_hi = q;
+  rs.c_lo = __fdiv_rn(r, temperature);
   return rs;
 }
 
@@ -240,6 +245,21 @@ __device__ __forceinline__ double mass_double(float z, const RowScale& rs, const
 
 // ------------------------------------------------------------------ warp / block helpers
 
+// Barrier over the kThreads threads that work on rows (named barrier 1).  A
+// kernel may run an extra producer warp that takes no part in it.
+__device__ __forceinline__ void cta_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory"); }
+
+// cta_sync() that also returns how many of the kThreads threads passed `pred`.
+__device__ __forceinline__ int cta_sync_count(bool pred) {
+  int r;
+  asm volatile(
+      "{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %1, 0;\n\tbar.red.popc.u32 %0, 1, %2, q;\n\t}"
+      : "=r"(r)
+      : "r"(int(pred)), "n"(kThreads)
+      : "memory");
+  return r;
+}
+
 __device__ __forceinline__ uint64_t shfl_xor_u64(uint64_t v, int mask) {
   const uint32_t lo = __shfl_xor_sync(0xFFFFFFFFu, uint32_t(v), mask);
   const uint32_t hi = __shfl_xor_sync(0xFFFFFFFFu, uint32_t(v >> 32), mask);
@@ -330,9 +350,9 @@ template <typename U>
 __device__ __forceinline__ U block_sum(U v, U* scratch) {
   v = warp_sum<U>(v);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  __syncthreads();
+  cta_sync();
   if (lane == 0) scratch[warp] = v;
-  __syncthreads();
+  cta_sync();
   U total = 0;
 #pragma unroll
   for (int w = 0; w < kWarps; ++w) total += scratch[w];
@@ -351,9 +371,9 @@ __device__ __forceinline__ uint64_t block_max_u64(uint64_t v, uint64_t* scratch)
     v = w > v ? w : v;
   }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  __syncthreads();
+  cta_sync();
   if (lane == 0) scratch[warp] = v;
-  __syncthreads();
+  cta_sync();
   uint64_t best = scratch[0];
 #pragma unroll
   for (int w = 1; w < kWarps; ++w) best = scratch[w] > best ? scratch[w] : best;
@@ -433,40 +453,58 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t addr, uint32_t parity
   }
 }
 
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+// Arrive (release, cluster scope) on the mbarrier at `bar` in the CTA of cluster rank `rank`.
+__device__ __forceinline__ void mbar_arrive_rank(const uint64_t* bar, uint32_t rank) {
+  const uint32_t remote = map_rank(smem_addr(bar), rank);
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote) : "memory");
+}
+
+// A group of CTAs of one cluster (cluster ranks first .. first + ranks - 1)
+// that synchronise through one mbarrier per CTA.
 struct ClusterBarrier {
   uint64_t* bar;      // this CTA's mbarrier (shared memory)
   uint32_t parity;
   uint32_t ranks;
+  uint32_t first;
   int* ok;            // shared flag: 0 after a timeout
 
-  __device__ void init(uint64_t* mbar, int* ok_flag, uint32_t nranks) {
+  // Thread 0 initialises this CTA's mbarrier.  Before the first sync() every
+  // member's barrier must be initialised and visible: the caller issues
+  // fence.mbarrier_init and a cluster-wide synchronisation.
+  __device__ void setup(uint64_t* mbar, int* ok_flag, uint32_t first_rank, uint32_t nranks) {
     bar = mbar;
     ok = ok_flag;
     ranks = nranks;
+    first = first_rank;
     parity = 0;
     if (threadIdx.x == 0) {
-      asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(nranks) : "memory");
-      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+      mbar_init(bar, nranks);
       *ok = 1;
     }
-    __syncthreads();
+  }
+
+  // setup() for the whole cluster, followed by the fence and cluster sync.
+  __device__ void init(uint64_t* mbar, int* ok_flag, uint32_t nranks) {
+    setup(mbar, ok_flag, 0, nranks);
+    if (threadIdx.x == 0) asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    cta_sync();
     hw_cluster_sync();   // every peer's mbarrier exists before any remote arrive
   }
 
-  // All CTAs of the cluster reach this point; writes made before it are
-  // visible to every CTA after it.  Returns false after a timeout.
+  // All members reach this point; writes made before it are visible to every
+  // member after it.  Returns false after a timeout.
   __device__ bool sync() {
-    __syncthreads();
+    cta_sync();
     if (threadIdx.x == 0) {
       asm volatile("fence.acq_rel.cluster;" ::: "memory");
-      const uint32_t local = smem_addr(bar);
-      for (uint32_t r = 0; r < ranks; ++r) {
-        const uint32_t remote = map_rank(local, r);
-        asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote) : "memory");
-      }
-      if (!mbar_wait_bounded(local, parity)) *ok = 0;
+      for (uint32_t r = 0; r < ranks; ++r) mbar_arrive_rank(bar, first + r);
+      if (!mbar_wait_bounded(smem_addr(bar), parity)) *ok = 0;
     }
-    __syncthreads();
+    cta_sync();
     parity ^= 1u;
     return *ok != 0;
   }

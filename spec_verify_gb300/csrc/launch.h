@@ -20,6 +20,8 @@ struct LaunchShape {
   int cluster = 1;   // CTAs per row
   int slice = 0;     // elements per CTA
   size_t smem = 0;   // dynamic shared memory per CTA
+  bool pdl = false;  // programmatic launch: the kernel may start before the previous kernel on the
+                     // stream ends, and waits for it (griddepcontrol.wait) before touching memory
 };
 
 // Records `err` as the last CUDA error of this thread and returns SMP_ERR_CUDA.
@@ -36,9 +38,16 @@ int device_sms(int dev);
 // launch shape), or 0.
 int forced_cluster();
 
+// True when the environment variable SMP_VERBOSE is set: launch shapes are
+// printed to stderr.
+bool verbose();
+
 // Sets the dynamic shared memory limit and, for clusters above 8, the
 // non-portable cluster size attribute of `kernel` (once per device and size).
 cudaError_t prepare_kernel(const void* kernel, int dev, const LaunchShape& ls);
+
+// Number of clusters of shape `ls` that can be resident at once (cached).
+cudaError_t max_active_clusters(const void* kernel, int dev, const LaunchShape& ls, int* out);
 
 // Launches `kernel(*args)` with a cluster of ls.cluster CTAs along x.
 template <typename Args>
@@ -49,13 +58,19 @@ cudaError_t launch_cluster(const void* kernel, dim3 grid, dim3 block, const Laun
   cfg.blockDim = block;
   cfg.dynamicSmemBytes = ls.smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = unsigned(ls.cluster);
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  unsigned n = 1;
+  if (ls.pdl) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = n;
   void* params[1] = {args};
   return cudaLaunchKernelExC(&cfg, kernel, params);
 }

@@ -71,18 +71,21 @@ struct RowCtx {
   const T* s;          // slice: element i has global id lo + i
   int n;               // elements in this CTA's slice (may be 0)
   int lo;              // global id of element 0
-  uint32_t rank;
-  uint32_t nranks;
-  ClusterBarrier cb;
+  uint32_t rank;        // index of this CTA within the group
+  uint32_t nranks;      // CTAs working on the row
+  uint32_t first;       // cluster rank of member 0 (members are first .. first + nranks - 1)
+  ClusterBarrier* cb;  // barrier of the group (its phase state outlives one row)
   int mb;              // mailbox buffer in use
   bool alive;          // false after a timeout
 
   __device__ Mailbox& mine() { return sh->mbox[mb]; }
-  __device__ uint32_t peer_addr(const void* field, uint32_t r) const { return map_rank(smem_addr(field), r); }
+  __device__ uint32_t peer_addr(const void* field, uint32_t r) const {
+    return map_rank(smem_addr(field), first + r);
+  }
 
   // Publish-then-read: call after writing mine(); returns after the barrier.
   __device__ bool exchange() {
-    alive = alive && cb.sync();
+    alive = alive && cb->sync();
     return alive;
   }
   __device__ void flip() { mb ^= 1; }
@@ -289,7 +292,7 @@ __device__ Boundary radix_select(RowCtx<T>& c, uint32_t k, const MassTarget& tar
     const int shift = 8 * (kL - 1 - lvl);
     sh->hist_cnt[tid] = 0;
     if (kMass) sh->hist_mass[tid] = 0;
-    __syncthreads();
+    cta_sync();
     for (int i = tid; i < c.n; i += kThreads) {
       const uint32_t key = elem_key<T>(c.s[i]);
       if (lvl > 0 && (key >> (shift + 8)) != prefix) continue;
@@ -300,7 +303,7 @@ __device__ Boundary radix_select(RowCtx<T>& c, uint32_t k, const MassTarget& tar
         if (e) atomicAdd(reinterpret_cast<unsigned long long*>(&sh->hist_mass[d]), (unsigned long long)e);
       }
     }
-    __syncthreads();
+    cta_sync();
     c.mine().count[tid] = sh->hist_cnt[tid];
     if (kMass) c.mine().mass[tid] = sh->hist_mass[tid];
     c.exchange();
@@ -316,7 +319,7 @@ __device__ Boundary radix_select(RowCtx<T>& c, uint32_t k, const MassTarget& tar
     }
     sh->tot_cnt[tid] = tc;
     if (kMass) sh->tot_mass[tid] = tm;
-    __syncthreads();
+    cta_sync();
     // Warp 0 finds the crossing digit, scanning digits from 255 down.
     if (tid < 32) {
       const int lane = tid;
@@ -379,7 +382,7 @@ __device__ Boundary radix_select(RowCtx<T>& c, uint32_t k, const MassTarget& tar
         sh->bcast64[0] = found_mass_above;
       }
     }
-    __syncthreads();
+    cta_sync();
     const uint32_t d = sh->bcast32[0];
     above = sh->bcast32[1];
     mass_above = sh->bcast64[0];
@@ -387,7 +390,7 @@ __device__ Boundary radix_select(RowCtx<T>& c, uint32_t k, const MassTarget& tar
     if (lvl == kL - 1 && tid == int(d)) {
       for (uint32_t r = 0; r < c.nranks; ++r) sh->rank_cnt[r] = my_rank_cnt[r];
     }
-    __syncthreads();
+    cta_sync();
     c.flip();
   }
   out.key = prefix;
@@ -420,7 +423,7 @@ __device__ Boundary radix_select(RowCtx<T>& c, uint32_t k, const MassTarget& tar
     }
     out.n = n;
   }
-  __syncthreads();
+  cta_sync();
   return out;
 }
 
@@ -438,13 +441,13 @@ __device__ uint32_t nth_with_key(RowCtx<T>& c, uint32_t key, uint32_t q) {
   // exclusive scan of counts over threads
   const uint32_t inc = warp_inclusive_scan<uint32_t>(cnt);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  __syncthreads();
+  cta_sync();
   if (lane == 31) sh->red32[warp] = inc;
-  __syncthreads();
+  cta_sync();
   uint32_t before = inc - cnt;
   for (int w = 0; w < warp; ++w) before += sh->red32[w];
   if (threadIdx.x == 0) sh->bcast32[4] = 0xFFFFFFFFu;
-  __syncthreads();
+  cta_sync();
   if (before < q && q <= before + cnt) {
     uint32_t seen = before;
     for (int i = b0; i < b1; ++i) {
@@ -454,7 +457,7 @@ __device__ uint32_t nth_with_key(RowCtx<T>& c, uint32_t key, uint32_t q) {
       }
     }
   }
-  __syncthreads();
+  cta_sync();
   return sh->bcast32[4];
 }
 
@@ -470,10 +473,10 @@ __device__ int find_crossing(RowCtx<T>& c, W t, F weight, W* scratch_red, int* r
   for (int i = b0; i < b1; ++i) sum += weight(i);
   const W inc = warp_inclusive_scan<W>(sum);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  __syncthreads();
+  cta_sync();
   if (lane == 31) scratch_red[warp] = inc;
   if (threadIdx.x == 0) *result = -1;
-  __syncthreads();
+  cta_sync();
   W before = inc - sum;
   for (int w = 0; w < warp; ++w) before += scratch_red[w];
   if (sum > 0 && before <= t && t < before + sum) {
@@ -486,7 +489,7 @@ __device__ int find_crossing(RowCtx<T>& c, W t, F weight, W* scratch_red, int* r
       }
     }
   }
-  __syncthreads();
+  cta_sync();
   return *result;
 }
 

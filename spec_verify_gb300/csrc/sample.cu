@@ -3,22 +3,39 @@
 // section 39.2) and an id-order inverse-CDF draw ("Choosing the next word",
 // section "Where the randomness comes from, and where it stops").
 //
-// One thread-block cluster per row; each CTA keeps one contiguous slice of the
-// row in shared memory, read from HBM exactly once.  All decisions are made on
-// exact integers: logit keys for order and ties, 64-bit fixed-point masses for
-// the top-p crossing and the draw, so the result does not depend on how the row
-// is split or scheduled.
+// Rows are independent, so each CTA owns whole rows and no CTA ever waits for
+// another.  Two paths, chosen from a row's knobs:
+//
+//  * candidate path -- greedy rows, min-p rows, and top-k rows with small k
+//    (no top-p).  The kept set S is a short prefix of the order (logit
+//    descending, id ascending).  The row streams once from HBM through a TMA
+//    ring in shared memory; every element at or above a running lower bound
+//    of S's boundary becomes a candidate, and S is selected exactly among the
+//    candidates at the end of the row.
+//
+//  * general path -- top-p rows, unfiltered sampling, large k, or a candidate
+//    overflow: exact radix selection over logit keys with 64-bit fixed-point
+//    masses (row_ops.cuh), run by the row's CTA over global memory.
+//
+// All decisions use exact integers (keys, fixed-point masses), so results do
+// not depend on how rows are scheduled.
 #include <cuda_runtime.h>
-
-#include <algorithm>
-#include <cmath>
-#include <mutex>
+#include <stdio.h>
 
 #include "launch.h"
 #include "row_ops.cuh"
 #include "smp.h"
 
 namespace smp {
+
+constexpr int kBufBytes = 32768;                       // one TMA copy: a batch of the row
+constexpr int kBufs = 2;                               // batches in flight per CTA (double buffering)
+constexpr int kSubBytes = kBufBytes / kWarps;          // the part of a batch one warp processes
+constexpr int kVecPerLane = kSubBytes / 16 / 32;       // 16-byte vectors per lane and batch
+constexpr int kCandMax = 2048;    // candidate list capacity per row
+constexpr int kCompactAt = 1024;  // top-k: shrink the candidate list when it grows past this
+constexpr int kFinalMax = kThreads;   // candidates at or above the final threshold (one per thread)
+constexpr int kFastTopK = 128;    // top-k rows up to this k take the candidate path
 
 struct SampleArgs {
   const void* logits;
@@ -32,7 +49,6 @@ struct SampleArgs {
   int32_t* status;
   float* full_probs;   // debug: [B, V] p~ or NULL
   int32_t* kept;       // debug: [B] |S| or NULL
-  int slice;           // elements per CTA
 };
 
 __device__ __forceinline__ bool sampling_params_valid(const smp_row_params& p) {
@@ -44,10 +60,133 @@ __device__ __forceinline__ bool sampling_params_valid(const smp_row_params& p) {
   return true;
 }
 
+__device__ __forceinline__ bool row_is_greedy(const smp_row_params& p) {
+  return p.greedy != 0 || p.temperature == 0.0f;
+}
+
+// Candidate path: greedy, or valid knobs without top-p and with min-p or a small top-k.
+__device__ __forceinline__ bool row_is_fast(const smp_row_params& p, int V) {
+  if (row_is_greedy(p)) return true;
+  if (!sampling_params_valid(p)) return false;
+  if (p.top_p < 1.0f) return false;
+  const bool minp = p.min_p > 0.0f && p.min_p < 1.0f;
+  const bool topk = p.top_k > 0 && p.top_k < V;
+  return minp || (topk && p.top_k <= kFastTopK);
+}
+
+// Lower bound, in logits, of {z : exp((z - m) / T) >= min_p} for a row maximum
+// of at least m: m + T ln(min_p), lowered by a margin that covers the float
+// rounding of the expression.
+__device__ __forceinline__ float minp_lower_bound(float m, float temperature, float min_p) {
+  const float w = temperature * logf(min_p);
+  const float t = m + w;
+  return t - (fabsf(m) + fabsf(w)) * 0x1p-20f - 0x1p-126f;
+}
+
+// ------------------------------------------------------------------ slices and TMA
+
+__device__ __forceinline__ void tma_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+               "r"(bytes)
+               : "memory");
+  if (bytes)
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
+// Wait (every thread) for a TMA phase; false after the time limit.
+__device__ __forceinline__ bool wait_full(uint64_t* bar, uint32_t parity) {
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 0;; ++it) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    if (done) return true;
+    if ((it & 255u) == 255u && global_timer_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+// ------------------------------------------------------------------ vector passes
+
 template <typename T>
-__device__ __forceinline__ uint32_t key_of_float(float v) {
-  if (KeyTraits<T>::kBits == 32) return key_of_bits(__float_as_uint(v));
-  return key_of_bits(__float_as_uint(v) & 0xFFFF0000u) >> 16;
+struct VecOps;
+
+template <>
+struct VecOps<uint16_t> {
+  static constexpr int kPer = 8;
+  static __device__ __forceinline__ uint32_t max2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+  }
+  static __device__ __forceinline__ uint32_t neg_inf() { return 0xFF80FF80u; }
+  // max of the 8 values of x, packed in two halves
+  static __device__ __forceinline__ uint32_t vmax(const uint4& x) {
+    return max2(max2(x.x, x.y), max2(x.z, x.w));
+  }
+  static __device__ __forceinline__ float finish(uint32_t m) {
+    return fmaxf(__uint_as_float(m & 0xFFFF0000u), __uint_as_float(m << 16));
+  }
+};
+
+template <>
+struct VecOps<float> {
+  static constexpr int kPer = 4;
+  static __device__ __forceinline__ uint32_t max2(uint32_t a, uint32_t b) {
+    return __float_as_uint(fmaxf(__uint_as_float(a), __uint_as_float(b)));
+  }
+  static __device__ __forceinline__ uint32_t neg_inf() { return 0xFF800000u; }
+  static __device__ __forceinline__ uint32_t vmax(const uint4& x) {
+    return __float_as_uint(fmaxf(fmaxf(__uint_as_float(x.x), __uint_as_float(x.y)),
+                                 fmaxf(__uint_as_float(x.z), __uint_as_float(x.w))));
+  }
+  static __device__ __forceinline__ float finish(uint32_t m) { return __uint_as_float(m); }
+};
+
+__device__ __forceinline__ float block_max_f(float v, float* scratch) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  cta_sync();
+  if (lane == 0) scratch[warp] = v;
+  cta_sync();
+  float r = scratch[0];
+#pragma unroll
+  for (int w = 1; w < kWarps; ++w) r = fmaxf(r, scratch[w]);
+  return r;
+}
+
+// The k-th largest (1 <= k <= kThreads) of one float per thread, as a value v
+// with at least k of the inputs >= v.  Bit-wise search over the order keys.
+template <typename T>
+__device__ __forceinline__ float kth_largest(float x, int k) {
+  const uint32_t key = key_of_bits(__float_as_uint(x));
+  uint32_t t = 0;
+  const int low = KeyTraits<T>::kBits == 16 ? 16 : 0;   // bf16 keys carry no information below bit 16
+  for (int bit = 31; bit >= low; --bit) {
+    const uint32_t cand = t | (1u << bit);
+    if (cta_sync_count(key >= cand) >= k) t = cand;
+  }
+  return value_of_key(t);
+}
+
+// Largest packed (key, ~id) of a slice (shared or global memory).
+template <typename T>
+__device__ uint64_t slice_best(const T* s, int n, int lo) {
+  uint64_t best = 0;
+  for (int i = threadIdx.x; i < n; i += kThreads) {
+    const uint64_t p = pack_key_id(elem_key<T>(s[i]), uint32_t(lo + i));
+    best = p > best ? p : best;
+  }
+  return best;
 }
 
 // Smallest key whose value z satisfies exp((z - m) / T) >= min_p, i.e. the
@@ -62,13 +201,14 @@ __device__ uint32_t minp_threshold_key(RowShared* sh, const RowScale& rs, float 
     const int lane = threadIdx.x;
     const double thr = double(min_p);
     const float est = rs.m + temperature * logf(min_p);
-    const uint32_t k0 = key_of_float<T>(est);
+    const uint32_t k0 = KeyTraits<T>::kBits == 32 ? key_of_bits(__float_as_uint(est))
+                                                  : (key_of_bits(__float_as_uint(est) & 0xFFFF0000u) >> 16);
     uint32_t lo = 0, hi = key_max;   // the answer lies in [lo, hi]; the property holds at hi
     uint32_t start = k0 > 16u ? k0 - 16u : 0u;
     uint32_t stride = 1;
     if (start > hi) start = hi;
     for (int iter = 0; iter < 64 && lo < hi; ++iter) {
-      uint64_t cand64 = uint64_t(start) + uint64_t(lane) * stride;
+      const uint64_t cand64 = uint64_t(start) + uint64_t(lane) * stride;
       const uint32_t cand = cand64 > hi ? hi : uint32_t(cand64);
       const bool ok = mass_double(key_value<T>(cand), rs, sh->table) >= thr;
       const uint32_t mask = __ballot_sync(0xFFFFFFFFu, ok);
@@ -90,46 +230,33 @@ __device__ uint32_t minp_threshold_key(RowShared* sh, const RowScale& rs, float 
     }
     if (lane == 0) sh->bcast32[6] = hi;
   }
-  __syncthreads();
+  cta_sync();
   const uint32_t r = sh->bcast32[6];
-  __syncthreads();
+  cta_sync();
   return r;
 }
 
+__device__ __forceinline__ void write_error_row(const SampleArgs& a, int b, int flags) {
+  a.out_ids[b] = -1;
+  if (a.out_probs) a.out_probs[b] = __int_as_float(0x7FC00000);
+  if (a.kept) a.kept[b] = 0;
+  if (a.status) atomicOr(a.status, flags);
+}
+
+// ------------------------------------------------------------------ general path
+
+// One row by exact radix selection across the group of CTAs of `c`, each
+// holding its slice at c.s.  `best` is this CTA's packed (key, ~id) maximum.
 template <typename T>
-__global__ void __launch_bounds__(kThreads, 1) sample_kernel(SampleArgs a) {
-  extern __shared__ __align__(16) unsigned char dyn_smem[];
-  __shared__ RowShared sh;
-  const uint32_t nranks = cluster_size();
-  const uint32_t rank = cluster_rank();
-  const int b = int(blockIdx.x / nranks);
+__device__ void general_row(RowCtx<T>& c, const SampleArgs& a, int b, const smp_row_params& prm, uint64_t best) {
+  RowShared& sh = *c.sh;
   const int V = a.vocab;
-  if (threadIdx.x < 64) sh.table[threadIdx.x] = kExp2Table[threadIdx.x];
-
-  RowCtx<T> c;
-  c.sh = &sh;
-  c.rank = rank;
-  c.nranks = nranks;
-  c.mb = 0;
-  c.alive = true;
-  c.cb.init(&sh.mbar, &sh.ok, nranks);
-
-  const T* row = reinterpret_cast<const T*>(a.logits) + size_t(b) * size_t(V);
-  const int lo = int(rank) * a.slice;
-  int n = V - lo;
-  n = n < 0 ? 0 : (n > a.slice ? a.slice : n);
-  c.lo = lo;
-  c.n = n;
-  T* s = reinterpret_cast<T*>(dyn_smem + slice_smem_offset(row, lo, n));
-  c.s = s;
-
-  uint64_t best = load_slice(row, lo, n, s);
-  __syncthreads();
+  const T* s = c.s;
+  const int n = c.n, lo = c.lo;
   best = cluster_max(c, best);
   const uint32_t key_max = uint32_t(best >> 32);
   const uint32_t argmax = ~uint32_t(best);
-  const smp_row_params prm = a.params[b];
-  const bool greedy = prm.greedy != 0 || prm.temperature == 0.0f;
+  const bool greedy = row_is_greedy(prm);
 
   int flags = 0;
   if (!c.alive) flags |= kRowTimeout;
@@ -137,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1) sample_kernel(SampleArgs a) {
   else if (!greedy && !sampling_params_valid(prm)) flags |= kRowBadParams;
 
   if (flags == 0 && greedy) {
-    if (rank == 0 && threadIdx.x == 0) {
+    if (c.rank == 0 && threadIdx.x == 0) {
       a.out_ids[b] = int32_t(argmax);
       if (a.out_probs) a.out_probs[b] = 1.0f;
       if (a.kept) a.kept[b] = 1;
@@ -237,7 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1) sample_kernel(SampleArgs a) {
         if (a.out_probs) a.out_probs[b] = float(double(e) / double(z_kept));
       }
     }
-    if (a.kept && rank == 0 && threadIdx.x == 0) a.kept[b] = int32_t(len);
+    if (a.kept && c.rank == 0 && threadIdx.x == 0) a.kept[b] = int32_t(len);
     if (a.full_probs) {
       float* f = a.full_probs + size_t(b) * V + lo;
       const float zf = float(z_kept);
@@ -250,50 +377,614 @@ __global__ void __launch_bounds__(kThreads, 1) sample_kernel(SampleArgs a) {
   }
 
   if (flags) {
-    if (rank == 0 && threadIdx.x == 0) {
-      a.out_ids[b] = -1;
-      if (a.out_probs) a.out_probs[b] = __int_as_float(0x7FC00000);
-      if (a.kept) a.kept[b] = 0;
-      if (a.status) atomicOr(a.status, flags);
-    }
+    if (c.rank == 0 && threadIdx.x == 0) write_error_row(a, b, flags);
     if (a.full_probs && !(flags & kRowTimeout)) {
       float* f = a.full_probs + size_t(b) * V + lo;
       for (int i = threadIdx.x; i < n; i += kThreads) f[i] = __int_as_float(0x7FC00000);
     }
   }
-  c.exchange();   // no CTA leaves while a peer may still read its mailboxes
+  c.exchange();   // no CTA moves on while a peer may still read its mailboxes
+}
+
+// ------------------------------------------------------------------ candidate path
+
+struct StreamShared {
+  uint64_t full[kBufs];       // TMA completion of each batch buffer
+  uint64_t solo_bar;          // barrier of the single-CTA general path
+  int solo_ok;
+  int timeout;                // a wait ran out of time
+  uint32_t cand_n;            // candidates appended for the current row (> kCandMax: overflow)
+  uint32_t fin_n;             // candidates at or above the final threshold
+  uint32_t maxkey;            // running row maximum as an order key
+  unsigned long long zsum;    // Z_S in fixed point
+  float red[kWarps];
+  uint32_t redu[kWarps];
+  uint64_t red64[kWarps];
+  uint32_t bc[2];
+  uint32_t hist[256];
+  uint32_t cand_id[kCandMax];
+  float cand_val[kCandMax];
+  uint32_t f_id[kFinalMax];
+  float f_val[kFinalMax];
+  uint64_t f_mass[kFinalMax];   // E_i of the kept candidates, 0 for the others
+};
+
+// Byte layout of a row: the 16-byte aligned middle [a0, a1) streams through
+// shared memory in batches of kBufBytes; the few elements before and after it
+// are read directly.
+struct RowGeom {
+  const char* r0;      // first byte of the row
+  uintptr_t a0, a1;    // aligned middle (a1 <= a0: no middle)
+  int nchunks;         // batches of kBufBytes
+  int head;            // elements before a0
+  int tail0;           // first element after a1
+};
+
+template <typename T>
+__device__ __forceinline__ RowGeom row_geom(const SampleArgs& a, int row) {
+  RowGeom g;
+  g.r0 = reinterpret_cast<const char*>(a.logits) + size_t(row) * a.vocab * sizeof(T);
+  const uintptr_t r0 = reinterpret_cast<uintptr_t>(g.r0);
+  const uintptr_t r1 = r0 + size_t(a.vocab) * sizeof(T);
+  g.a0 = (r0 + 15) & ~uintptr_t(15);
+  g.a1 = r1 & ~uintptr_t(15);
+  if (g.a1 > g.a0) {
+    g.nchunks = int((g.a1 - g.a0 + kBufBytes - 1) / kBufBytes);
+    g.head = int((g.a0 - r0) / sizeof(T));
+    g.tail0 = int((g.a1 - r0) / sizeof(T));
+  } else {
+    g.nchunks = 0;
+    g.head = a.vocab;
+    g.tail0 = a.vocab;
+  }
+  return g;
+}
+
+// Sum of one u32 per thread over the CTA (every thread gets it).
+__device__ __forceinline__ uint32_t block_sum_u32(uint32_t v, uint32_t* scratch) {
+  v = warp_sum<uint32_t>(v);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  cta_sync();
+  if (lane == 0) scratch[warp] = v;
+  cta_sync();
+  uint32_t t = 0;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) t += scratch[w];
+  return t;
+}
+
+// The k-th largest of vals[0..n) (1 <= k <= n), exactly, as a float: radix
+// selection over the order keys with 8-bit digits (two levels for bf16
+// values, four for binary32), one shared 256-bin histogram per level.
+template <typename T>
+__device__ float kth_largest_list(const float* vals, int n, int k, uint32_t* hist, uint32_t* bcast) {
+  constexpr int kLevels = KeyTraits<T>::kBits == 16 ? 2 : 4;
+  uint32_t prefix = 0;
+  uint32_t need = uint32_t(k);
+  for (int lvl = 0; lvl < kLevels; ++lvl) {
+    const int shift = 24 - 8 * lvl;
+    hist[threadIdx.x] = 0;
+    cta_sync();
+    for (int i = threadIdx.x; i < n; i += kThreads) {
+      const uint32_t key = key_of_bits(__float_as_uint(vals[i]));
+      if (lvl == 0 || (key >> (shift + 8)) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+    }
+    cta_sync();
+    if (threadIdx.x < 32) {
+      // digits 255..0 in lane order: lane l covers 255 - 8l .. 248 - 8l
+      uint32_t c[8], sum = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        c[j] = hist[255 - (threadIdx.x * 8 + j)];
+        sum += c[j];
+      }
+      const uint32_t incl = warp_inclusive_scan<uint32_t>(sum);
+      uint32_t run = incl - sum;
+      int found = -1;
+      uint32_t above = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (found < 0 && run + c[j] >= need) {
+          found = 255 - (threadIdx.x * 8 + j);
+          above = run;
+        }
+        run += c[j];
+      }
+      const uint32_t hits = __ballot_sync(0xFFFFFFFFu, found >= 0);
+      const int src = hits ? __ffs(hits) - 1 : 0;
+      if (threadIdx.x == src) {
+        bcast[0] = uint32_t(found < 0 ? 0 : found);
+        bcast[1] = above;
+      }
+    }
+    cta_sync();
+    prefix = (prefix << 8) | bcast[0];
+    need -= bcast[1];
+    cta_sync();
+  }
+  return value_of_key(kLevels == 2 ? (prefix << 16) | ((prefix & 0x8000u) ? 0u : 0xFFFFu) : prefix);
+}
+
+// Keep only candidates >= theta (order changes).
+__device__ void compact_candidates(StreamShared& ss, float theta) {
+  const int n = min(int(ss.cand_n), kCandMax);
+  uint32_t id[kCandMax / kThreads];
+  float val[kCandMax / kThreads];
+#pragma unroll
+  for (int j = 0; j < kCandMax / kThreads; ++j) {
+    const int i = threadIdx.x + j * kThreads;
+    id[j] = i < n ? ss.cand_id[i] : 0u;
+    val[j] = i < n ? ss.cand_val[i] : -INFINITY;
+  }
+  cta_sync();
+  if (threadIdx.x == 0) ss.cand_n = 0;
+  cta_sync();
+#pragma unroll
+  for (int j = 0; j < kCandMax / kThreads; ++j) {
+    const int i = threadIdx.x + j * kThreads;
+    if (i < n && val[j] >= theta) {
+      const uint32_t slot = atomicAdd(&ss.cand_n, 1u);
+      ss.cand_id[slot] = id[j];
+      ss.cand_val[slot] = val[j];
+    }
+  }
+  cta_sync();
+}
+
+__device__ __forceinline__ void push_candidate(StreamShared& ss, uint32_t id, float z) {
+  const uint32_t slot = atomicAdd(&ss.cand_n, 1u);
+  if (slot < uint32_t(kCandMax)) {
+    ss.cand_id[slot] = id;
+    ss.cand_val[slot] = z;
+  }
+}
+
+// Exact selection and draw of a min-p / top-k candidate-path row.  The
+// candidates hold every element at or above the collection thresholds, which
+// are lower bounds of the kept set's boundary; row_max is the row's largest
+// logit.  Returns false if the row needs the general path (too many
+// candidates).
+template <typename T>
+__device__ bool finalize_candidates(StreamShared& ss, RowShared& sh, const SampleArgs& a, int b,
+                                    const smp_row_params& prm, float row_max) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int V = a.vocab;
+  const bool minp = prm.min_p > 0.0f && prm.min_p < 1.0f;
+  const bool topk = prm.top_k > 0 && prm.top_k < V;
+  if (!isfinite(row_max)) {
+    if (tid == 0) write_error_row(a, b, kRowNonFinite);
+    if (a.full_probs)
+      for (int i = tid; i < V; i += kThreads) a.full_probs[size_t(b) * V + i] = __int_as_float(0x7FC00000);
+    return true;
+  }
+  if (ss.cand_n > uint32_t(kCandMax)) return false;
+  const int n = int(ss.cand_n);
+
+  // The kept set lies at or above theta: min-p's lower bound at the row
+  // maximum and the k-th largest value (the candidates hold every element at
+  // or above it, so their k-th largest is the row's).
+  float theta = -INFINITY;
+  if (minp) theta = minp_lower_bound(row_max, prm.temperature, prm.min_p);
+  float kth = -INFINITY;
+  if (topk) {
+    if (n < prm.top_k) return false;
+    kth = kth_largest_list<T>(ss.cand_val, n, prm.top_k, ss.hist, ss.bc);
+    theta = fmaxf(theta, kth);
+  }
+  if (tid == 0) {
+    ss.fin_n = 0;
+    ss.zsum = 0;
+  }
+  cta_sync();
+  for (int i = tid; i < n; i += kThreads) {
+    if (!(ss.cand_val[i] >= theta)) continue;
+    const uint32_t slot = atomicAdd(&ss.fin_n, 1u);
+    if (slot < uint32_t(kFinalMax)) {
+      ss.f_id[slot] = ss.cand_id[i];
+      ss.f_val[slot] = ss.cand_val[i];
+    }
+  }
+  cta_sync();
+  if (ss.fin_n > uint32_t(kFinalMax)) return false;
+  const int m = int(ss.fin_n);
+
+  // Membership of the kept set S, one remaining candidate per thread.
+  const bool have = tid < m;
+  const float z = have ? ss.f_val[tid] : -INFINITY;
+  const uint32_t id = have ? ss.f_id[tid] : 0xFFFFFFFFu;
+  bool keep = have;
+  if (topk) {
+    // Every value above the k-th largest, then the lowest ids among those equal to it.
+    const int above = cta_sync_count(have && z > kth);
+    if (have && z == kth) {
+      int tie_rank = 0;
+      for (int j = 0; j < m; ++j) tie_rank += ss.f_val[j] == kth && ss.f_id[j] < id;
+      keep = tie_rank < prm.top_k - above;
+    }
+  }
+  const RowScale rs = make_row_scale(row_max, prm.temperature);
+  if (keep && minp) keep = mass_double(z, rs, sh.table) >= double(prm.min_p);
+  // Masses of S and their total Z_S.
+  const uint64_t e = keep ? mass_fixed(z, rs, sh.table) : 0;
+  if (have) ss.f_mass[tid] = e;
+  const uint64_t ws = warp_sum<uint64_t>(e);
+  if (lane == 0 && ws) atomicAdd(&ss.zsum, (unsigned long long)ws);
+  const int kept = cta_sync_count(keep);
+  const uint64_t z_kept = ss.zsum;
+  // The draw: the kept token (id order) whose cumulative mass interval holds
+  // t = floor(u * Z_S), u = Philox draw 0 of row b.
+  const uint64_t t = uint64_t((u128(uniform53(a.seed, a.offset, uint64_t(b), 0)) * z_kept) >> 53);
+  if (keep && e) {
+    uint64_t before = 0;
+    for (int j = 0; j < m; ++j) before += ss.f_id[j] < id ? ss.f_mass[j] : 0;
+    if (before <= t && t - before < e) {
+      a.out_ids[b] = int32_t(id);
+      if (a.out_probs) a.out_probs[b] = float(double(e) / double(z_kept));
+    }
+  }
+  if (tid == 0 && a.kept) a.kept[b] = kept;
+  if (a.full_probs) {
+    for (int i = tid; i < V; i += kThreads) a.full_probs[size_t(b) * V + i] = 0.0f;
+    cta_sync();
+    if (keep && e) a.full_probs[size_t(b) * V + id] = __fdiv_rn(float(e), float(z_kept));
+  }
+  return true;
+}
+
+// ------------------------------------------------------------------ the kernel
+//
+// One CTA per row (CTA i takes rows i, i + grid, ...).  A candidate-path row
+// streams through two kBufBytes buffers in shared memory, each filled by one
+// TMA bulk copy; thread 0 refills a buffer as soon as the CTA is done with it,
+// running ahead across row boundaries.  The first batches of a CTA's first row
+// are requested before the row's knobs are read.  Each warp takes one
+// kSubBytes part of a batch (kVecPerLane 16-byte vectors per lane).
+//   greedy:  every lane keeps its (max, lowest id) in registers; one CTA-wide
+//            arg-max at the end of the row.
+//   min-p:   candidates are the elements >= running maximum + T ln(min_p)
+//            (lowered by a rounding margin); the running maximum is shared
+//            through an atomicMax on order keys.
+//   top-k:   candidates are the elements >= the k-th largest per-lane
+//            maximum of the first batch, raised to the k-th largest candidate
+//            when the list is compacted.
+// A warp gathers its candidates of a batch in a per-lane bit mask and appends
+// them with one atomic.  Every threshold is a lower bound of the kept set's
+// boundary, so the candidates contain the kept set; the end of the row selects
+// it exactly.  General-path rows, and rows whose candidates overflow, run the
+// exact radix selection of general_row on this CTA over global memory.
+
+// Cursor over the batches of this CTA's candidate-path rows (thread 0 only).
+template <typename T>
+struct BatchCursor {
+  int row;
+  int batch;
+  int nbatch;
+  uint32_t issued;   // copies requested so far
+
+  // Start at this CTA's first row before its knobs are known.
+  __device__ void begin(const SampleArgs& a) {
+    row = blockIdx.x;
+    batch = 0;
+    nbatch = row < a.batch ? row_geom<T>(a, row).nchunks : 0;
+    issued = 0;
+  }
+  // The first row's knobs are known: a general-path row stops after the
+  // batches already requested.
+  __device__ void known(bool fast) {
+    if (!fast) nbatch = batch;
+  }
+  __device__ void settle(const SampleArgs& a) {
+    while (row < a.batch && batch >= nbatch) {
+      row += gridDim.x;
+      batch = 0;
+      nbatch = 0;
+      if (row < a.batch) {
+        const smp_row_params prm = a.params[row];
+        nbatch = row_is_fast(prm, a.vocab) ? row_geom<T>(a, row).nchunks : 0;
+      }
+    }
+  }
+  __device__ void issue(const SampleArgs& a, unsigned char* dst, uint64_t* bar) {
+    settle(a);
+    if (row >= a.batch) return;
+    const RowGeom g = row_geom<T>(a, row);
+    const uintptr_t src = g.a0 + uintptr_t(batch) * kBufBytes;
+    const uint32_t bytes = uint32_t(min(uintptr_t(kBufBytes), g.a1 - src));
+    tma_load(dst, reinterpret_cast<const void*>(src), bytes, bar);
+    ++batch;
+    ++issued;
+  }
+};
+
+// Append the candidates of one warp's batch part: bit j * kPer + q of `mask`
+// marks element q of this lane's vector j (vector lane + 32 j of the part).
+template <typename T>
+__device__ __forceinline__ void push_mask(StreamShared& ss, uint64_t mask, const T* part, uint32_t id0) {
+  constexpr int kPer = VecOps<T>::kPer;
+  const int lane = threadIdx.x & 31;
+  const uint32_t cnt = uint32_t(__popcll(mask));
+  if (!__any_sync(0xFFFFFFFFu, cnt != 0)) return;
+  const uint32_t incl = warp_inclusive_scan<uint32_t>(cnt);
+  const uint32_t total = __shfl_sync(0xFFFFFFFFu, incl, 31);
+  uint32_t base = 0;
+  if (lane == 31) base = atomicAdd(&ss.cand_n, total);
+  base = __shfl_sync(0xFFFFFFFFu, base, 31) + incl - cnt;
+  while (mask) {
+    const int bit = __ffsll(mask) - 1;
+    mask &= mask - 1;
+    const int e = (lane + (bit / kPer) * 32) * kPer + bit % kPer;
+    if (base < uint32_t(kCandMax)) {
+      ss.cand_id[base] = id0 + uint32_t(e);
+      ss.cand_val[base] = Elem<T>::widen(part[e]);
+    }
+    ++base;
+  }
+}
+
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void allow_dependent_launch() { asm volatile("griddepcontrol.launch_dependents;"); }
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads, 2) sample_kernel(SampleArgs a) {
+  extern __shared__ __align__(128) unsigned char ring[];
+  __shared__ RowShared sh;
+  __shared__ StreamShared ss;
+  using V = VecOps<T>;
+  constexpr int kPer = V::kPer;
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  const int B = a.batch;
+  const int Vn = a.vocab;
+  BatchCursor<T> cur;
+  if (tid == 0) {
+    for (int i = 0; i < kBufs; ++i) mbar_init(&ss.full[i], 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  // Inputs may come from the previous kernel on the stream (programmatic launch).
+  grid_dependency_wait();
+  if (tid == 0) {
+    cur.begin(a);
+    for (int i = 0; i < kBufs; ++i) cur.issue(a, ring + size_t(i) * kBufBytes, &ss.full[i]);
+    ss.timeout = 0;
+  }
+  allow_dependent_launch();
+  if (tid < 64) sh.table[tid] = kExp2Table[tid];
+  ClusterBarrier solo;
+  solo.setup(&ss.solo_bar, &ss.solo_ok, cluster_rank(), 1);
+  cta_sync();
+
+  uint32_t consumed = 0;   // batches consumed so far (the buffers' running index)
+  bool alive = true;
+  for (int row = blockIdx.x; row < B && alive; row += gridDim.x) {
+    const smp_row_params prm = a.params[row];
+    const RowGeom geo = row_geom<T>(a, row);
+    const bool first = row == int(blockIdx.x);
+    const bool fast = row_is_fast(prm, Vn);
+    RowCtx<T> sc;
+    sc.sh = &sh;
+    sc.rank = 0;
+    sc.nranks = 1;
+    sc.first = cluster_rank();
+    sc.cb = &solo;
+    sc.mb = 0;
+    sc.alive = true;
+    sc.s = reinterpret_cast<const T*>(geo.r0);
+    sc.n = Vn;
+    sc.lo = 0;
+    if (!fast) {
+      if (first && geo.nchunks > 0) {
+        // Let the speculative copies land and hand their buffers to the next rows.
+        const int spec = min(kBufs, geo.nchunks);
+        if (tid == 0) {
+          cur.known(false);
+          for (int s = 0; s < spec; ++s) {
+            const uint32_t k = consumed + uint32_t(s);
+            if (!wait_full(&ss.full[k % kBufs], (k / kBufs) & 1)) {
+              ss.timeout = 1;
+              break;
+            }
+            cur.issue(a, ring + size_t(k % kBufs) * kBufBytes, &ss.full[k % kBufs]);
+          }
+        }
+        cta_sync();
+        if (ss.timeout) {
+          alive = false;
+          break;
+        }
+        consumed += uint32_t(spec);
+      }
+      general_row<T>(sc, a, row, prm, slice_best<T>(sc.s, Vn, 0));
+      alive = sc.alive;
+      continue;
+    }
+    const bool greedy = row_is_greedy(prm);
+    const bool minp = !greedy && prm.min_p > 0.0f && prm.min_p < 1.0f;
+    const bool topk = !greedy && prm.top_k > 0 && prm.top_k < Vn;
+    if (tid == 0) {
+      ss.cand_n = 0;
+      ss.maxkey = 0;
+    }
+    cta_sync();
+    const uint32_t id_base = uint32_t((geo.a0 - reinterpret_cast<uintptr_t>(geo.r0)) / sizeof(T));
+    float best_z = -INFINITY;      // greedy: this lane's maximum and its lowest id
+    uint32_t best_id = 0xFFFFFFFFu;
+    float tau = -INFINITY;         // top-k: lower bound of the k-th largest, the same in every thread
+    const float mp_w = minp ? prm.temperature * logf(prm.min_p) : 0.0f;
+    auto threshold = [&](float run_max) {
+      float theta = -INFINITY;
+      if (minp) theta = run_max + mp_w - (fabsf(run_max) + fabsf(mp_w)) * 0x1p-20f - 0x1p-126f;
+      if (topk) theta = fmaxf(theta, tau);
+      return theta;
+    };
+
+    for (int bt = 0; bt < geo.nchunks; ++bt) {
+      const uint32_t bi = consumed % kBufs;
+      if (!wait_full(&ss.full[bi], (consumed / kBufs) & 1)) ss.timeout = 1;
+      // This warp's part of the batch.
+      const uintptr_t bstart = geo.a0 + uintptr_t(bt) * kBufBytes;
+      const int bvec = int(min(uintptr_t(kBufBytes), geo.a1 - bstart) / 16);
+      const int v0 = warp * (kSubBytes / 16);
+      const int nvec = max(0, min(bvec - v0, kSubBytes / 16));
+      const uint4* vec = reinterpret_cast<const uint4*>(ring + size_t(bi) * kBufBytes) + v0;
+      const T* part = reinterpret_cast<const T*>(vec);
+      const uint32_t id0 = id_base + uint32_t(bt) * (kBufBytes / sizeof(T)) + uint32_t(v0 * kPer);
+      float vmf[kVecPerLane];
+#pragma unroll
+      for (int j = 0; j < kVecPerLane; ++j) {
+        const int v = lane + j * 32;
+        vmf[j] = V::finish(v < nvec ? V::vmax(vec[v]) : V::neg_inf());
+      }
+      if (greedy) {
+#pragma unroll
+        for (int j = 0; j < kVecPerLane; ++j) {
+          if (vmf[j] > best_z) {
+            const int e0 = (lane + j * 32) * kPer;
+#pragma unroll
+            for (int q = 0; q < kPer; ++q) {
+              const float z = Elem<T>::widen(part[e0 + q]);
+              if (z > best_z) {
+                best_z = z;
+                best_id = id0 + uint32_t(e0 + q);
+              }
+            }
+          }
+        }
+      } else {
+        float lane_max = vmf[0];
+#pragma unroll
+        for (int j = 1; j < kVecPerLane; ++j) lane_max = fmaxf(lane_max, vmf[j]);
+        const uint32_t lane_key = lane_max > -INFINITY ? key_of_bits(__float_as_uint(lane_max)) : 0u;
+        const uint32_t wkey = __reduce_max_sync(0xFFFFFFFFu, lane_key);
+        float theta;
+        if (bt == 0) {
+          // The first batch sets the scale: the CTA-wide maximum.
+          if (lane == 0 && wkey) atomicMax(&ss.maxkey, wkey);
+          if (topk) tau = kth_largest<T>(lane_max, prm.top_k);
+          else cta_sync();
+          theta = threshold(value_of_key(ss.maxkey));
+        } else {
+          // Any value of the shared running maximum is a valid lower bound.
+          const uint32_t shared_key = *reinterpret_cast<volatile uint32_t*>(&ss.maxkey);
+          theta = threshold(value_of_key(lane_key > shared_key ? lane_key : shared_key));
+        }
+        uint64_t mask = 0;
+#pragma unroll
+        for (int j = 0; j < kVecPerLane; ++j) {
+          if (vmf[j] >= theta) {
+            const int e0 = (lane + j * 32) * kPer;
+#pragma unroll
+            for (int q = 0; q < kPer; ++q)
+              if (Elem<T>::widen(part[e0 + q]) >= theta) mask |= 1ull << (j * kPer + q);
+          }
+        }
+        push_mask<T>(ss, mask, part, id0);
+        if (bt > 0 && lane == 0 && wkey) atomicMax(&ss.maxkey, wkey);
+      }
+      cta_sync();   // the buffer is free
+      ++consumed;
+      if (ss.timeout) {
+        alive = false;
+        break;
+      }
+      if (tid == 0) cur.issue(a, ring + size_t(bi) * kBufBytes, &ss.full[bi]);
+      if (topk && ss.cand_n > uint32_t(kCompactAt) && ss.cand_n <= uint32_t(kCandMax)) {
+        tau = fmaxf(tau, kth_largest_list<T>(ss.cand_val, int(ss.cand_n), prm.top_k, ss.hist, ss.bc));
+        compact_candidates(ss, tau);
+      }
+    }
+    if (!alive) break;
+
+    if (greedy) {
+      // Elements outside the aligned middle; then the CTA-wide (max, lowest id).
+      uint64_t best = pack_key_id(key_of_bits(__float_as_uint(best_z)), best_id);
+      for (int i = tid; i < geo.head; i += kThreads) {
+        const uint64_t p = pack_key_id(key_of_bits(__float_as_uint(Elem<T>::widen(sc.s[i]))), uint32_t(i));
+        best = p > best ? p : best;
+      }
+      for (int i = geo.tail0 + tid; i < Vn; i += kThreads) {
+        const uint64_t p = pack_key_id(key_of_bits(__float_as_uint(Elem<T>::widen(sc.s[i]))), uint32_t(i));
+        best = p > best ? p : best;
+      }
+      best = block_max_u64(best, ss.red64);
+      const float row_max = value_of_key(uint32_t(best >> 32));
+      const uint32_t tok = ~uint32_t(best);
+      if (!isfinite(row_max)) {
+        if (tid == 0) write_error_row(a, row, kRowNonFinite);
+        if (a.full_probs)
+          for (int i = tid; i < Vn; i += kThreads) a.full_probs[size_t(row) * Vn + i] = __int_as_float(0x7FC00000);
+      } else {
+        if (tid == 0) {
+          a.out_ids[row] = int32_t(tok);
+          if (a.out_probs) a.out_probs[row] = 1.0f;
+          if (a.kept) a.kept[row] = 1;
+        }
+        if (a.full_probs)
+          for (int i = tid; i < Vn; i += kThreads)
+            a.full_probs[size_t(row) * Vn + i] = uint32_t(i) == tok ? 1.0f : 0.0f;
+      }
+      cta_sync();
+      continue;
+    }
+
+    float run_max = value_of_key(ss.maxkey);
+    if (geo.head > 0 || geo.tail0 < Vn) {
+      // Elements outside the aligned middle join the candidates directly.
+      float emax = -INFINITY;
+      for (int i = tid; i < geo.head; i += kThreads) emax = fmaxf(emax, Elem<T>::widen(sc.s[i]));
+      for (int i = geo.tail0 + tid; i < Vn; i += kThreads) emax = fmaxf(emax, Elem<T>::widen(sc.s[i]));
+      run_max = fmaxf(run_max, block_max_f(emax, ss.red));
+      const float theta = threshold(run_max);
+      for (int i = tid; i < geo.head; i += kThreads) {
+        const float z = Elem<T>::widen(sc.s[i]);
+        if (z >= theta) push_candidate(ss, uint32_t(i), z);
+      }
+      for (int i = geo.tail0 + tid; i < Vn; i += kThreads) {
+        const float z = Elem<T>::widen(sc.s[i]);
+        if (z >= theta) push_candidate(ss, uint32_t(i), z);
+      }
+      cta_sync();
+    }
+    if (!finalize_candidates<T>(ss, sh, a, row, prm, run_max)) {
+      cta_sync();
+      general_row<T>(sc, a, row, prm, slice_best<T>(sc.s, Vn, 0));
+      alive = sc.alive;
+    }
+    cta_sync();
+  }
+  if (!alive) {
+    // A wait ran out of time: report it and let the copies in flight land.
+    if (tid == 0) {
+      if (a.status) atomicOr(a.status, kRowTimeout);
+      for (uint32_t k = consumed; k < cur.issued; ++k) wait_full(&ss.full[k % kBufs], (k / kBufs) & 1);
+    }
+    cta_sync();
+  }
 }
 
 // ------------------------------------------------------------------ host side
 
-// Shape of the launch for a row of `vocab` elements of `elem` bytes.
-static LaunchShape sample_shape(int batch, int vocab, int elem, int num_sms) {
-  LaunchShape ls;
-  int cluster = 1;
-  auto slice_of = [&](int cl) { return ((vocab + cl - 1) / cl + 15) / 16 * 16; };
-  while (cluster < kMaxCluster && size_t(slice_of(cluster)) * elem > kSliceTargetBytes) cluster *= 2;
-  while (cluster < kMaxCluster && int64_t(batch) * cluster < 2 * num_sms &&
-         size_t(slice_of(cluster * 2)) * elem >= kSliceMinBytes)
-    cluster *= 2;
-  if (forced_cluster()) cluster = forced_cluster();
-  ls.cluster = cluster;
-  ls.slice = slice_of(cluster);
-  ls.smem = size_t(ls.slice) * elem + 32;
-  return ls;
-}
-
 template <typename T>
-static smp_status launch_sample(const SampleArgs& args, int elem, cudaStream_t stream) {
+static smp_status launch_sample(const SampleArgs& args, cudaStream_t stream) {
   const int dev = current_device();
   if (dev < 0) return fail_cuda(cudaGetLastError());
-  const LaunchShape ls = sample_shape(args.batch, args.vocab, elem, device_sms(dev));
-  if (ls.smem > kMaxDynamicSmem) return SMP_ERR_UNSUPPORTED;
-  SampleArgs a = args;
-  a.slice = ls.slice;
-  cudaError_t err = prepare_kernel(reinterpret_cast<const void*>(&sample_kernel<T>), dev, ls);
+  LaunchShape ls;
+  ls.cluster = 1;
+  ls.smem = size_t(kBufs) * kBufBytes;
+  ls.pdl = true;
+  const void* kernel = reinterpret_cast<const void*>(&sample_kernel<T>);
+  cudaError_t err = prepare_kernel(kernel, dev, ls);
   if (err != cudaSuccess) return fail_cuda(err);
-  err = launch_cluster(reinterpret_cast<const void*>(&sample_kernel<T>), dim3(args.batch * ls.cluster),
-                       dim3(kThreads), ls, stream, &a);
+  int per_sm = 0;
+  err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, ls.smem);
+  if (err != cudaSuccess) return fail_cuda(err);
+  if (per_sm <= 0) return SMP_ERR_UNSUPPORTED;
+  const int resident = per_sm * device_sms(dev);
+  const int grid = args.batch < resident ? args.batch : resident;
+  if (verbose())
+    fprintf(stderr, "smp_sample: batch %d vocab %d grid %d (%d CTAs/SM) ring %zu bytes\n", args.batch,
+            args.vocab, grid, per_sm, ls.smem);
+  SampleArgs a = args;
+  err = launch_cluster(kernel, dim3(grid), dim3(kThreads), ls, stream, &a);
   if (err != cudaSuccess) return fail_cuda(err);
   return SMP_OK;
 }
@@ -327,8 +1018,8 @@ static smp_status sample_common(const void* logits, int32_t batch, int32_t vocab
   a.status = status;
   a.full_probs = full;
   a.kept = kept;
-  if (dtype == SMP_F32) return launch_sample<float>(a, 4, st);
-  return launch_sample<uint16_t>(a, 2, st);
+  if (dtype == SMP_F32) return launch_sample<float>(a, st);
+  return launch_sample<uint16_t>(a, st);
 }
 
 }  // namespace smp

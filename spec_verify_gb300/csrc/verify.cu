@@ -66,13 +66,16 @@ __global__ void __launch_bounds__(kThreads, 1) verify_pos_kernel(VerifyArgs a) {
   const int V = a.vocab;
   if (threadIdx.x < 64) sh.table[threadIdx.x] = kExp2Table[threadIdx.x];
 
+  ClusterBarrier cbar;
   RowCtx<T> c;
   c.sh = &sh;
   c.rank = rank;
   c.nranks = nranks;
+  c.first = 0;
   c.mb = 0;
   c.alive = true;
-  c.cb.init(&sh.mbar, &sh.ok, nranks);
+  cbar.init(&sh.mbar, &sh.ok, nranks);
+  c.cb = &cbar;
 
   const T* row = logit_row<T>(a, b, j);
   const int lo = int(rank) * a.slice;
@@ -128,13 +131,16 @@ __global__ void __launch_bounds__(kThreads, 1) verify_resolve_kernel(VerifyArgs 
   const PosStat* st = a.ws + size_t(b) * rows_per_b;
   if (threadIdx.x < 64) sh.table[threadIdx.x] = kExp2Table[threadIdx.x];
 
+  ClusterBarrier cbar;
   RowCtx<T> c;
   c.sh = &sh;
   c.rank = rank;
   c.nranks = nranks;
+  c.first = 0;
   c.mb = 0;
   c.alive = true;
-  c.cb.init(&sh.mbar, &sh.ok, nranks);
+  cbar.init(&sh.mbar, &sh.ok, nranks);
+  c.cb = &cbar;
 
   // Accept tests of eq. 39.3 in position order: u_i < p_i(x) / max(q_i(x), 1e-300).
   if (threadIdx.x == 0) {

@@ -15,6 +15,22 @@ namespace smp {
 
 static thread_local int g_last_cuda_error = 0;
 
+__global__ void clear_status_kernel(int32_t* status) {
+  asm volatile("griddepcontrol.launch_dependents;");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (threadIdx.x == 0) *status = 0;
+}
+
+smp_status clear_status(int32_t* status, cudaStream_t stream) {
+  LaunchShape ls;
+  ls.pdl = true;
+  int32_t* arg = status;
+  const cudaError_t err =
+      launch_cluster(reinterpret_cast<const void*>(&clear_status_kernel), dim3(1), dim3(32), ls, stream, &arg);
+  if (err != cudaSuccess) return fail_cuda(err);
+  return SMP_OK;
+}
+
 smp_status fail_cuda(cudaError_t err) {
   g_last_cuda_error = int(err);
   return SMP_ERR_CUDA;

@@ -247,6 +247,12 @@ __device__ __forceinline__ double mass_double(float z, const RowScale& rs, const
 
 // Barrier over the kThreads threads that work on rows (named barrier 1).  A
 // kernel may run an extra producer warp that takes no part in it.
+// Programmatic dependent launch: wait until the previous kernel on the stream
+// has finished and its writes are visible (a no-op for a normal launch), and
+// let the next kernel on the stream be scheduled early (it waits in turn).
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void allow_dependent_launch() { asm volatile("griddepcontrol.launch_dependents;"); }
+
 __device__ __forceinline__ void cta_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory"); }
 
 // cta_sync() that also returns how many of the kThreads threads passed `pred`.

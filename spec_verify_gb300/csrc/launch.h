@@ -27,6 +27,13 @@ struct LaunchShape {
 // Records `err` as the last CUDA error of this thread and returns SMP_ERR_CUDA.
 smp_status fail_cuda(cudaError_t err);
 
+// Clears the device status word with a one-CTA kernel launched as a
+// programmatic dependent of the previous kernel on `stream`: it lets the next
+// kernel be scheduled at once and waits for the previous one before the store.
+// Kernels launched after it with LaunchShape::pdl must call
+// grid_dependency_wait() before they touch memory.
+smp_status clear_status(int32_t* status, cudaStream_t stream);
+
 // Current device, or -1 if it cannot be queried.
 int current_device();
 

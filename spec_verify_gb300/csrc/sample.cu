@@ -721,9 +721,6 @@ __device__ __forceinline__ void push_mask(StreamShared& ss, uint64_t mask, const
   }
 }
 
-__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ void allow_dependent_launch() { asm volatile("griddepcontrol.launch_dependents;"); }
-
 template <typename T>
 __global__ void __launch_bounds__(kThreads, 2) sample_kernel(SampleArgs a) {
   extern __shared__ __align__(128) unsigned char ring[];
@@ -1003,8 +1000,8 @@ static smp_status sample_common(const void* logits, int32_t batch, int32_t vocab
     return SMP_ERR_INVALID_ARG;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (status) {
-    const cudaError_t err = cudaMemsetAsync(status, 0, sizeof(int32_t), st);
-    if (err != cudaSuccess) return fail_cuda(err);
+    const smp_status rc = clear_status(status, st);
+    if (rc != SMP_OK) return rc;
   }
   SampleArgs a{};
   a.logits = logits;

@@ -64,6 +64,8 @@ __global__ void __launch_bounds__(kThreads, 1) verify_pos_kernel(VerifyArgs a) {
   const int b = pr / rows_per_b;
   const int j = pr % rows_per_b;
   const int V = a.vocab;
+  grid_dependency_wait();
+  allow_dependent_launch();
   if (threadIdx.x < 64) sh.table[threadIdx.x] = kExp2Table[threadIdx.x];
 
   ClusterBarrier cbar;
@@ -129,6 +131,8 @@ __global__ void __launch_bounds__(kThreads, 1) verify_resolve_kernel(VerifyArgs 
   const int V = a.vocab;
   const int rows_per_b = 2 * K + 1;
   const PosStat* st = a.ws + size_t(b) * rows_per_b;
+  grid_dependency_wait();   // the position statistics come from verify_pos_kernel
+  allow_dependent_launch();
   if (threadIdx.x < 64) sh.table[threadIdx.x] = kExp2Table[threadIdx.x];
 
   ClusterBarrier cbar;
@@ -254,6 +258,7 @@ static LaunchShape verify_shape(int rows, int vocab, int elem, int num_sms, int 
   ls.slice = slice_of(cluster);
   const size_t one = (size_t(ls.slice) * elem + 32 + 15) & ~size_t(15);
   ls.smem = one * buffers;
+  ls.pdl = true;
   return ls;
 }
 
@@ -310,8 +315,8 @@ extern "C" smp_status smp_spec_verify(const void* p_logits, const void* q_logits
     return SMP_ERR_WORKSPACE;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (status) {
-    const cudaError_t err = cudaMemsetAsync(status, 0, sizeof(int32_t), st);
-    if (err != cudaSuccess) return fail_cuda(err);
+    const smp_status rc = clear_status(status, st);
+    if (rc != SMP_OK) return rc;
   }
   VerifyArgs a{};
   a.p = p_logits;

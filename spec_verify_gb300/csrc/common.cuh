@@ -212,9 +212,8 @@ __device__ __forceinline__ ExpParts exp_parts(float z, const RowScale& rs, const
 // 2^s as a float for s in [-126, 127].
 __device__ __forceinline__ float pow2f(int s) { return __int_as_float((s + 127) << 23); }
 
-// The fixed-point mass E = round(exp((z - m) / T) * 2^F).
-__device__ __forceinline__ uint64_t mass_fixed(float z, const RowScale& rs, const FloatPair* table) {
-  const ExpParts e = exp_parts(z, rs, table, -float(kFixedBits + 3));
+// The fixed-point mass E = round(e * 2^F) of an exponential in parts.
+__device__ __forceinline__ uint64_t fixed_from_parts(const ExpParts& e) {
   if (e.kind == 1) return kFixedOne;
   if (e.kind == 2) return 0;
   const int s = kFixedBits + e.n;           // E = (hi + lo) * 2^s
@@ -235,12 +234,21 @@ __device__ __forceinline__ uint64_t mass_fixed(float z, const RowScale& rs, cons
   return v <= 0.0f ? 0ull : uint64_t(v);
 }
 
-// exp((z - m) / T) as a double (head + tail, scaled); 0 below 2^-1000.
-__device__ __forceinline__ double mass_double(float z, const RowScale& rs, const FloatPair* table) {
-  const ExpParts e = exp_parts(z, rs, table, -1000.0f);
+// An exponential in parts as a double (head + tail, scaled).
+__device__ __forceinline__ double double_from_parts(const ExpParts& e) {
   if (e.kind == 1) return 1.0;
   if (e.kind == 2) return 0.0;
   return ldexp(double(e.hi) + double(e.lo), e.n);
+}
+
+// The fixed-point mass E = round(exp((z - m) / T) * 2^F).
+__device__ __forceinline__ uint64_t mass_fixed(float z, const RowScale& rs, const FloatPair* table) {
+  return fixed_from_parts(exp_parts(z, rs, table, -float(kFixedBits + 3)));
+}
+
+// exp((z - m) / T) as a double (head + tail, scaled); 0 below 2^-1000.
+__device__ __forceinline__ double mass_double(float z, const RowScale& rs, const FloatPair* table) {
+  return double_from_parts(exp_parts(z, rs, table, -1000.0f));
 }
 
 // ------------------------------------------------------------------ warp / block helpers
@@ -366,6 +374,29 @@ __device__ __forceinline__ U block_sum(U v, U* scratch) {
 }
 
 // Largest key, lowest id among equal keys, packed as (key << 32) | ~id.
+// Warp-aggregated shared-memory updates.  Every lane of the warp must call
+// these together; many lanes hitting one address would otherwise serialise.
+
+// hist[digit] += 1 for every lane with `valid`: one atomic per distinct digit.
+__device__ __forceinline__ void warp_hist_add(uint32_t* hist, uint32_t digit, bool valid) {
+  const uint32_t peers = __match_any_sync(0xFFFFFFFFu, valid ? digit : 0xFFFFFFFFu);
+  const int lane = threadIdx.x & 31;
+  if (valid && lane == __ffs(peers) - 1) atomicAdd(&hist[digit], uint32_t(__popc(peers)));
+}
+
+// Reserves one slot of a list counted by *counter for every lane with
+// `take`; returns the lane's slot (undefined for the others).
+__device__ __forceinline__ uint32_t warp_append(uint32_t* counter, bool take) {
+  const uint32_t m = __ballot_sync(0xFFFFFFFFu, take);
+  if (m == 0) return 0;
+  const int lane = threadIdx.x & 31;
+  const int leader = __ffs(m) - 1;
+  uint32_t base = 0;
+  if (lane == leader) base = atomicAdd(counter, uint32_t(__popc(m)));
+  base = __shfl_sync(0xFFFFFFFFu, base, leader);
+  return base + uint32_t(__popc(m & ((1u << lane) - 1u)));
+}
+
 __device__ __forceinline__ uint64_t pack_key_id(uint32_t key, uint32_t id) {
   return (uint64_t(key) << 32) | uint64_t(~id);
 }

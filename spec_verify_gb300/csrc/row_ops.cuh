@@ -62,12 +62,12 @@ struct RowShared {
   uint32_t red32[kWarps];
   uint64_t bcast64[8];
   uint32_t bcast32[8];
-  FloatPair table[64];
 };
 
 template <typename T>
 struct RowCtx {
   RowShared* sh;
+  const FloatPair* table;   // 2^(j/64) table of the exponential, in shared memory
   const T* s;          // slice: element i has global id lo + i
   int n;               // elements in this CTA's slice (may be 0)
   int lo;              // global id of element 0
@@ -299,7 +299,7 @@ __device__ Boundary radix_select(RowCtx<T>& c, uint32_t k, const MassTarget& tar
       const uint32_t d = (key >> shift) & 255u;
       atomicAdd(&sh->hist_cnt[d], 1u);
       if (kMass) {
-        const uint64_t e = mass_fixed(Elem<T>::widen(c.s[i]), rs, sh->table);
+        const uint64_t e = mass_fixed(Elem<T>::widen(c.s[i]), rs, c.table);
         if (e) atomicAdd(reinterpret_cast<unsigned long long*>(&sh->hist_mass[d]), (unsigned long long)e);
       }
     }

@@ -32,9 +32,9 @@ constexpr int kBufBytes = 32768;                       // one TMA copy: a batch 
 constexpr int kBufs = 2;                               // batches in flight per CTA (double buffering)
 constexpr int kSubBytes = kBufBytes / kWarps;          // the part of a batch one warp processes
 constexpr int kVecPerLane = kSubBytes / 16 / 32;       // 16-byte vectors per lane and batch
-constexpr int kCandMax = 2048;    // candidate list capacity per row
-constexpr int kCompactAt = 1024;  // top-k: shrink the candidate list when it grows past this
+constexpr int kCandMax = 1024;    // candidate list capacity per row
 constexpr int kFinalMax = kThreads;   // candidates at or above the final threshold (one per thread)
+constexpr int kSegs = 8;          // segment maxima kept per lane and row (min-p / top-k rows)
 constexpr int kFastTopK = 128;    // top-k rows up to this k take the candidate path
 
 struct SampleArgs {
@@ -85,15 +85,24 @@ __device__ __forceinline__ float minp_lower_bound(float m, float temperature, fl
 
 // ------------------------------------------------------------------ slices and TMA
 
-__device__ __forceinline__ void tma_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+// L2 policy for data read once: evicted before anything else, so that a row
+// streaming through L2 does not push out the kernel's code and small inputs.
+__device__ __forceinline__ uint64_t evict_first_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ void tma_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                         uint64_t policy) {
   asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
                "r"(bytes)
                : "memory");
   if (bytes)
     asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            smem_addr(dst)),
-        "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], "
+        "%4;" ::"r"(smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
         : "memory");
 }
 
@@ -135,6 +144,11 @@ struct VecOps<uint16_t> {
   static __device__ __forceinline__ float finish(uint32_t m) {
     return fmaxf(__uint_as_float(m & 0xFFFF0000u), __uint_as_float(m << 16));
   }
+  // element q (0..7, a compile-time constant once unrolled) of x
+  static __device__ __forceinline__ float elem(const uint4& x, int q) {
+    const uint32_t w = q < 2 ? x.x : q < 4 ? x.y : q < 6 ? x.z : x.w;
+    return __uint_as_float((q & 1) ? (w & 0xFFFF0000u) : (w << 16));
+  }
 };
 
 template <>
@@ -149,6 +163,9 @@ struct VecOps<float> {
                                  fmaxf(__uint_as_float(x.z), __uint_as_float(x.w))));
   }
   static __device__ __forceinline__ float finish(uint32_t m) { return __uint_as_float(m); }
+  static __device__ __forceinline__ float elem(const uint4& x, int q) {
+    return __uint_as_float(q == 0 ? x.x : q == 1 ? x.y : q == 2 ? x.z : x.w);
+  }
 };
 
 __device__ __forceinline__ float block_max_f(float v, float* scratch) {
@@ -162,20 +179,6 @@ __device__ __forceinline__ float block_max_f(float v, float* scratch) {
 #pragma unroll
   for (int w = 1; w < kWarps; ++w) r = fmaxf(r, scratch[w]);
   return r;
-}
-
-// The k-th largest (1 <= k <= kThreads) of one float per thread, as a value v
-// with at least k of the inputs >= v.  Bit-wise search over the order keys.
-template <typename T>
-__device__ __forceinline__ float kth_largest(float x, int k) {
-  const uint32_t key = key_of_bits(__float_as_uint(x));
-  uint32_t t = 0;
-  const int low = KeyTraits<T>::kBits == 16 ? 16 : 0;   // bf16 keys carry no information below bit 16
-  for (int bit = 31; bit >= low; --bit) {
-    const uint32_t cand = t | (1u << bit);
-    if (cta_sync_count(key >= cand) >= k) t = cand;
-  }
-  return value_of_key(t);
 }
 
 // Largest packed (key, ~id) of a slice (shared or global memory).
@@ -195,7 +198,7 @@ __device__ uint64_t slice_best(const T* s, int n, int lo) {
 // expressed on logits.  Warp 0 probes 32 keys per step, starting around the
 // estimate m + T ln(min_p); every thread gets the result.
 template <typename T>
-__device__ uint32_t minp_threshold_key(RowShared* sh, const RowScale& rs, float temperature,
+__device__ uint32_t minp_threshold_key(RowShared* sh, const FloatPair* table, const RowScale& rs, float temperature,
                                        float min_p, uint32_t key_max) {
   if (threadIdx.x < 32) {
     const int lane = threadIdx.x;
@@ -210,7 +213,7 @@ __device__ uint32_t minp_threshold_key(RowShared* sh, const RowScale& rs, float 
     for (int iter = 0; iter < 64 && lo < hi; ++iter) {
       const uint64_t cand64 = uint64_t(start) + uint64_t(lane) * stride;
       const uint32_t cand = cand64 > hi ? hi : uint32_t(cand64);
-      const bool ok = mass_double(key_value<T>(cand), rs, sh->table) >= thr;
+      const bool ok = mass_double(key_value<T>(cand), rs, table) >= thr;
       const uint32_t mask = __ballot_sync(0xFFFFFFFFu, ok);
       const uint32_t last = __shfl_sync(0xFFFFFFFFu, cand, 31);
       if (mask == 0) {
@@ -284,7 +287,7 @@ __device__ void general_row(RowCtx<T>& c, const SampleArgs& a, int b, const smp_
     const bool topp = prm.top_p < 1.0f;
     const bool minp = prm.min_p > 0.0f && prm.min_p < 1.0f;
     uint32_t key_min_p = 0;
-    if (minp) key_min_p = minp_threshold_key<T>(&sh, rs, prm.temperature, prm.min_p, key_max);
+    if (minp) key_min_p = minp_threshold_key<T>(&sh, c.table, rs, prm.temperature, prm.min_p, key_max);
 
     // Row statistics: size of the min-p set and the total mass Z.
     uint64_t stats[4] = {0, 0, 0, 0};
@@ -293,7 +296,7 @@ __device__ void general_row(RowCtx<T>& c, const SampleArgs& a, int b, const smp_
       for (int i = threadIdx.x; i < n; i += kThreads) {
         const T v = s[i];
         if (minp && elem_key<T>(v) >= key_min_p) ++cnt;
-        if (topp) z += mass_fixed(Elem<T>::widen(v), rs, sh.table);
+        if (topp) z += mass_fixed(Elem<T>::widen(v), rs, c.table);
       }
       stats[0] = cnt;
       stats[1] = z;
@@ -340,7 +343,7 @@ __device__ void general_row(RowCtx<T>& c, const SampleArgs& a, int b, const smp_
       return key > bd.key || (key == bd.key && uint32_t(lo + i) <= id_cut);
     };
     auto weight = [&](int i) -> uint64_t {
-      return kept(i) ? mass_fixed(Elem<T>::widen(s[i]), rs, sh.table) : 0ull;
+      return kept(i) ? mass_fixed(Elem<T>::widen(s[i]), rs, c.table) : 0ull;
     };
 
     // Kept mass Z_S of this CTA, of the row, and the prefix over CTAs.
@@ -397,16 +400,31 @@ struct StreamShared {
   uint32_t fin_n;             // candidates at or above the final threshold
   uint32_t maxkey;            // running row maximum as an order key
   unsigned long long zsum;    // Z_S in fixed point
+  uint64_t u53;               // the row's uniform (53-bit integer) for the draw
+  float c_hi, c_lo;           // log2(e) / T of the row, head and tail
+  uint32_t qn;                // segments to read again
   float red[kWarps];
   uint32_t redu[kWarps];
   uint64_t red64[kWarps];
   uint32_t bc[2];
+};
+
+// Candidate lists of a candidate-path row.  They are never live while the
+// general path works on a row, so the two share their storage.
+struct CandShared {
+  float seg[kSegs][kThreads];   // per-lane segment maxima of the row being streamed
+  uint32_t q[kThreads];         // segments to read again: lane | segment << 8
   uint32_t hist[256];
   uint32_t cand_id[kCandMax];
   float cand_val[kCandMax];
   uint32_t f_id[kFinalMax];
   float f_val[kFinalMax];
   uint64_t f_mass[kFinalMax];   // E_i of the kept candidates, 0 for the others
+};
+
+union RowScratch {
+  RowShared row;
+  CandShared cand;
 };
 
 // Byte layout of a row: the 16-byte aligned middle [a0, a1) streams through
@@ -505,47 +523,20 @@ __device__ float kth_largest_list(const float* vals, int n, int k, uint32_t* his
   return value_of_key(kLevels == 2 ? (prefix << 16) | ((prefix & 0x8000u) ? 0u : 0xFFFFu) : prefix);
 }
 
-// Keep only candidates >= theta (order changes).
-__device__ void compact_candidates(StreamShared& ss, float theta) {
-  const int n = min(int(ss.cand_n), kCandMax);
-  uint32_t id[kCandMax / kThreads];
-  float val[kCandMax / kThreads];
-#pragma unroll
-  for (int j = 0; j < kCandMax / kThreads; ++j) {
-    const int i = threadIdx.x + j * kThreads;
-    id[j] = i < n ? ss.cand_id[i] : 0u;
-    val[j] = i < n ? ss.cand_val[i] : -INFINITY;
-  }
-  cta_sync();
-  if (threadIdx.x == 0) ss.cand_n = 0;
-  cta_sync();
-#pragma unroll
-  for (int j = 0; j < kCandMax / kThreads; ++j) {
-    const int i = threadIdx.x + j * kThreads;
-    if (i < n && val[j] >= theta) {
-      const uint32_t slot = atomicAdd(&ss.cand_n, 1u);
-      ss.cand_id[slot] = id[j];
-      ss.cand_val[slot] = val[j];
-    }
-  }
-  cta_sync();
-}
-
-__device__ __forceinline__ void push_candidate(StreamShared& ss, uint32_t id, float z) {
+__device__ __forceinline__ void push_candidate(StreamShared& ss, CandShared& cs, uint32_t id, float z) {
   const uint32_t slot = atomicAdd(&ss.cand_n, 1u);
   if (slot < uint32_t(kCandMax)) {
-    ss.cand_id[slot] = id;
-    ss.cand_val[slot] = z;
+    cs.cand_id[slot] = id;
+    cs.cand_val[slot] = z;
   }
 }
 
 // Exact selection and draw of a min-p / top-k candidate-path row.  The
-// candidates hold every element at or above the collection thresholds, which
-// are lower bounds of the kept set's boundary; row_max is the row's largest
-// logit.  Returns false if the row needs the general path (too many
-// candidates).
+// candidates hold every element at or above a lower bound of the kept set's
+// boundary; row_max is the row's largest logit.  Returns false if the row
+// needs the general path.
 template <typename T>
-__device__ bool finalize_candidates(StreamShared& ss, RowShared& sh, const SampleArgs& a, int b,
+__device__ bool finalize_candidates(StreamShared& ss, CandShared& cs, const FloatPair* table, const SampleArgs& a, int b,
                                     const smp_row_params& prm, float row_max) {
   const int tid = threadIdx.x, lane = tid & 31;
   const int V = a.vocab;
@@ -558,68 +549,73 @@ __device__ bool finalize_candidates(StreamShared& ss, RowShared& sh, const Sampl
     return true;
   }
   if (ss.cand_n > uint32_t(kCandMax)) return false;
-  const int n = int(ss.cand_n);
-
-  // The kept set lies at or above theta: min-p's lower bound at the row
-  // maximum and the k-th largest value (the candidates hold every element at
-  // or above it, so their k-th largest is the row's).
-  float theta = -INFINITY;
-  if (minp) theta = minp_lower_bound(row_max, prm.temperature, prm.min_p);
-  float kth = -INFINITY;
-  if (topk) {
-    if (n < prm.top_k) return false;
-    kth = kth_largest_list<T>(ss.cand_val, n, prm.top_k, ss.hist, ss.bc);
-    theta = fmaxf(theta, kth);
-  }
-  if (tid == 0) {
-    ss.fin_n = 0;
-    ss.zsum = 0;
-  }
-  cta_sync();
-  for (int i = tid; i < n; i += kThreads) {
-    if (!(ss.cand_val[i] >= theta)) continue;
-    const uint32_t slot = atomicAdd(&ss.fin_n, 1u);
-    if (slot < uint32_t(kFinalMax)) {
-      ss.f_id[slot] = ss.cand_id[i];
-      ss.f_val[slot] = ss.cand_val[i];
+  int n = int(ss.cand_n);
+  const float* vals = cs.cand_val;
+  const uint32_t* ids = cs.cand_id;
+  if (n > kFinalMax) {
+    // Too many to rank one per thread: keep those at or above the k-th largest value.
+    if (!topk || n < prm.top_k) return false;
+    float theta = kth_largest_list<T>(cs.cand_val, n, prm.top_k, cs.hist, ss.bc);
+    if (minp) theta = fmaxf(theta, minp_lower_bound(row_max, prm.temperature, prm.min_p));
+    if (tid == 0) ss.fin_n = 0;
+    cta_sync();
+    for (int i = tid; i < n; i += kThreads) {
+      if (!(cs.cand_val[i] >= theta)) continue;
+      const uint32_t slot = atomicAdd(&ss.fin_n, 1u);
+      if (slot < uint32_t(kFinalMax)) {
+        cs.f_id[slot] = cs.cand_id[i];
+        cs.f_val[slot] = cs.cand_val[i];
+      }
     }
+    cta_sync();
+    if (ss.fin_n > uint32_t(kFinalMax)) return false;
+    n = int(ss.fin_n);
+    vals = cs.f_val;
+    ids = cs.f_id;
   }
-  cta_sync();
-  if (ss.fin_n > uint32_t(kFinalMax)) return false;
-  const int m = int(ss.fin_n);
+  // Fewer candidates than k: some of the top k are NaN (ranked as -inf).
+  if (topk && n < prm.top_k) return false;
 
-  // Membership of the kept set S, one remaining candidate per thread.
-  const bool have = tid < m;
-  const float z = have ? ss.f_val[tid] : -INFINITY;
-  const uint32_t id = have ? ss.f_id[tid] : 0xFFFFFFFFu;
+  // Membership of the kept set S, one candidate per thread.
+  const bool have = tid < n;
+  const float z = have ? vals[tid] : -INFINITY;
+  const uint32_t id = have ? ids[tid] : 0xFFFFFFFFu;
   bool keep = have;
-  if (topk) {
-    // Every value above the k-th largest, then the lowest ids among those equal to it.
-    const int above = cta_sync_count(have && z > kth);
-    if (have && z == kth) {
-      int tie_rank = 0;
-      for (int j = 0; j < m; ++j) tie_rank += ss.f_val[j] == kth && ss.f_id[j] < id;
-      keep = tie_rank < prm.top_k - above;
+  if (topk && have) {
+    // Rank in the order (logit descending, id ascending).  Every element
+    // ranked above a candidate is a candidate, so this is its rank in the row.
+    int rank = 0;
+    for (int j = 0; j < n; ++j) {
+      const float v = vals[j];
+      rank += (v > z) || (v == z && ids[j] < id);
     }
+    keep = rank < prm.top_k;
   }
-  const RowScale rs = make_row_scale(row_max, prm.temperature);
-  if (keep && minp) keep = mass_double(z, rs, sh.table) >= double(prm.min_p);
-  // Masses of S and their total Z_S.
-  const uint64_t e = keep ? mass_fixed(z, rs, sh.table) : 0;
-  if (have) ss.f_mass[tid] = e;
+  // One exponential per candidate gives both the exact min-p test and the mass.
+  RowScale rs;
+  rs.m = row_max;
+  rs.c_hi = ss.c_hi;
+  rs.c_lo = ss.c_lo;
+  uint64_t e = 0;
+  if (keep) {
+    const ExpParts p = exp_parts(z, rs, table, -1000.0f);
+    if (minp) keep = double_from_parts(p) >= double(prm.min_p);
+    if (keep) e = fixed_from_parts(p);
+  }
+  if (have) cs.f_mass[tid] = e;
   const uint64_t ws = warp_sum<uint64_t>(e);
   if (lane == 0 && ws) atomicAdd(&ss.zsum, (unsigned long long)ws);
   const int kept = cta_sync_count(keep);
   const uint64_t z_kept = ss.zsum;
   // The draw: the kept token (id order) whose cumulative mass interval holds
   // t = floor(u * Z_S), u = Philox draw 0 of row b.
-  const uint64_t t = uint64_t((u128(uniform53(a.seed, a.offset, uint64_t(b), 0)) * z_kept) >> 53);
+  const uint64_t t = uint64_t((u128(ss.u53) * z_kept) >> 53);
   if (keep && e) {
     uint64_t before = 0;
-    for (int j = 0; j < m; ++j) before += ss.f_id[j] < id ? ss.f_mass[j] : 0;
+    for (int j = 0; j < n; ++j) before += ids[j] < id ? cs.f_mass[j] : 0;
     if (before <= t && t - before < e) {
       a.out_ids[b] = int32_t(id);
-      if (a.out_probs) a.out_probs[b] = float(double(e) / double(z_kept));
+      if (a.out_probs) a.out_probs[b] = __fdiv_rn(float(e), float(z_kept));
     }
   }
   if (tid == 0 && a.kept) a.kept[b] = kept;
@@ -629,6 +625,20 @@ __device__ bool finalize_candidates(StreamShared& ss, RowShared& sh, const Sampl
     if (keep && e) a.full_probs[size_t(b) * V + id] = __fdiv_rn(float(e), float(z_kept));
   }
   return true;
+}
+
+// The k-th largest (1 <= k <= kThreads) of one float per thread, as a value v
+// with at least k of the inputs >= v: bit-wise search over the order keys.
+template <typename T>
+__device__ __forceinline__ float kth_largest(float x, int k) {
+  const uint32_t key = key_of_bits(__float_as_uint(x));
+  uint32_t t = 0;
+  const int low = KeyTraits<T>::kBits == 16 ? 16 : 0;   // bf16 keys carry no information below bit 16
+  for (int bit = 31; bit >= low; --bit) {
+    const uint32_t cand = t | (1u << bit);
+    if (cta_sync_count(key >= cand) >= k) t = cand;
+  }
+  return value_of_key(t);
 }
 
 // ------------------------------------------------------------------ the kernel
@@ -660,6 +670,7 @@ struct BatchCursor {
   int batch;
   int nbatch;
   uint32_t issued;   // copies requested so far
+  uint64_t policy;   // L2 policy of the copies
 
   // Start at this CTA's first row before its knobs are known.
   __device__ void begin(const SampleArgs& a) {
@@ -667,6 +678,7 @@ struct BatchCursor {
     batch = 0;
     nbatch = row < a.batch ? row_geom<T>(a, row).nchunks : 0;
     issued = 0;
+    policy = evict_first_policy();
   }
   // The first row's knobs are known: a general-path row stops after the
   // batches already requested.
@@ -690,42 +702,20 @@ struct BatchCursor {
     const RowGeom g = row_geom<T>(a, row);
     const uintptr_t src = g.a0 + uintptr_t(batch) * kBufBytes;
     const uint32_t bytes = uint32_t(min(uintptr_t(kBufBytes), g.a1 - src));
-    tma_load(dst, reinterpret_cast<const void*>(src), bytes, bar);
+    tma_load(dst, reinterpret_cast<const void*>(src), bytes, bar, policy);
     ++batch;
     ++issued;
   }
 };
 
-// Append the candidates of one warp's batch part: bit j * kPer + q of `mask`
-// marks element q of this lane's vector j (vector lane + 32 j of the part).
-template <typename T>
-__device__ __forceinline__ void push_mask(StreamShared& ss, uint64_t mask, const T* part, uint32_t id0) {
-  constexpr int kPer = VecOps<T>::kPer;
-  const int lane = threadIdx.x & 31;
-  const uint32_t cnt = uint32_t(__popcll(mask));
-  if (!__any_sync(0xFFFFFFFFu, cnt != 0)) return;
-  const uint32_t incl = warp_inclusive_scan<uint32_t>(cnt);
-  const uint32_t total = __shfl_sync(0xFFFFFFFFu, incl, 31);
-  uint32_t base = 0;
-  if (lane == 31) base = atomicAdd(&ss.cand_n, total);
-  base = __shfl_sync(0xFFFFFFFFu, base, 31) + incl - cnt;
-  while (mask) {
-    const int bit = __ffsll(mask) - 1;
-    mask &= mask - 1;
-    const int e = (lane + (bit / kPer) * 32) * kPer + bit % kPer;
-    if (base < uint32_t(kCandMax)) {
-      ss.cand_id[base] = id0 + uint32_t(e);
-      ss.cand_val[base] = Elem<T>::widen(part[e]);
-    }
-    ++base;
-  }
-}
-
 template <typename T>
 __global__ void __launch_bounds__(kThreads, 2) sample_kernel(SampleArgs a) {
   extern __shared__ __align__(128) unsigned char ring[];
-  __shared__ RowShared sh;
   __shared__ StreamShared ss;
+  __shared__ FloatPair table[64];
+  __shared__ RowScratch scratch;
+  RowShared& sh = scratch.row;
+  CandShared& cs = scratch.cand;
   using V = VecOps<T>;
   constexpr int kPer = V::kPer;
   const int tid = threadIdx.x;
@@ -745,7 +735,7 @@ __global__ void __launch_bounds__(kThreads, 2) sample_kernel(SampleArgs a) {
     ss.timeout = 0;
   }
   allow_dependent_launch();
-  if (tid < 64) sh.table[tid] = kExp2Table[tid];
+  if (tid < 64) table[tid] = kExp2Table[tid];
   ClusterBarrier solo;
   solo.setup(&ss.solo_bar, &ss.solo_ok, cluster_rank(), 1);
   cta_sync();
@@ -759,6 +749,7 @@ __global__ void __launch_bounds__(kThreads, 2) sample_kernel(SampleArgs a) {
     const bool fast = row_is_fast(prm, Vn);
     RowCtx<T> sc;
     sc.sh = &sh;
+    sc.table = table;
     sc.rank = 0;
     sc.nranks = 1;
     sc.first = cluster_rank();
@@ -801,18 +792,22 @@ __global__ void __launch_bounds__(kThreads, 2) sample_kernel(SampleArgs a) {
       ss.cand_n = 0;
       ss.maxkey = 0;
     }
+    if (!greedy && tid == kThreads - 1) {
+      // Row constants of the draw, off the critical path of the stream.
+      ss.u53 = uniform53(a.seed, a.offset, uint64_t(row), 0);
+      const RowScale r0 = make_row_scale(0.0f, prm.temperature);
+      ss.c_hi = r0.c_hi;
+      ss.c_lo = r0.c_lo;
+      ss.zsum = 0;
+    }
     cta_sync();
     const uint32_t id_base = uint32_t((geo.a0 - reinterpret_cast<uintptr_t>(geo.r0)) / sizeof(T));
+    const int v0 = warp * (kSubBytes / 16);            // this warp's first vector in every batch
+    const int seg_len = (geo.nchunks + kSegs - 1) / kSegs;   // batches per segment
     float best_z = -INFINITY;      // greedy: this lane's maximum and its lowest id
     uint32_t best_id = 0xFFFFFFFFu;
-    float tau = -INFINITY;         // top-k: lower bound of the k-th largest, the same in every thread
-    const float mp_w = minp ? prm.temperature * logf(prm.min_p) : 0.0f;
-    auto threshold = [&](float run_max) {
-      float theta = -INFINITY;
-      if (minp) theta = run_max + mp_w - (fabsf(run_max) + fabsf(mp_w)) * 0x1p-20f - 0x1p-126f;
-      if (topk) theta = fmaxf(theta, tau);
-      return theta;
-    };
+    float seg_max = -INFINITY;     // other rows: this lane's maximum over the current segment
+    float lane_row_max = -INFINITY;   // ... and over the row
 
     for (int bt = 0; bt < geo.nchunks; ++bt) {
       const uint32_t bi = consumed % kBufs;
@@ -820,63 +815,49 @@ __global__ void __launch_bounds__(kThreads, 2) sample_kernel(SampleArgs a) {
       // This warp's part of the batch.
       const uintptr_t bstart = geo.a0 + uintptr_t(bt) * kBufBytes;
       const int bvec = int(min(uintptr_t(kBufBytes), geo.a1 - bstart) / 16);
-      const int v0 = warp * (kSubBytes / 16);
       const int nvec = max(0, min(bvec - v0, kSubBytes / 16));
       const uint4* vec = reinterpret_cast<const uint4*>(ring + size_t(bi) * kBufBytes) + v0;
       const T* part = reinterpret_cast<const T*>(vec);
       const uint32_t id0 = id_base + uint32_t(bt) * (kBufBytes / sizeof(T)) + uint32_t(v0 * kPer);
-      float vmf[kVecPerLane];
+      // The lane's batch maximum: one packed maximum over its vectors.
+      uint32_t pm = V::neg_inf();
 #pragma unroll
       for (int j = 0; j < kVecPerLane; ++j) {
         const int v = lane + j * 32;
-        vmf[j] = V::finish(v < nvec ? V::vmax(vec[v]) : V::neg_inf());
+        if (v < nvec) pm = V::max2(pm, V::vmax(vec[v]));
       }
+      const float lane_max = V::finish(pm);
+      const uint32_t lane_key = lane_max > -INFINITY ? key_of_bits(__float_as_uint(lane_max)) : 0u;
+      const uint32_t wkey = __reduce_max_sync(0xFFFFFFFFu, lane_key);
       if (greedy) {
-#pragma unroll
-        for (int j = 0; j < kVecPerLane; ++j) {
-          if (vmf[j] > best_z) {
+        // Only a lane whose batch maximum beats its own best and reaches the
+        // CTA's running maximum can hold the row's arg-max: locate its first
+        // occurrence (ids rise with j, then q).
+        const uint32_t shared_key = *reinterpret_cast<volatile uint32_t*>(&ss.maxkey);
+        const float shared_max = shared_key ? value_of_key(shared_key) : -INFINITY;
+        if (lane_max > best_z && lane_max >= shared_max) {
+          for (int j = 0; j < kVecPerLane; ++j) {
             const int e0 = (lane + j * 32) * kPer;
+            int hit = -1;
 #pragma unroll
-            for (int q = 0; q < kPer; ++q) {
-              const float z = Elem<T>::widen(part[e0 + q]);
-              if (z > best_z) {
-                best_z = z;
-                best_id = id0 + uint32_t(e0 + q);
-              }
+            for (int q = kPer - 1; q >= 0; --q)
+              if (Elem<T>::widen(part[e0 + q]) == lane_max) hit = q;
+            if (hit >= 0) {
+              best_id = id0 + uint32_t(e0 + hit);
+              break;
             }
           }
+          best_z = lane_max;
         }
       } else {
-        float lane_max = vmf[0];
-#pragma unroll
-        for (int j = 1; j < kVecPerLane; ++j) lane_max = fmaxf(lane_max, vmf[j]);
-        const uint32_t lane_key = lane_max > -INFINITY ? key_of_bits(__float_as_uint(lane_max)) : 0u;
-        const uint32_t wkey = __reduce_max_sync(0xFFFFFFFFu, lane_key);
-        float theta;
-        if (bt == 0) {
-          // The first batch sets the scale: the CTA-wide maximum.
-          if (lane == 0 && wkey) atomicMax(&ss.maxkey, wkey);
-          if (topk) tau = kth_largest<T>(lane_max, prm.top_k);
-          else cta_sync();
-          theta = threshold(value_of_key(ss.maxkey));
-        } else {
-          // Any value of the shared running maximum is a valid lower bound.
-          const uint32_t shared_key = *reinterpret_cast<volatile uint32_t*>(&ss.maxkey);
-          theta = threshold(value_of_key(lane_key > shared_key ? lane_key : shared_key));
+        seg_max = fmaxf(seg_max, lane_max);
+        lane_row_max = fmaxf(lane_row_max, lane_max);
+        if (bt % seg_len == seg_len - 1 || bt == geo.nchunks - 1) {
+          cs.seg[bt / seg_len][tid] = seg_max;
+          seg_max = -INFINITY;
         }
-        uint64_t mask = 0;
-#pragma unroll
-        for (int j = 0; j < kVecPerLane; ++j) {
-          if (vmf[j] >= theta) {
-            const int e0 = (lane + j * 32) * kPer;
-#pragma unroll
-            for (int q = 0; q < kPer; ++q)
-              if (Elem<T>::widen(part[e0 + q]) >= theta) mask |= 1ull << (j * kPer + q);
-          }
-        }
-        push_mask<T>(ss, mask, part, id0);
-        if (bt > 0 && lane == 0 && wkey) atomicMax(&ss.maxkey, wkey);
       }
+      if (lane == 0 && wkey) atomicMax(&ss.maxkey, wkey);
       cta_sync();   // the buffer is free
       ++consumed;
       if (ss.timeout) {
@@ -884,10 +865,6 @@ __global__ void __launch_bounds__(kThreads, 2) sample_kernel(SampleArgs a) {
         break;
       }
       if (tid == 0) cur.issue(a, ring + size_t(bi) * kBufBytes, &ss.full[bi]);
-      if (topk && ss.cand_n > uint32_t(kCompactAt) && ss.cand_n <= uint32_t(kCandMax)) {
-        tau = fmaxf(tau, kth_largest_list<T>(ss.cand_val, int(ss.cand_n), prm.top_k, ss.hist, ss.bc));
-        compact_candidates(ss, tau);
-      }
     }
     if (!alive) break;
 
@@ -923,25 +900,80 @@ __global__ void __launch_bounds__(kThreads, 2) sample_kernel(SampleArgs a) {
       continue;
     }
 
-    float run_max = value_of_key(ss.maxkey);
-    if (geo.head > 0 || geo.tail0 < Vn) {
-      // Elements outside the aligned middle join the candidates directly.
+    // The row maximum, with the elements outside the aligned middle.
+    float run_max = ss.maxkey ? value_of_key(ss.maxkey) : -INFINITY;
+    const bool edges = geo.head > 0 || geo.tail0 < Vn;
+    if (edges) {
       float emax = -INFINITY;
       for (int i = tid; i < geo.head; i += kThreads) emax = fmaxf(emax, Elem<T>::widen(sc.s[i]));
       for (int i = geo.tail0 + tid; i < Vn; i += kThreads) emax = fmaxf(emax, Elem<T>::widen(sc.s[i]));
       run_max = fmaxf(run_max, block_max_f(emax, ss.red));
-      const float theta = threshold(run_max);
+    }
+    // A lower bound theta of the kept set's boundary: min-p's at the row
+    // maximum, and the k-th largest per-lane maximum (k lanes hold an element
+    // at least that large, so the k-th largest element is too).
+    float theta = -INFINITY;
+    if (minp) theta = minp_lower_bound(run_max, prm.temperature, prm.min_p);
+    const int nseg = (geo.nchunks + seg_len - 1) / seg_len;
+    if (topk) theta = fmaxf(theta, kth_largest<T>(lane_row_max, prm.top_k));
+    // Candidates: every element >= theta, from the segments whose maximum
+    // reaches it (read again from global memory, normally still in L2) and
+    // from the edges.
+    if (tid == 0) ss.qn = 0;
+    cta_sync();
+    if (!isnan(theta)) {
+      // The (lane, segment) pairs to read again, then one pass in which every
+      // thread takes one of them (all its loads in flight at once).
+      for (int sgi = 0; sgi < nseg; ++sgi) {
+        if (cs.seg[sgi][tid] >= theta) {
+          const uint32_t slot = atomicAdd(&ss.qn, 1u);
+          if (slot < uint32_t(kThreads)) cs.q[slot] = uint32_t(tid) | (uint32_t(sgi) << 8);
+        }
+      }
+      cta_sync();
+      const int qn = int(ss.qn);
+      if (qn > kThreads) {
+        if (tid == 0) ss.cand_n = uint32_t(kCandMax) + 1;   // too many: the general path takes the row
+      } else {
+        for (int w = tid; w < qn * seg_len; w += kThreads) {
+          const uint32_t pr = cs.q[w / seg_len];
+          const int owner = int(pr & 255u);
+          const int bt = int(pr >> 8) * seg_len + w % seg_len;
+          if (bt >= geo.nchunks) continue;
+          const int ov0 = (owner >> 5) * (kSubBytes / 16);
+          const int ol = owner & 31;
+          const uintptr_t bstart = geo.a0 + uintptr_t(bt) * kBufBytes;
+          const int bvec = int(min(uintptr_t(kBufBytes), geo.a1 - bstart) / 16);
+          const int nvec = max(0, min(bvec - ov0, kSubBytes / 16));
+          const uint4* gv = reinterpret_cast<const uint4*>(bstart) + ov0;
+          const uint32_t id0 = id_base + uint32_t(bt) * (kBufBytes / sizeof(T)) + uint32_t(ov0 * kPer);
+          uint4 xv[kVecPerLane];
+#pragma unroll
+          for (int j = 0; j < kVecPerLane; ++j) {
+            const int v = ol + j * 32;
+            xv[j] = v < nvec ? __ldg(gv + v) : make_uint4(V::neg_inf(), V::neg_inf(), V::neg_inf(), V::neg_inf());
+          }
+          for (int j = 0; j < kVecPerLane; ++j) {
+            if (!(V::finish(V::vmax(xv[j])) >= theta)) continue;
+            const T* e = reinterpret_cast<const T*>(&xv[j]);
+            for (int q = 0; q < kPer; ++q) {
+              const float z = Elem<T>::widen(e[q]);
+              if (z >= theta) push_candidate(ss, cs, id0 + uint32_t((ol + j * 32) * kPer + q), z);
+            }
+          }
+        }
+      }
       for (int i = tid; i < geo.head; i += kThreads) {
         const float z = Elem<T>::widen(sc.s[i]);
-        if (z >= theta) push_candidate(ss, uint32_t(i), z);
+        if (z >= theta) push_candidate(ss, cs, uint32_t(i), z);
       }
       for (int i = geo.tail0 + tid; i < Vn; i += kThreads) {
         const float z = Elem<T>::widen(sc.s[i]);
-        if (z >= theta) push_candidate(ss, uint32_t(i), z);
+        if (z >= theta) push_candidate(ss, cs, uint32_t(i), z);
       }
-      cta_sync();
     }
-    if (!finalize_candidates<T>(ss, sh, a, row, prm, run_max)) {
+    cta_sync();
+    if (!finalize_candidates<T>(ss, cs, table, a, row, prm, run_max)) {
       cta_sync();
       general_row<T>(sc, a, row, prm, slice_best<T>(sc.s, Vn, 0));
       alive = sc.alive;

@@ -57,6 +57,7 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads, 1) verify_pos_kernel(VerifyArgs a) {
   extern __shared__ __align__(16) unsigned char dyn_smem[];
   __shared__ RowShared sh;
+  __shared__ FloatPair table[64];
   const uint32_t nranks = cluster_size();
   const uint32_t rank = cluster_rank();
   const int rows_per_b = 2 * a.k + 1;
@@ -66,11 +67,12 @@ __global__ void __launch_bounds__(kThreads, 1) verify_pos_kernel(VerifyArgs a) {
   const int V = a.vocab;
   grid_dependency_wait();
   allow_dependent_launch();
-  if (threadIdx.x < 64) sh.table[threadIdx.x] = kExp2Table[threadIdx.x];
+  if (threadIdx.x < 64) table[threadIdx.x] = kExp2Table[threadIdx.x];
 
   ClusterBarrier cbar;
   RowCtx<T> c;
   c.sh = &sh;
+  c.table = table;
   c.rank = rank;
   c.nranks = nranks;
   c.first = 0;
@@ -97,7 +99,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_pos_kernel(VerifyArgs a) {
   const RowScale rs = make_row_scale(m, 1.0f);
   uint64_t z = 0;
   if (!flags)
-    for (int i = threadIdx.x; i < n; i += kThreads) z += mass_fixed(Elem<T>::widen(s[i]), rs, sh.table);
+    for (int i = threadIdx.x; i < n; i += kThreads) z += mass_fixed(Elem<T>::widen(s[i]), rs, table);
   uint64_t tot[4] = {z, 0, 0, 0};
   cluster_sum4(c, tot, 1, nullptr);
   if (!c.alive) flags |= kRowTimeout;
@@ -107,7 +109,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_pos_kernel(VerifyArgs a) {
     if (i < a.k) {
       const int x = a.drafts[size_t(b) * a.k + i];
       if (x < 0 || x >= V) flags |= kRowBadDraft;
-      else if (!flags) ex = mass_double(Elem<T>::widen(row[x]), rs, sh.table);
+      else if (!flags) ex = mass_double(Elem<T>::widen(row[x]), rs, table);
     }
     PosStat st;
     st.m = m;
@@ -123,6 +125,7 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads, 1) verify_resolve_kernel(VerifyArgs a) {
   extern __shared__ __align__(16) unsigned char dyn_smem[];
   __shared__ RowShared sh;
+  __shared__ FloatPair table[64];
   __shared__ int32_t decision[2];   // first rejection j, row flags
   const uint32_t nranks = cluster_size();
   const uint32_t rank = cluster_rank();
@@ -133,11 +136,12 @@ __global__ void __launch_bounds__(kThreads, 1) verify_resolve_kernel(VerifyArgs 
   const PosStat* st = a.ws + size_t(b) * rows_per_b;
   grid_dependency_wait();   // the position statistics come from verify_pos_kernel
   allow_dependent_launch();
-  if (threadIdx.x < 64) sh.table[threadIdx.x] = kExp2Table[threadIdx.x];
+  if (threadIdx.x < 64) table[threadIdx.x] = kExp2Table[threadIdx.x];
 
   ClusterBarrier cbar;
   RowCtx<T> c;
   c.sh = &sh;
+  c.table = table;
   c.rank = rank;
   c.nranks = nranks;
   c.first = 0;
@@ -206,11 +210,11 @@ __global__ void __launch_bounds__(kThreads, 1) verify_resolve_kernel(VerifyArgs 
   // integers, eq. 39.4), or the target masses for the bonus draw.
   bool use_p = !residual;
   auto w_res = [&](int i) -> u128 {
-    const u128 ep = u128(mass_fixed(Elem<T>::widen(sp[i]), rp, sh.table)) * Q.z;
-    const u128 eq = u128(mass_fixed(Elem<T>::widen(sq[i]), rq, sh.table)) * P.z;
+    const u128 ep = u128(mass_fixed(Elem<T>::widen(sp[i]), rp, table)) * Q.z;
+    const u128 eq = u128(mass_fixed(Elem<T>::widen(sq[i]), rq, table)) * P.z;
     return ep > eq ? ep - eq : u128(0);
   };
-  auto w_p = [&](int i) -> u128 { return u128(mass_fixed(Elem<T>::widen(sp[i]), rp, sh.table)); };
+  auto w_p = [&](int i) -> u128 { return u128(mass_fixed(Elem<T>::widen(sp[i]), rp, table)); };
   u128 local = 0, before = 0, total = 0;
   if (residual) {
     for (int i = threadIdx.x; i < n; i += kThreads) local += w_res(i);

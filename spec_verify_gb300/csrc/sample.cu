@@ -419,7 +419,10 @@ struct CandShared {
   float cand_val[kCandMax];
   uint32_t f_id[kFinalMax];
   float f_val[kFinalMax];
-  uint64_t f_mass[kFinalMax];   // E_i of the kept candidates, 0 for the others
+  // The ranked candidates, padded to whole 128-bit loads: (key << 32 | ~id),
+  // whose order is the kept-set order, and (id, E_i) with E_i = 0 outside S.
+  __align__(16) unsigned long long pk[kFinalMax + 8];
+  __align__(16) ulonglong2 idm[kFinalMax + 8];
 };
 
 union RowScratch {
@@ -580,16 +583,25 @@ __device__ bool finalize_candidates(StreamShared& ss, CandShared& cs, const Floa
   const bool have = tid < n;
   const float z = have ? vals[tid] : -INFINITY;
   const uint32_t id = have ? ids[tid] : 0xFFFFFFFFu;
+  const int n8 = (n + 7) & ~7;
+  if (tid < n8) cs.pk[tid] = have ? (uint64_t(key_of_bits(__float_as_uint(z))) << 32) | uint64_t(~id) : 0ull;
+  if (topk) cta_sync();
   bool keep = have;
   if (topk && have) {
-    // Rank in the order (logit descending, id ascending).  Every element
-    // ranked above a candidate is a candidate, so this is its rank in the row.
-    int rank = 0;
-    for (int j = 0; j < n; ++j) {
-      const float v = vals[j];
-      rank += (v > z) || (v == z && ids[j] < id);
+    // Rank in the order (logit descending, id ascending): the number of
+    // larger packed keys.  Every element ranked above a candidate is a
+    // candidate, so this is its rank in the row.
+    const unsigned long long me = cs.pk[tid];
+    const ulonglong2* p2 = reinterpret_cast<const ulonglong2*>(cs.pk);
+    int c[4] = {0, 0, 0, 0};
+    for (int j = 0; j < n8 / 2; j += 4) {
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const ulonglong2 q = p2[j + u];
+        c[u] += int(q.x > me) + int(q.y > me);
+      }
     }
-    keep = rank < prm.top_k;
+    keep = c[0] + c[1] + c[2] + c[3] < prm.top_k;
   }
   // One exponential per candidate gives both the exact min-p test and the mass.
   RowScale rs;
@@ -602,7 +614,7 @@ __device__ bool finalize_candidates(StreamShared& ss, CandShared& cs, const Floa
     if (minp) keep = double_from_parts(p) >= double(prm.min_p);
     if (keep) e = fixed_from_parts(p);
   }
-  if (have) cs.f_mass[tid] = e;
+  if (tid < n8) cs.idm[tid] = make_ulonglong2(have ? id : 0xFFFFFFFFull, e);
   const uint64_t ws = warp_sum<uint64_t>(e);
   if (lane == 0 && ws) atomicAdd(&ss.zsum, (unsigned long long)ws);
   const int kept = cta_sync_count(keep);
@@ -611,8 +623,15 @@ __device__ bool finalize_candidates(StreamShared& ss, CandShared& cs, const Floa
   // t = floor(u * Z_S), u = Philox draw 0 of row b.
   const uint64_t t = uint64_t((u128(ss.u53) * z_kept) >> 53);
   if (keep && e) {
-    uint64_t before = 0;
-    for (int j = 0; j < n; ++j) before += ids[j] < id ? cs.f_mass[j] : 0;
+    uint64_t c[4] = {0, 0, 0, 0};
+    for (int j = 0; j < n8; j += 4) {
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const ulonglong2 q = cs.idm[j + u];
+        c[u] += q.x < id ? q.y : 0ull;
+      }
+    }
+    const uint64_t before = c[0] + c[1] + c[2] + c[3];
     if (before <= t && t - before < e) {
       a.out_ids[b] = int32_t(id);
       if (a.out_probs) a.out_probs[b] = __fdiv_rn(float(e), float(z_kept));

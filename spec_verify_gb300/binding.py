@@ -120,7 +120,8 @@ def sample(logits, params, seed=0, offset=0, out_ids=None, out_probs=None, statu
 
     params: record array (spec_verify_gb300.workloads.PARAMS_DTYPE) or a
     device byte tensor holding it.  Returns (ids int32 [B], probs float32 [B],
-    status int32 [1]) on the logits' device.
+    status int32 [1]) on the logits' device; status=False passes no status
+    word (the call then skips clearing it) and returns None in its place.
     """
     torch = _torch()
     lib = load()
@@ -131,7 +132,10 @@ def sample(logits, params, seed=0, offset=0, out_ids=None, out_probs=None, statu
     prm = params_to_device(params, dev)
     out_ids = out_ids if out_ids is not None else torch.empty(batch, dtype=torch.int32, device=dev)
     out_probs = out_probs if out_probs is not None else torch.empty(batch, dtype=torch.float32, device=dev)
-    status = status if status is not None else torch.empty(1, dtype=torch.int32, device=dev)
+    if status is False:
+        status = None
+    elif status is None:
+        status = torch.empty(1, dtype=torch.int32, device=dev)
     _check(lib.smp_sample(_ptr(logits), batch, vocab, _dtype_code(logits), _ptr(prm), seed, offset,
                           _ptr(out_ids), _ptr(out_probs), _ptr(status), _stream(stream)))
     return out_ids, out_probs, status

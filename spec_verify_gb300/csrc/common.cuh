@@ -246,6 +246,32 @@ __device__ __forceinline__ uint64_t mass_fixed(float z, const RowScale& rs, cons
   return fixed_from_parts(exp_parts(z, rs, table, -float(kFixedBits + 3)));
 }
 
+// The fixed-point mass round(exp((z - m) / T) * 2^F) from the binary32
+// exp2f (relative error a few units in the last place, about 3e-7), for row
+// sums that need that accuracy rather than the double-float value.  The
+// argument is formed with the head + tail of log2(e) / T.
+__device__ __forceinline__ uint64_t mass_fast(float z, const RowScale& rs) {
+  const float d = __fsub_rn(z, rs.m);
+  if (d == 0.0f) return kFixedOne;
+  const float y = __fmaf_rn(d, rs.c_hi, __fmul_rn(d, rs.c_lo));
+  if (!(y > -float(kFixedBits + 3))) return 0;   // also -inf and NaN
+  return __float2ull_rn(__fmul_rn(exp2f(y), float(kFixedOne)));
+}
+
+// 2^y by the ex2.approx instruction (flushes results below 2^-126 to 0).
+__device__ __forceinline__ float ex2_approx(float y) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(y));
+  return r;
+}
+
+// exp((z - m) / T) in binary32 (0 for -inf, NaN and below 2^-126).
+__device__ __forceinline__ float exp_fast(float z, const RowScale& rs) {
+  const float d = __fsub_rn(z, rs.m);
+  const float y = __fmaf_rn(d, rs.c_hi, __fmul_rn(d, rs.c_lo));
+  return y > -126.0f ? ex2_approx(y) : 0.0f;
+}
+
 // exp((z - m) / T) as a double (head + tail, scaled); 0 below 2^-1000.
 __device__ __forceinline__ double mass_double(float z, const RowScale& rs, const FloatPair* table) {
   return double_from_parts(exp_parts(z, rs, table, -1000.0f));
@@ -253,14 +279,14 @@ __device__ __forceinline__ double mass_double(float z, const RowScale& rs, const
 
 // ------------------------------------------------------------------ warp / block helpers
 
-// Barrier over the kThreads threads that work on rows (named barrier 1).  A
-// kernel may run an extra producer warp that takes no part in it.
 // Programmatic dependent launch: wait until the previous kernel on the stream
 // has finished and its writes are visible (a no-op for a normal launch), and
 // let the next kernel on the stream be scheduled early (it waits in turn).
 __device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void allow_dependent_launch() { asm volatile("griddepcontrol.launch_dependents;"); }
 
+// Barrier over the kThreads threads that work on rows (named barrier 1).  A
+// kernel may run an extra producer warp that takes no part in it.
 __device__ __forceinline__ void cta_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory"); }
 
 // cta_sync() that also returns how many of the kThreads threads passed `pred`.
@@ -290,6 +316,15 @@ __device__ __forceinline__ u128 shfl_xor_u128(u128 v, int mask) {
   const uint64_t lo = shfl_xor_u64(uint64_t(v), mask);
   const uint64_t hi = shfl_xor_u64(uint64_t(v >> 64), mask);
   return (u128(hi) << 64) | lo;
+}
+
+__device__ __forceinline__ u128 shfl_u128(u128 v, int src) {
+  const uint64_t lo = uint64_t(v), hi = uint64_t(v >> 64);
+  const uint64_t lo2 = (uint64_t(__shfl_sync(0xFFFFFFFFu, uint32_t(lo >> 32), src)) << 32) |
+                       __shfl_sync(0xFFFFFFFFu, uint32_t(lo), src);
+  const uint64_t hi2 = (uint64_t(__shfl_sync(0xFFFFFFFFu, uint32_t(hi >> 32), src)) << 32) |
+                       __shfl_sync(0xFFFFFFFFu, uint32_t(hi), src);
+  return (u128(hi2) << 64) | lo2;
 }
 
 __device__ __forceinline__ u128 shfl_up_u128(u128 v, int delta) {

@@ -27,6 +27,63 @@ __device__ __forceinline__ uint32_t elem_key(T v) {
   return KeyTraits<T>::kBits == 32 ? k : (k >> 16);
 }
 
+// Operations on one 16-byte vector of elements: packed maximum, element access.
+template <typename T>
+struct VecOps;
+
+template <>
+struct VecOps<uint16_t> {
+  static constexpr int kPer = 8;
+  static __device__ __forceinline__ uint32_t max2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+  }
+  static __device__ __forceinline__ uint32_t neg_inf() { return 0xFF80FF80u; }
+  // max of the 8 values of x, packed in two halves
+  static __device__ __forceinline__ uint32_t vmax(const uint4& x) {
+    return max2(max2(x.x, x.y), max2(x.z, x.w));
+  }
+  static __device__ __forceinline__ float finish(uint32_t m) {
+    return fmaxf(__uint_as_float(m & 0xFFFF0000u), __uint_as_float(m << 16));
+  }
+  // element q (0..7, a compile-time constant once unrolled) of x
+  static __device__ __forceinline__ float elem(const uint4& x, int q) {
+    const uint32_t w = q < 2 ? x.x : q < 4 ? x.y : q < 6 ? x.z : x.w;
+    return __uint_as_float((q & 1) ? (w & 0xFFFF0000u) : (w << 16));
+  }
+};
+
+template <>
+struct VecOps<float> {
+  static constexpr int kPer = 4;
+  static __device__ __forceinline__ uint32_t max2(uint32_t a, uint32_t b) {
+    return __float_as_uint(fmaxf(__uint_as_float(a), __uint_as_float(b)));
+  }
+  static __device__ __forceinline__ uint32_t neg_inf() { return 0xFF800000u; }
+  static __device__ __forceinline__ uint32_t vmax(const uint4& x) {
+    return __float_as_uint(fmaxf(fmaxf(__uint_as_float(x.x), __uint_as_float(x.y)),
+                                 fmaxf(__uint_as_float(x.z), __uint_as_float(x.w))));
+  }
+  static __device__ __forceinline__ float finish(uint32_t m) { return __uint_as_float(m); }
+  static __device__ __forceinline__ float elem(const uint4& x, int q) {
+    return __uint_as_float(q == 0 ? x.x : q == 1 ? x.y : q == 2 ? x.z : x.w);
+  }
+};
+
+__device__ __forceinline__ float block_max_f(float v, float* scratch) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  cta_sync();
+  if (lane == 0) scratch[warp] = v;
+  cta_sync();
+  float r = scratch[0];
+#pragma unroll
+  for (int w = 1; w < kWarps; ++w) r = fmaxf(r, scratch[w]);
+  return r;
+}
+
 template <typename T>
 __device__ __forceinline__ float key_value(uint32_t key) {
   if (KeyTraits<T>::kBits == 32) return value_of_key(key);

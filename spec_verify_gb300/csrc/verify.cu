@@ -4,14 +4,13 @@
 // "Speculative decoding").
 //
 // Two kernels on the caller's stream:
-//   verify_pos_kernel      one cluster per logit row (b, position, target or
-//                          draft): the row maximum, the exact fixed-point mass
-//                          Z and the draft token's mass, written to the
+//   verify_pos_kernel      one CTA per logit row (b, position, target or
+//                          draft): the row maximum, the fixed-point mass Z
+//                          and the draft token's mass, written to the
 //                          workspace;
-//   verify_resolve_kernel  one cluster per batch row: the accept tests in
-//                          order, then the replacement draw from
-//                          max(0, p_j - q_j) at the first rejection j, or the
-//                          bonus draw from p_K.
+//   verify_resolve_kernel  one CTA per batch row: the accept tests in order,
+//                          then the replacement draw from max(0, p_j - q_j) at
+//                          the first rejection j, or the bonus draw from p_K.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -43,7 +42,6 @@ struct VerifyArgs {
   int32_t* ids;
   int32_t* status;
   PosStat* ws;
-  int slice;
 };
 
 template <typename T>
@@ -53,239 +51,323 @@ __device__ __forceinline__ const T* logit_row(const VerifyArgs& a, int b, int j)
   return reinterpret_cast<const T*>(a.q) + (size_t(b) * a.k + (j - a.k - 1)) * V;
 }
 
+constexpr int kPosUnroll = 16;   // 16-byte loads in flight per thread in verify_pos_kernel
+
+__device__ __forceinline__ uint4 load_stream(const uint4* p) {
+  uint4 x;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(x.x), "=r"(x.y), "=r"(x.z), "=r"(x.w)
+               : "l"(p));
+  return x;
+}
+
+// One CTA per logit row.  Pass 1 streams the row from HBM for its maximum;
+// pass 2 reads it again (now in L2) for the fixed-point mass Z.  Thread 0
+// adds the draft token's mass (double-float exponential) and the flags.
 template <typename T>
-__global__ void __launch_bounds__(kThreads, 1) verify_pos_kernel(VerifyArgs a) {
-  extern __shared__ __align__(16) unsigned char dyn_smem[];
-  __shared__ RowShared sh;
+__global__ void __launch_bounds__(kThreads, 2) verify_pos_kernel(VerifyArgs a) {
+  using V = VecOps<T>;
+  constexpr int kPer = V::kPer;
   __shared__ FloatPair table[64];
-  const uint32_t nranks = cluster_size();
-  const uint32_t rank = cluster_rank();
+  __shared__ float redf[kWarps];
+  __shared__ uint64_t red64[kWarps];
+  const int tid = threadIdx.x;
   const int rows_per_b = 2 * a.k + 1;
-  const int pr = int(blockIdx.x / nranks);
+  const int pr = int(blockIdx.x);
   const int b = pr / rows_per_b;
   const int j = pr % rows_per_b;
-  const int V = a.vocab;
+  const int Vn = a.vocab;
   grid_dependency_wait();
   allow_dependent_launch();
-  if (threadIdx.x < 64) table[threadIdx.x] = kExp2Table[threadIdx.x];
-
-  ClusterBarrier cbar;
-  RowCtx<T> c;
-  c.sh = &sh;
-  c.table = table;
-  c.rank = rank;
-  c.nranks = nranks;
-  c.first = 0;
-  c.mb = 0;
-  c.alive = true;
-  cbar.init(&sh.mbar, &sh.ok, nranks);
-  c.cb = &cbar;
+  if (tid < 64) table[tid] = kExp2Table[tid];
 
   const T* row = logit_row<T>(a, b, j);
-  const int lo = int(rank) * a.slice;
-  int n = V - lo;
-  n = n < 0 ? 0 : (n > a.slice ? a.slice : n);
-  c.lo = lo;
-  c.n = n;
-  T* s = reinterpret_cast<T*>(dyn_smem + slice_smem_offset(row, lo, n));
-  c.s = s;
-  uint64_t best = load_slice(row, lo, n, s);
-  __syncthreads();
-  best = cluster_max(c, best);
-  const uint32_t key_max = uint32_t(best >> 32);
+  // The 16-byte aligned middle of the row, and the elements before and after it.
+  const uintptr_t r0 = reinterpret_cast<uintptr_t>(row);
+  const uintptr_t r1 = r0 + size_t(Vn) * sizeof(T);
+  const uintptr_t m0 = (r0 + 15) & ~uintptr_t(15);
+  const uintptr_t m1 = r1 & ~uintptr_t(15);
+  const bool middle = m1 > m0;
+  const int head = middle ? int((m0 - r0) / sizeof(T)) : Vn;
+  const int tail0 = middle ? int((m1 - r0) / sizeof(T)) : Vn;
+  const int nvec = middle ? int((m1 - m0) / 16) : 0;
+  const uint4* vec = reinterpret_cast<const uint4*>(m0);
+  const uint32_t ninf = V::neg_inf();
+
+  uint32_t pm = ninf;
+  for (int v0 = 0; v0 < nvec; v0 += kThreads * kPosUnroll) {
+    uint4 x[kPosUnroll];
+#pragma unroll
+    for (int u = 0; u < kPosUnroll; ++u) {
+      const int i = v0 + tid + u * kThreads;
+      x[u] = i < nvec ? load_stream(vec + i) : make_uint4(ninf, ninf, ninf, ninf);
+    }
+#pragma unroll
+    for (int u = 0; u < kPosUnroll; ++u) pm = V::max2(pm, V::vmax(x[u]));
+  }
+  float mx = V::finish(pm);
+  for (int i = tid; i < head; i += kThreads) mx = fmaxf(mx, Elem<T>::widen(row[i]));
+  for (int i = tail0 + tid; i < Vn; i += kThreads) mx = fmaxf(mx, Elem<T>::widen(row[i]));
+  const float m = block_max_f(mx, redf);
   int flags = 0;
-  if (!key_finite<T>(key_max)) flags |= kRowNonFinite;
-  const float m = key_value<T>(key_max);
+  if (!isfinite(m)) flags |= kRowNonFinite;
   const RowScale rs = make_row_scale(m, 1.0f);
-  uint64_t z = 0;
-  if (!flags)
-    for (int i = threadIdx.x; i < n; i += kThreads) z += mass_fixed(Elem<T>::widen(s[i]), rs, table);
-  uint64_t tot[4] = {z, 0, 0, 0};
-  cluster_sum4(c, tot, 1, nullptr);
-  if (!c.alive) flags |= kRowTimeout;
-  if (rank == 0 && threadIdx.x == 0) {
+
+  // Z = sum of exp(z - m): binary32 exponentials summed as trees (per vector,
+  // then per group of kPosUnroll vectors), each thread's total turned into
+  // fixed point once; relative error about 3e-7.
+  float zf = 0.0f;
+  if (!flags) {
+    for (int v0 = 0; v0 < nvec; v0 += kThreads * kPosUnroll) {
+      uint4 x[kPosUnroll];
+#pragma unroll
+      for (int u = 0; u < kPosUnroll; ++u) {
+        const int i = v0 + tid + u * kThreads;
+        x[u] = i < nvec ? __ldg(vec + i) : make_uint4(ninf, ninf, ninf, ninf);
+      }
+      float vs[kPosUnroll];
+#pragma unroll
+      for (int u = 0; u < kPosUnroll; ++u) {
+        float e[kPer];
+#pragma unroll
+        for (int q = 0; q < kPer; ++q) e[q] = exp_fast(V::elem(x[u], q), rs);
+#pragma unroll
+        for (int w = kPer / 2; w > 0; w /= 2)
+#pragma unroll
+          for (int q = 0; q < w; ++q) e[q] += e[q + w];
+        vs[u] = e[0];
+      }
+#pragma unroll
+      for (int w = kPosUnroll / 2; w > 0; w /= 2)
+#pragma unroll
+        for (int u = 0; u < w; ++u) vs[u] += vs[u + w];
+      zf += vs[0];
+    }
+    for (int i = tid; i < head; i += kThreads) zf += exp_fast(Elem<T>::widen(row[i]), rs);
+    for (int i = tail0 + tid; i < Vn; i += kThreads) zf += exp_fast(Elem<T>::widen(row[i]), rs);
+  }
+  uint64_t z = __float2ull_rn(__fmul_rn(zf, float(kFixedOne)));
+  z = warp_sum<uint64_t>(z);
+  if ((tid & 31) == 0) red64[tid >> 5] = z;
+  cta_sync();
+  if (tid == 0) {
+    uint64_t tot = 0;
+    for (int w = 0; w < kWarps; ++w) tot += red64[w];
     const int i = j <= a.k ? j : j - a.k - 1;   // draft position of this row
     double ex = 0.0;
     if (i < a.k) {
       const int x = a.drafts[size_t(b) * a.k + i];
-      if (x < 0 || x >= V) flags |= kRowBadDraft;
+      if (x < 0 || x >= Vn) flags |= kRowBadDraft;
       else if (!flags) ex = mass_double(Elem<T>::widen(row[x]), rs, table);
     }
     PosStat st;
     st.m = m;
     st.flags = flags;
-    st.z = tot[0];
+    st.z = tot;
     st.ex = ex;
     a.ws[pr] = st;
   }
-  c.exchange();
 }
 
+constexpr int kResolveThreads = 512;
+constexpr int kResolveWarps = kResolveThreads / 32;
+
+// Exclusive prefix over the CTA of one u64 per thread (thread order), and the total.
+__device__ __forceinline__ uint64_t resolve_scan(uint64_t v, uint64_t* warp_tot, uint64_t* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint64_t incl = warp_inclusive_scan<uint64_t>(v);
+  if (lane == 31) warp_tot[warp] = incl;
+  __syncthreads();
+  uint64_t before = incl - v, all = 0;
+  for (int w = 0; w < kResolveWarps; ++w) {
+    const uint64_t t = warp_tot[w];
+    if (w < warp) before += t;
+    all += t;
+  }
+  __syncthreads();   // warp_tot may be written again
+  *total = all;
+  return before;
+}
+
+// One CTA per batch row: the accept tests of eq. 39.3 in position order, then
+// the replacement draw from max(0, p_j - q_j) (eq. 39.4) at the first
+// rejection j, or the bonus draw from p_K.  Thread t owns the token ids
+// [t C, (t + 1) C): weights are 31-bit fixed point with exact integer sums, a
+// CTA scan finds the owner of the crossing, and warp 0 walks that chunk.
 template <typename T>
-__global__ void __launch_bounds__(kThreads, 1) verify_resolve_kernel(VerifyArgs a) {
-  extern __shared__ __align__(16) unsigned char dyn_smem[];
-  __shared__ RowShared sh;
-  __shared__ FloatPair table[64];
+__global__ void __launch_bounds__(kResolveThreads, 1) verify_resolve_kernel(VerifyArgs a) {
   __shared__ int32_t decision[2];   // first rejection j, row flags
-  const uint32_t nranks = cluster_size();
-  const uint32_t rank = cluster_rank();
-  const int b = int(blockIdx.x / nranks);
+  __shared__ uint64_t warp_tot[kResolveWarps];
+  __shared__ int owner;             // thread whose ids hold the draw
+  __shared__ uint64_t owner_before;
+  const int tid = threadIdx.x;
+  const int b = int(blockIdx.x);
   const int K = a.k;
   const int V = a.vocab;
   const int rows_per_b = 2 * K + 1;
   const PosStat* st = a.ws + size_t(b) * rows_per_b;
   grid_dependency_wait();   // the position statistics come from verify_pos_kernel
   allow_dependent_launch();
-  if (threadIdx.x < 64) table[threadIdx.x] = kExp2Table[threadIdx.x];
 
-  ClusterBarrier cbar;
-  RowCtx<T> c;
-  c.sh = &sh;
-  c.table = table;
-  c.rank = rank;
-  c.nranks = nranks;
-  c.first = 0;
-  c.mb = 0;
-  c.alive = true;
-  cbar.init(&sh.mbar, &sh.ok, nranks);
-  c.cb = &cbar;
-
-  // Accept tests of eq. 39.3 in position order: u_i < p_i(x) / max(q_i(x), 1e-300).
-  if (threadIdx.x == 0) {
-    int flags = 0;
-    for (int r = 0; r < rows_per_b; ++r) flags |= st[r].flags;
-    int jrej = K;
-    if (!flags) {
-      const double scale = 1.0 / double(kFixedOne);
-      for (int i = 0; i < K; ++i) {
-        const PosStat& P = st[i];
-        const PosStat& Q = st[K + 1 + i];
-        const double p = P.ex / (double(P.z) * scale);
-        const double q = Q.ex / (double(Q.z) * scale);
-        const double u = double(uniform53(a.seed, a.offset, uint64_t(b), uint64_t(i))) * 0x1p-53;
-        if (!(u < p / fmax(q, 1e-300))) {
-          jrej = i;
-          break;
-        }
-      }
+  // Accept tests u_i < p_i(x) / max(q_i(x), 1e-300), one lane per position
+  // (K <= 32), as the product form u_i * max(q, 1e-300) < p with
+  // p = ex_p / (Z_p 2^-F), q = ex_q / (Z_q 2^-F); the first failing position
+  // is the rejection.
+  if (tid < 32) {
+    const int i = tid;
+    int fl = 0;
+    for (int r = i; r < rows_per_b; r += 32) fl |= st[r].flags;
+    for (int o = 16; o; o >>= 1) fl |= __shfl_xor_sync(0xFFFFFFFFu, fl, o);
+    bool reject = false;
+    if (!fl && i < K) {
+      const PosStat& P = st[i];
+      const PosStat& Q = st[K + 1 + i];
+      const double zp = double(P.z) * (1.0 / double(kFixedOne));
+      const double zq = double(Q.z) * (1.0 / double(kFixedOne));
+      const double u = double(uniform53(a.seed, a.offset, uint64_t(b), uint64_t(i))) * 0x1p-53;
+      // u * max(ex_q / zq, 1e-300) < ex_p / zp, multiplied through by zp * zq > 0
+      const double lhs = Q.ex > 0.0 ? u * Q.ex * zp : u * 1e-300 * zp * zq;
+      reject = !(lhs < P.ex * zq);
     }
-    decision[0] = jrej;
-    decision[1] = flags;
+    const uint32_t rej = __ballot_sync(0xFFFFFFFFu, reject);
+    if (tid == 0) {
+      decision[0] = rej ? __ffs(rej) - 1 : K;
+      decision[1] = fl;
+    }
   }
   __syncthreads();
   const int jrej = decision[0];
   const int flags = decision[1];
-
   if (flags) {
-    if (rank == 0 && threadIdx.x == 0) {
+    if (tid == 0) {
       a.accepted[b] = -1;
       for (int i = 0; i <= K; ++i) a.ids[size_t(b) * (K + 1) + i] = -1;
       if (a.status) atomicOr(a.status, flags & (kRowNonFinite | kRowBadDraft | kRowTimeout));
     }
-    c.exchange();
     return;
   }
 
-  const int lo = int(rank) * a.slice;
-  int n = V - lo;
-  n = n < 0 ? 0 : (n > a.slice ? a.slice : n);
-  c.lo = lo;
-  c.n = n;
   const bool residual = jrej < K;
   const T* prow = logit_row<T>(a, b, jrej);               // p_j (or p_K for the bonus)
   const T* qrow = residual ? logit_row<T>(a, b, K + 1 + jrej) : prow;
   const PosStat P = st[jrej];
   const PosStat Q = residual ? st[K + 1 + jrej] : P;
-  const size_t slice_bytes = (size_t(a.slice) * sizeof(T) + 32 + 15) & ~size_t(15);
-  T* sp = reinterpret_cast<T*>(dyn_smem + slice_smem_offset(prow, lo, n));
-  T* sq = reinterpret_cast<T*>(dyn_smem + slice_bytes + slice_smem_offset(qrow, lo, n));
-  load_slice(prow, lo, n, sp);
-  if (residual) load_slice(qrow, lo, n, sq);
-  __syncthreads();
-  c.s = sp;
   const RowScale rp = make_row_scale(P.m, 1.0f);
   const RowScale rq = make_row_scale(Q.m, 1.0f);
+  // Thread t owns ids [c0, c1): a whole number of 16-byte groups of the row
+  // (rows whose base is not 16-byte aligned fall back to element loads).
+  constexpr int kPer = 16 / int(sizeof(T));
+  const bool vec_ok = ((reinterpret_cast<uintptr_t>(prow) | reinterpret_cast<uintptr_t>(qrow)) & 15) == 0;
+  const int per = (V + kResolveThreads - 1) / kResolveThreads;
+  const int chunk = (per + kPer - 1) / kPer * kPer;
+  const int c0 = min(V, tid * chunk), c1 = min(V, c0 + chunk);
 
-  // Weights of the final draw: max(0, p - q) scaled by Z_p Z_q (exact
-  // integers, eq. 39.4), or the target masses for the bonus draw.
+  // Weights in 31-bit fixed point: max(0, p - q) with p = e_p / Z_p and
+  // q = e_q / Z_q in binary32 (eq. 39.4), or e_p / Z_p for a draw from p.
+  // The sums are exact integers, so the scan and the walk agree.
   bool use_p = !residual;
-  auto w_res = [&](int i) -> u128 {
-    const u128 ep = u128(mass_fixed(Elem<T>::widen(sp[i]), rp, table)) * Q.z;
-    const u128 eq = u128(mass_fixed(Elem<T>::widen(sq[i]), rq, table)) * P.z;
-    return ep > eq ? ep - eq : u128(0);
+  const float inv_zp = float(double(kFixedOne) / double(P.z));
+  const float inv_zq = float(double(kFixedOne) / double(Q.z));
+  auto weight_of = [&](float zp, float zq) -> uint64_t {
+    const float p = __fmul_rn(exp_fast(zp, rp), inv_zp);
+    const float r = use_p ? p : fmaxf(0.0f, __fsub_rn(p, __fmul_rn(exp_fast(zq, rq), inv_zq)));
+    return uint64_t(__float2uint_rn(__fmul_rn(r, 0x1p31f)));
   };
-  auto w_p = [&](int i) -> u128 { return u128(mass_fixed(Elem<T>::widen(sp[i]), rp, table)); };
-  u128 local = 0, before = 0, total = 0;
-  if (residual) {
-    for (int i = threadIdx.x; i < n; i += kThreads) local += w_res(i);
-    total = cluster_sum128(c, local, &before);
-    if (total == 0) use_p = true;   // zero residual mass: draw from p_j
+  // Weights of ids [g, g + kPer) into w (ids >= c1 get 0); loads of a group issued together.
+  constexpr int kGroups = 32 / kPer;   // groups of kPer ids in flight per thread (32 ids)
+  auto chunk_sum = [&]() -> uint64_t {
+    uint64_t sum = 0;
+    for (int g0 = c0; g0 < c1; g0 += kGroups * kPer) {
+      float zp[kGroups][kPer], zq[kGroups][kPer];
+#pragma unroll
+      for (int gi = 0; gi < kGroups; ++gi) {
+        const int g = g0 + gi * kPer;
+#pragma unroll
+        for (int e = 0; e < kPer; ++e) {
+          zp[gi][e] = -INFINITY;
+          zq[gi][e] = -INFINITY;
+        }
+        if (g < c1) {
+          if (vec_ok && g + kPer <= V) {
+            const uint4 xp = __ldg(reinterpret_cast<const uint4*>(prow + g));
+            const uint4 xq = use_p ? xp : __ldg(reinterpret_cast<const uint4*>(qrow + g));
+#pragma unroll
+            for (int e = 0; e < kPer; ++e) {
+              zp[gi][e] = VecOps<T>::elem(xp, e);
+              zq[gi][e] = VecOps<T>::elem(xq, e);
+            }
+          } else {
+            for (int e = 0; e < kPer && g + e < c1; ++e) {
+              zp[gi][e] = Elem<T>::widen(prow[g + e]);
+              zq[gi][e] = Elem<T>::widen(qrow[g + e]);
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int gi = 0; gi < kGroups; ++gi)
+#pragma unroll
+        for (int e = 0; e < kPer; ++e) sum += weight_of(zp[gi][e], zq[gi][e]);
+    }
+    return sum;
+  };
+  uint64_t total = 0;
+  uint64_t local = chunk_sum();
+  uint64_t before = resolve_scan(local, warp_tot, &total);
+  if (residual && total == 0) {   // zero residual mass (rounding only): draw from p_j
+    use_p = true;
+    local = chunk_sum();
+    before = resolve_scan(local, warp_tot, &total);
   }
-  if (use_p) {
-    local = 0;
-    for (int i = threadIdx.x; i < n; i += kThreads) local += w_p(i);
-    total = cluster_sum128(c, local, &before);
-  }
-  const u128 mine = block_sum<u128>(local, sh.red128);
   const uint64_t u53 = uniform53(a.seed, a.offset, uint64_t(b), uint64_t(K));
-  const u128 t = scale_by_uniform(u53, total);
-  if (c.alive && mine > 0 && t >= before && t - before < mine) {
-    int idx;
-    if (use_p)
-      idx = find_crossing<T, u128>(c, t - before, w_p, sh.red128, reinterpret_cast<int*>(&sh.bcast32[7]));
-    else
-      idx = find_crossing<T, u128>(c, t - before, w_res, sh.red128, reinterpret_cast<int*>(&sh.bcast32[7]));
-    if (threadIdx.x == 0 && idx >= 0) a.ids[size_t(b) * (K + 1) + jrej] = lo + idx;
+  const uint64_t t = uint64_t((u128(u53) * total) >> 53);
+  // The chunk whose cumulative interval holds t is walked by warp 0, 32 ids
+  // per step: weights, a warp scan, the first id whose running total passes t.
+  if (tid == 0) owner = -1;
+  __syncthreads();
+  if (local > 0 && t >= before && t - before < local) {
+    owner = tid;
+    owner_before = before;
   }
-  if (rank == 0 && threadIdx.x == 0) {
-    a.accepted[b] = c.alive ? jrej : -1;
+  __syncthreads();
+  if (owner >= 0 && tid < 32) {
+    const int lane = tid;
+    const int o0 = min(V, owner * chunk), o1 = min(V, o0 + chunk);
+    uint64_t run = owner_before;
+    for (int base = o0; base < o1; base += 32) {
+      const int i = base + lane;
+      const uint64_t w = i < o1 ? weight_of(Elem<T>::widen(prow[i]), Elem<T>::widen(qrow[i])) : 0ull;
+      const uint64_t incl = warp_inclusive_scan<uint64_t>(w);
+      const uint32_t hit = __ballot_sync(0xFFFFFFFFu, i < o1 && run + incl > t);
+      if (hit) {
+        if (lane == __ffs(hit) - 1) a.ids[size_t(b) * (K + 1) + jrej] = i;
+        break;
+      }
+      run += __shfl_sync(0xFFFFFFFFu, incl, 31);
+    }
+  }
+  if (tid == 0) {
+    a.accepted[b] = jrej;
     for (int i = 0; i < jrej; ++i) a.ids[size_t(b) * (K + 1) + i] = a.drafts[size_t(b) * K + i];
     for (int i = jrej + 1; i <= K; ++i) a.ids[size_t(b) * (K + 1) + i] = -1;
-    if (!c.alive && a.status) atomicOr(a.status, kRowTimeout);
   }
-  c.exchange();
 }
 
 // ------------------------------------------------------------------ host side
-
-static LaunchShape verify_shape(int rows, int vocab, int elem, int num_sms, int buffers) {
-  LaunchShape ls;
-  int cluster = 1;
-  auto slice_of = [&](int cl) { return ((vocab + cl - 1) / cl + 15) / 16 * 16; };
-  while (cluster < kMaxCluster && size_t(slice_of(cluster)) * elem * buffers > kSliceTargetBytes)
-    cluster *= 2;
-  while (cluster < kMaxCluster && int64_t(rows) * cluster < 2 * num_sms &&
-         size_t(slice_of(cluster * 2)) * elem >= kSliceMinBytes)
-    cluster *= 2;
-  if (forced_cluster()) cluster = forced_cluster();
-  ls.cluster = cluster;
-  ls.slice = slice_of(cluster);
-  const size_t one = (size_t(ls.slice) * elem + 32 + 15) & ~size_t(15);
-  ls.smem = one * buffers;
-  ls.pdl = true;
-  return ls;
-}
 
 template <typename T>
 static smp_status launch_verify(VerifyArgs a, cudaStream_t stream) {
   const int dev = current_device();
   if (dev < 0) return fail_cuda(cudaGetLastError());
-  const int sms = device_sms(dev);
-  const int elem = int(sizeof(T));
   const int rows = a.batch * (2 * a.k + 1);
-  const LaunchShape lp = verify_shape(rows, a.vocab, elem, sms, 1);
-  const LaunchShape lr = verify_shape(a.batch, a.vocab, elem, sms, 2);
-  if (lp.smem > kMaxDynamicSmem || lr.smem > kMaxDynamicSmem) return SMP_ERR_UNSUPPORTED;
-  cudaError_t err = prepare_kernel(reinterpret_cast<const void*>(&verify_pos_kernel<T>), dev, lp);
-  if (err == cudaSuccess) err = prepare_kernel(reinterpret_cast<const void*>(&verify_resolve_kernel<T>), dev, lr);
+  LaunchShape ls;   // one CTA per logit row, then one per batch row; no dynamic shared memory
+  ls.pdl = true;
+  cudaError_t err;
+  err = launch_cluster(reinterpret_cast<const void*>(&verify_pos_kernel<T>), dim3(rows), dim3(kThreads), ls,
+                       stream, &a);
   if (err != cudaSuccess) return fail_cuda(err);
-  a.slice = lp.slice;
-  err = launch_cluster(reinterpret_cast<const void*>(&verify_pos_kernel<T>), dim3(rows * lp.cluster),
-                       dim3(kThreads), lp, stream, &a);
-  if (err != cudaSuccess) return fail_cuda(err);
-  a.slice = lr.slice;
-  err = launch_cluster(reinterpret_cast<const void*>(&verify_resolve_kernel<T>),
-                       dim3(a.batch * lr.cluster), dim3(kThreads), lr, stream, &a);
+  err = launch_cluster(reinterpret_cast<const void*>(&verify_resolve_kernel<T>), dim3(a.batch),
+                       dim3(kResolveThreads), ls, stream, &a);
   if (err != cudaSuccess) return fail_cuda(err);
   return SMP_OK;
 }

@@ -8,9 +8,10 @@
 //                          draft): the row maximum, the fixed-point mass Z
 //                          and the draft token's mass, written to the
 //                          workspace;
-//   verify_resolve_kernel  one CTA per batch row: the accept tests in order,
-//                          then the replacement draw from max(0, p_j - q_j) at
-//                          the first rejection j, or the bonus draw from p_K.
+//   verify_resolve_kernel  one cluster per batch row: the accept tests in
+//                          order, then the replacement draw from
+//                          max(0, p_j - q_j) at the first rejection j, or the
+//                          bonus draw from p_K.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -169,8 +170,9 @@ __global__ void __launch_bounds__(kThreads, 2) verify_pos_kernel(VerifyArgs a) {
   }
 }
 
-constexpr int kResolveThreads = 512;
+constexpr int kResolveThreads = 256;
 constexpr int kResolveWarps = kResolveThreads / 32;
+constexpr int kResolveMaxCluster = 8;   // CTAs (one cluster) per batch row
 
 // Exclusive prefix over the CTA of one u64 per thread (thread order), and the total.
 __device__ __forceinline__ uint64_t resolve_scan(uint64_t v, uint64_t* warp_tot, uint64_t* total) {
@@ -189,19 +191,41 @@ __device__ __forceinline__ uint64_t resolve_scan(uint64_t v, uint64_t* warp_tot,
   return before;
 }
 
-// One CTA per batch row: the accept tests of eq. 39.3 in position order, then
-// the replacement draw from max(0, p_j - q_j) (eq. 39.4) at the first
-// rejection j, or the bonus draw from p_K.  Thread t owns the token ids
-// [t C, (t + 1) C): weights are 31-bit fixed point with exact integer sums, a
-// CTA scan finds the owner of the crossing, and warp 0 walks that chunk.
+// Sum of one u64 per CTA of the cluster: this CTA's exclusive prefix (cluster
+// rank order) and the cluster total.  `slot` is this CTA's shared word; every
+// CTA reads every peer's word between two cluster barriers.
+__device__ __forceinline__ uint64_t cluster_prefix(uint64_t v, uint64_t* slot, uint64_t* total) {
+  const uint32_t rank = cluster_rank(), n = cluster_size();
+  if (threadIdx.x == 0) *slot = v;
+  hw_cluster_sync();
+  uint64_t before = 0, all = 0;
+  const uint32_t addr = smem_addr(slot);
+  for (uint32_t r = 0; r < n; ++r) {
+    const uint64_t t = ld_cluster_u64(map_rank(addr, r));
+    if (r < rank) before += t;
+    all += t;
+  }
+  hw_cluster_sync();   // no CTA rewrites its slot or exits while a peer may read it
+  *total = all;
+  return before;
+}
+
+// One cluster per batch row: the accept tests of eq. 39.3 in position order,
+// then the replacement draw from max(0, p_j - q_j) (eq. 39.4) at the first
+// rejection j, or the bonus draw from p_K.  Thread g of the cluster (rank-major)
+// owns the token ids [g C, (g + 1) C): weights are 31-bit fixed point with
+// exact integer sums; CTA and cluster scans find the chunk that holds the
+// draw, and warp 0 of its CTA walks it.
 template <typename T>
-__global__ void __launch_bounds__(kResolveThreads, 1) verify_resolve_kernel(VerifyArgs a) {
+__global__ void __launch_bounds__(kResolveThreads, 2) verify_resolve_kernel(VerifyArgs a) {
   __shared__ int32_t decision[2];   // first rejection j, row flags
   __shared__ uint64_t warp_tot[kResolveWarps];
+  __shared__ uint64_t cta_slot;
   __shared__ int owner;             // thread whose ids hold the draw
   __shared__ uint64_t owner_before;
   const int tid = threadIdx.x;
-  const int b = int(blockIdx.x);
+  const uint32_t rank = cluster_rank(), nranks = cluster_size();
+  const int b = int(blockIdx.x / nranks);
   const int K = a.k;
   const int V = a.vocab;
   const int rows_per_b = 2 * K + 1;
@@ -212,7 +236,7 @@ __global__ void __launch_bounds__(kResolveThreads, 1) verify_resolve_kernel(Veri
   // Accept tests u_i < p_i(x) / max(q_i(x), 1e-300), one lane per position
   // (K <= 32), as the product form u_i * max(q, 1e-300) < p with
   // p = ex_p / (Z_p 2^-F), q = ex_q / (Z_q 2^-F); the first failing position
-  // is the rejection.
+  // is the rejection.  Every CTA of the cluster decides alike.
   if (tid < 32) {
     const int i = tid;
     int fl = 0;
@@ -239,7 +263,7 @@ __global__ void __launch_bounds__(kResolveThreads, 1) verify_resolve_kernel(Veri
   const int jrej = decision[0];
   const int flags = decision[1];
   if (flags) {
-    if (tid == 0) {
+    if (rank == 0 && tid == 0) {
       a.accepted[b] = -1;
       for (int i = 0; i <= K; ++i) a.ids[size_t(b) * (K + 1) + i] = -1;
       if (a.status) atomicOr(a.status, flags & (kRowNonFinite | kRowBadDraft | kRowTimeout));
@@ -254,17 +278,19 @@ __global__ void __launch_bounds__(kResolveThreads, 1) verify_resolve_kernel(Veri
   const PosStat Q = residual ? st[K + 1 + jrej] : P;
   const RowScale rp = make_row_scale(P.m, 1.0f);
   const RowScale rq = make_row_scale(Q.m, 1.0f);
-  // Thread t owns ids [c0, c1): a whole number of 16-byte groups of the row
+  // Thread g owns ids [c0, c1): a whole number of 16-byte groups of the row
   // (rows whose base is not 16-byte aligned fall back to element loads).
   constexpr int kPer = 16 / int(sizeof(T));
   const bool vec_ok = ((reinterpret_cast<uintptr_t>(prow) | reinterpret_cast<uintptr_t>(qrow)) & 15) == 0;
-  const int per = (V + kResolveThreads - 1) / kResolveThreads;
+  const int nthreads = int(nranks) * kResolveThreads;
+  const int per = (V + nthreads - 1) / nthreads;
   const int chunk = (per + kPer - 1) / kPer * kPer;
-  const int c0 = min(V, tid * chunk), c1 = min(V, c0 + chunk);
+  const int g = int(rank) * kResolveThreads + tid;
+  const int c0 = min(V, g * chunk), c1 = min(V, c0 + chunk);
 
   // Weights in 31-bit fixed point: max(0, p - q) with p = e_p / Z_p and
   // q = e_q / Z_q in binary32 (eq. 39.4), or e_p / Z_p for a draw from p.
-  // The sums are exact integers, so the scan and the walk agree.
+  // The sums are exact integers, so the scans and the walk agree.
   bool use_p = !residual;
   const float inv_zp = float(double(kFixedOne) / double(P.z));
   const float inv_zq = float(double(kFixedOne) / double(Q.z));
@@ -273,7 +299,6 @@ __global__ void __launch_bounds__(kResolveThreads, 1) verify_resolve_kernel(Veri
     const float r = use_p ? p : fmaxf(0.0f, __fsub_rn(p, __fmul_rn(exp_fast(zq, rq), inv_zq)));
     return uint64_t(__float2uint_rn(__fmul_rn(r, 0x1p31f)));
   };
-  // Weights of ids [g, g + kPer) into w (ids >= c1 get 0); loads of a group issued together.
   constexpr int kGroups = 32 / kPer;   // groups of kPer ids in flight per thread (32 ids)
   auto chunk_sum = [&]() -> uint64_t {
     uint64_t sum = 0;
@@ -281,25 +306,25 @@ __global__ void __launch_bounds__(kResolveThreads, 1) verify_resolve_kernel(Veri
       float zp[kGroups][kPer], zq[kGroups][kPer];
 #pragma unroll
       for (int gi = 0; gi < kGroups; ++gi) {
-        const int g = g0 + gi * kPer;
+        const int gg = g0 + gi * kPer;
 #pragma unroll
         for (int e = 0; e < kPer; ++e) {
           zp[gi][e] = -INFINITY;
           zq[gi][e] = -INFINITY;
         }
-        if (g < c1) {
-          if (vec_ok && g + kPer <= V) {
-            const uint4 xp = __ldg(reinterpret_cast<const uint4*>(prow + g));
-            const uint4 xq = use_p ? xp : __ldg(reinterpret_cast<const uint4*>(qrow + g));
+        if (gg < c1) {
+          if (vec_ok && gg + kPer <= V) {
+            const uint4 xp = __ldg(reinterpret_cast<const uint4*>(prow + gg));
+            const uint4 xq = use_p ? xp : __ldg(reinterpret_cast<const uint4*>(qrow + gg));
 #pragma unroll
             for (int e = 0; e < kPer; ++e) {
               zp[gi][e] = VecOps<T>::elem(xp, e);
               zq[gi][e] = VecOps<T>::elem(xq, e);
             }
           } else {
-            for (int e = 0; e < kPer && g + e < c1; ++e) {
-              zp[gi][e] = Elem<T>::widen(prow[g + e]);
-              zq[gi][e] = Elem<T>::widen(qrow[g + e]);
+            for (int e = 0; e < kPer && gg + e < c1; ++e) {
+              zp[gi][e] = Elem<T>::widen(prow[gg + e]);
+              zq[gi][e] = Elem<T>::widen(qrow[gg + e]);
             }
           }
         }
@@ -311,18 +336,21 @@ __global__ void __launch_bounds__(kResolveThreads, 1) verify_resolve_kernel(Veri
     }
     return sum;
   };
-  uint64_t total = 0;
-  uint64_t local = chunk_sum();
-  uint64_t before = resolve_scan(local, warp_tot, &total);
+  uint64_t local = chunk_sum(), cta_total = 0, total = 0;
+  uint64_t before = resolve_scan(local, warp_tot, &cta_total);
+  uint64_t cta_before = cluster_prefix(cta_total, &cta_slot, &total);
   if (residual && total == 0) {   // zero residual mass (rounding only): draw from p_j
     use_p = true;
     local = chunk_sum();
-    before = resolve_scan(local, warp_tot, &total);
+    before = resolve_scan(local, warp_tot, &cta_total);
+    cta_before = cluster_prefix(cta_total, &cta_slot, &total);
   }
+  before += cta_before;
   const uint64_t u53 = uniform53(a.seed, a.offset, uint64_t(b), uint64_t(K));
   const uint64_t t = uint64_t((u128(u53) * total) >> 53);
-  // The chunk whose cumulative interval holds t is walked by warp 0, 32 ids
-  // per step: weights, a warp scan, the first id whose running total passes t.
+  // The chunk whose cumulative interval holds t is walked by warp 0 of its
+  // CTA, 32 ids per step: weights, a warp scan, the first id whose running
+  // total passes t.
   if (tid == 0) owner = -1;
   __syncthreads();
   if (local > 0 && t >= before && t - before < local) {
@@ -332,7 +360,7 @@ __global__ void __launch_bounds__(kResolveThreads, 1) verify_resolve_kernel(Veri
   __syncthreads();
   if (owner >= 0 && tid < 32) {
     const int lane = tid;
-    const int o0 = min(V, owner * chunk), o1 = min(V, o0 + chunk);
+    const int o0 = min(V, (int(rank) * kResolveThreads + owner) * chunk), o1 = min(V, o0 + chunk);
     uint64_t run = owner_before;
     for (int base = o0; base < o1; base += 32) {
       const int i = base + lane;
@@ -346,7 +374,7 @@ __global__ void __launch_bounds__(kResolveThreads, 1) verify_resolve_kernel(Veri
       run += __shfl_sync(0xFFFFFFFFu, incl, 31);
     }
   }
-  if (tid == 0) {
+  if (rank == 0 && tid == 0) {
     a.accepted[b] = jrej;
     for (int i = 0; i < jrej; ++i) a.ids[size_t(b) * (K + 1) + i] = a.drafts[size_t(b) * K + i];
     for (int i = jrej + 1; i <= K; ++i) a.ids[size_t(b) * (K + 1) + i] = -1;
@@ -366,8 +394,13 @@ static smp_status launch_verify(VerifyArgs a, cudaStream_t stream) {
   err = launch_cluster(reinterpret_cast<const void*>(&verify_pos_kernel<T>), dim3(rows), dim3(kThreads), ls,
                        stream, &a);
   if (err != cudaSuccess) return fail_cuda(err);
-  err = launch_cluster(reinterpret_cast<const void*>(&verify_resolve_kernel<T>), dim3(a.batch),
-                       dim3(kResolveThreads), ls, stream, &a);
+  // Enough CTAs per batch row to cover the GPU twice over, at most one portable cluster.
+  LaunchShape lr = ls;
+  const int sms = device_sms(dev);
+  while (lr.cluster < kResolveMaxCluster && int64_t(a.batch) * lr.cluster < 2 * sms) lr.cluster *= 2;
+  if (forced_cluster() && forced_cluster() <= kResolveMaxCluster) lr.cluster = forced_cluster();
+  err = launch_cluster(reinterpret_cast<const void*>(&verify_resolve_kernel<T>), dim3(a.batch * lr.cluster),
+                       dim3(kResolveThreads), lr, stream, &a);
   if (err != cudaSuccess) return fail_cuda(err);
   return SMP_OK;
 }

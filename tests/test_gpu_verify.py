@@ -103,3 +103,19 @@ def test_verify_output_follows_target_chi_square():
         target = over.softmax64(zp[pos]) * reached.sum()
         stat = float(np.sum((counts - target) ** 2 / target))
         assert stat < crit[vocab - 1], (pos, stat)
+
+
+def test_verify_results_do_not_depend_on_cluster_size(monkeypatch):
+    vb = workloads.verify_workload(batch=12, k=3, vocab=5003, dtype="f32", seed_id=31)
+    drafts = oracle_drafts(vb.values("q"), 1, 0)
+    outs = []
+    for cluster in ("1", "2", "4", "8"):
+        monkeypatch.setenv("SMP_FORCE_CLUSTER", cluster)
+        outs.append(run_verify(vb.p, vb.q, vb.dtype, drafts, 4, 9))
+    monkeypatch.delenv("SMP_FORCE_CLUSTER")
+    for acc, ids, status in outs:
+        assert status == 0
+        assert np.array_equal(acc, outs[0][0])
+        assert np.array_equal(ids, outs[0][1])
+    want = over.spec_verify(vb.values("p"), vb.values("q"), drafts, 4, 9)
+    compare_verify(want, outs[0][0], outs[0][1]).check()

@@ -14,7 +14,6 @@ constexpr int kThreads = 256;                 // threads per CTA
 constexpr int kWarps = kThreads / 32;
 constexpr int kFixedBits = 44;                // E = round(e * 2^44)
 constexpr uint64_t kFixedOne = 1ull << kFixedBits;
-constexpr int kMaxCluster = 16;
 
 // Row status flags (mirror SMP_ROW_* of smp.h).
 constexpr int kRowBadParams = 1;
@@ -97,14 +96,6 @@ __device__ __forceinline__ uint64_t philox_word0(uint64_t seed, uint64_t offset,
 __device__ __forceinline__ uint64_t uniform53(uint64_t seed, uint64_t offset, uint64_t row,
                                               uint64_t draw) {
   return philox_word0(seed, offset, row, draw) >> 11;
-}
-
-// floor(u * total) for u = U * 2^-53 and a 128-bit total.
-__device__ __forceinline__ u128 scale_by_uniform(uint64_t u53, u128 total) {
-  const uint64_t t_hi = uint64_t(total >> 64), t_lo = uint64_t(total);
-  const u128 a = u128(u53) * t_hi;     // < 2^117
-  const u128 b = u128(u53) * t_lo;     // < 2^117
-  return (a << 11) + (b >> 53);
 }
 
 // ------------------------------------------------------------------ double-float exponential
@@ -246,18 +237,6 @@ __device__ __forceinline__ uint64_t mass_fixed(float z, const RowScale& rs, cons
   return fixed_from_parts(exp_parts(z, rs, table, -float(kFixedBits + 3)));
 }
 
-// The fixed-point mass round(exp((z - m) / T) * 2^F) from the binary32
-// exp2f (relative error a few units in the last place, about 3e-7), for row
-// sums that need that accuracy rather than the double-float value.  The
-// argument is formed with the head + tail of log2(e) / T.
-__device__ __forceinline__ uint64_t mass_fast(float z, const RowScale& rs) {
-  const float d = __fsub_rn(z, rs.m);
-  if (d == 0.0f) return kFixedOne;
-  const float y = __fmaf_rn(d, rs.c_hi, __fmul_rn(d, rs.c_lo));
-  if (!(y > -float(kFixedBits + 3))) return 0;   // also -inf and NaN
-  return __float2ull_rn(__fmul_rn(exp2f(y), float(kFixedOne)));
-}
-
 // 2^y by the ex2.approx instruction (flushes results below 2^-126 to 0).
 __device__ __forceinline__ float ex2_approx(float y) {
   float r;
@@ -289,6 +268,9 @@ __device__ __forceinline__ void allow_dependent_launch() { asm volatile("griddep
 // kernel may run an extra producer warp that takes no part in it.
 __device__ __forceinline__ void cta_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory"); }
 
+// A global word written earlier in this kernel (by this CTA, before a barrier).
+__device__ __forceinline__ int32_t load_volatile(const int32_t* p) { return *reinterpret_cast<const volatile int32_t*>(p); }
+
 // cta_sync() that also returns how many of the kThreads threads passed `pred`.
 __device__ __forceinline__ int cta_sync_count(bool pred) {
   int r;
@@ -316,15 +298,6 @@ __device__ __forceinline__ u128 shfl_xor_u128(u128 v, int mask) {
   const uint64_t lo = shfl_xor_u64(uint64_t(v), mask);
   const uint64_t hi = shfl_xor_u64(uint64_t(v >> 64), mask);
   return (u128(hi) << 64) | lo;
-}
-
-__device__ __forceinline__ u128 shfl_u128(u128 v, int src) {
-  const uint64_t lo = uint64_t(v), hi = uint64_t(v >> 64);
-  const uint64_t lo2 = (uint64_t(__shfl_sync(0xFFFFFFFFu, uint32_t(lo >> 32), src)) << 32) |
-                       __shfl_sync(0xFFFFFFFFu, uint32_t(lo), src);
-  const uint64_t hi2 = (uint64_t(__shfl_sync(0xFFFFFFFFu, uint32_t(hi >> 32), src)) << 32) |
-                       __shfl_sync(0xFFFFFFFFu, uint32_t(hi), src);
-  return (u128(hi2) << 64) | lo2;
 }
 
 __device__ __forceinline__ u128 shfl_up_u128(u128 v, int delta) {
@@ -394,43 +367,9 @@ __device__ __forceinline__ u128 warp_inclusive_scan<u128>(u128 v) {
   return v;
 }
 
-// Sum over the CTA; every thread gets the result.  `scratch` holds kWarps values.
-template <typename U>
-__device__ __forceinline__ U block_sum(U v, U* scratch) {
-  v = warp_sum<U>(v);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  cta_sync();
-  if (lane == 0) scratch[warp] = v;
-  cta_sync();
-  U total = 0;
-#pragma unroll
-  for (int w = 0; w < kWarps; ++w) total += scratch[w];
-  return total;
-}
-
 // Largest key, lowest id among equal keys, packed as (key << 32) | ~id.
 // Warp-aggregated shared-memory updates.  Every lane of the warp must call
 // these together; many lanes hitting one address would otherwise serialise.
-
-// hist[digit] += 1 for every lane with `valid`: one atomic per distinct digit.
-__device__ __forceinline__ void warp_hist_add(uint32_t* hist, uint32_t digit, bool valid) {
-  const uint32_t peers = __match_any_sync(0xFFFFFFFFu, valid ? digit : 0xFFFFFFFFu);
-  const int lane = threadIdx.x & 31;
-  if (valid && lane == __ffs(peers) - 1) atomicAdd(&hist[digit], uint32_t(__popc(peers)));
-}
-
-// Reserves one slot of a list counted by *counter for every lane with
-// `take`; returns the lane's slot (undefined for the others).
-__device__ __forceinline__ uint32_t warp_append(uint32_t* counter, bool take) {
-  const uint32_t m = __ballot_sync(0xFFFFFFFFu, take);
-  if (m == 0) return 0;
-  const int lane = threadIdx.x & 31;
-  const int leader = __ffs(m) - 1;
-  uint32_t base = 0;
-  if (lane == leader) base = atomicAdd(counter, uint32_t(__popc(m)));
-  base = __shfl_sync(0xFFFFFFFFu, base, leader);
-  return base + uint32_t(__popc(m & ((1u << lane) - 1u)));
-}
 
 __device__ __forceinline__ uint64_t pack_key_id(uint32_t key, uint32_t id) {
   return (uint64_t(key) << 32) | uint64_t(~id);
@@ -484,12 +423,6 @@ __device__ __forceinline__ uint32_t map_rank(uint32_t addr, uint32_t rank) {
   return r;
 }
 
-__device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t addr) {
-  uint32_t v;
-  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
-  return v;
-}
-
 __device__ __forceinline__ uint64_t ld_cluster_u64(uint32_t addr) {
   uint64_t v;
   asm volatile("ld.shared::cluster.u64 %0, [%1];" : "=l"(v) : "r"(addr) : "memory");
@@ -508,78 +441,8 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s
 
-// Wait until the mbarrier at `addr` completes the phase of parity `parity`.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t addr, uint32_t parity) {
-  const uint64_t t0 = global_timer_ns();
-  for (uint32_t it = 0;; ++it) {
-    uint32_t done;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(done)
-        : "r"(addr), "r"(parity)
-        : "memory");
-    if (done) return true;
-    if ((it & 255u) == 255u && global_timer_ns() - t0 > kWaitLimitNs) return false;
-  }
-}
-
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
 }
-
-// Arrive (release, cluster scope) on the mbarrier at `bar` in the CTA of cluster rank `rank`.
-__device__ __forceinline__ void mbar_arrive_rank(const uint64_t* bar, uint32_t rank) {
-  const uint32_t remote = map_rank(smem_addr(bar), rank);
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote) : "memory");
-}
-
-// A group of CTAs of one cluster (cluster ranks first .. first + ranks - 1)
-// that synchronise through one mbarrier per CTA.
-struct ClusterBarrier {
-  uint64_t* bar;      // this CTA's mbarrier (shared memory)
-  uint32_t parity;
-  uint32_t ranks;
-  uint32_t first;
-  int* ok;            // shared flag: 0 after a timeout
-
-  // Thread 0 initialises this CTA's mbarrier.  Before the first sync() every
-  // member's barrier must be initialised and visible: the caller issues
-  // fence.mbarrier_init and a cluster-wide synchronisation.
-  __device__ void setup(uint64_t* mbar, int* ok_flag, uint32_t first_rank, uint32_t nranks) {
-    bar = mbar;
-    ok = ok_flag;
-    ranks = nranks;
-    first = first_rank;
-    parity = 0;
-    if (threadIdx.x == 0) {
-      mbar_init(bar, nranks);
-      *ok = 1;
-    }
-  }
-
-  // setup() for the whole cluster, followed by the fence and cluster sync.
-  __device__ void init(uint64_t* mbar, int* ok_flag, uint32_t nranks) {
-    setup(mbar, ok_flag, 0, nranks);
-    if (threadIdx.x == 0) asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    cta_sync();
-    hw_cluster_sync();   // every peer's mbarrier exists before any remote arrive
-  }
-
-  // All members reach this point; writes made before it are visible to every
-  // member after it.  Returns false after a timeout.
-  __device__ bool sync() {
-    cta_sync();
-    if (threadIdx.x == 0) {
-      asm volatile("fence.acq_rel.cluster;" ::: "memory");
-      for (uint32_t r = 0; r < ranks; ++r) mbar_arrive_rank(bar, first + r);
-      if (!mbar_wait_bounded(smem_addr(bar), parity)) *ok = 0;
-    }
-    cta_sync();
-    parity ^= 1u;
-    return *ok != 0;
-  }
-};
 
 }  // namespace smp

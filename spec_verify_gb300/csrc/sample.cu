@@ -36,6 +36,9 @@ constexpr int kCandMax = 1024;    // candidate list capacity per row
 constexpr int kFinalMax = kThreads;   // candidates at or above the final threshold (one per thread)
 constexpr int kSegs = 8;          // segment maxima kept per lane and row (min-p / top-k rows)
 constexpr int kFastTopK = 128;    // top-k rows up to this k take the candidate path
+// out_ids value that marks a row for the general path at the end of the CTA's
+// rows (never a result: results are token ids >= 0, or -1).
+constexpr int32_t kHandOff = int32_t(0x80000000u);
 
 struct SampleArgs {
   const void* logits;
@@ -126,16 +129,6 @@ __device__ __forceinline__ bool wait_full(uint64_t* bar, uint32_t parity) {
 // ------------------------------------------------------------------ vector passes
 
 
-// Largest packed (key, ~id) of a slice (shared or global memory).
-template <typename T>
-__device__ uint64_t slice_best(const T* s, int n, int lo) {
-  uint64_t best = 0;
-  for (int i = threadIdx.x; i < n; i += kThreads) {
-    const uint64_t p = pack_key_id(elem_key<T>(s[i]), uint32_t(lo + i));
-    best = p > best ? p : best;
-  }
-  return best;
-}
 
 // Smallest key whose value z satisfies exp((z - m) / T) >= min_p, i.e. the
 // min-p threshold p_i >= min_p * max_j p_j ("Inference: Sampling, the KV
@@ -143,7 +136,7 @@ __device__ uint64_t slice_best(const T* s, int n, int lo) {
 // expressed on logits.  Warp 0 probes 32 keys per step, starting around the
 // estimate m + T ln(min_p); every thread gets the result.
 template <typename T>
-__device__ uint32_t minp_threshold_key(RowShared* sh, const FloatPair* table, const RowScale& rs, float temperature,
+__device__ uint32_t minp_threshold_key(uint32_t* bcast, const FloatPair* table, const RowScale& rs, float temperature,
                                        float min_p, uint32_t key_max) {
   if (threadIdx.x < 32) {
     const int lane = threadIdx.x;
@@ -176,10 +169,10 @@ __device__ uint32_t minp_threshold_key(RowShared* sh, const FloatPair* table, co
       stride = uint32_t((span + 31) / 32);
       start = lo;
     }
-    if (lane == 0) sh->bcast32[6] = hi;
+    if (lane == 0) bcast[6] = hi;
   }
   cta_sync();
-  const uint32_t r = sh->bcast32[6];
+  const uint32_t r = bcast[6];
   cta_sync();
   return r;
 }
@@ -193,153 +186,25 @@ __device__ __forceinline__ void write_error_row(const SampleArgs& a, int b, int 
 
 // ------------------------------------------------------------------ general path
 
-// One row by exact radix selection across the group of CTAs of `c`, each
-// holding its slice at c.s.  `best` is this CTA's packed (key, ~id) maximum.
-template <typename T>
-__device__ void general_row(RowCtx<T>& c, const SampleArgs& a, int b, const smp_row_params& prm, uint64_t best) {
-  RowShared& sh = *c.sh;
-  const int V = a.vocab;
-  const T* s = c.s;
-  const int n = c.n, lo = c.lo;
-  best = cluster_max(c, best);
-  const uint32_t key_max = uint32_t(best >> 32);
-  const uint32_t argmax = ~uint32_t(best);
-  const bool greedy = row_is_greedy(prm);
-
-  int flags = 0;
-  if (!c.alive) flags |= kRowTimeout;
-  else if (!key_finite<T>(key_max)) flags |= kRowNonFinite;
-  else if (!greedy && !sampling_params_valid(prm)) flags |= kRowBadParams;
-
-  if (flags == 0 && greedy) {
-    if (c.rank == 0 && threadIdx.x == 0) {
-      a.out_ids[b] = int32_t(argmax);
-      if (a.out_probs) a.out_probs[b] = 1.0f;
-      if (a.kept) a.kept[b] = 1;
-    }
-    if (a.full_probs) {
-      float* f = a.full_probs + size_t(b) * V + lo;
-      for (int i = threadIdx.x; i < n; i += kThreads) f[i] = (uint32_t(lo + i) == argmax) ? 1.0f : 0.0f;
-    }
-    c.exchange();
-    return;
-  }
-
-  if (flags == 0) {
-    const float m = key_value<T>(key_max);
-    const RowScale rs = make_row_scale(m, prm.temperature);
-    const bool topk = prm.top_k > 0 && prm.top_k < V;
-    const bool topp = prm.top_p < 1.0f;
-    const bool minp = prm.min_p > 0.0f && prm.min_p < 1.0f;
-    uint32_t key_min_p = 0;
-    if (minp) key_min_p = minp_threshold_key<T>(&sh, c.table, rs, prm.temperature, prm.min_p, key_max);
-
-    // Row statistics: size of the min-p set and the total mass Z.
-    uint64_t stats[4] = {0, 0, 0, 0};
-    if (minp || topp) {
-      uint64_t cnt = 0, z = 0;
-      for (int i = threadIdx.x; i < n; i += kThreads) {
-        const T v = s[i];
-        if (minp && elem_key<T>(v) >= key_min_p) ++cnt;
-        if (topp) z += mass_fixed(Elem<T>::widen(v), rs, c.table);
-      }
-      stats[0] = cnt;
-      stats[1] = z;
-      cluster_sum4(c, stats, 2, nullptr);
-    }
-    const uint64_t len_m = minp ? stats[0] : uint64_t(V);
-    const uint64_t z_total = stats[1];
-
-    Boundary bk{}, bp{};
-    uint64_t len_k = uint64_t(V), len_p = uint64_t(V);
-    if (topk) {
-      bk = radix_select<T, false>(c, uint32_t(prm.top_k), MassTarget{}, rs);
-      len_k = uint64_t(prm.top_k);
-    }
-    if (topp) {
-      const MassTarget tgt = make_mass_target(prm.top_p, z_total);
-      bp = radix_select<T, true>(c, 0, tgt, rs);
-      len_p = uint64_t(bp.above) + bp.n;
-    }
-    // The kept set is the shortest of the prefixes (eq. 39.2 on the
-    // intersection of the masks).
-    uint64_t len = len_k < len_p ? len_k : len_p;
-    len = len < len_m ? len : len_m;
-    int mode = 0;   // 0: all; 1: key >= key_min_p; 2: boundary (key, id_cut)
-    Boundary bd{};
-    if (len < uint64_t(V)) {
-      if (minp && len == len_m) mode = 1;
-      else {
-        mode = 2;
-        bd = (topk && len == len_k) ? bk : bp;
-      }
-    }
-    uint32_t id_cut = 0xFFFFFFFFu;
-    if (mode == 2 && bd.n < bd.tie_total) {
-      uint32_t mine = 0xFFFFFFFFu;
-      if (bd.n > bd.tie_base && bd.n <= bd.tie_base + bd.tie_local)
-        mine = nth_with_key(c, bd.key, bd.n - bd.tie_base);
-      id_cut = cluster_min_id(c, mine);
-    }
-    auto kept = [&](int i) -> bool {
-      if (mode == 0) return true;
-      const uint32_t key = elem_key<T>(s[i]);
-      if (mode == 1) return key >= key_min_p;
-      return key > bd.key || (key == bd.key && uint32_t(lo + i) <= id_cut);
-    };
-    auto weight = [&](int i) -> uint64_t {
-      return kept(i) ? mass_fixed(Elem<T>::widen(s[i]), rs, c.table) : 0ull;
-    };
-
-    // Kept mass Z_S of this CTA, of the row, and the prefix over CTAs.
-    uint64_t zs = 0;
-    for (int i = threadIdx.x; i < n; i += kThreads) zs += weight(i);
-    uint64_t tot[4] = {zs, 0, 0, 0};
-    uint64_t z_before = 0, z_local = 0;
-    cluster_sum4(c, tot, 1, &z_before, &z_local);
-    const uint64_t z_kept = tot[0];
-
-    // The draw: the first kept token (id order) whose running mass exceeds
-    // t = floor(u * Z_S), u = Philox draw 0 of row b.
-    const uint64_t u53 = uniform53(a.seed, a.offset, uint64_t(b), 0);
-    const uint64_t t = uint64_t((u128(u53) * z_kept) >> 53);
-    if (c.alive && z_local > 0 && t >= z_before && t - z_before < z_local) {
-      const int idx = find_crossing<T, uint64_t>(c, t - z_before, weight, sh.red64,
-                                                 reinterpret_cast<int*>(&sh.bcast32[7]));
-      if (threadIdx.x == 0 && idx >= 0) {
-        const uint64_t e = weight(idx);
-        a.out_ids[b] = lo + idx;
-        if (a.out_probs) a.out_probs[b] = float(double(e) / double(z_kept));
-      }
-    }
-    if (a.kept && c.rank == 0 && threadIdx.x == 0) a.kept[b] = int32_t(len);
-    if (a.full_probs) {
-      float* f = a.full_probs + size_t(b) * V + lo;
-      const float zf = float(z_kept);
-      for (int i = threadIdx.x; i < n; i += kThreads) {
-        const uint64_t e = weight(i);
-        f[i] = e ? __fdiv_rn(float(e), zf) : 0.0f;
-      }
-    }
-    if (!c.alive) flags |= kRowTimeout;
-  }
-
-  if (flags) {
-    if (c.rank == 0 && threadIdx.x == 0) write_error_row(a, b, flags);
-    if (a.full_probs && !(flags & kRowTimeout)) {
-      float* f = a.full_probs + size_t(b) * V + lo;
-      for (int i = threadIdx.x; i < n; i += kThreads) f[i] = __int_as_float(0x7FC00000);
-    }
-  }
-  c.exchange();   // no CTA moves on while a peer may still read its mailboxes
+// Sum of one u32 per thread over the CTA (every thread gets it).
+__device__ __forceinline__ uint32_t block_sum_u32(uint32_t v, uint32_t* scratch) {
+  v = warp_sum<uint32_t>(v);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  cta_sync();
+  if (lane == 0) scratch[warp] = v;
+  cta_sync();
+  uint32_t t = 0;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) t += scratch[w];
+  return t;
 }
+
+#include "general.cuh"
 
 // ------------------------------------------------------------------ candidate path
 
 struct StreamShared {
   uint64_t full[kBufs];       // TMA completion of each batch buffer
-  uint64_t solo_bar;          // barrier of the single-CTA general path
-  int solo_ok;
   int timeout;                // a wait ran out of time
   uint32_t cand_n;            // candidates appended for the current row (> kCandMax: overflow)
   uint32_t fin_n;             // candidates at or above the final threshold
@@ -348,14 +213,15 @@ struct StreamShared {
   uint64_t u53;               // the row's uniform (53-bit integer) for the draw
   float c_hi, c_lo;           // log2(e) / T of the row, head and tail
   uint32_t qn;                // segments to read again
+  uint32_t handoffs;          // rows of this CTA marked for the general path
   float red[kWarps];
   uint32_t redu[kWarps];
   uint64_t red64[kWarps];
   uint32_t bc[2];
 };
 
-// Candidate lists of a candidate-path row.  They are never live while the
-// general path works on a row, so the two share their storage.
+// Candidate lists of a candidate-path row.  The general path runs after the
+// last of them and shares their storage.
 struct CandShared {
   float seg[kSegs][kThreads];   // per-lane segment maxima of the row being streamed
   uint32_t q[kThreads];         // segments to read again: lane | segment << 8
@@ -371,8 +237,8 @@ struct CandShared {
 };
 
 union RowScratch {
-  RowShared row;
   CandShared cand;
+  GenShared gen;
 };
 
 // Byte layout of a row: the 16-byte aligned middle [a0, a1) streams through
@@ -406,18 +272,6 @@ __device__ __forceinline__ RowGeom row_geom(const SampleArgs& a, int row) {
   return g;
 }
 
-// Sum of one u32 per thread over the CTA (every thread gets it).
-__device__ __forceinline__ uint32_t block_sum_u32(uint32_t v, uint32_t* scratch) {
-  v = warp_sum<uint32_t>(v);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  cta_sync();
-  if (lane == 0) scratch[warp] = v;
-  cta_sync();
-  uint32_t t = 0;
-#pragma unroll
-  for (int w = 0; w < kWarps; ++w) t += scratch[w];
-  return t;
-}
 
 // The k-th largest of vals[0..n) (1 <= k <= n), exactly, as a float: radix
 // selection over the order keys with 8-bit digits (two levels for bf16
@@ -624,8 +478,9 @@ __device__ __forceinline__ float kth_largest(float x, int k) {
 // A warp gathers its candidates of a batch in a per-lane bit mask and appends
 // them with one atomic.  Every threshold is a lower bound of the kept set's
 // boundary, so the candidates contain the kept set; the end of the row selects
-// it exactly.  General-path rows, and rows whose candidates overflow, run the
-// exact radix selection of general_row on this CTA over global memory.
+// it exactly.  General-path rows, and rows whose candidates overflow, are
+// marked (out_ids = kHandOff) and taken by the general path once the CTA's
+// candidate-path rows are done, so that none of its state is live across it.
 
 // Cursor over the batches of this CTA's candidate-path rows (thread 0 only).
 template <typename T>
@@ -678,7 +533,6 @@ __global__ void __launch_bounds__(kThreads, 2) sample_kernel(SampleArgs a) {
   __shared__ StreamShared ss;
   __shared__ FloatPair table[64];
   __shared__ RowScratch scratch;
-  RowShared& sh = scratch.row;
   CandShared& cs = scratch.cand;
   using V = VecOps<T>;
   constexpr int kPer = V::kPer;
@@ -697,32 +551,21 @@ __global__ void __launch_bounds__(kThreads, 2) sample_kernel(SampleArgs a) {
     cur.begin(a);
     for (int i = 0; i < kBufs; ++i) cur.issue(a, ring + size_t(i) * kBufBytes, &ss.full[i]);
     ss.timeout = 0;
+    ss.handoffs = 0;
   }
   allow_dependent_launch();
   if (tid < 64) table[tid] = kExp2Table[tid];
-  ClusterBarrier solo;
-  solo.setup(&ss.solo_bar, &ss.solo_ok, cluster_rank(), 1);
   cta_sync();
 
   uint32_t consumed = 0;   // batches consumed so far (the buffers' running index)
   bool alive = true;
-  for (int row = blockIdx.x; row < B && alive; row += gridDim.x) {
+  int row = blockIdx.x;   // after the loop: the row a wait ran out of time on
+  for (; row < B && alive; row += gridDim.x) {
     const smp_row_params prm = a.params[row];
     const RowGeom geo = row_geom<T>(a, row);
     const bool first = row == int(blockIdx.x);
     const bool fast = row_is_fast(prm, Vn);
-    RowCtx<T> sc;
-    sc.sh = &sh;
-    sc.table = table;
-    sc.rank = 0;
-    sc.nranks = 1;
-    sc.first = cluster_rank();
-    sc.cb = &solo;
-    sc.mb = 0;
-    sc.alive = true;
-    sc.s = reinterpret_cast<const T*>(geo.r0);
-    sc.n = Vn;
-    sc.lo = 0;
+    const T* rowp = reinterpret_cast<const T*>(geo.r0);
     if (!fast) {
       if (first && geo.nchunks > 0) {
         // Let the speculative copies land and hand their buffers to the next rows.
@@ -745,8 +588,10 @@ __global__ void __launch_bounds__(kThreads, 2) sample_kernel(SampleArgs a) {
         }
         consumed += uint32_t(spec);
       }
-      general_row<T>(sc, a, row, prm, slice_best<T>(sc.s, Vn, 0));
-      alive = sc.alive;
+      if (tid == 0) {
+        a.out_ids[row] = kHandOff;
+        ++ss.handoffs;
+      }
       continue;
     }
     const bool greedy = row_is_greedy(prm);
@@ -836,11 +681,11 @@ __global__ void __launch_bounds__(kThreads, 2) sample_kernel(SampleArgs a) {
       // Elements outside the aligned middle; then the CTA-wide (max, lowest id).
       uint64_t best = pack_key_id(key_of_bits(__float_as_uint(best_z)), best_id);
       for (int i = tid; i < geo.head; i += kThreads) {
-        const uint64_t p = pack_key_id(key_of_bits(__float_as_uint(Elem<T>::widen(sc.s[i]))), uint32_t(i));
+        const uint64_t p = pack_key_id(key_of_bits(__float_as_uint(Elem<T>::widen(rowp[i]))), uint32_t(i));
         best = p > best ? p : best;
       }
       for (int i = geo.tail0 + tid; i < Vn; i += kThreads) {
-        const uint64_t p = pack_key_id(key_of_bits(__float_as_uint(Elem<T>::widen(sc.s[i]))), uint32_t(i));
+        const uint64_t p = pack_key_id(key_of_bits(__float_as_uint(Elem<T>::widen(rowp[i]))), uint32_t(i));
         best = p > best ? p : best;
       }
       best = block_max_u64(best, ss.red64);
@@ -869,8 +714,8 @@ __global__ void __launch_bounds__(kThreads, 2) sample_kernel(SampleArgs a) {
     const bool edges = geo.head > 0 || geo.tail0 < Vn;
     if (edges) {
       float emax = -INFINITY;
-      for (int i = tid; i < geo.head; i += kThreads) emax = fmaxf(emax, Elem<T>::widen(sc.s[i]));
-      for (int i = geo.tail0 + tid; i < Vn; i += kThreads) emax = fmaxf(emax, Elem<T>::widen(sc.s[i]));
+      for (int i = tid; i < geo.head; i += kThreads) emax = fmaxf(emax, Elem<T>::widen(rowp[i]));
+      for (int i = geo.tail0 + tid; i < Vn; i += kThreads) emax = fmaxf(emax, Elem<T>::widen(rowp[i]));
       run_max = fmaxf(run_max, block_max_f(emax, ss.red));
     }
     // A lower bound theta of the kept set's boundary: min-p's at the row
@@ -928,29 +773,47 @@ __global__ void __launch_bounds__(kThreads, 2) sample_kernel(SampleArgs a) {
         }
       }
       for (int i = tid; i < geo.head; i += kThreads) {
-        const float z = Elem<T>::widen(sc.s[i]);
+        const float z = Elem<T>::widen(rowp[i]);
         if (z >= theta) push_candidate(ss, cs, uint32_t(i), z);
       }
       for (int i = geo.tail0 + tid; i < Vn; i += kThreads) {
-        const float z = Elem<T>::widen(sc.s[i]);
+        const float z = Elem<T>::widen(rowp[i]);
         if (z >= theta) push_candidate(ss, cs, uint32_t(i), z);
       }
     }
     cta_sync();
-    if (!finalize_candidates<T>(ss, cs, table, a, row, prm, run_max)) {
-      cta_sync();
-      general_row<T>(sc, a, row, prm, slice_best<T>(sc.s, Vn, 0));
-      alive = sc.alive;
+    if (!finalize_candidates<T>(ss, cs, table, a, row, prm, run_max) && tid == 0) {
+      a.out_ids[row] = kHandOff;
+      ++ss.handoffs;
     }
     cta_sync();
   }
+  // Thread 0 marks rows and counts them without a barrier after the last
+  // row: every thread must see the same marks and count before it branches.
+  cta_sync();
   if (!alive) {
-    // A wait ran out of time: report it and let the copies in flight land.
-    if (tid == 0) {
-      if (a.status) atomicOr(a.status, kRowTimeout);
+    // A wait ran out of time: let the copies in flight land, and give the
+    // rows from that one on, and the marked rows, the error result.
+    if (tid == 0)
       for (uint32_t k = consumed; k < cur.issued; ++k) wait_full(&ss.full[k % kBufs], (k / kBufs) & 1);
+    for (int r = blockIdx.x; r < B; r += gridDim.x) {
+      if (r < row && load_volatile(a.out_ids + r) != kHandOff) continue;
+      cta_sync();
+      if (tid == 0) write_error_row(a, r, kRowTimeout);
+      if (a.full_probs)
+        for (int i = tid; i < Vn; i += kThreads) a.full_probs[size_t(r) * Vn + i] = __int_as_float(0x7FC00000);
     }
     cta_sync();
+    return;
+  }
+  // The marked rows, by the general path (its state overlays the candidate lists).
+  if (ss.handoffs == 0) return;
+  for (int r = blockIdx.x; r < B; r += gridDim.x) {
+    // Every thread reads the mark before the row's first barrier; the row's
+    // result replaces it only after later barriers.
+    if (load_volatile(a.out_ids + r) != kHandOff) continue;
+    const smp_row_params prm = a.params[r];
+    general_row<T>(scratch.gen, table, a, r, prm);
   }
 }
 

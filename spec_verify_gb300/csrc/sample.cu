@@ -500,9 +500,10 @@ struct BatchCursor {
     policy = evict_first_policy();
   }
   // The first row's knobs are known: a general-path row stops after the
-  // batches already requested.
+  // batches already requested.  When the ring is deeper than that row, the
+  // cursor has moved on to later rows, whose knobs it read: nothing to stop.
   __device__ void known(bool fast) {
-    if (!fast) nbatch = batch;
+    if (!fast && row == int(blockIdx.x)) nbatch = batch;
   }
   __device__ void settle(const SampleArgs& a) {
     while (row < a.batch && batch >= nbatch) {

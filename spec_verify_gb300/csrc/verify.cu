@@ -213,7 +213,7 @@ __device__ __forceinline__ uint64_t cluster_prefix(uint64_t v, uint64_t* slot, u
 // One cluster per batch row: the accept tests of eq. 39.3 in position order,
 // then the replacement draw from max(0, p_j - q_j) (eq. 39.4) at the first
 // rejection j, or the bonus draw from p_K.  Thread g of the cluster (rank-major)
-// owns the token ids [g C, (g + 1) C): weights are 31-bit fixed point with
+// owns the token ids [g C, (g + 1) C): weights are 52-bit fixed point with
 // exact integer sums; CTA and cluster scans find the chunk that holds the
 // draw, and warp 0 of its CTA walks it.
 template <typename T>
@@ -288,16 +288,18 @@ __global__ void __launch_bounds__(kResolveThreads, 2) verify_resolve_kernel(Veri
   const int g = int(rank) * kResolveThreads + tid;
   const int c0 = min(V, g * chunk), c1 = min(V, c0 + chunk);
 
-  // Weights in 31-bit fixed point: max(0, p - q) with p = e_p / Z_p and
-  // q = e_q / Z_q in binary32 (eq. 39.4), or e_p / Z_p for a draw from p.
-  // The sums are exact integers, so the scans and the walk agree.
+  // Weights in fixed point with 52 fraction bits: max(0, p - q) with
+  // p = e_p / Z_p and q = e_q / Z_q in binary32 (eq. 39.4), or e_p / Z_p for a
+  // draw from p.  r * 2^52 is the binary32 r exactly for r >= 2^-28 (below,
+  // within 2^-53), and the row's total stays below 2^53 because the p sum to
+  // 1.  The sums are exact integers, so the scans and the walk agree.
   bool use_p = !residual;
   const float inv_zp = float(double(kFixedOne) / double(P.z));
   const float inv_zq = float(double(kFixedOne) / double(Q.z));
   auto weight_of = [&](float zp, float zq) -> uint64_t {
     const float p = __fmul_rn(exp_fast(zp, rp), inv_zp);
     const float r = use_p ? p : fmaxf(0.0f, __fsub_rn(p, __fmul_rn(exp_fast(zq, rq), inv_zq)));
-    return uint64_t(__float2uint_rn(__fmul_rn(r, 0x1p31f)));
+    return __float2ull_rn(__fmul_rn(r, 0x1p52f));
   };
   constexpr int kGroups = 32 / kPer;   // groups of kPer ids in flight per thread (32 ids)
   auto chunk_sum = [&]() -> uint64_t {

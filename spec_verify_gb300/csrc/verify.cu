@@ -62,9 +62,10 @@ __device__ __forceinline__ uint4 load_stream(const uint4* p) {
   return x;
 }
 
-// One CTA per logit row.  Pass 1 streams the row from HBM for its maximum;
-// pass 2 reads it again (now in L2) for the fixed-point mass Z.  Thread 0
-// adds the draft token's mass (double-float exponential) and the flags.
+// One CTA per logit row, one pass over it: the maximum and the fixed-point
+// mass Z (online: a running maximum per thread, its sum rescaled when the
+// maximum rises).  Thread 0 adds the draft token's mass (double-float
+// exponential) and the flags.
 template <typename T>
 __global__ void __launch_bounds__(kThreads, 2) verify_pos_kernel(VerifyArgs a) {
   using V = VecOps<T>;
@@ -95,7 +96,25 @@ __global__ void __launch_bounds__(kThreads, 2) verify_pos_kernel(VerifyArgs a) {
   const uint4* vec = reinterpret_cast<const uint4*>(m0);
   const uint32_t ninf = V::neg_inf();
 
-  uint32_t pm = ninf;
+  // The draft token's logit, requested now so that the load overlaps the stream.
+  const int ipos = j <= a.k ? j : j - a.k - 1;   // draft position of this row
+  int xd = -1;
+  float zx = -INFINITY;
+  if (tid == 0 && ipos < a.k) {
+    xd = a.drafts[size_t(b) * a.k + ipos];
+    if (xd >= 0 && xd < Vn) zx = Elem<T>::widen(row[xd]);
+  }
+
+  // One pass over the row: each thread keeps a running maximum (rs.m) and
+  // the binary32 sum st of exp(z - rs.m) over its elements, rescaled when the
+  // maximum of a group of kPosUnroll vectors raises it.  The exponentials of
+  // a group are summed as trees (per vector, then over the group).
+  RowScale rs = make_row_scale(-INFINITY, 1.0f);
+  float st = 0.0f;
+  auto raise_to = [&](float g) {   // g > rs.m
+    st = rs.m > -INFINITY ? __fmul_rn(st, exp_fast(rs.m, RowScale{g, rs.c_hi, rs.c_lo})) : 0.0f;
+    rs.m = g;
+  };
   for (int v0 = 0; v0 < nvec; v0 += kThreads * kPosUnroll) {
     uint4 x[kPosUnroll];
 #pragma unroll
@@ -103,29 +122,12 @@ __global__ void __launch_bounds__(kThreads, 2) verify_pos_kernel(VerifyArgs a) {
       const int i = v0 + tid + u * kThreads;
       x[u] = i < nvec ? load_stream(vec + i) : make_uint4(ninf, ninf, ninf, ninf);
     }
+    uint32_t pm = ninf;
 #pragma unroll
     for (int u = 0; u < kPosUnroll; ++u) pm = V::max2(pm, V::vmax(x[u]));
-  }
-  float mx = V::finish(pm);
-  for (int i = tid; i < head; i += kThreads) mx = fmaxf(mx, Elem<T>::widen(row[i]));
-  for (int i = tail0 + tid; i < Vn; i += kThreads) mx = fmaxf(mx, Elem<T>::widen(row[i]));
-  const float m = block_max_f(mx, redf);
-  int flags = 0;
-  if (!isfinite(m)) flags |= kRowNonFinite;
-  const RowScale rs = make_row_scale(m, 1.0f);
-
-  // Z = sum of exp(z - m): binary32 exponentials summed as trees (per vector,
-  // then per group of kPosUnroll vectors), each thread's total turned into
-  // fixed point once; relative error about 3e-7.
-  float zf = 0.0f;
-  if (!flags) {
-    for (int v0 = 0; v0 < nvec; v0 += kThreads * kPosUnroll) {
-      uint4 x[kPosUnroll];
-#pragma unroll
-      for (int u = 0; u < kPosUnroll; ++u) {
-        const int i = v0 + tid + u * kThreads;
-        x[u] = i < nvec ? __ldg(vec + i) : make_uint4(ninf, ninf, ninf, ninf);
-      }
+    const float gm = V::finish(pm);
+    if (gm > rs.m) raise_to(gm);
+    if (rs.m > -INFINITY) {
       float vs[kPosUnroll];
 #pragma unroll
       for (int u = 0; u < kPosUnroll; ++u) {
@@ -142,11 +144,24 @@ __global__ void __launch_bounds__(kThreads, 2) verify_pos_kernel(VerifyArgs a) {
       for (int w = kPosUnroll / 2; w > 0; w /= 2)
 #pragma unroll
         for (int u = 0; u < w; ++u) vs[u] += vs[u + w];
-      zf += vs[0];
+      st += vs[0];
     }
-    for (int i = tid; i < head; i += kThreads) zf += exp_fast(Elem<T>::widen(row[i]), rs);
-    for (int i = tail0 + tid; i < Vn; i += kThreads) zf += exp_fast(Elem<T>::widen(row[i]), rs);
   }
+  auto edge = [&](float z) {
+    if (z > rs.m) raise_to(z);
+    if (rs.m > -INFINITY) st += exp_fast(z, rs);
+  };
+  for (int i = tid; i < head; i += kThreads) edge(Elem<T>::widen(row[i]));
+  for (int i = tail0 + tid; i < Vn; i += kThreads) edge(Elem<T>::widen(row[i]));
+  const float m = block_max_f(rs.m, redf);
+  int flags = 0;
+  if (!isfinite(m)) flags |= kRowNonFinite;
+  const RowScale rm = make_row_scale(m, 1.0f);
+
+  // Z = sum over threads of st * exp(rs.m - m): each thread's share in
+  // fixed point once, summed exactly.  Relative error about 3e-7.
+  float zf = 0.0f;
+  if (!flags && rs.m > -INFINITY) zf = __fmul_rn(st, exp_fast(rs.m, rm));
   uint64_t z = __float2ull_rn(__fmul_rn(zf, float(kFixedOne)));
   z = warp_sum<uint64_t>(z);
   if ((tid & 31) == 0) red64[tid >> 5] = z;
@@ -154,12 +169,10 @@ __global__ void __launch_bounds__(kThreads, 2) verify_pos_kernel(VerifyArgs a) {
   if (tid == 0) {
     uint64_t tot = 0;
     for (int w = 0; w < kWarps; ++w) tot += red64[w];
-    const int i = j <= a.k ? j : j - a.k - 1;   // draft position of this row
     double ex = 0.0;
-    if (i < a.k) {
-      const int x = a.drafts[size_t(b) * a.k + i];
-      if (x < 0 || x >= Vn) flags |= kRowBadDraft;
-      else if (!flags) ex = mass_double(Elem<T>::widen(row[x]), rs, table);
+    if (ipos < a.k) {
+      if (xd < 0 || xd >= Vn) flags |= kRowBadDraft;
+      else if (!flags) ex = mass_double(zx, rm, table);
     }
     PosStat st;
     st.m = m;
@@ -219,6 +232,7 @@ __device__ __forceinline__ uint64_t cluster_prefix(uint64_t v, uint64_t* slot, u
 template <typename T>
 __global__ void __launch_bounds__(kResolveThreads, 2) verify_resolve_kernel(VerifyArgs a) {
   __shared__ int32_t decision[2];   // first rejection j, row flags
+  __shared__ float inv_z[2];        // 2^F / Z of the drawn row's p and q (binary32)
   __shared__ uint64_t warp_tot[kResolveWarps];
   __shared__ uint64_t cta_slot;
   __shared__ int owner;             // thread whose ids hold the draw
@@ -255,8 +269,14 @@ __global__ void __launch_bounds__(kResolveThreads, 2) verify_resolve_kernel(Veri
     }
     const uint32_t rej = __ballot_sync(0xFFFFFFFFu, reject);
     if (tid == 0) {
-      decision[0] = rej ? __ffs(rej) - 1 : K;
+      const int jr = rej ? __ffs(rej) - 1 : K;
+      decision[0] = jr;
       decision[1] = fl;
+      // The reciprocals of the drawn row's Z, once (FP64 is slow on this part).
+      if (!fl) {
+        inv_z[0] = float(double(kFixedOne) / double(st[jr].z));
+        inv_z[1] = jr < K ? float(double(kFixedOne) / double(st[K + 1 + jr].z)) : inv_z[0];
+      }
     }
   }
   __syncthreads();
@@ -294,8 +314,8 @@ __global__ void __launch_bounds__(kResolveThreads, 2) verify_resolve_kernel(Veri
   // within 2^-53), and the row's total stays below 2^53 because the p sum to
   // 1.  The sums are exact integers, so the scans and the walk agree.
   bool use_p = !residual;
-  const float inv_zp = float(double(kFixedOne) / double(P.z));
-  const float inv_zq = float(double(kFixedOne) / double(Q.z));
+  const float inv_zp = inv_z[0];
+  const float inv_zq = inv_z[1];
   auto weight_of = [&](float zp, float zq) -> uint64_t {
     const float p = __fmul_rn(exp_fast(zp, rp), inv_zp);
     const float r = use_p ? p : fmaxf(0.0f, __fsub_rn(p, __fmul_rn(exp_fast(zq, rq), inv_zq)));

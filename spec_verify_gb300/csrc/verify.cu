@@ -205,22 +205,26 @@ __device__ __forceinline__ uint64_t resolve_scan(uint64_t v, uint64_t* warp_tot,
 }
 
 // Sum of one u64 per CTA of the cluster: this CTA's exclusive prefix (cluster
-// rank order) and the cluster total.  `slot` is this CTA's shared word; every
-// CTA reads every peer's word between two cluster barriers.
-__device__ __forceinline__ uint64_t cluster_prefix(uint64_t v, uint64_t* slot, uint64_t* total) {
+// rank order) and the cluster total.  `slot` is this CTA's shared word; between
+// two cluster barriers warp 0 reads every peer's word (lane r from rank r) and
+// leaves the two sums in bc[0..1] for the CTA.
+__device__ __forceinline__ uint64_t cluster_prefix(uint64_t v, uint64_t* slot, uint64_t* bc, uint64_t* total) {
   const uint32_t rank = cluster_rank(), n = cluster_size();
   if (threadIdx.x == 0) *slot = v;
   hw_cluster_sync();
-  uint64_t before = 0, all = 0;
-  const uint32_t addr = smem_addr(slot);
-  for (uint32_t r = 0; r < n; ++r) {
-    const uint64_t t = ld_cluster_u64(map_rank(addr, r));
-    if (r < rank) before += t;
-    all += t;
+  if (threadIdx.x < 32) {
+    const uint32_t r = threadIdx.x;
+    const uint64_t t = r < n ? ld_cluster_u64(map_rank(smem_addr(slot), r)) : 0ull;
+    const uint64_t before = warp_sum<uint64_t>(r < rank ? t : 0ull);
+    const uint64_t all = warp_sum<uint64_t>(t);
+    if (r == 0) {
+      bc[0] = before;
+      bc[1] = all;
+    }
   }
   hw_cluster_sync();   // no CTA rewrites its slot or exits while a peer may read it
-  *total = all;
-  return before;
+  *total = bc[1];
+  return bc[0];
 }
 
 // One cluster per batch row: the accept tests of eq. 39.3 in position order,
@@ -235,6 +239,7 @@ __global__ void __launch_bounds__(kResolveThreads, 2) verify_resolve_kernel(Veri
   __shared__ float inv_z[2];        // 2^F / Z of the drawn row's p and q (binary32)
   __shared__ uint64_t warp_tot[kResolveWarps];
   __shared__ uint64_t cta_slot;
+  __shared__ uint64_t cta_bc[2];
   __shared__ int owner;             // thread whose ids hold the draw
   __shared__ uint64_t owner_before;
   const int tid = threadIdx.x;
@@ -244,6 +249,9 @@ __global__ void __launch_bounds__(kResolveThreads, 2) verify_resolve_kernel(Veri
   const int V = a.vocab;
   const int rows_per_b = 2 * K + 1;
   const PosStat* st = a.ws + size_t(b) * rows_per_b;
+  // The uniforms depend on nothing the position kernel writes: drawn while it runs.
+  const uint64_t u_acc = threadIdx.x < K ? uniform53(a.seed, a.offset, uint64_t(b), uint64_t(threadIdx.x)) : 0ull;
+  const uint64_t u53 = uniform53(a.seed, a.offset, uint64_t(b), uint64_t(K));
   grid_dependency_wait();   // the position statistics come from verify_pos_kernel
   allow_dependent_launch();
 
@@ -262,7 +270,7 @@ __global__ void __launch_bounds__(kResolveThreads, 2) verify_resolve_kernel(Veri
       const PosStat& Q = st[K + 1 + i];
       const double zp = double(P.z) * (1.0 / double(kFixedOne));
       const double zq = double(Q.z) * (1.0 / double(kFixedOne));
-      const double u = double(uniform53(a.seed, a.offset, uint64_t(b), uint64_t(i))) * 0x1p-53;
+      const double u = double(u_acc) * 0x1p-53;
       // u * max(ex_q / zq, 1e-300) < ex_p / zp, multiplied through by zp * zq > 0
       const double lhs = Q.ex > 0.0 ? u * Q.ex * zp : u * 1e-300 * zp * zq;
       reject = !(lhs < P.ex * zq);
@@ -360,15 +368,14 @@ __global__ void __launch_bounds__(kResolveThreads, 2) verify_resolve_kernel(Veri
   };
   uint64_t local = chunk_sum(), cta_total = 0, total = 0;
   uint64_t before = resolve_scan(local, warp_tot, &cta_total);
-  uint64_t cta_before = cluster_prefix(cta_total, &cta_slot, &total);
+  uint64_t cta_before = cluster_prefix(cta_total, &cta_slot, cta_bc, &total);
   if (residual && total == 0) {   // zero residual mass (rounding only): draw from p_j
     use_p = true;
     local = chunk_sum();
     before = resolve_scan(local, warp_tot, &cta_total);
-    cta_before = cluster_prefix(cta_total, &cta_slot, &total);
+    cta_before = cluster_prefix(cta_total, &cta_slot, cta_bc, &total);
   }
   before += cta_before;
-  const uint64_t u53 = uniform53(a.seed, a.offset, uint64_t(b), uint64_t(K));
   const uint64_t t = uint64_t((u128(u53) * total) >> 53);
   // The chunk whose cumulative interval holds t is walked by warp 0 of its
   // CTA, 32 ids per step: weights, a warp scan, the first id whose running

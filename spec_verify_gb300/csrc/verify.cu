@@ -204,17 +204,20 @@ __device__ __forceinline__ uint64_t resolve_scan(uint64_t v, uint64_t* warp_tot,
   return before;
 }
 
-// Sum of one u64 per CTA of the cluster: this CTA's exclusive prefix (cluster
-// rank order) and the cluster total.  `slot` is this CTA's shared word; between
-// two cluster barriers warp 0 reads every peer's word (lane r from rank r) and
-// leaves the two sums in bc[0..1] for the CTA.
-__device__ __forceinline__ uint64_t cluster_prefix(uint64_t v, uint64_t* slot, uint64_t* bc, uint64_t* total) {
+// Sum of one u64 per CTA of the cluster (v, the same in every thread of the
+// CTA): this CTA's exclusive prefix (cluster rank order) and the cluster
+// total.  Lane r of warp 0 stores v into slots[rank] of the CTA of rank r; one
+// cluster barrier (release / acquire) makes every value local, and no CTA
+// touches a peer's memory after it.  Every CTA of the cluster must have
+// passed a cluster barrier before the first call (peers have started), and
+// each call needs its own `slots` array of kResolveMaxCluster words.
+__device__ __forceinline__ uint64_t cluster_prefix(uint64_t v, uint64_t* slots, uint64_t* bc, uint64_t* total) {
   const uint32_t rank = cluster_rank(), n = cluster_size();
-  if (threadIdx.x == 0) *slot = v;
+  if (threadIdx.x < n) st_cluster_u64(map_rank(smem_addr(slots + rank), threadIdx.x), v);
   hw_cluster_sync();
   if (threadIdx.x < 32) {
     const uint32_t r = threadIdx.x;
-    const uint64_t t = r < n ? ld_cluster_u64(map_rank(smem_addr(slot), r)) : 0ull;
+    const uint64_t t = r < n ? slots[r] : 0ull;
     const uint64_t before = warp_sum<uint64_t>(r < rank ? t : 0ull);
     const uint64_t all = warp_sum<uint64_t>(t);
     if (r == 0) {
@@ -222,7 +225,7 @@ __device__ __forceinline__ uint64_t cluster_prefix(uint64_t v, uint64_t* slot, u
       bc[1] = all;
     }
   }
-  hw_cluster_sync();   // no CTA rewrites its slot or exits while a peer may read it
+  __syncthreads();
   *total = bc[1];
   return bc[0];
 }
@@ -238,7 +241,7 @@ __global__ void __launch_bounds__(kResolveThreads, 2) verify_resolve_kernel(Veri
   __shared__ int32_t decision[2];   // first rejection j, row flags
   __shared__ float inv_z[2];        // 2^F / Z of the drawn row's p and q (binary32)
   __shared__ uint64_t warp_tot[kResolveWarps];
-  __shared__ uint64_t cta_slot;
+  __shared__ uint64_t cta_slots[2][kResolveMaxCluster];   // one array per cluster_prefix call
   __shared__ uint64_t cta_bc[2];
   __shared__ int owner;             // thread whose ids hold the draw
   __shared__ uint64_t owner_before;
@@ -252,6 +255,7 @@ __global__ void __launch_bounds__(kResolveThreads, 2) verify_resolve_kernel(Veri
   // The uniforms depend on nothing the position kernel writes: drawn while it runs.
   const uint64_t u_acc = threadIdx.x < K ? uniform53(a.seed, a.offset, uint64_t(b), uint64_t(threadIdx.x)) : 0ull;
   const uint64_t u53 = uniform53(a.seed, a.offset, uint64_t(b), uint64_t(K));
+  hw_cluster_sync();        // every CTA of the cluster has started (remote stores below)
   grid_dependency_wait();   // the position statistics come from verify_pos_kernel
   allow_dependent_launch();
 
@@ -280,10 +284,11 @@ __global__ void __launch_bounds__(kResolveThreads, 2) verify_resolve_kernel(Veri
       const int jr = rej ? __ffs(rej) - 1 : K;
       decision[0] = jr;
       decision[1] = fl;
-      // The reciprocals of the drawn row's Z, once (FP64 is slow on this part).
+      // The reciprocals of the drawn row's Z, once, in binary32 (within an
+      // ulp of 2^F / Z; FP64 is slow on this part).
       if (!fl) {
-        inv_z[0] = float(double(kFixedOne) / double(st[jr].z));
-        inv_z[1] = jr < K ? float(double(kFixedOne) / double(st[K + 1 + jr].z)) : inv_z[0];
+        inv_z[0] = __fdiv_rn(float(kFixedOne), __ull2float_rn(st[jr].z));
+        inv_z[1] = jr < K ? __fdiv_rn(float(kFixedOne), __ull2float_rn(st[K + 1 + jr].z)) : inv_z[0];
       }
     }
   }
@@ -329,7 +334,7 @@ __global__ void __launch_bounds__(kResolveThreads, 2) verify_resolve_kernel(Veri
     const float r = use_p ? p : fmaxf(0.0f, __fsub_rn(p, __fmul_rn(exp_fast(zq, rq), inv_zq)));
     return __float2ull_rn(__fmul_rn(r, 0x1p52f));
   };
-  constexpr int kGroups = 32 / kPer;   // groups of kPer ids in flight per thread (32 ids)
+  constexpr int kGroups = 16 / kPer;   // groups of kPer ids in flight per thread (16 ids)
   auto chunk_sum = [&]() -> uint64_t {
     uint64_t sum = 0;
     for (int g0 = c0; g0 < c1; g0 += kGroups * kPer) {
@@ -368,12 +373,12 @@ __global__ void __launch_bounds__(kResolveThreads, 2) verify_resolve_kernel(Veri
   };
   uint64_t local = chunk_sum(), cta_total = 0, total = 0;
   uint64_t before = resolve_scan(local, warp_tot, &cta_total);
-  uint64_t cta_before = cluster_prefix(cta_total, &cta_slot, cta_bc, &total);
+  uint64_t cta_before = cluster_prefix(cta_total, cta_slots[0], cta_bc, &total);
   if (residual && total == 0) {   // zero residual mass (rounding only): draw from p_j
     use_p = true;
     local = chunk_sum();
     before = resolve_scan(local, warp_tot, &cta_total);
-    cta_before = cluster_prefix(cta_total, &cta_slot, cta_bc, &total);
+    cta_before = cluster_prefix(cta_total, cta_slots[1], cta_bc, &total);
   }
   before += cta_before;
   const uint64_t t = uint64_t((u128(u53) * total) >> 53);

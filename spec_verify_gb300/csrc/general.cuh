@@ -191,9 +191,12 @@ __device__ GenBoundary gen_select(const T* row, int V, GenShared& gs, uint32_t k
   MassTarget target{};
   for (int lvl = 0; lvl < kL; ++lvl) {
     const int shift = kBits - 8 * (lvl + 1);
+    // Every bin of the last level is one key, whose elements share one mass:
+    // that level counts, and a bin's mass is its count times the key's mass.
+    const bool sweep_mass = kMass && lvl < kL - 1;
     for (int i = tid; i < kWarps * 256; i += kThreads) {
       (&gs.cnt[0][0])[i] = 0;
-      if (kMass) (&gs.mass[0][0])[i] = 0;
+      if (sweep_mass) (&gs.mass[0][0])[i] = 0;
     }
     cta_sync();
     gen_sweep<T>(row, V, [&](int, float z) {
@@ -201,7 +204,7 @@ __device__ GenBoundary gen_select(const T* row, int V, GenShared& gs, uint32_t k
       if (lvl > 0 && (key >> (shift + 8)) != prefix) return;
       const uint32_t d = (key >> shift) & 255u;
       atomicAdd(&gs.cnt[warp][d], 1u);
-      if (kMass) {
+      if (sweep_mass) {
         const uint64_t e = mass_fixed(z, rs, table);
         if (e) atomicAdd(&gs.mass[warp][d], (unsigned long long)e);
       }
@@ -213,8 +216,10 @@ __device__ GenBoundary gen_select(const T* row, int V, GenShared& gs, uint32_t k
 #pragma unroll
       for (int w = 0; w < kWarps; ++w) {
         c += gs.cnt[w][tid];
-        if (kMass) mm += gs.mass[w][tid];
+        if (sweep_mass) mm += gs.mass[w][tid];
       }
+      if (kMass && !sweep_mass && c)
+        mm = (unsigned long long)c * mass_fixed(key_value<T>((prefix << 8) | uint32_t(tid)), rs, table);
       gs.tot_cnt[tid] = c;
       if (kMass) gs.tot_mass[tid] = mm;
     }

@@ -345,14 +345,29 @@ def run_gpu(args):
     params_host = torch.from_numpy(batch.params.view(np.uint8).copy()).pin_memory()
     ids_host = torch.empty(B, dtype=torch.int32).pin_memory()
     probs_host = torch.empty(B, dtype=torch.float32).pin_memory()
-    dev_in = torch.empty_like(logits[0])
-    dev_params = torch.empty_like(params)
+    # Two input buffers: step i's copy (on its own stream) overlaps step
+    # i - 1's sampler call; a buffer is refilled only after the call that read
+    # it has finished.  Every step still copies its whole input.
+    dev_in = [torch.empty_like(logits[0]) for _ in range(2)]
+    dev_params = [torch.empty_like(params) for _ in range(2)]
+    copy_stream = torch.cuda.Stream()
+    compute = torch.cuda.current_stream()
+    copied = [torch.cuda.Event() for _ in range(2)]
+    freed = [torch.cuda.Event() for _ in range(2)]
+    for ev in freed:
+        ev.record(compute)
     e2e_steps = max(3, args.steps)
 
     def e2e_step(i):
-        dev_in.copy_(pinned, non_blocking=True)
-        dev_params.copy_(params_host, non_blocking=True)
-        binding.sample(dev_in, dev_params, seed, i, out_ids, out_probs, status)
+        k = i % 2
+        with torch.cuda.stream(copy_stream):
+            copy_stream.wait_event(freed[k])
+            dev_in[k].copy_(pinned, non_blocking=True)
+            dev_params[k].copy_(params_host, non_blocking=True)
+            copied[k].record(copy_stream)
+        compute.wait_event(copied[k])
+        binding.sample(dev_in[k], dev_params[k], seed, i, out_ids, out_probs, status)
+        freed[k].record(compute)
         ids_host.copy_(out_ids, non_blocking=True)
         probs_host.copy_(out_probs, non_blocking=True)
 
@@ -363,14 +378,16 @@ def run_gpu(args):
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record()
+    copy_stream.wait_stream(compute)   # the first copy starts after e0
     for i in range(e2e_steps):
         e2e_step(i)
+    compute.wait_stream(copy_stream)
     e1.record()
     barrier()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), dev)
     e2e = {"value": job_rate(B * e2e_steps, world, e2e_ms * 1e-3), "unit": UNIT,
            "h2d_bytes_per_step": sample_bytes + batch.params.nbytes, "d2h_bytes_per_step": B * 8,
-           "what": "pinned host logits+params -> device copy, smp_sample, ids+probs -> host, per step"}
+           "what": "pinned host logits+params -> device copy (own stream, two buffers: overlaps the previous step's call), smp_sample, ids+probs -> host, per step"}
 
     # ---------------- oracle on the host cores (rank 0, N = 1 only)
     cpu_baseline = None

@@ -23,7 +23,9 @@ constexpr int kGenU = 1;
 // Shared state of the general path.
 struct GenShared {
   uint32_t cnt[kWarps][256];
-  unsigned long long mass[kWarps][256];
+  // Fixed-point masses as three 15-bit limbs, each summed with 32-bit adds
+  // (per warp and digit below 2^15 * 2^16 = 2^31 for V <= 2^19).
+  uint32_t mass[kWarps][3][256];
   uint32_t tot_cnt[256];
   unsigned long long tot_mass[256];
   unsigned long long scan64[kWarps];
@@ -196,7 +198,11 @@ __device__ GenBoundary gen_select(const T* row, int V, GenShared& gs, uint32_t k
     const bool sweep_mass = kMass && lvl < kL - 1;
     for (int i = tid; i < kWarps * 256; i += kThreads) {
       (&gs.cnt[0][0])[i] = 0;
-      if (sweep_mass) (&gs.mass[0][0])[i] = 0;
+      if (sweep_mass) {
+        (&gs.mass[0][0][0])[3 * i] = 0;
+        (&gs.mass[0][0][0])[3 * i + 1] = 0;
+        (&gs.mass[0][0][0])[3 * i + 2] = 0;
+      }
     }
     cta_sync();
     gen_sweep<T>(row, V, [&](int, float z) {
@@ -206,7 +212,11 @@ __device__ GenBoundary gen_select(const T* row, int V, GenShared& gs, uint32_t k
       atomicAdd(&gs.cnt[warp][d], 1u);
       if (sweep_mass) {
         const uint64_t e = mass_fixed(z, rs, table);
-        if (e) atomicAdd(&gs.mass[warp][d], (unsigned long long)e);
+        if (e) {
+          atomicAdd(&gs.mass[warp][0][d], uint32_t(e) & 0x7FFFu);
+          atomicAdd(&gs.mass[warp][1][d], uint32_t(e >> 15) & 0x7FFFu);
+          atomicAdd(&gs.mass[warp][2][d], uint32_t(e >> 30));
+        }
       }
     });
     cta_sync();
@@ -216,7 +226,9 @@ __device__ GenBoundary gen_select(const T* row, int V, GenShared& gs, uint32_t k
 #pragma unroll
       for (int w = 0; w < kWarps; ++w) {
         c += gs.cnt[w][tid];
-        if (sweep_mass) mm += gs.mass[w][tid];
+        if (sweep_mass)
+          mm += (unsigned long long)gs.mass[w][0][tid] + ((unsigned long long)gs.mass[w][1][tid] << 15) +
+                ((unsigned long long)gs.mass[w][2][tid] << 30);
       }
       if (kMass && !sweep_mass && c)
         mm = (unsigned long long)c * mass_fixed(key_value<T>((prefix << 8) | uint32_t(tid)), rs, table);

@@ -220,8 +220,7 @@ struct StreamShared {
   uint32_t bc[2];
 };
 
-// Candidate lists of a candidate-path row.  The general path runs after the
-// last of them and shares their storage.
+// Candidate lists of a candidate-path row.
 struct CandShared {
   float seg[kSegs][kThreads];   // per-lane segment maxima of the row being streamed
   uint32_t q[kThreads];         // segments to read again: lane | segment << 8
@@ -236,10 +235,9 @@ struct CandShared {
   __align__(16) ulonglong2 idm[kFinalMax + 8];
 };
 
-union RowScratch {
-  CandShared cand;
-  GenShared gen;
-};
+// The general path runs after the CTA's last streamed batch has been
+// consumed, so its state lives in the (then idle) batch ring.
+static_assert(sizeof(GenShared) <= size_t(kBufs) * kBufBytes, "general-path state must fit the ring");
 
 // Byte layout of a row: the 16-byte aligned middle [a0, a1) streams through
 // shared memory in batches of kBufBytes; the few elements before and after it
@@ -533,8 +531,7 @@ __global__ void __launch_bounds__(kThreads, 2) sample_kernel(SampleArgs a) {
   extern __shared__ __align__(128) unsigned char ring[];
   __shared__ StreamShared ss;
   __shared__ FloatPair table[64];
-  __shared__ RowScratch scratch;
-  CandShared& cs = scratch.cand;
+  __shared__ CandShared cs;
   using V = VecOps<T>;
   constexpr int kPer = V::kPer;
   const int tid = threadIdx.x;
@@ -807,14 +804,15 @@ __global__ void __launch_bounds__(kThreads, 2) sample_kernel(SampleArgs a) {
     cta_sync();
     return;
   }
-  // The marked rows, by the general path (its state overlays the candidate lists).
+  // The marked rows, by the general path (its state overlays the idle ring).
   if (ss.handoffs == 0) return;
+  GenShared& gen = *reinterpret_cast<GenShared*>(ring);
   for (int r = blockIdx.x; r < B; r += gridDim.x) {
     // Every thread reads the mark before the row's first barrier; the row's
     // result replaces it only after later barriers.
     if (load_volatile(a.out_ids + r) != kHandOff) continue;
     const smp_row_params prm = a.params[r];
-    general_row<T>(scratch.gen, table, a, r, prm);
+    general_row<T>(gen, table, a, r, prm);
   }
 }
 

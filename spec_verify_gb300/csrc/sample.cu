@@ -32,6 +32,7 @@ constexpr int kBufBytes = 32768;                       // one TMA copy: a batch 
 constexpr int kBufs = 2;                               // batches in flight per CTA (double buffering)
 constexpr int kSubBytes = kBufBytes / kWarps;          // the part of a batch one warp processes
 constexpr int kVecPerLane = kSubBytes / 16 / 32;       // 16-byte vectors per lane and batch
+static_assert(kVecPerLane == 8, "a lane's unit is one 128-byte line, read in XOR-swizzled order");
 constexpr int kCandMax = 1024;    // candidate list capacity per row
 constexpr int kFinalMax = kThreads;   // candidates at or above the final threshold (one per thread)
 constexpr int kSegs = 8;          // segment maxima kept per lane and row (min-p / top-k rows)
@@ -464,7 +465,9 @@ __device__ __forceinline__ float kth_largest(float x, int k) {
 // TMA bulk copy; thread 0 refills a buffer as soon as the CTA is done with it,
 // running ahead across row boundaries.  The first batches of a CTA's first row
 // are requested before the row's knobs are read.  Each warp takes one
-// kSubBytes part of a batch (kVecPerLane 16-byte vectors per lane).
+// kSubBytes part of a batch; each lane one unit of kVecPerLane consecutive
+// 16-byte vectors (a 128-byte line, so that a unit read again from global
+// memory is one line).
 //   greedy:  every lane keeps its (max, lowest id) in registers; one CTA-wide
 //            arg-max at the end of the row.
 //   min-p:   candidates are the elements >= running maximum + T ln(min_p)
@@ -626,11 +629,14 @@ __global__ void __launch_bounds__(kThreads, 2) sample_kernel(SampleArgs a) {
       const uint4* vec = reinterpret_cast<const uint4*>(ring + size_t(bi) * kBufBytes) + v0;
       const T* part = reinterpret_cast<const T*>(vec);
       const uint32_t id0 = id_base + uint32_t(bt) * (kBufBytes / sizeof(T)) + uint32_t(v0 * kPer);
-      // The lane's batch maximum: one packed maximum over its vectors.
+      // The lane's batch maximum: one packed maximum over its unit, the
+      // kVecPerLane consecutive vectors (one 128-byte line) from lane *
+      // kVecPerLane, read in the order j ^ (lane % 8) so that the 32 lanes of
+      // a step touch all banks evenly.
       uint32_t pm = V::neg_inf();
 #pragma unroll
       for (int j = 0; j < kVecPerLane; ++j) {
-        const int v = lane + j * 32;
+        const int v = lane * kVecPerLane + (j ^ (lane & (kVecPerLane - 1)));
         if (v < nvec) pm = V::max2(pm, V::vmax(vec[v]));
       }
       const float lane_max = V::finish(pm);
@@ -639,12 +645,13 @@ __global__ void __launch_bounds__(kThreads, 2) sample_kernel(SampleArgs a) {
       if (greedy) {
         // Only a lane whose batch maximum beats its own best and reaches the
         // CTA's running maximum can hold the row's arg-max: locate its first
-        // occurrence (ids rise with j, then q).
+        // occurrence (ids rise with j, then q; the lane's valid vectors come
+        // first).
         const uint32_t shared_key = *reinterpret_cast<volatile uint32_t*>(&ss.maxkey);
         const float shared_max = shared_key ? value_of_key(shared_key) : -INFINITY;
         if (lane_max > best_z && lane_max >= shared_max) {
-          for (int j = 0; j < kVecPerLane; ++j) {
-            const int e0 = (lane + j * 32) * kPer;
+          for (int j = 0; j < kVecPerLane && lane * kVecPerLane + j < nvec; ++j) {
+            const int e0 = (lane * kVecPerLane + j) * kPer;
             int hit = -1;
 #pragma unroll
             for (int q = kPer - 1; q >= 0; --q)
@@ -754,10 +761,10 @@ __global__ void __launch_bounds__(kThreads, 2) sample_kernel(SampleArgs a) {
           const int nvec = max(0, min(bvec - ov0, kSubBytes / 16));
           const uint4* gv = reinterpret_cast<const uint4*>(bstart) + ov0;
           const uint32_t id0 = id_base + uint32_t(bt) * (kBufBytes / sizeof(T)) + uint32_t(ov0 * kPer);
-          uint4 xv[kVecPerLane];
+          uint4 xv[kVecPerLane];   // the owner's unit: one 128-byte line
 #pragma unroll
           for (int j = 0; j < kVecPerLane; ++j) {
-            const int v = ol + j * 32;
+            const int v = ol * kVecPerLane + j;
             xv[j] = v < nvec ? __ldg(gv + v) : make_uint4(V::neg_inf(), V::neg_inf(), V::neg_inf(), V::neg_inf());
           }
           for (int j = 0; j < kVecPerLane; ++j) {
@@ -765,7 +772,7 @@ __global__ void __launch_bounds__(kThreads, 2) sample_kernel(SampleArgs a) {
             const T* e = reinterpret_cast<const T*>(&xv[j]);
             for (int q = 0; q < kPer; ++q) {
               const float z = Elem<T>::widen(e[q]);
-              if (z >= theta) push_candidate(ss, cs, id0 + uint32_t((ol + j * 32) * kPer + q), z);
+              if (z >= theta) push_candidate(ss, cs, id0 + uint32_t((ol * kVecPerLane + j) * kPer + q), z);
             }
           }
         }

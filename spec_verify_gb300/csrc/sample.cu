@@ -332,6 +332,21 @@ __device__ __forceinline__ void push_candidate(StreamShared& ss, CandShared& cs,
   }
 }
 
+// (hi + lo) * 2^n >= x for an exponential in parts and 0 < x < 1, exactly,
+// in binary32: hi * 2^n and lo * 2^n are exact for n >= -100, and within a
+// factor of two of x the difference hi * 2^n - x is exact (Sterbenz), so its
+// sum with lo * 2^n has the sign of the comparison.
+__device__ __forceinline__ bool parts_at_least(const ExpParts& e, float x) {
+  if (e.kind == 1) return true;
+  if (e.kind == 2) return false;
+  if (e.n < -100) return double_from_parts(e) >= double(x);
+  const float sc = pow2f(e.n);
+  const float vh = __fmul_rn(e.hi, sc), vl = __fmul_rn(e.lo, sc);
+  if (vh >= __fmul_rn(2.0f, x)) return true;
+  if (__fmul_rn(2.0f, vh) < x) return false;
+  return __fsub_rn(vh, x) >= -vl;
+}
+
 // Exact selection and draw of a min-p / top-k candidate-path row.  The
 // candidates hold every element at or above a lower bound of the kept set's
 // boundary; row_max is the row's largest logit.  Returns false if the row
@@ -409,7 +424,7 @@ __device__ bool finalize_candidates(StreamShared& ss, CandShared& cs, const Floa
   uint64_t e = 0;
   if (keep) {
     const ExpParts p = exp_parts(z, rs, table, -1000.0f);
-    if (minp) keep = double_from_parts(p) >= double(prm.min_p);
+    if (minp) keep = parts_at_least(p, prm.min_p);
     if (keep) e = fixed_from_parts(p);
   }
   if (tid < n8) cs.idm[tid] = make_ulonglong2(have ? id : 0xFFFFFFFFull, e);
@@ -442,20 +457,6 @@ __device__ bool finalize_candidates(StreamShared& ss, CandShared& cs, const Floa
     if (keep && e) a.full_probs[size_t(b) * V + id] = __fdiv_rn(float(e), float(z_kept));
   }
   return true;
-}
-
-// The k-th largest (1 <= k <= kThreads) of one float per thread, as a value v
-// with at least k of the inputs >= v: bit-wise search over the order keys.
-template <typename T>
-__device__ __forceinline__ float kth_largest(float x, int k) {
-  const uint32_t key = key_of_bits(__float_as_uint(x));
-  uint32_t t = 0;
-  const int low = KeyTraits<T>::kBits == 16 ? 16 : 0;   // bf16 keys carry no information below bit 16
-  for (int bit = 31; bit >= low; --bit) {
-    const uint32_t cand = t | (1u << bit);
-    if (cta_sync_count(key >= cand) >= k) t = cand;
-  }
-  return value_of_key(t);
 }
 
 // ------------------------------------------------------------------ the kernel
@@ -729,7 +730,13 @@ __global__ void __launch_bounds__(kThreads, 2) sample_kernel(SampleArgs a) {
     float theta = -INFINITY;
     if (minp) theta = minp_lower_bound(run_max, prm.temperature, prm.min_p);
     const int nseg = (geo.nchunks + seg_len - 1) / seg_len;
-    if (topk) theta = fmaxf(theta, kth_largest<T>(lane_row_max, prm.top_k));
+    if (topk) {
+      // Two 8-bit radix levels over the lane maxima (the candidate values are
+      // not in use yet).
+      cs.cand_val[tid] = lane_row_max;
+      cta_sync();
+      theta = fmaxf(theta, kth_largest_list<T>(cs.cand_val, kThreads, prm.top_k, cs.hist, ss.bc));
+    }
     // Candidates: every element >= theta, from the segments whose maximum
     // reaches it (read again from global memory, normally still in L2) and
     // from the edges.

@@ -45,6 +45,27 @@ struct VecOps<uint16_t> {
     const uint32_t w = q < 2 ? x.x : q < 4 ? x.y : q < 6 ? x.z : x.w;
     return __uint_as_float((q & 1) ? (w & 0xFFFF0000u) : (w << 16));
   }
+  // The threshold for ge_mask: the smallest bf16 value >= theta, in both
+  // halves (a bf16 element is >= theta exactly when it is >= that value).
+  static __device__ __forceinline__ uint32_t threshold(float theta) {
+    const uint32_t b = __float_as_uint(theta);
+    if ((b & 0x7FFFFFFFu) > 0x7F800000u) return 0x7FC07FC0u;   // NaN: no element qualifies
+    uint32_t h = b >> 16;
+    if ((b & 0xFFFFu) && !(b & 0x80000000u)) ++h;   // positive and inexact: round up
+    return h | (h << 16);                            // (negative: truncation rounds up)
+  }
+  // Bit q set when element q of x >= the threshold (NaN elements never).
+  static __device__ __forceinline__ uint32_t ge_mask(const uint4& x, uint32_t t) {
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+    uint32_t m = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      uint32_t r;
+      asm("set.ge.u32.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(w[i]), "r"(t));
+      m |= ((r & 1u) << (2 * i)) | (((r >> 16) & 1u) << (2 * i + 1));
+    }
+    return m;
+  }
 };
 
 template <>
@@ -61,6 +82,12 @@ struct VecOps<float> {
   static __device__ __forceinline__ float finish(uint32_t m) { return __uint_as_float(m); }
   static __device__ __forceinline__ float elem(const uint4& x, int q) {
     return __uint_as_float(q == 0 ? x.x : q == 1 ? x.y : q == 2 ? x.z : x.w);
+  }
+  static __device__ __forceinline__ uint32_t threshold(float theta) { return __float_as_uint(theta); }
+  static __device__ __forceinline__ uint32_t ge_mask(const uint4& x, uint32_t t) {
+    const float th = __uint_as_float(t);
+    return (__uint_as_float(x.x) >= th ? 1u : 0u) | (__uint_as_float(x.y) >= th ? 2u : 0u) |
+           (__uint_as_float(x.z) >= th ? 4u : 0u) | (__uint_as_float(x.w) >= th ? 8u : 0u);
   }
 };
 

@@ -332,6 +332,34 @@ __device__ __forceinline__ void push_candidate(StreamShared& ss, CandShared& cs,
   }
 }
 
+// The candidates of one unit held in registers (its first nv vectors, token
+// ids from id_first on): every element >= theta, found through a bit mask per
+// vector and pushed by a short loop over the set bits.  The row end runs this
+// once per row, so its code is kept small.
+template <typename T>
+__device__ __forceinline__ void push_unit(StreamShared& ss, CandShared& cs, const uint4 (&xv)[kVecPerLane], int nv,
+                                          uint32_t id_first, float theta) {
+  using V = VecOps<T>;
+  constexpr int kPer = V::kPer;
+  static_assert(kVecPerLane * kPer <= 64, "one 64-bit mask per unit");
+  const uint32_t t = V::threshold(theta);
+  unsigned long long m = 0;
+#pragma unroll
+  for (int j = 0; j < kVecPerLane; ++j)
+    if (j < nv) m |= (unsigned long long)V::ge_mask(xv[j], t) << (j * kPer);
+#pragma unroll 1
+  while (m) {
+    const int p = __ffsll((long long)m) - 1;
+    m &= m - 1ull;
+    const int j = p / kPer, q = p % kPer;
+    uint4 x = xv[0];
+#pragma unroll
+    for (int jj = 1; jj < kVecPerLane; ++jj)
+      if (j == jj) x = xv[jj];
+    push_candidate(ss, cs, id_first + uint32_t(p), V::elem(x, q));
+  }
+}
+
 // (hi + lo) * 2^n >= x for an exponential in parts and 0 < x < 1, exactly,
 // in binary32: hi * 2^n and lo * 2^n are exact for n >= -100, and within a
 // factor of two of x the difference hi * 2^n - x is exact (Sterbenz), so its
@@ -774,14 +802,8 @@ __global__ void __launch_bounds__(kThreads, 2) sample_kernel(SampleArgs a) {
             const int v = ol * kVecPerLane + j;
             xv[j] = v < nvec ? __ldg(gv + v) : make_uint4(V::neg_inf(), V::neg_inf(), V::neg_inf(), V::neg_inf());
           }
-          for (int j = 0; j < kVecPerLane; ++j) {
-            if (!(V::finish(V::vmax(xv[j])) >= theta)) continue;
-            const T* e = reinterpret_cast<const T*>(&xv[j]);
-            for (int q = 0; q < kPer; ++q) {
-              const float z = Elem<T>::widen(e[q]);
-              if (z >= theta) push_candidate(ss, cs, id0 + uint32_t((ol * kVecPerLane + j) * kPer + q), z);
-            }
-          }
+          push_unit<T>(ss, cs, xv, min(kVecPerLane, max(0, nvec - ol * kVecPerLane)),
+                       id0 + uint32_t(ol * kVecPerLane * kPer), theta);
         }
       }
       for (int i = tid; i < geo.head; i += kThreads) {

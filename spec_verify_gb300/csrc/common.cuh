@@ -136,6 +136,15 @@ __device__ __forceinline__ RowScale make_row_scale(float m, float temperature) {
   return rs;
 }
 
+// make_row_scale(m, 1) without the divisions: c = log2(e) as head + tail.
+__device__ __forceinline__ RowScale make_row_scale_unit(float m) {
+  RowScale rs;
+  rs.m = m;
+  rs.c_hi = 0x1.715476p+0f;
+  rs.c_lo = 0x1.4ae0cp-26f;
+  return rs;
+}
+
 // Result of the exponential before scaling: e = (hi + lo) * 2^n, hi in [~0.98, ~2.03).
 struct ExpParts {
   float hi;
@@ -218,11 +227,13 @@ __device__ __forceinline__ uint64_t fixed_from_parts(const ExpParts& e) {
     const uint64_t mant = uint64_t((b & 0x7FFFFFu) | 0x800000u);
     const int sh = int((b >> 23) & 0xFF) - 127 - 23;
     const uint64_t head = mant << sh;
-    const long long t = __float2ll_rn(ls);
+    // |lo| <= ulp(hi): |ls| < 2^22 for s <= F, so a 32-bit conversion suffices
+    // (64-bit float-to-integer conversions are slower on this part).
+    const int t = __float2int_rn(ls);
     return uint64_t((long long)head + t);
   }
-  const float v = rintf(__fadd_rn(hs, ls));
-  return v <= 0.0f ? 0ull : uint64_t(v);
+  const float v = rintf(__fadd_rn(hs, ls));      // an integer below 2^25
+  return v <= 0.0f ? 0ull : uint64_t(__float2uint_rz(v));
 }
 
 // An exponential in parts as a double (head + tail, scaled).

@@ -109,7 +109,7 @@ __global__ void __launch_bounds__(kThreads, 2) verify_pos_kernel(VerifyArgs a) {
   // the binary32 sum st of exp(z - rs.m) over its elements, rescaled when the
   // maximum of a group of kPosUnroll vectors raises it.  The exponentials of
   // a group are summed as trees (per vector, then over the group).
-  RowScale rs = make_row_scale(-INFINITY, 1.0f);
+  RowScale rs = make_row_scale_unit(-INFINITY);
   float st = 0.0f;
   auto raise_to = [&](float g) {   // g > rs.m
     st = rs.m > -INFINITY ? __fmul_rn(st, exp_fast(rs.m, RowScale{g, rs.c_hi, rs.c_lo})) : 0.0f;
@@ -156,7 +156,7 @@ __global__ void __launch_bounds__(kThreads, 2) verify_pos_kernel(VerifyArgs a) {
   const float m = block_max_f(rs.m, redf);
   int flags = 0;
   if (!isfinite(m)) flags |= kRowNonFinite;
-  const RowScale rm = make_row_scale(m, 1.0f);
+  const RowScale rm = make_row_scale_unit(m);
 
   // Z = sum over threads of st * exp(rs.m - m): each thread's share in
   // fixed point once, summed exactly.  Relative error about 3e-7.
@@ -240,6 +240,7 @@ template <typename T>
 __global__ void __launch_bounds__(kResolveThreads, 2) verify_resolve_kernel(VerifyArgs a) {
   __shared__ int32_t decision[2];   // first rejection j, row flags
   __shared__ float inv_z[2];        // 2^F / Z of the drawn row's p and q (binary32)
+  __shared__ float row_m[2];        // the drawn row's p and q maxima
   __shared__ uint64_t warp_tot[kResolveWarps];
   __shared__ uint64_t cta_slots[2][kResolveMaxCluster];   // one array per cluster_prefix call
   __shared__ uint64_t cta_bc[2];
@@ -264,14 +265,17 @@ __global__ void __launch_bounds__(kResolveThreads, 2) verify_resolve_kernel(Veri
   // p = ex_p / (Z_p 2^-F), q = ex_q / (Z_q 2^-F); the first failing position
   // is the rejection.  Every CTA of the cluster decides alike.
   if (tid < 32) {
+    // Lane i holds the statistics of p row i (i <= K) and q row i (i < K):
+    // all the rows' flags, its accept test, and, for the drawn row, the
+    // maxima and reciprocals the draw needs.
     const int i = tid;
-    int fl = 0;
-    for (int r = i; r < rows_per_b; r += 32) fl |= st[r].flags;
+    PosStat P{}, Q{};
+    if (i <= K) P = st[i];
+    if (i < K) Q = st[K + 1 + i];
+    int fl = (i <= K ? P.flags : 0) | (i < K ? Q.flags : 0);
     for (int o = 16; o; o >>= 1) fl |= __shfl_xor_sync(0xFFFFFFFFu, fl, o);
     bool reject = false;
     if (!fl && i < K) {
-      const PosStat& P = st[i];
-      const PosStat& Q = st[K + 1 + i];
       const double zp = double(P.z) * (1.0 / double(kFixedOne));
       const double zq = double(Q.z) * (1.0 / double(kFixedOne));
       const double u = double(u_acc) * 0x1p-53;
@@ -280,16 +284,18 @@ __global__ void __launch_bounds__(kResolveThreads, 2) verify_resolve_kernel(Veri
       reject = !(lhs < P.ex * zq);
     }
     const uint32_t rej = __ballot_sync(0xFFFFFFFFu, reject);
+    const int jr = rej ? __ffs(rej) - 1 : K;
     if (tid == 0) {
-      const int jr = rej ? __ffs(rej) - 1 : K;
       decision[0] = jr;
       decision[1] = fl;
-      // The reciprocals of the drawn row's Z, once, in binary32 (within an
-      // ulp of 2^F / Z; FP64 is slow on this part).
-      if (!fl) {
-        inv_z[0] = __fdiv_rn(float(kFixedOne), __ull2float_rn(st[jr].z));
-        inv_z[1] = jr < K ? __fdiv_rn(float(kFixedOne), __ull2float_rn(st[K + 1 + jr].z)) : inv_z[0];
-      }
+    }
+    // The reciprocals of the drawn row's Z, once, in binary32 (within an ulp
+    // of 2^F / Z; FP64 is slow on this part).
+    if (i == jr && !fl) {
+      row_m[0] = P.m;
+      inv_z[0] = __fdiv_rn(float(kFixedOne), __ull2float_rn(P.z));
+      row_m[1] = jr < K ? Q.m : P.m;
+      inv_z[1] = jr < K ? __fdiv_rn(float(kFixedOne), __ull2float_rn(Q.z)) : inv_z[0];
     }
   }
   __syncthreads();
@@ -307,10 +313,8 @@ __global__ void __launch_bounds__(kResolveThreads, 2) verify_resolve_kernel(Veri
   const bool residual = jrej < K;
   const T* prow = logit_row<T>(a, b, jrej);               // p_j (or p_K for the bonus)
   const T* qrow = residual ? logit_row<T>(a, b, K + 1 + jrej) : prow;
-  const PosStat P = st[jrej];
-  const PosStat Q = residual ? st[K + 1 + jrej] : P;
-  const RowScale rp = make_row_scale(P.m, 1.0f);
-  const RowScale rq = make_row_scale(Q.m, 1.0f);
+  const RowScale rp = make_row_scale_unit(row_m[0]);
+  const RowScale rq = make_row_scale_unit(row_m[1]);
   // Thread g owns ids [c0, c1): a whole number of 16-byte groups of the row
   // (rows whose base is not 16-byte aligned fall back to element loads).
   constexpr int kPer = 16 / int(sizeof(T));
@@ -332,42 +336,54 @@ __global__ void __launch_bounds__(kResolveThreads, 2) verify_resolve_kernel(Veri
   auto weight_of = [&](float zp, float zq) -> uint64_t {
     const float p = __fmul_rn(exp_fast(zp, rp), inv_zp);
     const float r = use_p ? p : fmaxf(0.0f, __fsub_rn(p, __fmul_rn(exp_fast(zq, rq), inv_zq)));
-    return __float2ull_rn(__fmul_rn(r, 0x1p52f));
+    // rn(r * 2^52) from two 32-bit conversions: s = r * 2^28 <= 2^28 splits
+    // exactly into its integer part and fraction; the fraction times 2^24
+    // rounds like the whole (the integer part times 2^24 is even).
+    const float sc = __fmul_rn(r, 0x1p28f);
+    const float hi = truncf(sc);
+    return (uint64_t(__float2uint_rz(hi)) << 24) + __float2uint_rn(__fmul_rn(__fsub_rn(sc, hi), 0x1p24f));
   };
   constexpr int kGroups = 16 / kPer;   // groups of kPer ids in flight per thread (16 ids)
+  // The thread's weights: all its vectors requested first, then a rolled
+  // loop over the groups (this code runs once per CTA, cold in the
+  // instruction cache, so it is kept short).
   auto chunk_sum = [&]() -> uint64_t {
     uint64_t sum = 0;
+    const uint32_t ninf = VecOps<T>::neg_inf();
     for (int g0 = c0; g0 < c1; g0 += kGroups * kPer) {
-      float zp[kGroups][kPer], zq[kGroups][kPer];
+      uint4 xp[kGroups], xq[kGroups];
 #pragma unroll
       for (int gi = 0; gi < kGroups; ++gi) {
         const int gg = g0 + gi * kPer;
-#pragma unroll
-        for (int e = 0; e < kPer; ++e) {
-          zp[gi][e] = -INFINITY;
-          zq[gi][e] = -INFINITY;
-        }
-        if (gg < c1) {
-          if (vec_ok && gg + kPer <= V) {
-            const uint4 xp = __ldg(reinterpret_cast<const uint4*>(prow + gg));
-            const uint4 xq = use_p ? xp : __ldg(reinterpret_cast<const uint4*>(qrow + gg));
-#pragma unroll
-            for (int e = 0; e < kPer; ++e) {
-              zp[gi][e] = VecOps<T>::elem(xp, e);
-              zq[gi][e] = VecOps<T>::elem(xq, e);
-            }
-          } else {
-            for (int e = 0; e < kPer && gg + e < c1; ++e) {
-              zp[gi][e] = Elem<T>::widen(prow[gg + e]);
-              zq[gi][e] = Elem<T>::widen(qrow[gg + e]);
-            }
-          }
+        xp[gi] = make_uint4(ninf, ninf, ninf, ninf);
+        xq[gi] = xp[gi];
+        if (gg < c1 && vec_ok && gg + kPer <= V) {
+          xp[gi] = __ldg(reinterpret_cast<const uint4*>(prow + gg));
+          xq[gi] = use_p ? xp[gi] : __ldg(reinterpret_cast<const uint4*>(qrow + gg));
         }
       }
+#pragma unroll 1
+      for (int gi = 0; gi < kGroups; ++gi) {
+        const int gg = g0 + gi * kPer;
+        if (gg >= c1) break;
+        uint4 vp = xp[0], vq = xq[0];
 #pragma unroll
-      for (int gi = 0; gi < kGroups; ++gi)
+        for (int k2 = 1; k2 < kGroups; ++k2)
+          if (gi == k2) {
+            vp = xp[k2];
+            vq = xq[k2];
+          }
+        const bool full = vec_ok && gg + kPer <= V;
 #pragma unroll
-        for (int e = 0; e < kPer; ++e) sum += weight_of(zp[gi][e], zq[gi][e]);
+        for (int e = 0; e < kPer; ++e) {
+          float zp = VecOps<T>::elem(vp, e), zq = VecOps<T>::elem(vq, e);
+          if (!full) {   // a row not 16-byte aligned, or its last ids
+            zp = gg + e < c1 ? Elem<T>::widen(prow[gg + e]) : -INFINITY;
+            zq = gg + e < c1 ? Elem<T>::widen(qrow[gg + e]) : -INFINITY;
+          }
+          sum += weight_of(zp, zq);
+        }
+      }
     }
     return sum;
   };

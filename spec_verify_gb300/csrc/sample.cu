@@ -332,6 +332,16 @@ __device__ __forceinline__ void push_candidate(StreamShared& ss, CandShared& cs,
   }
 }
 
+// Slots for n entries of this lane in a list counted by *counter, for every
+// lane of a converged warp: one atomic per warp.  Returns the lane's first slot.
+__device__ __forceinline__ uint32_t warp_reserve(uint32_t* counter, uint32_t n) {
+  const uint32_t incl = warp_inclusive_scan<uint32_t>(n);
+  uint32_t base = 0;
+  if ((threadIdx.x & 31) == 31 && incl) base = atomicAdd(counter, incl);   // lane 31 holds the total
+  base = __shfl_sync(0xFFFFFFFFu, base, 31);
+  return base + incl - n;
+}
+
 // The candidates of one unit held in registers (its first nv vectors, token
 // ids from id_first on): every element >= theta, found through a bit mask per
 // vector and pushed by a short loop over the set bits.  The row end runs this
@@ -773,11 +783,15 @@ __global__ void __launch_bounds__(kThreads, 2) sample_kernel(SampleArgs a) {
     if (!isnan(theta)) {
       // The (lane, segment) pairs to read again, then one pass in which every
       // thread takes one of them (all its loads in flight at once).
-      for (int sgi = 0; sgi < nseg; ++sgi) {
-        if (cs.seg[sgi][tid] >= theta) {
-          const uint32_t slot = atomicAdd(&ss.qn, 1u);
-          if (slot < uint32_t(kThreads)) cs.q[slot] = uint32_t(tid) | (uint32_t(sgi) << 8);
-        }
+      // Each lane lists its own pairs; a warp appends them with one atomic.
+      uint32_t hits = 0;   // this lane's segments at or above theta (nseg <= kSegs)
+      for (int sgi = 0; sgi < nseg; ++sgi) hits |= (cs.seg[sgi][tid] >= theta ? 1u : 0u) << sgi;
+      uint32_t slot = warp_reserve(&ss.qn, uint32_t(__popc(hits)));
+      while (hits) {
+        const int sgi = __ffs(hits) - 1;
+        hits &= hits - 1u;
+        if (slot < uint32_t(kThreads)) cs.q[slot] = uint32_t(tid) | (uint32_t(sgi) << 8);
+        ++slot;
       }
       cta_sync();
       const int qn = int(ss.qn);

@@ -81,8 +81,9 @@ __device__ __forceinline__ bool row_is_fast(const smp_row_params& p, int V) {
 // Lower bound, in logits, of {z : exp((z - m) / T) >= min_p} for a row maximum
 // of at least m: m + T ln(min_p), lowered by a margin that covers the float
 // rounding of the expression.
-__device__ __forceinline__ float minp_lower_bound(float m, float temperature, float min_p) {
-  const float w = temperature * logf(min_p);
+// The bound is increasing in m, so a running maximum gives a lower bound of
+// the final one.  w = T ln(min_p), computed once per row.
+__device__ __forceinline__ float minp_bound_w(float m, float w) {
   const float t = m + w;
   return t - (fabsf(m) + fabsf(w)) * 0x1p-20f - 0x1p-126f;
 }
@@ -213,6 +214,7 @@ struct StreamShared {
   unsigned long long zsum;    // Z_S in fixed point
   uint64_t u53;               // the row's uniform (53-bit integer) for the draw
   float c_hi, c_lo;           // log2(e) / T of the row, head and tail
+  float w_minp;               // T ln(min_p) of the row (min-p rows)
   uint32_t qn;                // segments to read again
   uint32_t handoffs;          // rows of this CTA marked for the general path
   float red[kWarps];
@@ -410,7 +412,7 @@ __device__ bool finalize_candidates(StreamShared& ss, CandShared& cs, const Floa
     // Too many to rank one per thread: keep those at or above the k-th largest value.
     if (!topk || n < prm.top_k) return false;
     float theta = kth_largest_list<T>(cs.cand_val, n, prm.top_k, cs.hist, ss.bc);
-    if (minp) theta = fmaxf(theta, minp_lower_bound(row_max, prm.temperature, prm.min_p));
+    if (minp) theta = fmaxf(theta, minp_bound_w(row_max, ss.w_minp));
     if (tid == 0) ss.fin_n = 0;
     cta_sync();
     for (int i = tid; i < n; i += kThreads) {
@@ -485,7 +487,7 @@ __device__ bool finalize_candidates(StreamShared& ss, CandShared& cs, const Floa
     const uint64_t before = c[0] + c[1] + c[2] + c[3];
     if (before <= t && t - before < e) {
       a.out_ids[b] = int32_t(id);
-      if (a.out_probs) a.out_probs[b] = __fdiv_rn(float(e), float(z_kept));
+      if (a.out_probs) a.out_probs[b] = __fdividef(float(e), float(z_kept));   // within 2 ulp
     }
   }
   if (tid == 0 && a.kept) a.kept[b] = kept;
@@ -647,6 +649,7 @@ __global__ void __launch_bounds__(kThreads, 2) sample_kernel(SampleArgs a) {
       const RowScale r0 = make_row_scale(0.0f, prm.temperature);
       ss.c_hi = r0.c_hi;
       ss.c_lo = r0.c_lo;
+      ss.w_minp = minp ? prm.temperature * logf(prm.min_p) : 0.0f;
       ss.zsum = 0;
     }
     cta_sync();
@@ -766,7 +769,7 @@ __global__ void __launch_bounds__(kThreads, 2) sample_kernel(SampleArgs a) {
     // maximum, and the k-th largest per-lane maximum (k lanes hold an element
     // at least that large, so the k-th largest element is too).
     float theta = -INFINITY;
-    if (minp) theta = minp_lower_bound(run_max, prm.temperature, prm.min_p);
+    if (minp) theta = minp_bound_w(run_max, ss.w_minp);
     const int nseg = (geo.nchunks + seg_len - 1) / seg_len;
     if (topk) {
       // Two 8-bit radix levels over the lane maxima (the candidate values are

@@ -19,7 +19,7 @@ follows one passage:
   stopping at the first one whose running total passes u -- "Choosing the next
   word", section "Where the randomness comes from, and where it stops".
 
-Readings taken where the pages leave a step open (each is listed in the design doc):
+Readings taken where the pages leave a step open:
 
 * all three masks are computed on the same post-temperature p and intersected
   (eq. 39.2, Listing 39.2); each mask is a prefix of the order

@@ -17,7 +17,19 @@ Follows the accept / resample / bonus rule as the pages state it:
 * every row of the batch accepts 0..K tokens on its own -- "Speculative
   decoding -- Hinglish notes", section "Batching Speculation".
 
-Readings (listed in the design doc): temperature 1 and no filters on p and q; the
+Variants:
+
+* temperature T > 0 on both distributions, p_T = softmax(z_p / T) and
+  q_T = softmax(z_q / T), with the accept rule unchanged -- "Speculative
+  decoding -- Hinglish notes", section "Temperature and Sampling";
+* greedy verification (T = 0 or the greedy flag): a draft is kept when it is
+  the target's top token (lowest id on ties), so the output is the target's
+  own greedy decoding; at the first mismatch the target's top token is
+  emitted, and if all K are kept the top token of position K -- "Inference:
+  Sampling, the KV Cache, Speculative Decoding and int8", section
+  "Speculative decoding".
+
+Readings taken where the pages leave a step open: by default temperature 1 and no filters on p and q; the
 uniforms are Philox draws 0..K-1 for the K accept tests and draw K for the one
 resample or bonus draw; if the residual has zero total mass (possible only
 through rounding) the replacement is drawn from p_i; the walk is the sampler's
@@ -39,11 +51,17 @@ from .sampler import ROW_BAD_PARAMS, ROW_NONFINITE, ROW_OK, logits_to_f64, walk
 Q_FLOOR = 1e-300
 
 
-def softmax64(row):
-    """Stable softmax of one logit row in float64 (temperature 1)."""
-    z = logits_to_f64(row)
+def softmax64(row, temperature=1.0):
+    """Stable softmax of one logit row divided by the temperature, in float64."""
+    z = logits_to_f64(row) / float(temperature)
     w = np.exp(z - np.max(z))
     return w / np.sum(w)
+
+
+def top_token(row):
+    """The arg-max of one logit row, lowest id on ties (NaN counts as -inf)."""
+    z = logits_to_f64(row)
+    return int(np.flatnonzero(z == np.max(z))[0])
 
 
 def accept_draft(p, q, x, u):
@@ -60,12 +78,13 @@ def residual_distribution(p, q):
     return p
 
 
-def verify_row(p_rows, q_rows, drafts, uniforms):
+def verify_row(p_rows, q_rows, drafts, uniforms, temperature=1.0, greedy=False):
     """Verify one batch row.
 
     p_rows:   [K+1, V] target logits; q_rows: [K, V] draft logits;
     drafts:   K draft token ids; uniforms: K+1 values (accept tests, then the
-              final draw).
+              final draw; unused when greedy);
+    temperature, greedy: the variants above (temperature 0 means greedy).
     Returns a dict with accepted (int), ids (list of K+1 ints, -1 past the
     emitted tokens), status, and the margins accept_margin (smallest |u_i -
     p/q| over the accept tests made) and draw_margin.
@@ -82,9 +101,18 @@ def verify_row(p_rows, q_rows, drafts, uniforms):
         out["status"] = ROW_BAD_PARAMS
         return out
     emitted = []
+    if greedy or float(temperature) == 0.0:
+        for i in range(k + 1):
+            top = top_token(p_rows[i])
+            if i < k and int(drafts[i]) == top:
+                emitted.append(top)
+                continue
+            out["accepted"] = i
+            out["ids"] = emitted + [top] + [-1] * (k - i)
+            return out
     for i in range(k):
-        p = softmax64(p_rows[i])
-        q = softmax64(q_rows[i])
+        p = softmax64(p_rows[i], temperature)
+        q = softmax64(q_rows[i], temperature)
         x = int(drafts[i])
         ratio = p[x] / max(q[x], Q_FLOOR)
         out["accept_margin"] = min(out["accept_margin"], abs(uniforms[i] - ratio))
@@ -97,7 +125,7 @@ def verify_row(p_rows, q_rows, drafts, uniforms):
         out["accepted"] = i
         out["ids"] = emitted + [token] + [-1] * (k - i)
         return out
-    p_bonus = softmax64(p_rows[k])
+    p_bonus = softmax64(p_rows[k], temperature)
     token = walk(p_bonus, uniforms[k])
     out["draw_margin"] = _draw_margin(p_bonus, uniforms[k])
     out["accepted"] = k
@@ -110,8 +138,8 @@ def _draw_margin(dist, u):
     return float(np.min(np.abs(np.concatenate(([0.0], running)) - u)))
 
 
-def spec_verify(p_logits, q_logits, draft_ids, seed, offset, rows=None):
-    """Run verify_row over a batch.
+def spec_verify(p_logits, q_logits, draft_ids, seed, offset, rows=None, temperature=1.0, greedy=False):
+    """Run verify_row over a batch (temperature and greedy for all its rows).
 
     p_logits: [B, K+1, V]; q_logits: [B, K, V]; draft_ids: [B, K].
     Uniform for batch row b, draw d: philox.uniform(seed, offset, b, d).
@@ -126,7 +154,7 @@ def spec_verify(p_logits, q_logits, draft_ids, seed, offset, rows=None):
     results = []
     for b in rows:
         us = [philox.uniform(seed, offset, int(b), d) for d in range(k + 1)]
-        res = verify_row(p_logits[b], q_logits[b], draft_ids[b], us)
+        res = verify_row(p_logits[b], q_logits[b], draft_ids[b], us, temperature, greedy)
         res["row"] = int(b)
         results.append(res)
     return results

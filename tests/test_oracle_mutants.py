@@ -15,6 +15,7 @@ import oracle.verify as verify_mod
 from tests import test_oracle_philox as t_philox
 from tests import test_oracle_pins as t_pins
 from tests import test_oracle_properties as t_props
+from tests import test_oracle_verify_variants as t_variants
 from tests.conftest import load_golden
 
 
@@ -75,6 +76,28 @@ def _uniform_second_word(seed, offset, row, draw):
     return (w1 >> 11) * 2.0 ** -53
 
 
+def _softmax64_times_t(row, temperature=1.0):
+    z = sampler_mod.logits_to_f64(row) * float(temperature)
+    w = np.exp(z - np.max(z))
+    return w / np.sum(w)
+
+
+def _top_token_last(row):
+    z = sampler_mod.logits_to_f64(row)
+    return int(np.flatnonzero(z == np.max(z))[-1])
+
+
+def _top_token_of_draft_model(original):
+    # greedy verification that ignores the drafts' agreement and keeps every draft
+    def wrapped(p_rows, q_rows, drafts, uniforms, temperature=1.0, greedy=False):
+        if greedy or float(temperature) == 0.0:
+            k = len(drafts)
+            return {"accepted": k, "ids": [int(x) for x in drafts] + [verify_mod.top_token(p_rows[k])],
+                    "status": 0, "accept_margin": float("inf"), "draw_margin": float("inf")}
+        return original(p_rows, q_rows, drafts, uniforms, temperature, greedy)
+    return wrapped
+
+
 def _fd_no_renorm(original):
     def wrapped(row, temperature, top_k=0, top_p=1.0, min_p=0.0):
         p, keep, _, diag = original(row, temperature, top_k, top_p, min_p)
@@ -106,6 +129,14 @@ MUTANTS = [
      [lambda: t_pins.test_three_token_example(load_golden)]),
     ("uniform from the wrong word", philox_mod, "uniform", _uniform_second_word,
      [t_philox.test_uniform_layout]),
+    ("verify temperature multiplies", verify_mod, "softmax64", _softmax64_times_t,
+     [lambda: t_variants.test_temperature_acts_on_logits_over_t(0.5, 2.0),
+      lambda: t_variants.test_temperature_acts_on_logits_over_t(2.0, 0.5)]),
+    ("greedy ties favour the higher id", verify_mod, "top_token", _top_token_last,
+     [t_variants.test_greedy_ties_go_to_the_lowest_id]),
+    ("greedy keeps every draft", verify_mod, "verify_row", _top_token_of_draft_model(verify_mod.verify_row),
+     [t_variants.test_greedy_emits_a_prefix_of_the_target_greedy_tokens,
+      t_variants.test_greedy_ties_go_to_the_lowest_id]),
     ("renormalisation dropped", sampler_mod, "filtered_distribution",
      _fd_no_renorm(sampler_mod.filtered_distribution),
      [lambda: t_pins.test_exercise_39_1(load_golden), t_props.test_renormalisation_invariants]),

@@ -1,0 +1,129 @@
+"""Pins of the verifier oracle's variants: temperature on p and q, and greedy
+verification ("Speculative decoding -- Hinglish notes", section "Temperature
+and Sampling"; "Inference: Sampling, the KV Cache, Speculative Decoding and
+int8", section "Speculative decoding").
+
+Each pin rests on something the pages or the mathematics fix, not on the
+oracle's own formulas:
+* greedy verification emits a prefix of the target's own greedy tokens (the
+  pages: its output is identical to plain greedy decoding with the target);
+* greedy verification is the T -> 0 limit of the stochastic rule when the
+  drafts are the draft model's greedy tokens (one-hot p and q);
+* softmax(z / T) depends on z / T only: T = 1/2 on z equals T = 1 on 2 z, and
+  T = 2 on z equals T = 1 on z / 2, exactly (powers of two);
+* with p = q every draft is kept at any temperature (ratio exactly 1).
+"""
+
+import numpy as np
+import pytest
+
+from oracle import philox
+from oracle import verify as over
+
+
+def batch(b, k, v, seed, scale=2.0):
+    rng = np.random.default_rng(seed)
+    p = (rng.standard_normal((b, k + 1, v)) * scale).astype(np.float32)
+    q = (rng.standard_normal((b, k, v)) * scale).astype(np.float32)
+    return p, q
+
+
+def targets_greedy(p_rows):
+    return [over.top_token(r) for r in p_rows]
+
+
+def test_greedy_emits_a_prefix_of_the_target_greedy_tokens():
+    b, k, v = 40, 5, 64
+    p, q = batch(b, k, v, seed=1)
+    rng = np.random.default_rng(2)
+    drafts = rng.integers(0, v, (b, k))
+    # make the first m drafts of row r the target's greedy tokens, m = r % (k + 1)
+    for r in range(b):
+        tops = targets_greedy(p[r])
+        m = r % (k + 1)
+        drafts[r, :m] = tops[:m]
+        if m < k and drafts[r, m] == tops[m]:
+            drafts[r, m] = (tops[m] + 1) % v
+    res = over.spec_verify(p, q, drafts, seed=0, offset=0, greedy=True)
+    for r, out in enumerate(res):
+        tops = targets_greedy(p[r])
+        m = r % (k + 1)
+        assert out["accepted"] == m
+        emitted = out["ids"][: m + 1]
+        assert emitted == tops[: m + 1]          # the target's greedy tokens
+        assert out["ids"][m + 1:] == [-1] * (k - m)
+    # temperature 0 is the same rule
+    res0 = over.spec_verify(p, q, drafts, seed=0, offset=0, temperature=0.0)
+    assert [x["ids"] for x in res0] == [x["ids"] for x in res]
+
+
+def test_greedy_is_the_zero_temperature_limit():
+    b, k, v = 30, 4, 48
+    p, q = batch(b, k, v, seed=3)
+    # separate every row's maximum by at least 1, so that T = 2^-10 gives exact one-hots
+    for arr in (p, q):
+        for idx in np.ndindex(arr.shape[:2]):
+            row = arr[idx]
+            row[np.argmax(row)] = np.max(row) + 1.0
+    drafts = np.array([[over.top_token(q[r, i]) for i in range(k)] for r in range(b)])
+    # some drafts agree with the target by construction
+    for r in range(0, b, 3):
+        for i in range(k):
+            q[r, i] = p[r, i][: v]
+        drafts[r] = [over.top_token(p[r, i]) for i in range(k)]
+    cold = over.spec_verify(p, q, drafts, seed=5, offset=2, temperature=2.0 ** -10)
+    greedy = over.spec_verify(p, q, drafts, seed=5, offset=2, greedy=True)
+    assert [x["ids"] for x in cold] == [x["ids"] for x in greedy]
+    assert [x["accepted"] for x in cold] == [x["accepted"] for x in greedy]
+    assert any(x["accepted"] == k for x in greedy) and any(x["accepted"] < k for x in greedy)
+
+
+@pytest.mark.parametrize("t, factor", [(0.5, 2.0), (2.0, 0.5)])
+def test_temperature_acts_on_logits_over_t(t, factor):
+    b, k, v = 24, 4, 40
+    p, q = batch(b, k, v, seed=7, scale=1.5)
+    drafts = np.random.default_rng(8).integers(0, v, (b, k))
+    hot = over.spec_verify(p, q, drafts, seed=1, offset=3, temperature=t)
+    scaled = over.spec_verify((p * np.float32(factor)).astype(np.float32),
+                              (q * np.float32(factor)).astype(np.float32), drafts, seed=1, offset=3)
+    assert [x["ids"] for x in hot] == [x["ids"] for x in scaled]
+    assert [x["accepted"] for x in hot] == [x["accepted"] for x in scaled]
+    # and the temperature matters: T = 1 on z gives other results somewhere
+    cool = over.spec_verify(p, q, drafts, seed=1, offset=3)
+    assert [x["ids"] for x in cool] != [x["ids"] for x in hot]
+
+
+@pytest.mark.parametrize("t", [0.3, 1.0, 2.5])
+def test_equal_distributions_keep_every_draft(t):
+    b, k, v = 16, 5, 32
+    p, _ = batch(b, k, v, seed=11)
+    q = p[:, :k].copy()
+    drafts = np.random.default_rng(12).integers(0, v, (b, k))
+    res = over.spec_verify(p, q, drafts, seed=2, offset=0, temperature=t)
+    for r, out in enumerate(res):
+        assert out["accepted"] == k
+        assert out["ids"][:k] == [int(x) for x in drafts[r]]
+        # the bonus is the walk of p_K at temperature t with draw K
+        u = philox.uniform(2, 0, r, k)
+        assert out["ids"][k] == over.walk(over.softmax64(p[r, k], t), u)
+
+
+def test_greedy_ties_go_to_the_lowest_id():
+    # np.argmax returns the first occurrence of the maximum: the textbook
+    # arg-max with the lowest id on ties, which greedy decoding follows
+    b, k, v = 12, 3, 20
+    rng = np.random.default_rng(13)
+    p = rng.integers(-3, 3, (b, k + 1, v)).astype(np.float32)   # many ties
+    q = rng.integers(-3, 3, (b, k, v)).astype(np.float32)
+    for r in range(b):
+        for i in range(k + 1):
+            assert over.top_token(p[r, i]) == int(np.argmax(p[r, i]))
+    drafts = np.array([[int(np.argmax(p[r, i])) for i in range(k)] for r in range(b)])
+    drafts[::2, 1] = (drafts[::2, 1] + 1) % v        # a mismatch at position 1 in even rows
+    res = over.spec_verify(p, q, drafts, seed=0, offset=0, greedy=True)
+    for r, out in enumerate(res):
+        want = [int(np.argmax(p[r, i])) for i in range(k + 1)]
+        if r % 2 == 0:
+            assert out["accepted"] == 1 and out["ids"] == want[:2] + [-1] * (k - 1)
+        else:
+            assert out["accepted"] == k and out["ids"] == want

@@ -33,7 +33,7 @@
 extern "C" {
 #endif
 
-#define SMP_ABI_VERSION 1
+#define SMP_ABI_VERSION 2
 
 /* Largest vocabulary the kernels accept (rows are kept in on-chip memory). */
 #define SMP_MAX_VOCAB (1 << 19)
@@ -81,7 +81,7 @@ typedef enum smp_status {
 } smp_status;
 
 /* Flags OR-ed into the device status word, one or more per affected row. */
-#define SMP_ROW_BAD_PARAMS 1   /* invalid knobs on a sampling row */
+#define SMP_ROW_BAD_PARAMS 1   /* invalid knobs on a sampling or verify row */
 #define SMP_ROW_NONFINITE 2    /* the row's maximum logit is not finite (all -inf/NaN, or +inf) */
 #define SMP_ROW_TIMEOUT 4      /* a bounded wait between the CTAs of a row ran out of time */
 #define SMP_ROW_BAD_DRAFT 8    /* a draft id outside [0, V) */
@@ -157,6 +157,40 @@ smp_status smp_spec_verify(const void* p_logits, const void* q_logits, const int
                            uint64_t seed, uint64_t offset, int32_t* out_accepted_len,
                            int32_t* out_ids, int32_t* status, void* workspace,
                            size_t workspace_bytes, void* stream);
+
+/*
+ * smp_spec_verify_params -- smp_spec_verify with per-row knobs: temperature
+ * on both distributions, or greedy verification.
+ *
+ *   temperature  p_T = softmax(p_logits / T) and q_T = softmax(q_logits / T)
+ *                replace p and q everywhere above; the accept rule
+ *                min(1, p_T(x) / q_T(x)) is unchanged ("Speculative decoding
+ *                -- Hinglish notes", section "Temperature and Sampling").
+ *   greedy       (the flag, or T == 0) a draft is kept when it is the
+ *                target's arg-max at its position (lowest id on ties); at the
+ *                first mismatch j the target's arg-max of position j is
+ *                emitted, and if all K are kept the arg-max of position K.
+ *                The output is then exactly greedy decoding with the target
+ *                ("Inference: Sampling, the KV Cache, Speculative Decoding
+ *                and int8", section "Speculative decoding").  No uniform is
+ *                used and q_logits is not read for that row (its values,
+ *                finite or not, do not matter).
+ *   params       device, [batch] smp_row_params, or NULL for T = 1 on every
+ *                row (then the call is smp_spec_verify).  Knob validity is
+ *                the sampler's: greedy rows ignore the other knobs; on other
+ *                rows T must be finite and > 0, and top_k, top_p and min_p
+ *                must be off (top_k 0 or >= vocab, top_p >= 1, min_p 0 or
+ *                >= 1) because this verifier applies no filters.  A row that
+ *                breaks this gets accepted length -1, ids -1 and
+ *                SMP_ROW_BAD_PARAMS.
+ * Every other argument, the workspace and the error behaviour are those of
+ * smp_spec_verify.
+ */
+smp_status smp_spec_verify_params(const void* p_logits, const void* q_logits, const int32_t* draft_ids,
+                                  int32_t batch, int32_t k, int32_t vocab, smp_dtype dtype,
+                                  const smp_row_params* params, uint64_t seed, uint64_t offset,
+                                  int32_t* out_accepted_len, int32_t* out_ids, int32_t* status,
+                                  void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * Size of the device array that smp_spec_verify_static uses as its workspace

@@ -46,7 +46,7 @@ import math
 import numpy as np
 
 from . import philox
-from .sampler import ROW_BAD_PARAMS, ROW_NONFINITE, ROW_OK, logits_to_f64, walk
+from .sampler import ROW_BAD_PARAMS, ROW_NONFINITE, ROW_OK, is_greedy, logits_to_f64, row_params_valid, walk
 
 Q_FLOOR = 1e-300
 
@@ -93,7 +93,9 @@ def verify_row(p_rows, q_rows, drafts, uniforms, temperature=1.0, greedy=False):
     vocab = p_rows.shape[1]
     out = {"accepted": -1, "ids": [-1] * (k + 1), "status": ROW_OK,
            "accept_margin": math.inf, "draw_margin": math.inf}
-    for row in list(p_rows) + list(q_rows):
+    greedy = bool(greedy) or float(temperature) == 0.0
+    # greedy verification reads no draft distribution, so only p is checked
+    for row in list(p_rows) + ([] if greedy else list(q_rows)):
         if not math.isfinite(np.max(logits_to_f64(row))):
             out["status"] = ROW_NONFINITE
             return out
@@ -101,7 +103,7 @@ def verify_row(p_rows, q_rows, drafts, uniforms, temperature=1.0, greedy=False):
         out["status"] = ROW_BAD_PARAMS
         return out
     emitted = []
-    if greedy or float(temperature) == 0.0:
+    if greedy:
         for i in range(k + 1):
             top = top_token(p_rows[i])
             if i < k and int(drafts[i]) == top:
@@ -138,8 +140,30 @@ def _draw_margin(dist, u):
     return float(np.min(np.abs(np.concatenate(([0.0], running)) - u)))
 
 
-def spec_verify(p_logits, q_logits, draft_ids, seed, offset, rows=None, temperature=1.0, greedy=False):
-    """Run verify_row over a batch (temperature and greedy for all its rows).
+def row_mode(prm, vocab):
+    """Status, temperature and greedy flag of one batch row's knobs.
+
+    prm: a record with fields temperature, top_k, top_p, min_p, greedy (the
+    sampler's knobs).  Greedy (the flag, or T = 0) ignores the other knobs, as
+    in sampling.  Otherwise the knobs must be valid sampling knobs with every
+    filter off (top_k 0 or >= V, top_p >= 1, min_p 0 or >= 1): this verifier
+    applies temperature only, and a row asking for a filter is an error row.
+    """
+    t, g = float(prm["temperature"]), int(prm["greedy"])
+    if is_greedy(t, g):
+        return ROW_OK, 0.0, True
+    if not row_params_valid(t, prm["top_k"], prm["top_p"], prm["min_p"]):
+        return ROW_BAD_PARAMS, t, False
+    k, top_p, min_p = int(prm["top_k"]), float(prm["top_p"]), float(prm["min_p"])
+    if 0 < k < vocab or top_p < 1.0 or 0.0 < min_p < 1.0:
+        return ROW_BAD_PARAMS, t, False
+    return ROW_OK, t, False
+
+
+def spec_verify(p_logits, q_logits, draft_ids, seed, offset, rows=None, temperature=1.0, greedy=False,
+                params=None):
+    """Run verify_row over a batch (temperature and greedy for all its rows,
+    or per row from `params`, one record per batch row, see row_mode).
 
     p_logits: [B, K+1, V]; q_logits: [B, K, V]; draft_ids: [B, K].
     Uniform for batch row b, draw d: philox.uniform(seed, offset, b, d).
@@ -154,7 +178,16 @@ def spec_verify(p_logits, q_logits, draft_ids, seed, offset, rows=None, temperat
     results = []
     for b in rows:
         us = [philox.uniform(seed, offset, int(b), d) for d in range(k + 1)]
-        res = verify_row(p_logits[b], q_logits[b], draft_ids[b], us, temperature, greedy)
+        if params is not None:
+            status, t_row, g_row = row_mode(params[b], p_logits.shape[-1])
+            if status != ROW_OK:
+                res = {"accepted": -1, "ids": [-1] * (k + 1), "status": status,
+                       "accept_margin": math.inf, "draw_margin": math.inf, "row": int(b)}
+                results.append(res)
+                continue
+        else:
+            t_row, g_row = temperature, greedy
+        res = verify_row(p_logits[b], q_logits[b], draft_ids[b], us, t_row, g_row)
         res["row"] = int(b)
         results.append(res)
     return results

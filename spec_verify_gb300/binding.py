@@ -26,7 +26,8 @@ ROW_BAD_DRAFT = 8
 
 # Symbols declared in include/smp.h.
 EXPORTS = ("smp_sample", "smp_filter_debug", "smp_spec_verify_workspace_bytes",
-           "smp_spec_verify", "smp_spec_verify_static", "smp_status_string", "smp_last_cuda_error",
+           "smp_spec_verify", "smp_spec_verify_params", "smp_spec_verify_static", "smp_status_string",
+           "smp_last_cuda_error",
            "smp_abi_version")
 
 STATIC_VERIFY_SCRATCH_BYTES = 1 << 20
@@ -61,6 +62,8 @@ def load():
     lib.smp_spec_verify_workspace_bytes.restype = sz
     lib.smp_spec_verify.argtypes = [vp, vp, vp, i32, i32, i32, i32, u64, u64, vp, vp, vp, vp, sz, vp]
     lib.smp_spec_verify.restype = i32
+    lib.smp_spec_verify_params.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, u64, u64, vp, vp, vp, vp, sz, vp]
+    lib.smp_spec_verify_params.restype = i32
     lib.smp_spec_verify_static.argtypes = [vp, vp, vp, i32, i32, i32, i32, u64, u64, vp, vp, vp, vp]
     lib.smp_spec_verify_static.restype = i32
     lib.smp_status_string.argtypes = [i32]
@@ -165,14 +168,8 @@ def spec_verify_workspace_bytes(batch, k):
     return int(load().smp_spec_verify_workspace_bytes(batch, k))
 
 
-def spec_verify(p_logits, q_logits, draft_ids, seed=0, offset=0, workspace=None, out_accepted=None,
-                out_ids=None, status=None, stream=None):
-    """smp_spec_verify on p [B, K+1, V], q [B, K, V] and draft ids [B, K] (int32).
-
-    Returns (accepted_len int32 [B], ids int32 [B, K+1], status int32 [1]).
-    """
+def _verify_shapes(p_logits, q_logits, draft_ids):
     torch = _torch()
-    lib = load()
     if p_logits.dim() != 3 or q_logits.dim() != 3 or draft_ids.dim() != 2:
         raise SmpError("expected p [B, K+1, V], q [B, K, V], draft_ids [B, K]")
     batch, k1, vocab = p_logits.shape
@@ -184,16 +181,51 @@ def spec_verify(p_logits, q_logits, draft_ids, seed=0, offset=0, workspace=None,
     for t in (p_logits, q_logits, draft_ids):
         if not t.is_cuda or not t.is_contiguous():
             raise SmpError("inputs must be contiguous CUDA tensors")
-    dev = p_logits.device
+    return batch, k, vocab
+
+
+def _verify_outputs(batch, k, dev, workspace, out_accepted, out_ids, status):
+    torch = _torch()
     need = spec_verify_workspace_bytes(batch, k)
     if workspace is None:
         workspace = torch.empty(max(need, 8), dtype=torch.uint8, device=dev)
     out_accepted = out_accepted if out_accepted is not None else torch.empty(batch, dtype=torch.int32, device=dev)
     out_ids = out_ids if out_ids is not None else torch.empty(batch, k + 1, dtype=torch.int32, device=dev)
     status = status if status is not None else torch.empty(1, dtype=torch.int32, device=dev)
+    return workspace, out_accepted, out_ids, status
+
+
+def spec_verify(p_logits, q_logits, draft_ids, seed=0, offset=0, workspace=None, out_accepted=None,
+                out_ids=None, status=None, stream=None):
+    """smp_spec_verify on p [B, K+1, V], q [B, K, V] and draft ids [B, K] (int32).
+
+    Returns (accepted_len int32 [B], ids int32 [B, K+1], status int32 [1]).
+    """
+    lib = load()
+    batch, k, vocab = _verify_shapes(p_logits, q_logits, draft_ids)
+    workspace, out_accepted, out_ids, status = _verify_outputs(batch, k, p_logits.device, workspace,
+                                                               out_accepted, out_ids, status)
     _check(lib.smp_spec_verify(_ptr(p_logits), _ptr(q_logits), _ptr(draft_ids), batch, k, vocab,
                                _dtype_code(p_logits), seed, offset, _ptr(out_accepted), _ptr(out_ids),
                                _ptr(status), _ptr(workspace), workspace.numel(), _stream(stream)))
+    return out_accepted, out_ids, status
+
+
+def spec_verify_params(p_logits, q_logits, draft_ids, params, seed=0, offset=0, workspace=None,
+                       out_accepted=None, out_ids=None, status=None, stream=None):
+    """smp_spec_verify_params: spec_verify with per-row knobs (temperature or
+    greedy), `params` a [B] record array of smp_row_params or a device byte
+    tensor holding it (None: temperature 1 on every row)."""
+    lib = load()
+    batch, k, vocab = _verify_shapes(p_logits, q_logits, draft_ids)
+    dev = p_logits.device
+    prm = params_to_device(params, dev) if params is not None else None
+    workspace, out_accepted, out_ids, status = _verify_outputs(batch, k, dev, workspace, out_accepted,
+                                                               out_ids, status)
+    _check(lib.smp_spec_verify_params(_ptr(p_logits), _ptr(q_logits), _ptr(draft_ids), batch, k, vocab,
+                                      _dtype_code(p_logits), _ptr(prm), seed, offset, _ptr(out_accepted),
+                                      _ptr(out_ids), _ptr(status), _ptr(workspace), workspace.numel(),
+                                      _stream(stream)))
     return out_accepted, out_ids, status
 
 

@@ -12,8 +12,14 @@
 //                          order, then the replacement draw from
 //                          max(0, p_j - q_j) at the first rejection j, or the
 //                          bonus draw from p_K.
+// Per-row knobs: temperature T on both distributions ("Speculative decoding
+// -- Hinglish notes", section "Temperature and Sampling"), or greedy
+// verification (a draft is kept when it is the target's arg-max: "Inference:
+// Sampling, the KV Cache, Speculative Decoding and int8", section
+// "Speculative decoding"), for which only the target rows are read.
 #include <cuda_runtime.h>
 
+#include <climits>
 #include <mutex>
 
 #include "launch.h"
@@ -25,9 +31,9 @@ namespace smp {
 // Statistics of one logit row, written by verify_pos_kernel.
 struct PosStat {
   float m;          // row maximum
-  int32_t flags;    // kRowNonFinite / kRowBadDraft
-  uint64_t z;       // sum of fixed-point masses
-  double ex;        // exp(z_x - m) of the draft token (0 if none)
+  int32_t flags;    // kRowNonFinite / kRowBadDraft / kRowBadParams
+  uint64_t z;       // sum of fixed-point masses; greedy rows: the arg-max id
+  double ex;        // exp((z_x - m) / T) of the draft token (0 if none)
 };
 
 struct VerifyArgs {
@@ -43,7 +49,33 @@ struct VerifyArgs {
   int32_t* ids;
   int32_t* status;
   PosStat* ws;
+  const smp_row_params* params;   // [batch] or nullptr (T = 1 on every row)
 };
+
+// How batch row b is verified: temperature T > 0, greedy, or an error row.
+// Greedy (the flag, or T == 0) ignores the other knobs; otherwise T must be
+// finite and positive and every filter off, since no filter is applied.
+struct RowMode {
+  float temperature;
+  bool greedy;
+  bool bad;
+};
+
+__device__ __forceinline__ RowMode row_mode(const VerifyArgs& a, int b) {
+  RowMode md{1.0f, false, false};
+  if (a.params == nullptr) return md;
+  const smp_row_params p = a.params[b];
+  if (p.greedy != 0 || p.temperature == 0.0f) {
+    md.greedy = true;
+    return md;
+  }
+  md.temperature = p.temperature;
+  const bool valid = isfinite(p.temperature) && p.temperature > 0.0f && p.top_k >= 0 && p.top_p >= 0.0f &&
+                     p.min_p >= 0.0f;   // NaN fails the comparisons
+  const bool filtered = (p.top_k > 0 && p.top_k < a.vocab) || p.top_p < 1.0f || (p.min_p > 0.0f && p.min_p < 1.0f);
+  md.bad = !valid || filtered;
+  return md;
+}
 
 template <typename T>
 __device__ __forceinline__ const T* logit_row(const VerifyArgs& a, int b, int j) {
@@ -60,6 +92,65 @@ __device__ __forceinline__ uint4 load_stream(const uint4* p) {
                : "=r"(x.x), "=r"(x.y), "=r"(x.z), "=r"(x.w)
                : "l"(p));
   return x;
+}
+
+// Greedy verification's statistic of one target row: the maximum and its
+// lowest id.  Each thread keeps (best, id) over its elements; its middle
+// vectors come in increasing id order, so a vector replaces the best only
+// when its maximum is strictly larger, and is then searched for the first
+// element equal to it.  NaN never compares larger or equal, so it counts as
+// -inf.  Returns the CTA's (maximum, lowest id holding it) in thread 0.
+template <typename T>
+__device__ __forceinline__ void greedy_row_argmax(const T* row, int Vn, int head, int tail0, const uint4* vec,
+                                                  int nvec, float* redf, uint64_t* red64, float* m_out,
+                                                  int* id_out) {
+  using V = VecOps<T>;
+  constexpr int kPer = V::kPer;
+  const int tid = threadIdx.x;
+  const uint32_t ninf = V::neg_inf();
+  float best = -INFINITY;
+  int bid = INT_MAX;
+  auto consider = [&](float z, int i) {
+    if (z > best || (z == best && i < bid)) {
+      best = z;
+      bid = i;
+    }
+  };
+  for (int i = tid; i < head; i += kThreads) consider(Elem<T>::widen(row[i]), i);
+  for (int v0 = 0; v0 < nvec; v0 += kThreads * kPosUnroll) {
+    uint4 x[kPosUnroll];
+#pragma unroll
+    for (int u = 0; u < kPosUnroll; ++u) {
+      const int i = v0 + tid + u * kThreads;
+      x[u] = i < nvec ? load_stream(vec + i) : make_uint4(ninf, ninf, ninf, ninf);
+    }
+#pragma unroll
+    for (int u = 0; u < kPosUnroll; ++u) {
+      const float vm = V::finish(V::vmax(x[u]));
+      if (vm > best) {
+        const int base = head + (v0 + tid + u * kThreads) * kPer;
+        int q0 = kPer - 1;
+#pragma unroll
+        for (int q = kPer - 1; q >= 0; --q)
+          if (V::elem(x[u], q) == vm) q0 = q;
+        best = vm;
+        bid = base + q0;
+      }
+    }
+  }
+  for (int i = tail0 + tid; i < Vn; i += kThreads) consider(Elem<T>::widen(row[i]), i);
+  const float m = block_max_f(best, redf);
+  int cand = best == m ? bid : INT_MAX;
+#pragma unroll
+  for (int o = 16; o; o >>= 1) cand = min(cand, __shfl_xor_sync(0xFFFFFFFFu, cand, o));
+  if ((tid & 31) == 0) red64[tid >> 5] = uint64_t(uint32_t(cand));
+  cta_sync();
+  if (tid == 0) {
+    int id = INT_MAX;
+    for (int w = 0; w < kWarps; ++w) id = min(id, int(uint32_t(red64[w])));
+    *m_out = m;
+    *id_out = id;
+  }
 }
 
 // One CTA per logit row, one pass over it: the maximum and the fixed-point
@@ -81,6 +172,19 @@ __global__ void __launch_bounds__(kThreads, 2) verify_pos_kernel(VerifyArgs a) {
   const int Vn = a.vocab;
   grid_dependency_wait();
   allow_dependent_launch();
+  const RowMode md = row_mode(a, b);
+  if (md.bad || (md.greedy && j > a.k)) {
+    // An error row's statistics carry the flag; greedy rows read no q row.
+    if (tid == 0) {
+      PosStat s;
+      s.m = 0.0f;
+      s.flags = md.bad ? kRowBadParams : 0;
+      s.z = 0;
+      s.ex = 0.0;
+      a.ws[pr] = s;
+    }
+    return;
+  }
   if (tid < 64) table[tid] = kExp2Table[tid];
 
   const T* row = logit_row<T>(a, b, j);
@@ -102,14 +206,29 @@ __global__ void __launch_bounds__(kThreads, 2) verify_pos_kernel(VerifyArgs a) {
   float zx = -INFINITY;
   if (tid == 0 && ipos < a.k) {
     xd = a.drafts[size_t(b) * a.k + ipos];
-    if (xd >= 0 && xd < Vn) zx = Elem<T>::widen(row[xd]);
+    if (xd >= 0 && xd < Vn && !md.greedy) zx = Elem<T>::widen(row[xd]);
+  }
+
+  if (md.greedy) {   // a target row of a greedy row: its arg-max, and the draft's range
+    float gm;
+    int gid;
+    greedy_row_argmax<T>(row, Vn, head, tail0, vec, nvec, redf, red64, &gm, &gid);
+    if (tid == 0) {
+      PosStat s;
+      s.m = gm;
+      s.flags = (isfinite(gm) ? 0 : kRowNonFinite) | (ipos < a.k && (xd < 0 || xd >= Vn) ? kRowBadDraft : 0);
+      s.z = uint64_t(uint32_t(gid));
+      s.ex = 0.0;
+      a.ws[pr] = s;
+    }
+    return;
   }
 
   // One pass over the row: each thread keeps a running maximum (rs.m) and
   // the binary32 sum st of exp(z - rs.m) over its elements, rescaled when the
   // maximum of a group of kPosUnroll vectors raises it.  The exponentials of
   // a group are summed as trees (per vector, then over the group).
-  RowScale rs = make_row_scale_unit(-INFINITY);
+  RowScale rs = make_row_scale(-INFINITY, md.temperature);
   float st = 0.0f;
   auto raise_to = [&](float g) {   // g > rs.m
     st = rs.m > -INFINITY ? __fmul_rn(st, exp_fast(rs.m, RowScale{g, rs.c_hi, rs.c_lo})) : 0.0f;
@@ -156,7 +275,7 @@ __global__ void __launch_bounds__(kThreads, 2) verify_pos_kernel(VerifyArgs a) {
   const float m = block_max_f(rs.m, redf);
   int flags = 0;
   if (!isfinite(m)) flags |= kRowNonFinite;
-  const RowScale rm = make_row_scale_unit(m);
+  const RowScale rm = make_row_scale(m, md.temperature);
 
   // Z = sum over threads of st * exp(rs.m - m): each thread's share in
   // fixed point once, summed exactly.  Relative error about 3e-7.
@@ -259,6 +378,32 @@ __global__ void __launch_bounds__(kResolveThreads, 2) verify_resolve_kernel(Veri
   hw_cluster_sync();        // every CTA of the cluster has started (remote stores below)
   grid_dependency_wait();   // the position statistics come from verify_pos_kernel
   allow_dependent_launch();
+  const RowMode md = row_mode(a, b);
+
+  // Greedy verification (and error rows): lane i compares draft i with the
+  // target's arg-max of position i; the first mismatch j emits the arg-max of
+  // position j (position K when every draft matches).  Rank 0's warp 0 writes
+  // the row; no uniform and no other CTA is needed.
+  if (md.greedy || md.bad) {
+    if (rank == 0 && tid < 32) {
+      const int i = tid;
+      PosStat P{};
+      if (i <= K) P = st[i];
+      int fl = (i <= K ? P.flags : 0) | (md.bad ? kRowBadParams : 0);
+      for (int o = 16; o; o >>= 1) fl |= __shfl_xor_sync(0xFFFFFFFFu, fl, o);
+      const int top = int(uint32_t(P.z));
+      const int draft = i < K ? a.drafts[size_t(b) * K + i] : -1;
+      const uint32_t miss = __ballot_sync(0xFFFFFFFFu, i < K && draft != top);
+      const int jr = miss ? __ffs(miss) - 1 : K;
+      const int top_j = __shfl_sync(0xFFFFFFFFu, top, jr);
+      if (i <= K) a.ids[size_t(b) * (K + 1) + i] = fl ? -1 : i < jr ? draft : i == jr ? top_j : -1;
+      if (i == 0) {
+        a.accepted[b] = fl ? -1 : jr;
+        if (fl && a.status) atomicOr(a.status, fl & (kRowNonFinite | kRowBadDraft | kRowBadParams));
+      }
+    }
+    return;
+  }
 
   // Accept tests u_i < p_i(x) / max(q_i(x), 1e-300), one lane per position
   // (K <= 32), as the product form u_i * max(q, 1e-300) < p with
@@ -305,7 +450,7 @@ __global__ void __launch_bounds__(kResolveThreads, 2) verify_resolve_kernel(Veri
     if (rank == 0 && tid == 0) {
       a.accepted[b] = -1;
       for (int i = 0; i <= K; ++i) a.ids[size_t(b) * (K + 1) + i] = -1;
-      if (a.status) atomicOr(a.status, flags & (kRowNonFinite | kRowBadDraft | kRowTimeout));
+      if (a.status) atomicOr(a.status, flags & (kRowNonFinite | kRowBadDraft | kRowTimeout | kRowBadParams));
     }
     return;
   }
@@ -313,8 +458,8 @@ __global__ void __launch_bounds__(kResolveThreads, 2) verify_resolve_kernel(Veri
   const bool residual = jrej < K;
   const T* prow = logit_row<T>(a, b, jrej);               // p_j (or p_K for the bonus)
   const T* qrow = residual ? logit_row<T>(a, b, K + 1 + jrej) : prow;
-  const RowScale rp = make_row_scale_unit(row_m[0]);
-  const RowScale rq = make_row_scale_unit(row_m[1]);
+  const RowScale rp = make_row_scale(row_m[0], md.temperature);
+  const RowScale rq = make_row_scale(row_m[1], md.temperature);
   // Thread g owns ids [c0, c1): a whole number of 16-byte groups of the row
   // (rows whose base is not 16-byte aligned fall back to element loads).
   constexpr int kPer = 16 / int(sizeof(T));
@@ -462,11 +607,12 @@ extern "C" size_t smp_spec_verify_workspace_bytes(int32_t batch, int32_t k) {
   return size_t(batch) * size_t(2 * k + 1) * sizeof(smp::PosStat);
 }
 
-extern "C" smp_status smp_spec_verify(const void* p_logits, const void* q_logits,
-                                      const int32_t* draft_ids, int32_t batch, int32_t k, int32_t vocab,
-                                      smp_dtype dtype, uint64_t seed, uint64_t offset,
-                                      int32_t* out_accepted_len, int32_t* out_ids, int32_t* status,
-                                      void* workspace, size_t workspace_bytes, void* stream) {
+extern "C" smp_status smp_spec_verify_params(const void* p_logits, const void* q_logits,
+                                             const int32_t* draft_ids, int32_t batch, int32_t k,
+                                             int32_t vocab, smp_dtype dtype, const smp_row_params* params,
+                                             uint64_t seed, uint64_t offset, int32_t* out_accepted_len,
+                                             int32_t* out_ids, int32_t* status, void* workspace,
+                                             size_t workspace_bytes, void* stream) {
   using namespace smp;
   if (dtype != SMP_F32 && dtype != SMP_BF16) return SMP_ERR_DTYPE;
   if (!p_logits || !q_logits || !draft_ids || !out_accepted_len || !out_ids) return SMP_ERR_INVALID_ARG;
@@ -477,7 +623,7 @@ extern "C" smp_status smp_spec_verify(const void* p_logits, const void* q_logits
   if (reinterpret_cast<uintptr_t>(p_logits) % elem || reinterpret_cast<uintptr_t>(q_logits) % elem)
     return SMP_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(draft_ids) % 4 || reinterpret_cast<uintptr_t>(out_ids) % 4 ||
-      reinterpret_cast<uintptr_t>(out_accepted_len) % 4)
+      reinterpret_cast<uintptr_t>(out_accepted_len) % 4 || reinterpret_cast<uintptr_t>(params) % 4)
     return SMP_ERR_INVALID_ARG;
   const size_t need = smp_spec_verify_workspace_bytes(batch, k);
   if (!workspace || workspace_bytes < need || reinterpret_cast<uintptr_t>(workspace) % 8)
@@ -500,8 +646,18 @@ extern "C" smp_status smp_spec_verify(const void* p_logits, const void* q_logits
   a.ids = out_ids;
   a.status = status;
   a.ws = reinterpret_cast<PosStat*>(workspace);
+  a.params = params;
   if (dtype == SMP_F32) return launch_verify<float>(a, st);
   return launch_verify<uint16_t>(a, st);
+}
+
+extern "C" smp_status smp_spec_verify(const void* p_logits, const void* q_logits,
+                                      const int32_t* draft_ids, int32_t batch, int32_t k, int32_t vocab,
+                                      smp_dtype dtype, uint64_t seed, uint64_t offset,
+                                      int32_t* out_accepted_len, int32_t* out_ids, int32_t* status,
+                                      void* workspace, size_t workspace_bytes, void* stream) {
+  return smp_spec_verify_params(p_logits, q_logits, draft_ids, batch, k, vocab, dtype, nullptr, seed, offset,
+                                out_accepted_len, out_ids, status, workspace, workspace_bytes, stream);
 }
 
 // ------------------------------------------------------------------ allocation-free variant

@@ -41,7 +41,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_version_and_strings(lib):
-    assert lib.smp_abi_version() == 1
+    assert lib.smp_abi_version() == 2
     for code in range(6):
         assert lib.smp_status_string(code).decode().startswith(binding.STATUS_NAMES[code])
 
@@ -64,6 +64,15 @@ def test_host_validation_without_gpu(lib):
     need = lib.smp_spec_verify_workspace_bytes(2, 4)
     assert need == 2 * 9 * 24
     assert lib.smp_spec_verify(fake, fake, fake, 2, 4, 8, 0, 0, 0, fake, fake, null, fake, need - 1, null) == 5
+    # the per-row-knob entry: the same checks, and a misaligned params pointer
+    assert lib.smp_spec_verify_params(fake, fake, fake, 2, 0, 8, 0, fake, 0, 0, fake, fake, null, fake,
+                                      1 << 20, null) == 1
+    assert lib.smp_spec_verify_params(fake, fake, fake, 2, 4, 8, 0, ctypes.c_void_p(0x1002), 0, 0, fake, fake,
+                                      null, fake, 1 << 20, null) == 1
+    assert lib.smp_spec_verify_params(fake, fake, fake, 2, 4, 8, 9, fake, 0, 0, fake, fake, null, fake,
+                                      1 << 20, null) == 2
+    assert lib.smp_spec_verify_params(fake, fake, fake, 2, 4, 8, 0, null, 0, 0, fake, fake, null, null,
+                                      1 << 20, null) == 5
     assert lib.smp_spec_verify_workspace_bytes(0, 4) == 0
     assert lib.smp_spec_verify_workspace_bytes(2, 17) == 0
 

@@ -127,3 +127,31 @@ def test_greedy_ties_go_to_the_lowest_id():
             assert out["accepted"] == 1 and out["ids"] == want[:2] + [-1] * (k - 1)
         else:
             assert out["accepted"] == k and out["ids"] == want
+
+
+def test_per_row_knobs():
+    # row_mode follows the sampler's knob rules; the verifier applies no filter
+    from spec_verify_gb300 import workloads
+    b, k, v = 10, 2, 30
+    p, q = batch(b, k, v, seed=17)
+    q[3] = np.nan                      # greedy rows never look at q
+    drafts = np.random.default_rng(18).integers(0, v, (b, k))
+    prm = workloads.make_params(b)
+    prm["temperature"][1] = 0.5
+    prm["greedy"][2] = 1
+    prm["temperature"][3] = 0.0
+    prm["temperature"][4] = -0.5
+    prm["top_k"][5] = 3
+    prm["top_p"][6] = 0.5
+    prm["min_p"][7] = 0.2
+    prm["top_k"][8] = v                # top_k >= V is off
+    prm["temperature"][9] = np.nan
+    res = over.spec_verify(p, q, drafts, 3, 1, params=prm)
+    status = [r["status"] for r in res]
+    assert status == [0, 0, 0, 0, 1, 1, 1, 1, 0, 1]
+    assert all(r["accepted"] == -1 and r["ids"] == [-1] * (k + 1) for r in res if r["status"])
+    same = over.spec_verify(p, q, drafts, 3, 1, rows=[0, 8])
+    assert [r["ids"] for r in same] == [res[0]["ids"], res[8]["ids"]]
+    assert res[1]["ids"] == over.spec_verify(p, q, drafts, 3, 1, rows=[1], temperature=0.5)[0]["ids"]
+    for r in (2, 3):
+        assert res[r]["ids"] == over.spec_verify(p, q, drafts, 3, 1, rows=[r], greedy=True)[0]["ids"]

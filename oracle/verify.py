@@ -27,9 +27,18 @@ Variants:
   own greedy decoding; at the first mismatch the target's top token is
   emitted, and if all K are kept the top token of position K -- "Inference:
   Sampling, the KV Cache, Speculative Decoding and int8", section
-  "Speculative decoding".
+  "Speculative decoding";
+* filters (top-k, top-p, min-p with the sampler's rules) on both
+  distributions: p and q become the renormalised filtered distributions of
+  eq. 39.2 at temperature T, computed exactly as the sampler computes them,
+  and the accept, residual and bonus rules run on those.  The same section
+  "Temperature and Sampling" says only that top-k and nucleus sampling act on
+  the adjusted distribution around acceptance sampling; the reading taken is
+  that both p and q are filtered, so that the output follows the target's
+  filtered distribution, as the exactness argument of eq. 39.4 requires.
 
-Readings taken where the pages leave a step open: by default temperature 1 and no filters on p and q; the
+Readings taken where the pages leave a step open: by default temperature 1
+and no filters on p and q; the
 uniforms are Philox draws 0..K-1 for the K accept tests and draw K for the one
 resample or bonus draw; if the residual has zero total mass (possible only
 through rounding) the replacement is drawn from p_i; the walk is the sampler's
@@ -46,7 +55,8 @@ import math
 import numpy as np
 
 from . import philox
-from .sampler import ROW_BAD_PARAMS, ROW_NONFINITE, ROW_OK, is_greedy, logits_to_f64, row_params_valid, walk
+from .sampler import (ROW_BAD_PARAMS, ROW_NONFINITE, ROW_OK, filtered_distribution, is_greedy, logits_to_f64,
+                      row_params_valid, walk)
 
 Q_FLOOR = 1e-300
 
@@ -78,21 +88,34 @@ def residual_distribution(p, q):
     return p
 
 
-def verify_row(p_rows, q_rows, drafts, uniforms, temperature=1.0, greedy=False):
+def _distribution(row, temperature, filters):
+    """p (or q) of one position: softmax(z / T), or, with filters, the
+    renormalised filtered distribution of eq. 39.2 computed as the sampler
+    does; returns (distribution, smallest filter margin)."""
+    if filters is None:
+        return softmax64(row, temperature), math.inf
+    top_k, top_p, min_p = filters
+    _, _, p_tilde, diag = filtered_distribution(row, temperature, top_k, top_p, min_p)
+    return p_tilde, min(diag["topp_margin"], diag["minp_margin"])
+
+
+def verify_row(p_rows, q_rows, drafts, uniforms, temperature=1.0, greedy=False, filters=None):
     """Verify one batch row.
 
     p_rows:   [K+1, V] target logits; q_rows: [K, V] draft logits;
     drafts:   K draft token ids; uniforms: K+1 values (accept tests, then the
               final draw; unused when greedy);
-    temperature, greedy: the variants above (temperature 0 means greedy).
+    temperature, greedy: the variants above (temperature 0 means greedy);
+    filters:  None, or (top_k, top_p, min_p) applied to every p and q row.
     Returns a dict with accepted (int), ids (list of K+1 ints, -1 past the
     emitted tokens), status, and the margins accept_margin (smallest |u_i -
-    p/q| over the accept tests made) and draw_margin.
+    p/q| over the accept tests made), draw_margin and filter_margin (the
+    smallest top-p or min-p margin of the distributions used).
     """
     k = len(drafts)
     vocab = p_rows.shape[1]
     out = {"accepted": -1, "ids": [-1] * (k + 1), "status": ROW_OK,
-           "accept_margin": math.inf, "draw_margin": math.inf}
+           "accept_margin": math.inf, "draw_margin": math.inf, "filter_margin": math.inf}
     greedy = bool(greedy) or float(temperature) == 0.0
     # greedy verification reads no draft distribution, so only p is checked
     for row in list(p_rows) + ([] if greedy else list(q_rows)):
@@ -113,8 +136,9 @@ def verify_row(p_rows, q_rows, drafts, uniforms, temperature=1.0, greedy=False):
             out["ids"] = emitted + [top] + [-1] * (k - i)
             return out
     for i in range(k):
-        p = softmax64(p_rows[i], temperature)
-        q = softmax64(q_rows[i], temperature)
+        p, mp = _distribution(p_rows[i], temperature, filters)
+        q, mq = _distribution(q_rows[i], temperature, filters)
+        out["filter_margin"] = min(out["filter_margin"], mp, mq)
         x = int(drafts[i])
         ratio = p[x] / max(q[x], Q_FLOOR)
         out["accept_margin"] = min(out["accept_margin"], abs(uniforms[i] - ratio))
@@ -127,7 +151,8 @@ def verify_row(p_rows, q_rows, drafts, uniforms, temperature=1.0, greedy=False):
         out["accepted"] = i
         out["ids"] = emitted + [token] + [-1] * (k - i)
         return out
-    p_bonus = softmax64(p_rows[k], temperature)
+    p_bonus, mb = _distribution(p_rows[k], temperature, filters)
+    out["filter_margin"] = min(out["filter_margin"], mb)
     token = walk(p_bonus, uniforms[k])
     out["draw_margin"] = _draw_margin(p_bonus, uniforms[k])
     out["accepted"] = k
@@ -141,23 +166,23 @@ def _draw_margin(dist, u):
 
 
 def row_mode(prm, vocab):
-    """Status, temperature and greedy flag of one batch row's knobs.
+    """Status, temperature, greedy flag and filters of one batch row's knobs.
 
     prm: a record with fields temperature, top_k, top_p, min_p, greedy (the
-    sampler's knobs).  Greedy (the flag, or T = 0) ignores the other knobs, as
-    in sampling.  Otherwise the knobs must be valid sampling knobs with every
-    filter off (top_k 0 or >= V, top_p >= 1, min_p 0 or >= 1): this verifier
-    applies temperature only, and a row asking for a filter is an error row.
+    sampler's knobs, with the sampler's validity rules).  Greedy (the flag, or
+    T = 0) ignores the other knobs, as in sampling.  Otherwise the filters
+    that are on (0 < top_k < V, top_p < 1, 0 < min_p < 1) apply to every p
+    and q row, or filters is None when all are off.
     """
     t, g = float(prm["temperature"]), int(prm["greedy"])
     if is_greedy(t, g):
-        return ROW_OK, 0.0, True
+        return ROW_OK, 0.0, True, None
     if not row_params_valid(t, prm["top_k"], prm["top_p"], prm["min_p"]):
-        return ROW_BAD_PARAMS, t, False
+        return ROW_BAD_PARAMS, t, False, None
     k, top_p, min_p = int(prm["top_k"]), float(prm["top_p"]), float(prm["min_p"])
     if 0 < k < vocab or top_p < 1.0 or 0.0 < min_p < 1.0:
-        return ROW_BAD_PARAMS, t, False
-    return ROW_OK, t, False
+        return ROW_OK, t, False, (k, top_p, min_p)
+    return ROW_OK, t, False, None
 
 
 def spec_verify(p_logits, q_logits, draft_ids, seed, offset, rows=None, temperature=1.0, greedy=False,
@@ -179,15 +204,15 @@ def spec_verify(p_logits, q_logits, draft_ids, seed, offset, rows=None, temperat
     for b in rows:
         us = [philox.uniform(seed, offset, int(b), d) for d in range(k + 1)]
         if params is not None:
-            status, t_row, g_row = row_mode(params[b], p_logits.shape[-1])
+            status, t_row, g_row, f_row = row_mode(params[b], p_logits.shape[-1])
             if status != ROW_OK:
-                res = {"accepted": -1, "ids": [-1] * (k + 1), "status": status,
-                       "accept_margin": math.inf, "draw_margin": math.inf, "row": int(b)}
+                res = {"accepted": -1, "ids": [-1] * (k + 1), "status": status, "accept_margin": math.inf,
+                       "draw_margin": math.inf, "filter_margin": math.inf, "row": int(b)}
                 results.append(res)
                 continue
         else:
-            t_row, g_row = temperature, greedy
-        res = verify_row(p_logits[b], q_logits[b], draft_ids[b], us, t_row, g_row)
+            t_row, g_row, f_row = temperature, greedy, None
+        res = verify_row(p_logits[b], q_logits[b], draft_ids[b], us, t_row, g_row, f_row)
         res["row"] = int(b)
         results.append(res)
     return results

@@ -89,13 +89,18 @@ def _top_token_last(row):
 
 def _top_token_of_draft_model(original):
     # greedy verification that ignores the drafts' agreement and keeps every draft
-    def wrapped(p_rows, q_rows, drafts, uniforms, temperature=1.0, greedy=False):
+    def wrapped(p_rows, q_rows, drafts, uniforms, temperature=1.0, greedy=False, filters=None):
         if greedy or float(temperature) == 0.0:
             k = len(drafts)
             return {"accepted": k, "ids": [int(x) for x in drafts] + [verify_mod.top_token(p_rows[k])],
-                    "status": 0, "accept_margin": float("inf"), "draw_margin": float("inf")}
-        return original(p_rows, q_rows, drafts, uniforms, temperature, greedy)
+                    "status": 0, "accept_margin": float("inf"), "draw_margin": float("inf"),
+                    "filter_margin": float("inf")}
+        return original(p_rows, q_rows, drafts, uniforms, temperature, greedy, filters)
     return wrapped
+
+
+def _distribution_unfiltered(row, temperature, filters):
+    return verify_mod.softmax64(row, temperature), float("inf")
 
 
 def _fd_no_renorm(original):
@@ -137,6 +142,10 @@ MUTANTS = [
     ("greedy keeps every draft", verify_mod, "verify_row", _top_token_of_draft_model(verify_mod.verify_row),
      [t_variants.test_greedy_emits_a_prefix_of_the_target_greedy_tokens,
       t_variants.test_greedy_ties_go_to_the_lowest_id]),
+    ("verify filters dropped", verify_mod, "_distribution", _distribution_unfiltered,
+     [t_variants.test_filters_with_disjoint_kept_sets_reject_every_draft,
+      lambda: t_variants.test_filtered_acceptance_rate_and_output({"top_k": 2}, [4 / 7, 3 / 7, 0, 0],
+                                                                   [3 / 7, 0, 4 / 7, 0])]),
     ("renormalisation dropped", sampler_mod, "filtered_distribution",
      _fd_no_renorm(sampler_mod.filtered_distribution),
      [lambda: t_pins.test_exercise_39_1(load_golden), t_props.test_renormalisation_invariants]),

@@ -148,10 +148,104 @@ def test_per_row_knobs():
     prm["temperature"][9] = np.nan
     res = over.spec_verify(p, q, drafts, 3, 1, params=prm)
     status = [r["status"] for r in res]
-    assert status == [0, 0, 0, 0, 1, 1, 1, 1, 0, 1]
+    assert status == [0, 0, 0, 0, 1, 0, 0, 0, 0, 1]   # rows 5..7 filtered, row 8 off
     assert all(r["accepted"] == -1 and r["ids"] == [-1] * (k + 1) for r in res if r["status"])
     same = over.spec_verify(p, q, drafts, 3, 1, rows=[0, 8])
     assert [r["ids"] for r in same] == [res[0]["ids"], res[8]["ids"]]
     assert res[1]["ids"] == over.spec_verify(p, q, drafts, 3, 1, rows=[1], temperature=0.5)[0]["ids"]
     for r in (2, 3):
         assert res[r]["ids"] == over.spec_verify(p, q, drafts, 3, 1, rows=[r], greedy=True)[0]["ids"]
+    assert over.row_mode(prm[5], v)[3] == (3, 1.0, 0.0)
+    assert over.row_mode(prm[8], v)[3] is None
+
+
+# ------------------------------------------------------------------ filters on p and q
+#
+# Hand-computed kept sets on four tokens with p = (.4, .3, .2, .1):
+#   top_k = 2   keeps {0, 1}:    p~ = (4/7, 3/7, 0, 0)
+#   min_p = 0.45 keeps p >= .18: p~ = (4/9, 3/9, 2/9, 0)
+#   top_p = 0.75 keeps .4+.3+.2: p~ = (4/9, 3/9, 2/9, 0)
+
+P4 = np.log([0.4, 0.3, 0.2, 0.1])
+CHI2_999 = {1: 10.83, 2: 13.82, 3: 16.27}
+
+
+def _tiled(rows, *dists):
+    return np.tile(np.stack(dists).astype(np.float32), (rows, 1, 1))
+
+
+def _drafts_from_filtered_q(Q, prm_one, seed=1):
+    from oracle import sampler as osam
+    b, k, v = Q.shape
+    prm = np.repeat(prm_one, b * k)
+    res = osam.sample(Q.reshape(b * k, v), prm, seed, 0)
+    return np.array([r["token"] for r in res], dtype=np.int32).reshape(b, k)
+
+
+def _chi2(counts, probs):
+    probs = np.asarray(probs, dtype=np.float64)
+    mask = probs > 0
+    assert np.all(counts[~mask] == 0)
+    exp = probs[mask] * counts.sum()
+    return float(np.sum((counts[mask] - exp) ** 2 / exp)), int(mask.sum()) - 1
+
+
+def test_filters_with_disjoint_kept_sets_reject_every_draft():
+    # q = (.1, .2, .3, .4) with top_k = 2 keeps {2, 3}, p keeps {0, 1}: sum min(p~, q~) = 0,
+    # so no draft is kept and the replacement follows p~ = (4/7, 3/7, 0, 0).  Filtering
+    # only one side would keep some drafts (sum min = 0.3 either way).
+    from spec_verify_gb300 import workloads
+    rows = 6000
+    prm = workloads.make_params(1, top_k=2)
+    P = _tiled(rows, P4, P4)
+    Q = _tiled(rows, np.log([0.1, 0.2, 0.3, 0.4]))
+    drafts = _drafts_from_filtered_q(Q, prm)
+    assert set(np.unique(drafts)) <= {2, 3}
+    res = over.spec_verify(P, Q, drafts, 4, 0, params=np.repeat(prm, rows))
+    assert all(r["accepted"] == 0 for r in res)
+    counts = np.bincount([r["ids"][0] for r in res], minlength=4)
+    stat, dof = _chi2(counts, [4 / 7, 3 / 7, 0, 0])
+    assert stat < CHI2_999[dof]
+
+
+@pytest.mark.parametrize("knob, p_tilde, q_tilde", [
+    ({"top_k": 2}, [4 / 7, 3 / 7, 0, 0], [3 / 7, 0, 4 / 7, 0]),
+    ({"min_p": 0.45}, [4 / 9, 3 / 9, 2 / 9, 0], [3 / 9, 0, 4 / 9, 2 / 9]),
+    ({"top_p": 0.75}, [4 / 9, 3 / 9, 2 / 9, 0], [3 / 9, 0, 4 / 9, 2 / 9]),
+])
+def test_filtered_acceptance_rate_and_output(knob, p_tilde, q_tilde):
+    # q = (.3, .1, .4, .2): with K = 1 the mean accepted length is
+    # alpha = sum min(p~, q~) ("Decoding & Speculative Sampling", section 39.4),
+    # and both emitted positions follow p~ (the bonus row is p again).
+    from spec_verify_gb300 import workloads
+    rows = 12000
+    prm = workloads.make_params(1, **knob)
+    P = _tiled(rows, P4, P4)
+    Q = _tiled(rows, np.log([0.3, 0.1, 0.4, 0.2]))
+    drafts = _drafts_from_filtered_q(Q, prm)
+    res = over.spec_verify(P, Q, drafts, 5, 0, params=np.repeat(prm, rows))
+    acc = np.array([r["accepted"] for r in res])
+    ids = np.array([r["ids"] for r in res])
+    alpha = float(np.sum(np.minimum(p_tilde, q_tilde)))
+    assert abs(acc.mean() - alpha) < 4 * np.sqrt(alpha * (1 - alpha) / rows)
+    for pos in (0, 1):
+        reached = acc >= pos
+        stat, dof = _chi2(np.bincount(ids[reached, pos], minlength=4), p_tilde)
+        assert stat < CHI2_999[dof], (pos, stat)
+
+
+def test_top_k_one_is_greedy_verification():
+    # top_k = 1 leaves one-hot p~ and q~ at the arg-max: a draft is kept iff it
+    # is the target's top token, and the replacement or bonus is that token.
+    from spec_verify_gb300 import workloads
+    b, k, v = 30, 4, 25
+    p, q = batch(b, k, v, seed=19)
+    rng = np.random.default_rng(20)
+    drafts = rng.integers(0, v, (b, k))
+    for r in range(0, b, 2):
+        m = r % (k + 1)
+        drafts[r, :m] = [over.top_token(p[r, i]) for i in range(m)]
+    top1 = over.spec_verify(p, q, drafts, 6, 0, params=workloads.make_params(b, top_k=1, temperature=0.7))
+    greedy = over.spec_verify(p, q, drafts, 6, 0, greedy=True)
+    assert [x["ids"] for x in top1] == [x["ids"] for x in greedy]
+    assert any(x["accepted"] > 0 for x in greedy)

@@ -46,7 +46,7 @@ VERIFY_DESC = "verify: B=32, K=4, V=32000, fp32; q = G[:, :4], p = G + N(0,1), G
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "sample_kernel_large_vocab.md")
-KERNEL_SOURCES = ["common.cuh", "row_ops.cuh", "general.cuh", "sample.cu", "exp_table.h"]
+KERNEL_SOURCES = ["common.cuh", "row_ops.cuh", "select.cuh", "general.cuh", "sample.cu", "exp_table.h"]
 
 
 def dist_env():

@@ -160,12 +160,23 @@ smp_status smp_spec_verify(const void* p_logits, const void* q_logits, const int
 
 /*
  * smp_spec_verify_params -- smp_spec_verify with per-row knobs: temperature
- * on both distributions, or greedy verification.
+ * and filters on both distributions, or greedy verification.
  *
  *   temperature  p_T = softmax(p_logits / T) and q_T = softmax(q_logits / T)
  *                replace p and q everywhere above; the accept rule
  *                min(1, p_T(x) / q_T(x)) is unchanged ("Speculative decoding
  *                -- Hinglish notes", section "Temperature and Sampling").
+ *   top_k, top_p, min_p  the filters that are on (as in smp_sample) apply to
+ *                every target and draft row: p and q become the renormalised
+ *                filtered distributions p~ and q~ of eq. 39.2 ("Decoding &
+ *                Speculative Sampling", section 39.2), selected exactly as
+ *                the sampler selects them, and the accept, residual and bonus
+ *                rules run on p~ and q~, so the output follows the target's
+ *                filtered distribution.  A draft outside the draft's kept
+ *                set has q~(x) = 0 (kept iff p~(x) > 0); one outside the
+ *                target's kept set is rejected.  Filtered rows take an exact
+ *                selection per logit row (several passes over it), so they
+ *                cost more than unfiltered ones.
  *   greedy       (the flag, or T == 0) a draft is kept when it is the
  *                target's arg-max at its position (lowest id on ties); at the
  *                first mismatch j the target's arg-max of position j is
@@ -174,15 +185,11 @@ smp_status smp_spec_verify(const void* p_logits, const void* q_logits, const int
  *                ("Inference: Sampling, the KV Cache, Speculative Decoding
  *                and int8", section "Speculative decoding").  No uniform is
  *                used and q_logits is not read for that row (its values,
- *                finite or not, do not matter).
- *   params       device, [batch] smp_row_params, or NULL for T = 1 on every
- *                row (then the call is smp_spec_verify).  Knob validity is
- *                the sampler's: greedy rows ignore the other knobs; on other
- *                rows T must be finite and > 0, and top_k, top_p and min_p
- *                must be off (top_k 0 or >= vocab, top_p >= 1, min_p 0 or
- *                >= 1) because this verifier applies no filters.  A row that
- *                breaks this gets accepted length -1, ids -1 and
- *                SMP_ROW_BAD_PARAMS.
+ *                finite or not, do not matter); the other knobs are ignored.
+ *   params       device, [batch] smp_row_params, or NULL for T = 1 and no
+ *                filters on every row (then the call is smp_spec_verify).
+ *                Knob validity is the sampler's; a row with invalid knobs
+ *                gets accepted length -1, ids -1 and SMP_ROW_BAD_PARAMS.
  * Every other argument, the workspace and the error behaviour are those of
  * smp_spec_verify.
  */
@@ -194,7 +201,7 @@ smp_status smp_spec_verify_params(const void* p_logits, const void* q_logits, co
 
 /*
  * Size of the device array that smp_spec_verify_static uses as its workspace
- * (1 MiB: enough for batch * (2k+1) <= 43690, e.g. 1024 rows with k = 16).
+ * (1 MiB: enough for batch * (2k+1) <= 32768, e.g. 1024 rows with k = 15).
  */
 #define SMP_STATIC_VERIFY_SCRATCH_BYTES (1u << 20)
 

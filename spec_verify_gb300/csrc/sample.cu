@@ -28,6 +28,8 @@
 
 namespace smp {
 
+#include "select.cuh"
+
 constexpr int kBufBytes = 32768;                       // one TMA copy: a batch of the row
 constexpr int kBufs = 2;                               // batches in flight per CTA (double buffering)
 constexpr int kSubBytes = kBufBytes / kWarps;          // the part of a batch one warp processes
@@ -54,19 +56,6 @@ struct SampleArgs {
   float* full_probs;   // debug: [B, V] p~ or NULL
   int32_t* kept;       // debug: [B] |S| or NULL
 };
-
-__device__ __forceinline__ bool sampling_params_valid(const smp_row_params& p) {
-  const float t = p.temperature;
-  if (!(isfinite(t) && t > 0.0f)) return false;
-  if (p.top_k < 0) return false;
-  if (isnan(p.top_p) || p.top_p < 0.0f) return false;
-  if (isnan(p.min_p) || p.min_p < 0.0f) return false;
-  return true;
-}
-
-__device__ __forceinline__ bool row_is_greedy(const smp_row_params& p) {
-  return p.greedy != 0 || p.temperature == 0.0f;
-}
 
 // Candidate path: greedy, or valid knobs without top-p and with min-p or a small top-k.
 __device__ __forceinline__ bool row_is_fast(const smp_row_params& p, int V) {
@@ -132,53 +121,6 @@ __device__ __forceinline__ bool wait_full(uint64_t* bar, uint32_t parity) {
 
 
 
-// Smallest key whose value z satisfies exp((z - m) / T) >= min_p, i.e. the
-// min-p threshold p_i >= min_p * max_j p_j ("Inference: Sampling, the KV
-// Cache, Speculative Decoding and int8", section "Picking the next token")
-// expressed on logits.  Warp 0 probes 32 keys per step, starting around the
-// estimate m + T ln(min_p); every thread gets the result.
-template <typename T>
-__device__ uint32_t minp_threshold_key(uint32_t* bcast, const FloatPair* table, const RowScale& rs, float temperature,
-                                       float min_p, uint32_t key_max) {
-  if (threadIdx.x < 32) {
-    const int lane = threadIdx.x;
-    const double thr = double(min_p);
-    const float est = rs.m + temperature * logf(min_p);
-    const uint32_t k0 = KeyTraits<T>::kBits == 32 ? key_of_bits(__float_as_uint(est))
-                                                  : (key_of_bits(__float_as_uint(est) & 0xFFFF0000u) >> 16);
-    uint32_t lo = 0, hi = key_max;   // the answer lies in [lo, hi]; the property holds at hi
-    uint32_t start = k0 > 16u ? k0 - 16u : 0u;
-    uint32_t stride = 1;
-    if (start > hi) start = hi;
-    for (int iter = 0; iter < 64 && lo < hi; ++iter) {
-      const uint64_t cand64 = uint64_t(start) + uint64_t(lane) * stride;
-      const uint32_t cand = cand64 > hi ? hi : uint32_t(cand64);
-      const bool ok = mass_double(key_value<T>(cand), rs, table) >= thr;
-      const uint32_t mask = __ballot_sync(0xFFFFFFFFu, ok);
-      const uint32_t last = __shfl_sync(0xFFFFFFFFu, cand, 31);
-      if (mask == 0) {
-        lo = last + 1 > hi ? hi : last + 1;
-      } else {
-        const int j = __ffs(mask) - 1;
-        const uint32_t cj = __shfl_sync(0xFFFFFFFFu, cand, j);
-        const uint32_t cprev = __shfl_sync(0xFFFFFFFFu, cand, j > 0 ? j - 1 : 0);
-        hi = cj;
-        if (j > 0) lo = cprev + 1;
-        else if (start <= lo) lo = cj;   // probes started at the bottom of the range
-      }
-      if (lo > hi) lo = hi;
-      const uint64_t span = uint64_t(hi - lo) + 1;
-      stride = uint32_t((span + 31) / 32);
-      start = lo;
-    }
-    if (lane == 0) bcast[6] = hi;
-  }
-  cta_sync();
-  const uint32_t r = bcast[6];
-  cta_sync();
-  return r;
-}
-
 __device__ __forceinline__ void write_error_row(const SampleArgs& a, int b, int flags) {
   a.out_ids[b] = -1;
   if (a.out_probs) a.out_probs[b] = __int_as_float(0x7FC00000);
@@ -187,19 +129,6 @@ __device__ __forceinline__ void write_error_row(const SampleArgs& a, int b, int 
 }
 
 // ------------------------------------------------------------------ general path
-
-// Sum of one u32 per thread over the CTA (every thread gets it).
-__device__ __forceinline__ uint32_t block_sum_u32(uint32_t v, uint32_t* scratch) {
-  v = warp_sum<uint32_t>(v);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  cta_sync();
-  if (lane == 0) scratch[warp] = v;
-  cta_sync();
-  uint32_t t = 0;
-#pragma unroll
-  for (int w = 0; w < kWarps; ++w) t += scratch[w];
-  return t;
-}
 
 #include "general.cuh"
 

@@ -1,0 +1,527 @@
+// Exact selection of a row's kept set, shared by the sampler's general path
+// and the verifier's filtered rows ("Decoding & Speculative Sampling",
+// section 39.2 and eq. 39.2): knob rules, the min-p threshold key, passes over
+// a row in global memory, MSB-first radix selection over order keys, and the
+// kept set S = the shortest of the enabled prefixes of the order (logit
+// descending, id ascending) with its exact fixed-point mass Z_S.
+//
+// Every pass reads the row as 16-byte vectors, kGenU per thread in flight, in
+// rounds of kThreads * kGenU vectors; inside a round thread t owns kGenU
+// consecutive vectors, so (round, thread, vector, element) is token-id order.
+// Histograms are private per warp (count histograms for top-k, count and
+// exact fixed-point mass histograms for top-p).
+//
+// Included inside namespace smp after row_ops.cuh.
+#pragma once
+
+// ------------------------------------------------------------------ knobs
+
+__device__ __forceinline__ bool sampling_params_valid(const smp_row_params& p) {
+  const float t = p.temperature;
+  if (!(isfinite(t) && t > 0.0f)) return false;
+  if (p.top_k < 0) return false;
+  if (isnan(p.top_p) || p.top_p < 0.0f) return false;
+  if (isnan(p.min_p) || p.min_p < 0.0f) return false;
+  return true;
+}
+
+__device__ __forceinline__ bool row_is_greedy(const smp_row_params& p) {
+  return p.greedy != 0 || p.temperature == 0.0f;
+}
+
+// ------------------------------------------------------------------ CTA helpers
+
+// Sum of one u32 per thread over the CTA (every thread gets it).
+__device__ __forceinline__ uint32_t block_sum_u32(uint32_t v, uint32_t* scratch) {
+  v = warp_sum<uint32_t>(v);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  cta_sync();
+  if (lane == 0) scratch[warp] = v;
+  cta_sync();
+  uint32_t t = 0;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) t += scratch[w];
+  return t;
+}
+
+// Smallest key whose value z satisfies exp((z - m) / T) >= min_p, i.e. the
+// min-p threshold p_i >= min_p * max_j p_j ("Inference: Sampling, the KV
+// Cache, Speculative Decoding and int8", section "Picking the next token")
+// expressed on logits.  Warp 0 probes 32 keys per step, starting around the
+// estimate m + T ln(min_p); every thread gets the result.
+template <typename T>
+__device__ uint32_t minp_threshold_key(uint32_t* bcast, const FloatPair* table, const RowScale& rs, float temperature,
+                                       float min_p, uint32_t key_max) {
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    const double thr = double(min_p);
+    const float est = rs.m + temperature * logf(min_p);
+    const uint32_t k0 = KeyTraits<T>::kBits == 32 ? key_of_bits(__float_as_uint(est))
+                                                  : (key_of_bits(__float_as_uint(est) & 0xFFFF0000u) >> 16);
+    uint32_t lo = 0, hi = key_max;   // the answer lies in [lo, hi]; the property holds at hi
+    uint32_t start = k0 > 16u ? k0 - 16u : 0u;
+    uint32_t stride = 1;
+    if (start > hi) start = hi;
+    for (int iter = 0; iter < 64 && lo < hi; ++iter) {
+      const uint64_t cand64 = uint64_t(start) + uint64_t(lane) * stride;
+      const uint32_t cand = cand64 > hi ? hi : uint32_t(cand64);
+      const bool ok = mass_double(key_value<T>(cand), rs, table) >= thr;
+      const uint32_t mask = __ballot_sync(0xFFFFFFFFu, ok);
+      const uint32_t last = __shfl_sync(0xFFFFFFFFu, cand, 31);
+      if (mask == 0) {
+        lo = last + 1 > hi ? hi : last + 1;
+      } else {
+        const int j = __ffs(mask) - 1;
+        const uint32_t cj = __shfl_sync(0xFFFFFFFFu, cand, j);
+        const uint32_t cprev = __shfl_sync(0xFFFFFFFFu, cand, j > 0 ? j - 1 : 0);
+        hi = cj;
+        if (j > 0) lo = cprev + 1;
+        else if (start <= lo) lo = cj;   // probes started at the bottom of the range
+      }
+      if (lo > hi) lo = hi;
+      const uint64_t span = uint64_t(hi - lo) + 1;
+      stride = uint32_t((span + 31) / 32);
+      start = lo;
+    }
+    if (lane == 0) bcast[6] = hi;
+  }
+  cta_sync();
+  const uint32_t r = bcast[6];
+  cta_sync();
+  return r;
+}
+
+// ------------------------------------------------------------------ passes and radix selection
+
+// 16-byte vectors per thread and round.  One keeps the exact exponential of
+// every element inlined without spilling next to the candidate path's state.
+constexpr int kGenU = 1;
+
+// Shared state of the general path.
+struct GenShared {
+  uint32_t cnt[kWarps][256];
+  // Fixed-point masses as three 15-bit limbs, each summed with 32-bit adds
+  // (per warp and digit below 2^15 * 2^16 = 2^31 for V <= 2^19).
+  uint32_t mass[kWarps][3][256];
+  uint32_t tot_cnt[256];
+  unsigned long long tot_mass[256];
+  unsigned long long scan64[kWarps];
+  uint32_t scan32[kWarps];
+  uint64_t red64[kWarps];
+  uint32_t bc32[8];
+  unsigned long long bc64[4];
+};
+
+// Sweep over every element of a row in no particular order: f(id, z).
+template <typename T, typename F>
+__device__ __forceinline__ void gen_sweep(const T* row, int V, F&& f) {
+  using Vo = VecOps<T>;
+  constexpr int kPer = Vo::kPer;
+  const uintptr_t r0 = reinterpret_cast<uintptr_t>(row);
+  const uintptr_t a0 = (r0 + 15) & ~uintptr_t(15), a1 = (r0 + size_t(V) * sizeof(T)) & ~uintptr_t(15);
+  const bool mid = a1 > a0;
+  const int head = mid ? int((a0 - r0) / sizeof(T)) : V;
+  const int tail0 = mid ? int((a1 - r0) / sizeof(T)) : V;
+  const int nvec = mid ? int((a1 - a0) / 16) : 0;
+  const uint4* vp = reinterpret_cast<const uint4*>(a0);
+  for (int v0 = threadIdx.x * kGenU; v0 < nvec; v0 += kThreads * kGenU) {
+    uint4 x[kGenU];
+#pragma unroll
+    for (int u = 0; u < kGenU; ++u)
+      if (v0 + u < nvec) x[u] = __ldg(vp + v0 + u);
+#pragma unroll
+    for (int u = 0; u < kGenU; ++u)
+      if (v0 + u < nvec) {
+#pragma unroll
+        for (int q = 0; q < kPer; ++q) f(head + (v0 + u) * kPer + q, Vo::elem(x[u], q));
+      }
+  }
+  for (int i = threadIdx.x; i < head; i += kThreads) f(i, Elem<T>::widen(row[i]));
+  for (int i = tail0 + threadIdx.x; i < V; i += kThreads) f(i, Elem<T>::widen(row[i]));
+}
+
+// Exclusive prefix over the CTA (thread order) of one value per thread, and the total.
+template <typename U>
+__device__ __forceinline__ U gen_scan(U v, U* warp_tot, U* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const U incl = warp_inclusive_scan<U>(v);
+  if (lane == 31) warp_tot[warp] = incl;
+  cta_sync();
+  U before = incl - v, all = 0;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    const U t = warp_tot[w];
+    if (w < warp) before += t;
+    all += t;
+  }
+  cta_sync();
+  *total = all;
+  return before;
+}
+
+// Walk of a row in token-id order until the running value of g(id, z) passes
+// `target` (strictly): returns that id, or -1.  g >= 0.  Each round is summed
+// per thread, scanned over the CTA, and the thread whose interval holds the
+// target walks its elements.  Elements before and after the aligned middle
+// come first and last, walked by thread 0.
+template <typename T, typename U, typename G>
+__device__ int gen_walk(const T* row, int V, U target, GenShared& gs, G&& g) {
+  using Vo = VecOps<T>;
+  constexpr int kPer = Vo::kPer;
+  const uintptr_t r0 = reinterpret_cast<uintptr_t>(row);
+  const uintptr_t a0 = (r0 + 15) & ~uintptr_t(15), a1 = (r0 + size_t(V) * sizeof(T)) & ~uintptr_t(15);
+  const bool mid = a1 > a0;
+  const int head = mid ? int((a0 - r0) / sizeof(T)) : V;
+  const int tail0 = mid ? int((a1 - r0) / sizeof(T)) : V;
+  const int nvec = mid ? int((a1 - a0) / 16) : 0;
+  const uint4* vp = reinterpret_cast<const uint4*>(a0);
+  U* warp_tot = reinterpret_cast<U*>(sizeof(U) == 8 ? static_cast<void*>(gs.scan64) : static_cast<void*>(gs.scan32));
+  U run = 0;
+  cta_sync();   // the previous reader of bc32[4] is done
+  if (threadIdx.x == 0) gs.bc32[4] = 0xFFFFFFFFu;
+  // head, by thread 0 (fewer than 16 / sizeof(T) elements, or the whole short row)
+  if (threadIdx.x == 0) {
+    U r = 0;
+    for (int i = 0; i < head; ++i) {
+      r += g(i, Elem<T>::widen(row[i]));
+      if (r > target) {
+        gs.bc32[4] = uint32_t(i);
+        break;
+      }
+    }
+    gs.bc64[3] = (unsigned long long)r;
+  }
+  cta_sync();
+  if (gs.bc32[4] != 0xFFFFFFFFu) return int(gs.bc32[4]);
+  run = U(gs.bc64[3]);
+  for (int base = 0; base < nvec; base += kThreads * kGenU) {
+    const int v0 = base + threadIdx.x * kGenU;
+    uint4 x[kGenU];
+#pragma unroll
+    for (int u = 0; u < kGenU; ++u)
+      if (v0 + u < nvec) x[u] = __ldg(vp + v0 + u);
+    U mine = 0;
+#pragma unroll
+    for (int u = 0; u < kGenU; ++u)
+      if (v0 + u < nvec) {
+#pragma unroll
+        for (int q = 0; q < kPer; ++q) mine += g(head + (v0 + u) * kPer + q, Vo::elem(x[u], q));
+      }
+    U total;
+    const U before = run + gen_scan<U>(mine, warp_tot, &total);
+    if (mine > 0 && before <= target && target - before < mine) {
+      U r = before;
+      bool done = false;
+      for (int u = 0; u < kGenU && v0 + u < nvec && !done; ++u) {
+        const uint4 xv = __ldg(vp + v0 + u);   // again, so that x stays in registers
+#pragma unroll
+        for (int q = 0; q < kPer; ++q) {
+          const int id = head + (v0 + u) * kPer + q;
+          r += done ? U(0) : g(id, Vo::elem(xv, q));
+          if (!done && r > target) {
+            gs.bc32[4] = uint32_t(id);
+            done = true;
+          }
+        }
+      }
+    }
+    cta_sync();
+    if (gs.bc32[4] != 0xFFFFFFFFu) return int(gs.bc32[4]);
+    run += total;
+  }
+  if (threadIdx.x == 0) {
+    U r = run;
+    for (int i = tail0; i < V; ++i) {
+      r += g(i, Elem<T>::widen(row[i]));
+      if (r > target) {
+        gs.bc32[4] = uint32_t(i);
+        break;
+      }
+    }
+  }
+  cta_sync();
+  return gs.bc32[4] == 0xFFFFFFFFu ? -1 : int(gs.bc32[4]);
+}
+
+// Boundary of a prefix of (key desc, id asc): the boundary key, the elements
+// above it, how many of its tie bucket are in the prefix, the bucket's size
+// and, with masses, the fixed-point mass above the key.
+struct GenBoundary {
+  uint32_t key;
+  uint32_t above;
+  uint32_t n;
+  uint32_t ties;
+  uint64_t mass_above;
+  uint64_t tie_mass;   // mass of one member of the tie bucket
+};
+
+// Radix selection, MSB-first 8-bit digits.  kMass = false: the prefix of
+// length k (counts only).  kMass = true: the shortest prefix whose mass
+// reaches the top-p target top_p * Z; the first level's mass total is Z,
+// returned in *z_total.
+template <typename T, bool kMass>
+__device__ GenBoundary gen_select(const T* row, int V, GenShared& gs, uint32_t k, float top_p,
+                                  const RowScale& rs, const FloatPair* table, uint64_t* z_total) {
+  constexpr int kL = KeyTraits<T>::kLevels;
+  constexpr int kBits = KeyTraits<T>::kBits;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  uint32_t prefix = 0, above = 0;
+  uint64_t mass_above = 0;
+  MassTarget target{};
+  for (int lvl = 0; lvl < kL; ++lvl) {
+    const int shift = kBits - 8 * (lvl + 1);
+    // Every bin of the last level is one key, whose elements share one mass:
+    // that level counts, and a bin's mass is its count times the key's mass.
+    const bool sweep_mass = kMass && lvl < kL - 1;
+    for (int i = tid; i < kWarps * 256; i += kThreads) {
+      (&gs.cnt[0][0])[i] = 0;
+      if (sweep_mass) {
+        (&gs.mass[0][0][0])[3 * i] = 0;
+        (&gs.mass[0][0][0])[3 * i + 1] = 0;
+        (&gs.mass[0][0][0])[3 * i + 2] = 0;
+      }
+    }
+    cta_sync();
+    gen_sweep<T>(row, V, [&](int, float z) {
+      const uint32_t key = kBits == 32 ? key_of_bits(__float_as_uint(z)) : (key_of_bits(__float_as_uint(z)) >> 16);
+      if (lvl > 0 && (key >> (shift + 8)) != prefix) return;
+      const uint32_t d = (key >> shift) & 255u;
+      atomicAdd(&gs.cnt[warp][d], 1u);
+      if (sweep_mass) {
+        const uint64_t e = mass_fixed(z, rs, table);
+        if (e) {
+          atomicAdd(&gs.mass[warp][0][d], uint32_t(e) & 0x7FFFu);
+          atomicAdd(&gs.mass[warp][1][d], uint32_t(e >> 15) & 0x7FFFu);
+          atomicAdd(&gs.mass[warp][2][d], uint32_t(e >> 30));
+        }
+      }
+    });
+    cta_sync();
+    {   // one digit per thread: sum the warps' histograms
+      uint32_t c = 0;
+      unsigned long long mm = 0;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        c += gs.cnt[w][tid];
+        if (sweep_mass)
+          mm += (unsigned long long)gs.mass[w][0][tid] + ((unsigned long long)gs.mass[w][1][tid] << 15) +
+                ((unsigned long long)gs.mass[w][2][tid] << 30);
+      }
+      if (kMass && !sweep_mass && c)
+        mm = (unsigned long long)c * mass_fixed(key_value<T>((prefix << 8) | uint32_t(tid)), rs, table);
+      gs.tot_cnt[tid] = c;
+      if (kMass) gs.tot_mass[tid] = mm;
+    }
+    cta_sync();
+    if (kMass && lvl == 0) {
+      // Z is the first level's total; the target compares exactly in 128 bits.
+      if (tid < 32) {
+        unsigned long long zz = 0;
+        for (int j = 0; j < 8; ++j) zz += gs.tot_mass[lane * 8 + j];
+        zz = warp_sum<uint64_t>(zz);
+        if (lane == 0) gs.bc64[2] = zz;
+      }
+      cta_sync();
+      *z_total = gs.bc64[2];
+      target = make_mass_target(top_p, *z_total);
+    }
+    // Warp 0 finds the crossing digit, from 255 down.
+    if (tid < 32) {
+      uint32_t lc = 0;
+      uint64_t lm = 0;
+      for (int j = 0; j < 8; ++j) {
+        const int d = 255 - (lane * 8 + j);
+        lc += gs.tot_cnt[d];
+        if (kMass) lm += gs.tot_mass[d];
+      }
+      const uint32_t ic = warp_inclusive_scan<uint32_t>(lc);
+      const uint64_t im = kMass ? warp_inclusive_scan<uint64_t>(lm) : 0;
+      uint32_t run_c = above + ic - lc;
+      uint64_t run_m = mass_above + im - lm;
+      int found = -1;
+      uint32_t f_above = 0;
+      uint64_t f_mass = 0;
+      int last = -1;
+      uint32_t l_above = 0;
+      uint64_t l_mass = 0;
+      for (int j = 0; j < 8; ++j) {
+        const int d = 255 - (lane * 8 + j);
+        const uint32_t c = gs.tot_cnt[d];
+        const uint32_t nc = run_c + c;
+        const uint64_t nm = kMass ? run_m + gs.tot_mass[d] : 0;
+        if (c) {
+          last = d;
+          l_above = run_c;
+          l_mass = run_m;
+        }
+        const bool hit = kMass ? (c > 0 && (target.trivial || mass_reaches(nm, target))) : (nc >= k);
+        if (hit && found < 0) {
+          found = d;
+          f_above = run_c;
+          f_mass = run_m;
+        }
+        run_c = nc;
+        run_m = nm;
+      }
+      const uint32_t hits = __ballot_sync(0xFFFFFFFFu, found >= 0);
+      int src;
+      if (hits) {
+        src = __ffs(hits) - 1;
+      } else {
+        // Nothing crossed (only possible through a degenerate target): the last non-empty digit.
+        const uint32_t nz = __ballot_sync(0xFFFFFFFFu, last >= 0);
+        src = nz ? 31 - __clz(nz) : 0;
+        found = last < 0 ? 0 : last;
+        f_above = l_above;
+        f_mass = l_mass;
+      }
+      if (lane == src) {
+        gs.bc32[0] = uint32_t(found);
+        gs.bc32[1] = f_above;
+        gs.bc64[0] = f_mass;
+      }
+    }
+    cta_sync();
+    const uint32_t d = gs.bc32[0];
+    above = gs.bc32[1];
+    mass_above = gs.bc64[0];
+    prefix = (prefix << 8) | d;
+    cta_sync();
+  }
+  GenBoundary out;
+  out.key = prefix;
+  out.above = above;
+  out.ties = gs.tot_cnt[prefix & 255u];
+  out.mass_above = mass_above;
+  out.tie_mass = 0;
+  if (!kMass) {
+    out.n = k - above;
+  } else {
+    const uint64_t bucket_mass = gs.tot_mass[prefix & 255u];
+    out.tie_mass = out.ties ? bucket_mass / out.ties : 0;   // every member has the same key, so the same mass
+    uint32_t n = 1;
+    if (!target.trivial && out.tie_mass > 0) {
+      const u128 have = u128(mass_above) << target.sh;
+      if (target.rhs > have) {
+        // smallest n >= 1 with (mass_above + n * tie_mass) << sh >= rhs
+        const u128 need = target.rhs - have;
+        const u128 step = u128(out.tie_mass) << target.sh;
+        uint32_t lo = 1, hi = out.ties;
+        while (lo < hi) {
+          const uint32_t mid = lo + (hi - lo) / 2;
+          if (u128(mid) * step >= need) hi = mid;
+          else lo = mid + 1;
+        }
+        n = lo;
+      }
+    }
+    out.n = n > out.ties ? out.ties : n;
+  }
+  return out;
+}
+
+// ------------------------------------------------------------------ the kept set
+
+// The kept set S of one row: token i with order key k_i is in S when
+//   k_i > key, or k_i == key and i <= id_cut
+// (every filter off: key 0, id_cut 0xFFFFFFFF, so every token is kept).
+// Each enabled mask (top-k, top-p, min-p) is a prefix of the order (logit
+// descending, id ascending), so their intersection is the shortest of them.
+struct KeptSet {
+  RowScale rs;       // row maximum and 1/T
+  uint32_t key;
+  uint32_t id_cut;
+  uint64_t len;      // |S|
+  uint64_t z_kept;   // Z_S: the sum of the kept tokens' fixed-point masses
+};
+
+template <typename T>
+__device__ __forceinline__ uint32_t order_key(float z) {
+  return KeyTraits<T>::kBits == 32 ? key_of_bits(__float_as_uint(z)) : (key_of_bits(__float_as_uint(z)) >> 16);
+}
+
+__device__ __forceinline__ bool in_kept_set(const KeptSet& ks, uint32_t key, uint32_t id) {
+  return key > ks.key || (key == ks.key && id <= ks.id_cut);
+}
+
+// The fixed-point mass of token i (logit z) if it is kept, else 0.
+template <typename T>
+__device__ __forceinline__ uint64_t kept_mass(const KeptSet& ks, const FloatPair* table, int i, float z) {
+  return in_kept_set(ks, order_key<T>(z), uint32_t(i)) ? mass_fixed(z, ks.rs, table) : 0ull;
+}
+
+// S and Z_S of a row whose maximum key is finite and whose knobs are valid
+// sampling knobs (not greedy): the min-p threshold key, the radix selections
+// of top-k and top-p, the tie member at the boundary (an id-order walk) and
+// Z_S (from the top-p histograms when top-p set the boundary, else a pass).
+// Every thread gets the result.
+template <typename T>
+__device__ KeptSet gen_kept_set(const T* row, int V, GenShared& gs, const FloatPair* table,
+                                const smp_row_params& prm, uint32_t key_max) {
+  const int tid = threadIdx.x;
+  KeptSet ks;
+  ks.rs = make_row_scale(key_value<T>(key_max), prm.temperature);
+  const bool topk = prm.top_k > 0 && prm.top_k < V;
+  const bool topp = prm.top_p < 1.0f;
+  const bool minp = prm.min_p > 0.0f && prm.min_p < 1.0f;
+
+  // Prefix lengths of the enabled filters.
+  uint64_t len_k = uint64_t(V), len_p = uint64_t(V), len_m = uint64_t(V);
+  uint32_t key_min_p = 0;
+  if (minp) {
+    key_min_p = minp_threshold_key<T>(gs.bc32, table, ks.rs, prm.temperature, prm.min_p, key_max);
+    uint32_t c = 0;
+    gen_sweep<T>(row, V, [&](int, float z) { c += order_key<T>(z) >= key_min_p; });
+    len_m = block_sum_u32(c, gs.scan32);
+  }
+  GenBoundary bk{}, bp{};
+  uint64_t z_total = 0;
+  if (topk) {
+    bk = gen_select<T, false>(row, V, gs, uint32_t(prm.top_k), 1.0f, ks.rs, table, &z_total);
+    len_k = uint64_t(prm.top_k);
+  }
+  if (topp) {
+    bp = gen_select<T, true>(row, V, gs, 0, prm.top_p, ks.rs, table, &z_total);
+    len_p = uint64_t(bp.above) + bp.n;
+  }
+  uint64_t len = len_k < len_p ? len_k : len_p;
+  len = len < len_m ? len : len_m;
+  ks.len = len;
+  ks.key = 0;
+  ks.id_cut = 0xFFFFFFFFu;
+  GenBoundary bd{};
+  bool from_p = false, cut = false;
+  if (len < uint64_t(V)) {
+    cut = true;
+    if (minp && len == len_m) {
+      ks.key = key_min_p;   // every token at or above the threshold key
+    } else {
+      from_p = !(topk && len == len_k);
+      bd = from_p ? bp : bk;
+      ks.key = bd.key;
+      if (bd.n < bd.ties) {   // the id of the n-th member (id order) of the boundary's tie bucket
+        const int id = gen_walk<T, uint32_t>(row, V, bd.n - 1, gs, [&](int, float z) -> uint32_t {
+          return order_key<T>(z) == bd.key ? 1u : 0u;
+        });
+        ks.id_cut = uint32_t(id);
+      }
+    }
+  }
+  if (cut && from_p) {
+    ks.z_kept = bd.mass_above + uint64_t(bd.n) * bd.tie_mass;
+  } else if (!cut && topp) {
+    ks.z_kept = z_total;
+  } else {
+    uint64_t zl = 0;
+    gen_sweep<T>(row, V, [&](int i, float z) { zl += kept_mass<T>(ks, table, i, z); });
+    zl = warp_sum<uint64_t>(zl);
+    if ((tid & 31) == 0) gs.scan64[tid >> 5] = zl;
+    cta_sync();
+    uint64_t zk = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) zk += gs.scan64[w];
+    cta_sync();
+    ks.z_kept = zk;
+  }
+  return ks;
+}

@@ -28,12 +28,16 @@
 
 namespace smp {
 
+#include "select.cuh"
+
 // Statistics of one logit row, written by verify_pos_kernel.
 struct PosStat {
   float m;          // row maximum
   int32_t flags;    // kRowNonFinite / kRowBadDraft / kRowBadParams
-  uint64_t z;       // sum of fixed-point masses; greedy rows: the arg-max id
-  double ex;        // exp((z_x - m) / T) of the draft token (0 if none)
+  uint64_t z;       // sum of fixed-point masses (filtered rows: Z_S); greedy rows: the arg-max id
+  double ex;        // exp((z_x - m) / T) of the draft token (0 if none, or not kept)
+  uint32_t kkey;    // kept set: order key > kkey, or == kkey with id <= kid
+  uint32_t kid;     // (unfiltered rows: 0 and 0xFFFFFFFF, every token)
 };
 
 struct VerifyArgs {
@@ -52,28 +56,28 @@ struct VerifyArgs {
   const smp_row_params* params;   // [batch] or nullptr (T = 1 on every row)
 };
 
-// How batch row b is verified: temperature T > 0, greedy, or an error row.
-// Greedy (the flag, or T == 0) ignores the other knobs; otherwise T must be
-// finite and positive and every filter off, since no filter is applied.
+// How batch row b is verified: temperature T > 0 with or without filters,
+// greedy, or an error row.  The knob rules are the sampler's: greedy (the
+// flag, or T == 0) ignores the other knobs; otherwise the knobs must be valid
+// sampling knobs, and the filters that are on apply to every p and q row.
 struct RowMode {
   float temperature;
   bool greedy;
   bool bad;
+  bool filtered;
 };
 
 __device__ __forceinline__ RowMode row_mode(const VerifyArgs& a, int b) {
-  RowMode md{1.0f, false, false};
+  RowMode md{1.0f, false, false, false};
   if (a.params == nullptr) return md;
   const smp_row_params p = a.params[b];
-  if (p.greedy != 0 || p.temperature == 0.0f) {
+  if (row_is_greedy(p)) {
     md.greedy = true;
     return md;
   }
   md.temperature = p.temperature;
-  const bool valid = isfinite(p.temperature) && p.temperature > 0.0f && p.top_k >= 0 && p.top_p >= 0.0f &&
-                     p.min_p >= 0.0f;   // NaN fails the comparisons
-  const bool filtered = (p.top_k > 0 && p.top_k < a.vocab) || p.top_p < 1.0f || (p.min_p > 0.0f && p.min_p < 1.0f);
-  md.bad = !valid || filtered;
+  md.bad = !sampling_params_valid(p);
+  md.filtered = (p.top_k > 0 && p.top_k < a.vocab) || p.top_p < 1.0f || (p.min_p > 0.0f && p.min_p < 1.0f);
   return md;
 }
 
@@ -157,6 +161,42 @@ __device__ __forceinline__ void greedy_row_argmax(const T* row, int Vn, int head
 // mass Z (online: a running maximum per thread, its sum rescaled when the
 // maximum rises).  Thread 0 adds the draft token's mass (double-float
 // exponential) and the flags.
+// The statistic of one logit row of a filtered batch row: the row maximum,
+// the kept set S of eq. 39.2 under the row's knobs (the sampler's exact
+// selection over global memory), Z_S and the draft token's mass if it is in S.
+// Kept out of line so that the streaming path keeps its registers.
+template <typename T>
+__device__ __noinline__ void filtered_pos_stat(const VerifyArgs& a, const T* row, int pr, int b, int ipos,
+                                               GenShared& gs, const FloatPair* table) {
+  const int tid = threadIdx.x;
+  const int Vn = a.vocab;
+  const smp_row_params prm = a.params[b];
+  uint32_t kmax = 0;
+  gen_sweep<T>(row, Vn, [&](int, float z) { kmax = max(kmax, order_key<T>(z)); });
+  kmax = uint32_t(block_max_u64(uint64_t(kmax), gs.red64));
+  int flags = key_finite<T>(kmax) ? 0 : kRowNonFinite;
+  int xd = -1;
+  if (ipos < a.k) {
+    xd = a.drafts[size_t(b) * a.k + ipos];
+    if (xd < 0 || xd >= Vn) flags |= kRowBadDraft;
+  }
+  PosStat s;
+  s.m = key_value<T>(kmax);
+  s.z = 0;
+  s.ex = 0.0;
+  s.kkey = 0;
+  s.kid = 0xFFFFFFFFu;
+  if (!flags) {
+    const KeptSet ks = gen_kept_set<T>(row, Vn, gs, table, prm, kmax);
+    s.z = ks.z_kept;
+    s.kkey = ks.key;
+    s.kid = ks.id_cut;
+    if (ipos < a.k) s.ex = double(kept_mass<T>(ks, table, xd, Elem<T>::widen(row[xd]))) * (1.0 / double(kFixedOne));
+  }
+  s.flags = flags;
+  if (tid == 0) a.ws[pr] = s;
+}
+
 template <typename T>
 __global__ void __launch_bounds__(kThreads, 2) verify_pos_kernel(VerifyArgs a) {
   using V = VecOps<T>;
@@ -164,6 +204,7 @@ __global__ void __launch_bounds__(kThreads, 2) verify_pos_kernel(VerifyArgs a) {
   __shared__ FloatPair table[64];
   __shared__ float redf[kWarps];
   __shared__ uint64_t red64[kWarps];
+  __shared__ GenShared gen_shared;   // histograms of the filtered rows' selection
   const int tid = threadIdx.x;
   const int rows_per_b = 2 * a.k + 1;
   const int pr = int(blockIdx.x);
@@ -181,6 +222,8 @@ __global__ void __launch_bounds__(kThreads, 2) verify_pos_kernel(VerifyArgs a) {
       s.flags = md.bad ? kRowBadParams : 0;
       s.z = 0;
       s.ex = 0.0;
+      s.kkey = 0;
+      s.kid = 0xFFFFFFFFu;
       a.ws[pr] = s;
     }
     return;
@@ -188,6 +231,12 @@ __global__ void __launch_bounds__(kThreads, 2) verify_pos_kernel(VerifyArgs a) {
   if (tid < 64) table[tid] = kExp2Table[tid];
 
   const T* row = logit_row<T>(a, b, j);
+  const int ipos = j <= a.k ? j : j - a.k - 1;   // draft position of this row
+  if (md.filtered) {
+    cta_sync();   // the table is complete
+    filtered_pos_stat<T>(a, row, pr, b, ipos, gen_shared, table);
+    return;
+  }
   // The 16-byte aligned middle of the row, and the elements before and after it.
   const uintptr_t r0 = reinterpret_cast<uintptr_t>(row);
   const uintptr_t r1 = r0 + size_t(Vn) * sizeof(T);
@@ -201,7 +250,6 @@ __global__ void __launch_bounds__(kThreads, 2) verify_pos_kernel(VerifyArgs a) {
   const uint32_t ninf = V::neg_inf();
 
   // The draft token's logit, requested now so that the load overlaps the stream.
-  const int ipos = j <= a.k ? j : j - a.k - 1;   // draft position of this row
   int xd = -1;
   float zx = -INFINITY;
   if (tid == 0 && ipos < a.k) {
@@ -219,6 +267,8 @@ __global__ void __launch_bounds__(kThreads, 2) verify_pos_kernel(VerifyArgs a) {
       s.flags = (isfinite(gm) ? 0 : kRowNonFinite) | (ipos < a.k && (xd < 0 || xd >= Vn) ? kRowBadDraft : 0);
       s.z = uint64_t(uint32_t(gid));
       s.ex = 0.0;
+      s.kkey = 0;
+      s.kid = 0xFFFFFFFFu;
       a.ws[pr] = s;
     }
     return;
@@ -298,6 +348,8 @@ __global__ void __launch_bounds__(kThreads, 2) verify_pos_kernel(VerifyArgs a) {
     st.flags = flags;
     st.z = tot;
     st.ex = ex;
+    st.kkey = 0;
+    st.kid = 0xFFFFFFFFu;
     a.ws[pr] = st;
   }
 }
@@ -360,6 +412,7 @@ __global__ void __launch_bounds__(kResolveThreads, 2) verify_resolve_kernel(Veri
   __shared__ int32_t decision[2];   // first rejection j, row flags
   __shared__ float inv_z[2];        // 2^F / Z of the drawn row's p and q (binary32)
   __shared__ float row_m[2];        // the drawn row's p and q maxima
+  __shared__ uint32_t kept_desc[4]; // the drawn row's p and q kept sets (key, id) when filtered
   __shared__ uint64_t warp_tot[kResolveWarps];
   __shared__ uint64_t cta_slots[2][kResolveMaxCluster];   // one array per cluster_prefix call
   __shared__ uint64_t cta_bc[2];
@@ -441,6 +494,10 @@ __global__ void __launch_bounds__(kResolveThreads, 2) verify_resolve_kernel(Veri
       inv_z[0] = __fdiv_rn(float(kFixedOne), __ull2float_rn(P.z));
       row_m[1] = jr < K ? Q.m : P.m;
       inv_z[1] = jr < K ? __fdiv_rn(float(kFixedOne), __ull2float_rn(Q.z)) : inv_z[0];
+      kept_desc[0] = P.kkey;
+      kept_desc[1] = P.kid;
+      kept_desc[2] = jr < K ? Q.kkey : P.kkey;
+      kept_desc[3] = jr < K ? Q.kid : P.kid;
     }
   }
   __syncthreads();
@@ -478,9 +535,21 @@ __global__ void __launch_bounds__(kResolveThreads, 2) verify_resolve_kernel(Veri
   bool use_p = !residual;
   const float inv_zp = inv_z[0];
   const float inv_zq = inv_z[1];
-  auto weight_of = [&](float zp, float zq) -> uint64_t {
-    const float p = __fmul_rn(exp_fast(zp, rp), inv_zp);
-    const float r = use_p ? p : fmaxf(0.0f, __fsub_rn(p, __fmul_rn(exp_fast(zq, rq), inv_zq)));
+  // Filtered rows: p~ and q~ are 0 outside their kept sets (eq. 39.2).
+  const bool filt = md.filtered;
+  KeptSet kp, kq;
+  kp.key = kept_desc[0];
+  kp.id_cut = kept_desc[1];
+  kq.key = kept_desc[2];
+  kq.id_cut = kept_desc[3];
+  auto weight_of = [&](int id, float zp, float zq) -> uint64_t {
+    float p = __fmul_rn(exp_fast(zp, rp), inv_zp);
+    float q = use_p ? 0.0f : __fmul_rn(exp_fast(zq, rq), inv_zq);
+    if (filt) {
+      if (!in_kept_set(kp, order_key<T>(zp), uint32_t(id))) p = 0.0f;
+      if (!in_kept_set(kq, order_key<T>(zq), uint32_t(id))) q = 0.0f;
+    }
+    const float r = use_p ? p : fmaxf(0.0f, __fsub_rn(p, q));
     // rn(r * 2^52) from two 32-bit conversions: s = r * 2^28 <= 2^28 splits
     // exactly into its integer part and fraction; the fraction times 2^24
     // rounds like the whole (the integer part times 2^24 is even).
@@ -526,7 +595,7 @@ __global__ void __launch_bounds__(kResolveThreads, 2) verify_resolve_kernel(Veri
             zp = gg + e < c1 ? Elem<T>::widen(prow[gg + e]) : -INFINITY;
             zq = gg + e < c1 ? Elem<T>::widen(qrow[gg + e]) : -INFINITY;
           }
-          sum += weight_of(zp, zq);
+          sum += weight_of(gg + e, zp, zq);
         }
       }
     }
@@ -559,7 +628,7 @@ __global__ void __launch_bounds__(kResolveThreads, 2) verify_resolve_kernel(Veri
     uint64_t run = owner_before;
     for (int base = o0; base < o1; base += 32) {
       const int i = base + lane;
-      const uint64_t w = i < o1 ? weight_of(Elem<T>::widen(prow[i]), Elem<T>::widen(qrow[i])) : 0ull;
+      const uint64_t w = i < o1 ? weight_of(i, Elem<T>::widen(prow[i]), Elem<T>::widen(qrow[i])) : 0ull;
       const uint64_t incl = warp_inclusive_scan<uint64_t>(w);
       const uint32_t hit = __ballot_sync(0xFFFFFFFFu, i < o1 && run + incl > t);
       if (hit) {

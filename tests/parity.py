@@ -76,7 +76,7 @@ def compare_verify(oracle_rows, gpu_acc, gpu_ids):
         v.compared += 1
         same = int(gpu_acc[b]) == res["accepted"] and list(map(int, gpu_ids[b])) == res["ids"]
         if not same:
-            margin = min(res["accept_margin"], res["draw_margin"])
+            margin = min(res["accept_margin"], res["draw_margin"], res.get("filter_margin", math.inf))
             entry = (b, int(gpu_acc[b]), list(map(int, gpu_ids[b])), res["accepted"], res["ids"], margin)
             (v.excused if margin < BAND else v.failed).append(entry)
     return v

@@ -62,7 +62,7 @@ def test_host_validation_without_gpu(lib):
     assert lib.smp_spec_verify(fake, fake, fake, 2, 17, 8, 0, 0, 0, fake, fake, null, fake, 1 << 20, null) == 1
     assert lib.smp_spec_verify(fake, fake, fake, 2, 4, 8, 0, 0, 0, fake, fake, null, null, 1 << 20, null) == 5
     need = lib.smp_spec_verify_workspace_bytes(2, 4)
-    assert need == 2 * 9 * 24
+    assert need == 2 * 9 * 32
     assert lib.smp_spec_verify(fake, fake, fake, 2, 4, 8, 0, 0, 0, fake, fake, null, fake, need - 1, null) == 5
     # the per-row-knob entry: the same checks, and a misaligned params pointer
     assert lib.smp_spec_verify_params(fake, fake, fake, 2, 0, 8, 0, fake, 0, 0, fake, fake, null, fake,

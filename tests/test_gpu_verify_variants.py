@@ -1,8 +1,9 @@
 """CUDA verifier with per-row knobs (smp_spec_verify_params, through the C ABI)
-against the fp64 oracle: temperature on p and q ("Speculative decoding --
-Hinglish notes", section "Temperature and Sampling"), greedy verification
-("Inference: Sampling, the KV Cache, Speculative Decoding and int8", section
-"Speculative decoding"), and rows whose knobs are invalid."""
+against the fp64 oracle: temperature and filters on p and q ("Speculative
+decoding -- Hinglish notes", section "Temperature and Sampling"; eq. 39.2 of
+"Decoding & Speculative Sampling"), greedy verification ("Inference: Sampling,
+the KV Cache, Speculative Decoding and int8", section "Speculative decoding"),
+and rows whose knobs are invalid."""
 
 import numpy as np
 import pytest
@@ -127,7 +128,7 @@ def test_mixed_modes_and_bad_knobs():
     drafts = drafts_from_q(vb.values("q"), np.where(prm["temperature"] > 0, prm["temperature"], 1.0)
                            .astype(np.float32).clip(0.1, 10))
     acc, ids, status = run(vb.p, vb.q, "f32", drafts, prm, 21, 4)
-    bad = [7, 8, 9, 10, 11, 12, 15]
+    bad = [7, 8, 9, 15]   # rows 10..12 are filtered (drafts drawn without the filters)
     assert status == binding.ROW_BAD_PARAMS
     assert all(acc[r] == -1 and np.all(ids[r] == -1) for r in bad)
     want = over.spec_verify(vb.values("p"), vb.values("q"), drafts, 21, 4, params=prm)
@@ -168,3 +169,62 @@ def test_temperature_verify_output_follows_target_chi_square():
         target = over.softmax64(zp[pos], t) * reached.sum()
         stat = float(np.sum((counts - target) ** 2 / target))
         assert stat < 24.32, (pos, stat)   # chi-square, 7 degrees of freedom, p = 0.001
+
+
+def drafts_from_filtered_q(q_values, prm):
+    """Draft ids drawn from q~ with each batch row's knobs (oracle sampler)."""
+    b, k, v = q_values.shape
+    res = osam.sample(q_values.reshape(b * k, v), np.repeat(prm, k), 1, 0)
+    return np.array([r["token"] for r in res], dtype=np.int32).reshape(b, k)
+
+
+FILTER_KNOBS = [  # (temperature, top_k, top_p, min_p)
+    (1.0, 5, 1.0, 0.0), (0.7, 40, 1.0, 0.0), (1.0, 0, 0.9, 0.0), (1.5, 0, 0.5, 0.0),
+    (1.0, 0, 1.0, 0.05), (0.8, 0, 1.0, 0.2), (0.9, 40, 0.9, 0.05), (1.2, 100, 0.95, 0.02),
+    (1.0, 0, 1.0, 0.0), (0.6, 1, 1.0, 0.0), (1.0, 0, 0.999, 0.0), (2.0, 3, 0.8, 0.1),
+]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("k,vocab", [(3, 517), (4, 4099), (4, 32000)])
+def test_filtered_parity(dtype, k, vocab):
+    batch = 24
+    vb = workloads.verify_workload(batch=batch, k=k, vocab=vocab, dtype=dtype, seed_id=400 + vocab % 97 + k)
+    prm = workloads.make_params(batch)
+    for r in range(batch):
+        t, tk, tp, mp = FILTER_KNOBS[r % len(FILTER_KNOBS)]
+        prm[r] = (t, tk, tp, mp, 0)
+    drafts = drafts_from_filtered_q(vb.values("q"), prm)
+    acc, ids, status = run(vb.p, vb.q, dtype, drafts, prm, 13, 7)
+    assert status == 0
+    want = over.spec_verify(vb.values("p"), vb.values("q"), drafts, 13, 7, params=prm)
+    compare_verify(want, acc, ids).check()
+    assert any(r["accepted"] < k for r in want) and any(r["accepted"] > 0 for r in want)
+
+
+def test_filtered_output_follows_filtered_target():
+    # p = (.4, .3, .2, .1), q = (.3, .1, .4, .2), top_k = 2 on both: p~ = (4/7, 3/7, 0, 0),
+    # q~ = (3/7, 0, 4/7, 0); mean accepted length sum min(p~, q~) = 3/7 (K = 1), and
+    # both emitted positions follow p~.
+    rows = 200_000
+    zp = np.log([0.4, 0.3, 0.2, 0.1]).astype(np.float32)
+    zq = np.log([0.3, 0.1, 0.4, 0.2]).astype(np.float32)
+    P = np.ascontiguousarray(np.tile(np.stack([zp, zp]), (rows, 1, 1)))
+    Q = np.ascontiguousarray(np.tile(zq[None], (rows, 1, 1)))
+    prm = workloads.make_params(rows, top_k=2)
+    ql = torch.from_numpy(Q.reshape(rows, 4)).cuda()
+    d, _, _ = binding.sample(ql, prm, 1, 0)
+    drafts = d.view(rows, 1).cpu().numpy()
+    assert set(np.unique(drafts)) == {0, 2}
+    acc, ids, status = run(P, Q, "f32", drafts, prm, 0, 0)
+    assert status == 0
+    alpha = 3 / 7
+    assert abs(acc.mean() - alpha) < 4 * np.sqrt(alpha * (1 - alpha) / rows)
+    p_tilde = np.array([4 / 7, 3 / 7, 0, 0])
+    for pos in (0, 1):
+        reached = acc >= pos
+        counts = np.bincount(ids[reached, pos], minlength=4)
+        assert counts[2] == 0 and counts[3] == 0
+        target = p_tilde[:2] * reached.sum()
+        stat = float(np.sum((counts[:2] - target) ** 2 / target))
+        assert stat < 10.83, (pos, stat)   # chi-square, 1 degree of freedom, p = 0.001

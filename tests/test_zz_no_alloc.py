@@ -78,7 +78,7 @@ def test_static_rejects_batches_beyond_the_array():
     lib = binding.load()
     fake = ctypes.c_void_p(0x1000)
     null = ctypes.c_void_p(0)
-    # 4096 rows with k = 16 need 4096 * 33 * 24 bytes, more than the 1 MiB array
+    # 4096 rows with k = 16 need 4096 * 33 * 32 bytes, more than the 1 MiB array
     assert binding.spec_verify_workspace_bytes(4096, 16) > binding.STATIC_VERIFY_SCRATCH_BYTES
     rc = lib.smp_spec_verify_static(fake, fake, fake, 4096, 16, 1000, binding.SMP_F32, 0, 0, fake, fake,
                                     null, null)

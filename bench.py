@@ -276,6 +276,20 @@ def run_gpu(args):
         binding.spec_verify(p_dev[i % v_copies], q_dev[i % v_copies], drafts, seed, i, ws, v_acc, v_ids,
                             v_status)
 
+    # Verifier variants on the same batch: temperature, greedy, filters (each
+    # with drafts drawn from q under the same knobs, by the CUDA sampler).
+    variant_knobs = {"temperature_0.8": dict(temperature=0.8), "greedy": dict(greedy=1),
+                     "top_k40_top_p0.9_T0.8": dict(temperature=0.8, top_k=40, top_p=0.9)}
+    variants = {}
+
+    def variant_call(name):
+        vprm, vdrafts, _ = variants[name]
+
+        def call(i):
+            binding.spec_verify_params(p_dev[i % v_copies], q_dev[i % v_copies], vdrafts, vprm, seed, i, ws,
+                                       v_acc, v_ids, v_status)
+        return call
+
     # warm-up (also sets kernel attributes before any capture)
     for i in range(max(args.warmup, 3)):
         sampler_call(i)
@@ -318,6 +332,33 @@ def run_gpu(args):
         kern_ms = timed(g_kern, 1)
         ver_ms = timed(g_ver, 1)
     clock_info = clocks.summary()
+    acc_mean = float(v_acc.float().mean().item())   # accepted lengths of the plain verifier's last call
+
+    # Verifier variants, set up and timed after the headline graphs.
+    for name, knobs in variant_knobs.items():
+        vprm = binding.params_to_device(workloads.make_params(vB, **knobs), dev)
+        dprm = workloads.make_params(vB * vK, **knobs)
+        dv, _, _ = binding.sample(q_dev[0].view(vB * vK, vV), dprm, vb.draft_seed, vb.draft_offset)
+        variants[name] = (vprm, dv.view(vB, vK).contiguous(), knobs)
+    var_ms = {}
+    for name in variants:
+        call = variant_call(name)
+        for i in range(max(args.warmup, 3)):
+            call(i)
+        torch.cuda.synchronize()
+        assert int(v_status.cpu()[0]) == 0
+        g = capture(call)
+        ms = timed(g, 1)
+        var_ms[name] = (ms, float(v_acc.float().mean().item()))   # accepted lengths of the last call
+        del g
+    verify_variants = {}
+    for name, (ms, accepted) in var_ms.items():
+        us = 1000.0 * ms / args.steps
+        nbytes = vb.p.nbytes if "greedy" in name else v_bytes   # greedy reads no draft row
+        verify_variants[name] = {"us_per_call": us, "mean_accepted": accepted,
+                                 "tok_s": world * vB * (accepted + 1.0) / (us * 1e-6),
+                                 "bytes_per_call": nbytes, "gbs": nbytes / (us * 1e-6) / 1e9,
+                                 "knobs": variants[name][2]}
 
     # per step: clear_status_kernel + sample_kernel, clear_status_kernel + verify_pos_kernel +
     # verify_resolve_kernel
@@ -326,7 +367,6 @@ def run_gpu(args):
     kern_us = 1000.0 * kern_ms / args.steps
     ver_us = 1000.0 * ver_ms / args.steps
     rows_per_s = job_rate(B, world, samp_us * 1e-6)
-    acc_mean = float(v_acc.float().mean().item())
     verify_tok_s = world * vB * (acc_mean + 1.0) / (ver_us * 1e-6)
 
     # roofline of the sampler kernel: logits read once, ids + probs written, params read
@@ -414,7 +454,8 @@ def run_gpu(args):
             "pct_of_measured_hbm": 100.0 * achieved / peak,
             "pct_of_8tbs_nominal": 100.0 * achieved / NOMINAL_HBM_GBS,
             "verify": {"tok_s": verify_tok_s, "us_per_call": ver_us, "mean_accepted": acc_mean,
-                       "bytes_per_call": v_bytes, "gbs": v_bytes / (ver_us * 1e-6) / 1e9},
+                       "bytes_per_call": v_bytes, "gbs": v_bytes / (ver_us * 1e-6) / 1e9,
+                       "variants": verify_variants},
             "roofline": roofline,
             "cpu_baseline": cpu_baseline,
             "e2e": e2e,

@@ -21,6 +21,7 @@
 
 #include <climits>
 #include <mutex>
+#include <type_traits>
 
 #include "launch.h"
 #include "row_ops.cuh"
@@ -67,9 +68,10 @@ struct RowMode {
   bool filtered;
 };
 
+template <bool kParams>
 __device__ __forceinline__ RowMode row_mode(const VerifyArgs& a, int b) {
   RowMode md{1.0f, false, false, false};
-  if (a.params == nullptr) return md;
+  if (!kParams || a.params == nullptr) return md;
   const smp_row_params p = a.params[b];
   if (row_is_greedy(p)) {
     md.greedy = true;
@@ -164,10 +166,10 @@ __device__ __forceinline__ void greedy_row_argmax(const T* row, int Vn, int head
 // The statistic of one logit row of a filtered batch row: the row maximum,
 // the kept set S of eq. 39.2 under the row's knobs (the sampler's exact
 // selection over global memory), Z_S and the draft token's mass if it is in S.
-// Kept out of line so that the streaming path keeps its registers.
 template <typename T>
-__device__ __noinline__ void filtered_pos_stat(const VerifyArgs& a, const T* row, int pr, int b, int ipos,
-                                               GenShared& gs, const FloatPair* table) {
+__device__ __forceinline__ void filtered_pos_stat(const VerifyArgs& a, const T* row, int pr, int b, int ipos,
+                                                  const FloatPair* table) {
+  __shared__ GenShared gs;   // histograms of the selection
   const int tid = threadIdx.x;
   const int Vn = a.vocab;
   const smp_row_params prm = a.params[b];
@@ -197,14 +199,16 @@ __device__ __noinline__ void filtered_pos_stat(const VerifyArgs& a, const T* row
   if (tid == 0) a.ws[pr] = s;
 }
 
-template <typename T>
+// kParams: the call has per-row knobs (smp_spec_verify_params with params);
+// without them the kernels carry neither the greedy nor the filtered code
+// and no selection state in shared memory.
+template <typename T, bool kParams>
 __global__ void __launch_bounds__(kThreads, 2) verify_pos_kernel(VerifyArgs a) {
   using V = VecOps<T>;
   constexpr int kPer = V::kPer;
   __shared__ FloatPair table[64];
   __shared__ float redf[kWarps];
   __shared__ uint64_t red64[kWarps];
-  __shared__ GenShared gen_shared;   // histograms of the filtered rows' selection
   const int tid = threadIdx.x;
   const int rows_per_b = 2 * a.k + 1;
   const int pr = int(blockIdx.x);
@@ -213,7 +217,7 @@ __global__ void __launch_bounds__(kThreads, 2) verify_pos_kernel(VerifyArgs a) {
   const int Vn = a.vocab;
   grid_dependency_wait();
   allow_dependent_launch();
-  const RowMode md = row_mode(a, b);
+  const RowMode md = row_mode<kParams>(a, b);
   if (md.bad || (md.greedy && j > a.k)) {
     // An error row's statistics carry the flag; greedy rows read no q row.
     if (tid == 0) {
@@ -232,10 +236,12 @@ __global__ void __launch_bounds__(kThreads, 2) verify_pos_kernel(VerifyArgs a) {
 
   const T* row = logit_row<T>(a, b, j);
   const int ipos = j <= a.k ? j : j - a.k - 1;   // draft position of this row
-  if (md.filtered) {
-    cta_sync();   // the table is complete
-    filtered_pos_stat<T>(a, row, pr, b, ipos, gen_shared, table);
-    return;
+  if constexpr (kParams) {
+    if (md.filtered) {
+      cta_sync();   // the table is complete
+      filtered_pos_stat<T>(a, row, pr, b, ipos, table);
+      return;
+    }
   }
   // The 16-byte aligned middle of the row, and the elements before and after it.
   const uintptr_t r0 = reinterpret_cast<uintptr_t>(row);
@@ -407,7 +413,7 @@ __device__ __forceinline__ uint64_t cluster_prefix(uint64_t v, uint64_t* slots, 
 // owns the token ids [g C, (g + 1) C): weights are 52-bit fixed point with
 // exact integer sums; CTA and cluster scans find the chunk that holds the
 // draw, and warp 0 of its CTA walks it.
-template <typename T>
+template <typename T, bool kParams>
 __global__ void __launch_bounds__(kResolveThreads, 2) verify_resolve_kernel(VerifyArgs a) {
   __shared__ int32_t decision[2];   // first rejection j, row flags
   __shared__ float inv_z[2];        // 2^F / Z of the drawn row's p and q (binary32)
@@ -431,7 +437,7 @@ __global__ void __launch_bounds__(kResolveThreads, 2) verify_resolve_kernel(Veri
   hw_cluster_sync();        // every CTA of the cluster has started (remote stores below)
   grid_dependency_wait();   // the position statistics come from verify_pos_kernel
   allow_dependent_launch();
-  const RowMode md = row_mode(a, b);
+  const RowMode md = row_mode<kParams>(a, b);
 
   // Greedy verification (and error rows): lane i compares draft i with the
   // target's arg-max of position i; the first mismatch j emits the arg-max of
@@ -542,10 +548,12 @@ __global__ void __launch_bounds__(kResolveThreads, 2) verify_resolve_kernel(Veri
   kp.id_cut = kept_desc[1];
   kq.key = kept_desc[2];
   kq.id_cut = kept_desc[3];
-  auto weight_of = [&](int id, float zp, float zq) -> uint64_t {
+  // kFilt (a std::bool_constant) selects the membership test at compile
+  // time, so unfiltered rows run the loops without it.
+  auto weight_of = [&](auto kFilt, int id, float zp, float zq) -> uint64_t {
     float p = __fmul_rn(exp_fast(zp, rp), inv_zp);
     float q = use_p ? 0.0f : __fmul_rn(exp_fast(zq, rq), inv_zq);
-    if (filt) {
+    if constexpr (decltype(kFilt)::value) {
       if (!in_kept_set(kp, order_key<T>(zp), uint32_t(id))) p = 0.0f;
       if (!in_kept_set(kq, order_key<T>(zq), uint32_t(id))) q = 0.0f;
     }
@@ -561,7 +569,7 @@ __global__ void __launch_bounds__(kResolveThreads, 2) verify_resolve_kernel(Veri
   // The thread's weights: all its vectors requested first, then a rolled
   // loop over the groups (this code runs once per CTA, cold in the
   // instruction cache, so it is kept short).
-  auto chunk_sum = [&]() -> uint64_t {
+  auto chunk_sum = [&](auto kFilt) -> uint64_t {
     uint64_t sum = 0;
     const uint32_t ninf = VecOps<T>::neg_inf();
     for (int g0 = c0; g0 < c1; g0 += kGroups * kPer) {
@@ -595,18 +603,19 @@ __global__ void __launch_bounds__(kResolveThreads, 2) verify_resolve_kernel(Veri
             zp = gg + e < c1 ? Elem<T>::widen(prow[gg + e]) : -INFINITY;
             zq = gg + e < c1 ? Elem<T>::widen(qrow[gg + e]) : -INFINITY;
           }
-          sum += weight_of(gg + e, zp, zq);
+          sum += weight_of(kFilt, gg + e, zp, zq);
         }
       }
     }
     return sum;
   };
-  uint64_t local = chunk_sum(), cta_total = 0, total = 0;
+  auto chunk_sum_row = [&]() { return filt ? chunk_sum(std::true_type{}) : chunk_sum(std::false_type{}); };
+  uint64_t local = chunk_sum_row(), cta_total = 0, total = 0;
   uint64_t before = resolve_scan(local, warp_tot, &cta_total);
   uint64_t cta_before = cluster_prefix(cta_total, cta_slots[0], cta_bc, &total);
   if (residual && total == 0) {   // zero residual mass (rounding only): draw from p_j
     use_p = true;
-    local = chunk_sum();
+    local = chunk_sum_row();
     before = resolve_scan(local, warp_tot, &cta_total);
     cta_before = cluster_prefix(cta_total, cta_slots[1], cta_bc, &total);
   }
@@ -628,7 +637,10 @@ __global__ void __launch_bounds__(kResolveThreads, 2) verify_resolve_kernel(Veri
     uint64_t run = owner_before;
     for (int base = o0; base < o1; base += 32) {
       const int i = base + lane;
-      const uint64_t w = i < o1 ? weight_of(i, Elem<T>::widen(prow[i]), Elem<T>::widen(qrow[i])) : 0ull;
+      const float zp = i < o1 ? Elem<T>::widen(prow[i]) : 0.0f, zq = i < o1 ? Elem<T>::widen(qrow[i]) : 0.0f;
+      const uint64_t w = i >= o1 ? 0ull
+                         : filt  ? weight_of(std::true_type{}, i, zp, zq)
+                                 : weight_of(std::false_type{}, i, zp, zq);
       const uint64_t incl = warp_inclusive_scan<uint64_t>(w);
       const uint32_t hit = __ballot_sync(0xFFFFFFFFu, i < o1 && run + incl > t);
       if (hit) {
@@ -655,7 +667,11 @@ static smp_status launch_verify(VerifyArgs a, cudaStream_t stream) {
   LaunchShape ls;   // one CTA per logit row, then one per batch row; no dynamic shared memory
   ls.pdl = true;
   cudaError_t err;
-  err = launch_cluster(reinterpret_cast<const void*>(&verify_pos_kernel<T>), dim3(rows), dim3(kThreads), ls,
+  const void* pos = a.params ? reinterpret_cast<const void*>(&verify_pos_kernel<T, true>)
+                             : reinterpret_cast<const void*>(&verify_pos_kernel<T, false>);
+  const void* resolve = a.params ? reinterpret_cast<const void*>(&verify_resolve_kernel<T, true>)
+                                 : reinterpret_cast<const void*>(&verify_resolve_kernel<T, false>);
+  err = launch_cluster(pos, dim3(rows), dim3(kThreads), ls,
                        stream, &a);
   if (err != cudaSuccess) return fail_cuda(err);
   // Enough CTAs per batch row to cover the GPU twice over, at most one portable cluster.
@@ -663,7 +679,7 @@ static smp_status launch_verify(VerifyArgs a, cudaStream_t stream) {
   const int sms = device_sms(dev);
   while (lr.cluster < kResolveMaxCluster && int64_t(a.batch) * lr.cluster < 2 * sms) lr.cluster *= 2;
   if (forced_cluster() && forced_cluster() <= kResolveMaxCluster) lr.cluster = forced_cluster();
-  err = launch_cluster(reinterpret_cast<const void*>(&verify_resolve_kernel<T>), dim3(a.batch * lr.cluster),
+  err = launch_cluster(resolve, dim3(a.batch * lr.cluster),
                        dim3(kResolveThreads), lr, stream, &a);
   if (err != cudaSuccess) return fail_cuda(err);
   return SMP_OK;

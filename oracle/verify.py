@@ -99,6 +99,19 @@ def _distribution(row, temperature, filters):
     return p_tilde, min(diag["topp_margin"], diag["minp_margin"])
 
 
+def acceptance_rates(p_rows, q_rows, temperature=1.0, filters=None):
+    """alpha_i = sum_x min(p_i(x), q_i(x)) for every draft position i: the
+    probability that position i's proposal is kept ("Decoding & Speculative
+    Sampling", section 39.4 and Listing 39.5), on the distributions the
+    verifier compares (temperature and filters applied)."""
+    out = []
+    for i in range(len(q_rows)):
+        p, _ = _distribution(p_rows[i], temperature, filters)
+        q, _ = _distribution(q_rows[i], temperature, filters)
+        out.append(float(np.sum(np.minimum(p, q))))
+    return out
+
+
 def verify_row(p_rows, q_rows, drafts, uniforms, temperature=1.0, greedy=False, filters=None):
     """Verify one batch row.
 
@@ -186,9 +199,11 @@ def row_mode(prm, vocab):
 
 
 def spec_verify(p_logits, q_logits, draft_ids, seed, offset, rows=None, temperature=1.0, greedy=False,
-                params=None):
+                params=None, alpha=False):
     """Run verify_row over a batch (temperature and greedy for all its rows,
     or per row from `params`, one record per batch row, see row_mode).
+    alpha: also return each row's acceptance rates ("alpha", K values; NaN
+    for greedy and error rows, which compare no distributions).
 
     p_logits: [B, K+1, V]; q_logits: [B, K, V]; draft_ids: [B, K].
     Uniform for batch row b, draw d: philox.uniform(seed, offset, b, d).
@@ -208,11 +223,19 @@ def spec_verify(p_logits, q_logits, draft_ids, seed, offset, rows=None, temperat
             if status != ROW_OK:
                 res = {"accepted": -1, "ids": [-1] * (k + 1), "status": status, "accept_margin": math.inf,
                        "draw_margin": math.inf, "filter_margin": math.inf, "row": int(b)}
+                if alpha:
+                    res["alpha"] = [math.nan] * k
                 results.append(res)
                 continue
         else:
             t_row, g_row, f_row = temperature, greedy, None
         res = verify_row(p_logits[b], q_logits[b], draft_ids[b], us, t_row, g_row, f_row)
+        if alpha:
+            g_eff = bool(g_row) or float(t_row) == 0.0
+            if res["status"] != ROW_OK or g_eff:
+                res["alpha"] = [math.nan] * k
+            else:
+                res["alpha"] = acceptance_rates(p_logits[b], q_logits[b], t_row, f_row)
         res["row"] = int(b)
         results.append(res)
     return results

@@ -103,6 +103,11 @@ def _distribution_unfiltered(row, temperature, filters):
     return verify_mod.softmax64(row, temperature), float("inf")
 
 
+def _alpha_of_p_only(p_rows, q_rows, temperature=1.0, filters=None):
+    return [float(np.sum(np.minimum(verify_mod.softmax64(p_rows[i], temperature), 1.0)))
+            for i in range(len(q_rows))]
+
+
 def _fd_no_renorm(original):
     def wrapped(row, temperature, top_k=0, top_p=1.0, min_p=0.0):
         p, keep, _, diag = original(row, temperature, top_k, top_p, min_p)
@@ -146,6 +151,9 @@ MUTANTS = [
      [t_variants.test_filters_with_disjoint_kept_sets_reject_every_draft,
       lambda: t_variants.test_filtered_acceptance_rate_and_output({"top_k": 2}, [4 / 7, 3 / 7, 0, 0],
                                                                    [3 / 7, 0, 4 / 7, 0])]),
+    ("acceptance rate ignores q", verify_mod, "acceptance_rates", _alpha_of_p_only,
+     [lambda: t_variants.test_acceptance_rate_three_token_example(load_golden),
+      t_variants.test_acceptance_rate_is_one_minus_total_variation]),
     ("renormalisation dropped", sampler_mod, "filtered_distribution",
      _fd_no_renorm(sampler_mod.filtered_distribution),
      [lambda: t_pins.test_exercise_39_1(load_golden), t_props.test_renormalisation_invariants]),

@@ -249,3 +249,60 @@ def test_top_k_one_is_greedy_verification():
     greedy = over.spec_verify(p, q, drafts, 6, 0, greedy=True)
     assert [x["ids"] for x in top1] == [x["ids"] for x in greedy]
     assert any(x["accepted"] > 0 for x in greedy)
+
+
+# ------------------------------------------------------------------ acceptance rates
+
+
+def test_acceptance_rate_three_token_example(golden):
+    # the page's example: p = (.2, .5, .3), q = (.5, .3, .2), total acceptance 0.7
+    g = golden("three_token_example.json")
+    p = np.log(np.array(g["p"]))[None].astype(np.float64)
+    q = np.log(np.array(g["q"]))[None].astype(np.float64)
+    assert abs(over.acceptance_rates(np.concatenate([p, p]), q)[0] - g["total_acceptance"]) < 1e-12
+
+
+def test_acceptance_rate_is_one_minus_total_variation():
+    # sum min(p, q) = 1 - (1/2) sum |p - q| for any two distributions
+    b, k, v = 6, 3, 50
+    p, q = batch(b, k, v, seed=23)
+    for r in range(b):
+        for t in (0.6, 1.0, 1.7):
+            got = over.acceptance_rates(p[r], q[r], t)
+            for i in range(k):
+                pi, qi = over.softmax64(p[r, i], t), over.softmax64(q[r, i], t)
+                assert abs(got[i] - (1.0 - 0.5 * np.sum(np.abs(pi - qi)))) < 1e-12
+
+
+def test_acceptance_rate_matches_simulated_acceptance():
+    # with K = 1 and drafts drawn from q, the accepted fraction estimates alpha_0
+    rows, v = 20000, 6
+    rng = np.random.default_rng(29)
+    zp = rng.normal(0, 1.2, (2, v)).astype(np.float32)
+    zq = rng.normal(0, 1.2, (1, v)).astype(np.float32)
+    P = np.tile(zp, (rows, 1, 1))
+    Q = np.tile(zq, (rows, 1, 1))
+    drafts = _drafts_from_filtered_q(Q, _unit_params())
+    res = over.spec_verify(P, Q, drafts, 8, 0, rows=range(rows), alpha=True)
+    alpha = res[0]["alpha"][0]
+    assert all(r["alpha"] == [alpha] for r in res[:5])
+    acc = np.mean([r["accepted"] for r in res])
+    assert abs(acc - alpha) < 4 * np.sqrt(alpha * (1 - alpha) / rows)
+
+
+def _unit_params():
+    from spec_verify_gb300 import workloads
+    return workloads.make_params(1)
+
+
+def test_acceptance_rate_filtered_and_undefined_rows():
+    from spec_verify_gb300 import workloads
+    rows = 3
+    P = _tiled(rows, P4, P4)
+    Q = _tiled(rows, np.log([0.3, 0.1, 0.4, 0.2]))
+    prm = workloads.make_params(rows, top_k=2)
+    prm["greedy"][1] = 1
+    prm["temperature"][2] = -1.0
+    res = over.spec_verify(P, Q, np.zeros((rows, 1), dtype=np.int32), 0, 0, params=prm, alpha=True)
+    assert abs(res[0]["alpha"][0] - 3 / 7) < 1e-7      # float32 logits; sum min((4/7, 3/7, 0, 0), (3/7, 0, 4/7, 0))
+    assert np.isnan(res[1]["alpha"][0]) and np.isnan(res[2]["alpha"][0])

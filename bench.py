@@ -279,7 +279,9 @@ def run_gpu(args):
     # Verifier variants on the same batch: temperature, greedy, filters (each
     # with drafts drawn from q under the same knobs, by the CUDA sampler).
     variant_knobs = {"temperature_0.8": dict(temperature=0.8), "greedy": dict(greedy=1),
-                     "top_k40_top_p0.9_T0.8": dict(temperature=0.8, top_k=40, top_p=0.9)}
+                     "top_k40_top_p0.9_T0.8": dict(temperature=0.8, top_k=40, top_p=0.9),
+                     "alpha_T1": dict()}   # T = 1, and the acceptance rates of every position
+    v_alpha = torch.empty(vB, vK, dtype=torch.float32, device=dev)
     variants = {}
 
     def variant_call(name):
@@ -287,7 +289,7 @@ def run_gpu(args):
 
         def call(i):
             binding.spec_verify_params(p_dev[i % v_copies], q_dev[i % v_copies], vdrafts, vprm, seed, i, ws,
-                                       v_acc, v_ids, v_status)
+                                       v_acc, v_ids, v_status, out_alpha=v_alpha if name == "alpha_T1" else None)
         return call
 
     # warm-up (also sets kernel attributes before any capture)

@@ -187,17 +187,28 @@ smp_status smp_spec_verify(const void* p_logits, const void* q_logits, const int
  *                used and q_logits is not read for that row (its values,
  *                finite or not, do not matter); the other knobs are ignored.
  *   params       device, [batch] smp_row_params, or NULL for T = 1 and no
- *                filters on every row (then the call is smp_spec_verify).
- *                Knob validity is the sampler's; a row with invalid knobs
- *                gets accepted length -1, ids -1 and SMP_ROW_BAD_PARAMS.
+ *                filters on every row (then, without out_alpha, the call is
+ *                smp_spec_verify).  Knob validity is the sampler's; a row
+ *                with invalid knobs gets accepted length -1, ids -1 and
+ *                SMP_ROW_BAD_PARAMS.
+ *   out_alpha    device, [batch, k] float, or NULL: the acceptance rate of
+ *                every draft position, alpha_i = sum_x min(p_i(x), q_i(x))
+ *                on the compared distributions (after temperature and
+ *                filters), the probability that a proposal drawn from q_i
+ *                is kept ("Decoding & Speculative Sampling", section 39.4
+ *                and Listing 39.5), computed for all k positions whatever
+ *                was accepted; within about 1e-5 (binary32 probabilities,
+ *                exact fixed-point sums).  NaN for greedy rows (no q is
+ *                compared) and error rows.  It costs one more pass over the
+ *                k (p, q) row pairs, normally from L2.
  * Every other argument, the workspace and the error behaviour are those of
  * smp_spec_verify.
  */
 smp_status smp_spec_verify_params(const void* p_logits, const void* q_logits, const int32_t* draft_ids,
                                   int32_t batch, int32_t k, int32_t vocab, smp_dtype dtype,
                                   const smp_row_params* params, uint64_t seed, uint64_t offset,
-                                  int32_t* out_accepted_len, int32_t* out_ids, int32_t* status,
-                                  void* workspace, size_t workspace_bytes, void* stream);
+                                  int32_t* out_accepted_len, int32_t* out_ids, float* out_alpha,
+                                  int32_t* status, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * Size of the device array that smp_spec_verify_static uses as its workspace

@@ -62,7 +62,8 @@ def load():
     lib.smp_spec_verify_workspace_bytes.restype = sz
     lib.smp_spec_verify.argtypes = [vp, vp, vp, i32, i32, i32, i32, u64, u64, vp, vp, vp, vp, sz, vp]
     lib.smp_spec_verify.restype = i32
-    lib.smp_spec_verify_params.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, u64, u64, vp, vp, vp, vp, sz, vp]
+    lib.smp_spec_verify_params.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, u64, u64, vp, vp, vp, vp, vp, sz,
+                                           vp]
     lib.smp_spec_verify_params.restype = i32
     lib.smp_spec_verify_static.argtypes = [vp, vp, vp, i32, i32, i32, i32, u64, u64, vp, vp, vp, vp]
     lib.smp_spec_verify_static.restype = i32
@@ -212,10 +213,12 @@ def spec_verify(p_logits, q_logits, draft_ids, seed=0, offset=0, workspace=None,
 
 
 def spec_verify_params(p_logits, q_logits, draft_ids, params, seed=0, offset=0, workspace=None,
-                       out_accepted=None, out_ids=None, status=None, stream=None):
-    """smp_spec_verify_params: spec_verify with per-row knobs (temperature or
-    greedy), `params` a [B] record array of smp_row_params or a device byte
-    tensor holding it (None: temperature 1 on every row)."""
+                       out_accepted=None, out_ids=None, status=None, stream=None, out_alpha=None):
+    """smp_spec_verify_params: spec_verify with per-row knobs (temperature,
+    filters, greedy), `params` a [B] record array of smp_row_params or a
+    device byte tensor holding it (None: temperature 1 on every row).
+    out_alpha: a float32 [B, K] CUDA tensor for the acceptance rates, or None
+    (not computed).  Returns (accepted_len, ids, status)."""
     lib = load()
     batch, k, vocab = _verify_shapes(p_logits, q_logits, draft_ids)
     dev = p_logits.device
@@ -224,8 +227,8 @@ def spec_verify_params(p_logits, q_logits, draft_ids, params, seed=0, offset=0, 
                                                                out_ids, status)
     _check(lib.smp_spec_verify_params(_ptr(p_logits), _ptr(q_logits), _ptr(draft_ids), batch, k, vocab,
                                       _dtype_code(p_logits), _ptr(prm), seed, offset, _ptr(out_accepted),
-                                      _ptr(out_ids), _ptr(status), _ptr(workspace), workspace.numel(),
-                                      _stream(stream)))
+                                      _ptr(out_ids), _ptr(out_alpha), _ptr(status), _ptr(workspace),
+                                      workspace.numel(), _stream(stream)))
     return out_accepted, out_ids, status
 
 

@@ -55,6 +55,7 @@ struct VerifyArgs {
   int32_t* status;
   PosStat* ws;
   const smp_row_params* params;   // [batch] or nullptr (T = 1 on every row)
+  float* alpha;                   // [batch, k] acceptance rates, or nullptr
 };
 
 // How batch row b is verified: temperature T > 0 with or without filters,
@@ -407,6 +408,30 @@ __device__ __forceinline__ uint64_t cluster_prefix(uint64_t v, uint64_t* slots, 
   return bc[0];
 }
 
+// Per-position state of the acceptance rates alpha_i = sum_x min(p_i, q_i)
+// (shared memory of the resolve kernel's knob instance, only when asked for).
+struct AlphaShared {
+  float m[2][SMP_MAX_DRAFT];            // maxima of p_i and q_i
+  float inv_z[2][SMP_MAX_DRAFT];        // 2^F / Z of p_i and q_i (binary32)
+  uint32_t kept[4][SMP_MAX_DRAFT];      // kept sets of p_i and q_i: (key, id) each
+  unsigned long long cta[SMP_MAX_DRAFT];                       // this CTA's sums
+  unsigned long long slots[kResolveMaxCluster][SMP_MAX_DRAFT];  // rank 0: every CTA's sums
+};
+
+__device__ __forceinline__ AlphaShared& alpha_shared() {
+  __shared__ AlphaShared s;
+  return s;
+}
+
+// rn(r * 2^52) for 0 <= r <= 1 from two 32-bit conversions: s = r * 2^28 <= 2^28
+// splits exactly into its integer part and fraction; the fraction times 2^24
+// rounds like the whole (the integer part times 2^24 is even).
+__device__ __forceinline__ uint64_t fixed52(float r) {
+  const float sc = __fmul_rn(r, 0x1p28f);
+  const float hi = truncf(sc);
+  return (uint64_t(__float2uint_rz(hi)) << 24) + __float2uint_rn(__fmul_rn(__fsub_rn(sc, hi), 0x1p24f));
+}
+
 // One cluster per batch row: the accept tests of eq. 39.3 in position order,
 // then the replacement draw from max(0, p_j - q_j) (eq. 39.4) at the first
 // rejection j, or the bonus draw from p_K.  Thread g of the cluster (rank-major)
@@ -456,6 +481,7 @@ __global__ void __launch_bounds__(kResolveThreads, 2) verify_resolve_kernel(Veri
       const int jr = miss ? __ffs(miss) - 1 : K;
       const int top_j = __shfl_sync(0xFFFFFFFFu, top, jr);
       if (i <= K) a.ids[size_t(b) * (K + 1) + i] = fl ? -1 : i < jr ? draft : i == jr ? top_j : -1;
+      if (a.alpha && i < K) a.alpha[size_t(b) * K + i] = __int_as_float(0x7FC00000);   // no q compared
       if (i == 0) {
         a.accepted[b] = fl ? -1 : jr;
         if (fl && a.status) atomicOr(a.status, fl & (kRowNonFinite | kRowBadDraft | kRowBadParams));
@@ -505,6 +531,20 @@ __global__ void __launch_bounds__(kResolveThreads, 2) verify_resolve_kernel(Veri
       kept_desc[2] = jr < K ? Q.kkey : P.kkey;
       kept_desc[3] = jr < K ? Q.kid : P.kid;
     }
+    if constexpr (kParams) {
+      if (a.alpha && i < K && !fl) {
+        AlphaShared& as = alpha_shared();
+        as.m[0][i] = P.m;
+        as.m[1][i] = Q.m;
+        as.inv_z[0][i] = __fdiv_rn(float(kFixedOne), __ull2float_rn(P.z));
+        as.inv_z[1][i] = __fdiv_rn(float(kFixedOne), __ull2float_rn(Q.z));
+        as.kept[0][i] = P.kkey;
+        as.kept[1][i] = P.kid;
+        as.kept[2][i] = Q.kkey;
+        as.kept[3][i] = Q.kid;
+        as.cta[i] = 0;
+      }
+    }
   }
   __syncthreads();
   const int jrej = decision[0];
@@ -513,6 +553,8 @@ __global__ void __launch_bounds__(kResolveThreads, 2) verify_resolve_kernel(Veri
     if (rank == 0 && tid == 0) {
       a.accepted[b] = -1;
       for (int i = 0; i <= K; ++i) a.ids[size_t(b) * (K + 1) + i] = -1;
+      if (a.alpha)
+        for (int i = 0; i < K; ++i) a.alpha[size_t(b) * K + i] = __int_as_float(0x7FC00000);
       if (a.status) atomicOr(a.status, flags & (kRowNonFinite | kRowBadDraft | kRowTimeout | kRowBadParams));
     }
     return;
@@ -526,7 +568,6 @@ __global__ void __launch_bounds__(kResolveThreads, 2) verify_resolve_kernel(Veri
   // Thread g owns ids [c0, c1): a whole number of 16-byte groups of the row
   // (rows whose base is not 16-byte aligned fall back to element loads).
   constexpr int kPer = 16 / int(sizeof(T));
-  const bool vec_ok = ((reinterpret_cast<uintptr_t>(prow) | reinterpret_cast<uintptr_t>(qrow)) & 15) == 0;
   const int nthreads = int(nranks) * kResolveThreads;
   const int per = (V + nthreads - 1) / nthreads;
   const int chunk = (per + kPer - 1) / kPer * kPer;
@@ -558,18 +599,15 @@ __global__ void __launch_bounds__(kResolveThreads, 2) verify_resolve_kernel(Veri
       if (!in_kept_set(kq, order_key<T>(zq), uint32_t(id))) q = 0.0f;
     }
     const float r = use_p ? p : fmaxf(0.0f, __fsub_rn(p, q));
-    // rn(r * 2^52) from two 32-bit conversions: s = r * 2^28 <= 2^28 splits
-    // exactly into its integer part and fraction; the fraction times 2^24
-    // rounds like the whole (the integer part times 2^24 is even).
-    const float sc = __fmul_rn(r, 0x1p28f);
-    const float hi = truncf(sc);
-    return (uint64_t(__float2uint_rz(hi)) << 24) + __float2uint_rn(__fmul_rn(__fsub_rn(sc, hi), 0x1p24f));
+    return fixed52(r);
   };
   constexpr int kGroups = 16 / kPer;   // groups of kPer ids in flight per thread (16 ids)
-  // The thread's weights: all its vectors requested first, then a rolled
+  // Sum of w(id, z_p, z_q) over the thread's ids of one row pair (q not read
+  // when read_q is false): all its vectors requested first, then a rolled
   // loop over the groups (this code runs once per CTA, cold in the
   // instruction cache, so it is kept short).
-  auto chunk_sum = [&](auto kFilt) -> uint64_t {
+  auto pair_sum = [&](const T* pr_, const T* qr_, bool read_q, auto&& w) -> uint64_t {
+    const bool vok = ((reinterpret_cast<uintptr_t>(pr_) | reinterpret_cast<uintptr_t>(qr_)) & 15) == 0;
     uint64_t sum = 0;
     const uint32_t ninf = VecOps<T>::neg_inf();
     for (int g0 = c0; g0 < c1; g0 += kGroups * kPer) {
@@ -579,9 +617,9 @@ __global__ void __launch_bounds__(kResolveThreads, 2) verify_resolve_kernel(Veri
         const int gg = g0 + gi * kPer;
         xp[gi] = make_uint4(ninf, ninf, ninf, ninf);
         xq[gi] = xp[gi];
-        if (gg < c1 && vec_ok && gg + kPer <= V) {
-          xp[gi] = __ldg(reinterpret_cast<const uint4*>(prow + gg));
-          xq[gi] = use_p ? xp[gi] : __ldg(reinterpret_cast<const uint4*>(qrow + gg));
+        if (gg < c1 && vok && gg + kPer <= V) {
+          xp[gi] = __ldg(reinterpret_cast<const uint4*>(pr_ + gg));
+          xq[gi] = read_q ? __ldg(reinterpret_cast<const uint4*>(qr_ + gg)) : xp[gi];
         }
       }
 #pragma unroll 1
@@ -595,19 +633,22 @@ __global__ void __launch_bounds__(kResolveThreads, 2) verify_resolve_kernel(Veri
             vp = xp[k2];
             vq = xq[k2];
           }
-        const bool full = vec_ok && gg + kPer <= V;
+        const bool full = vok && gg + kPer <= V;
 #pragma unroll
         for (int e = 0; e < kPer; ++e) {
           float zp = VecOps<T>::elem(vp, e), zq = VecOps<T>::elem(vq, e);
           if (!full) {   // a row not 16-byte aligned, or its last ids
-            zp = gg + e < c1 ? Elem<T>::widen(prow[gg + e]) : -INFINITY;
-            zq = gg + e < c1 ? Elem<T>::widen(qrow[gg + e]) : -INFINITY;
+            zp = gg + e < c1 ? Elem<T>::widen(pr_[gg + e]) : -INFINITY;
+            zq = gg + e < c1 ? Elem<T>::widen(qr_[gg + e]) : -INFINITY;
           }
-          sum += weight_of(kFilt, gg + e, zp, zq);
+          sum += w(gg + e, zp, zq);
         }
       }
     }
     return sum;
+  };
+  auto chunk_sum = [&](auto kFilt) -> uint64_t {
+    return pair_sum(prow, qrow, !use_p, [&](int id, float zp, float zq) { return weight_of(kFilt, id, zp, zq); });
   };
   auto chunk_sum_row = [&]() { return filt ? chunk_sum(std::true_type{}) : chunk_sum(std::false_type{}); };
   uint64_t local = chunk_sum_row(), cta_total = 0, total = 0;
@@ -655,6 +696,47 @@ __global__ void __launch_bounds__(kResolveThreads, 2) verify_resolve_kernel(Veri
     for (int i = 0; i < jrej; ++i) a.ids[size_t(b) * (K + 1) + i] = a.drafts[size_t(b) * K + i];
     for (int i = jrej + 1; i <= K; ++i) a.ids[size_t(b) * (K + 1) + i] = -1;
   }
+
+  // Acceptance rates alpha_i = sum_x min(p_i(x), q_i(x)) for every draft
+  // position ("Decoding & Speculative Sampling", section 39.4, Listing 39.5),
+  // on the compared distributions (binary32 p and q, 52-bit fixed-point sums
+  // over the same id chunks as the draw).  The p_i and q_i rows were read by
+  // the position kernel just before and are normally served by L2.
+  if constexpr (kParams) {
+    if (a.alpha) {
+      AlphaShared& as = alpha_shared();
+      for (int i = 0; i < K; ++i) {
+        const RowScale sp = make_row_scale(as.m[0][i], md.temperature);
+        const RowScale sq = make_row_scale(as.m[1][i], md.temperature);
+        const float izp = as.inv_z[0][i], izq = as.inv_z[1][i];
+        KeptSet kpi, kqi;
+        kpi.key = as.kept[0][i];
+        kpi.id_cut = as.kept[1][i];
+        kqi.key = as.kept[2][i];
+        kqi.id_cut = as.kept[3][i];
+        uint64_t sum = pair_sum(logit_row<T>(a, b, i), logit_row<T>(a, b, K + 1 + i), true,
+                                [&](int id, float zp, float zq) -> uint64_t {
+                                  float p = __fmul_rn(exp_fast(zp, sp), izp);
+                                  float q = __fmul_rn(exp_fast(zq, sq), izq);
+                                  if (filt) {
+                                    if (!in_kept_set(kpi, order_key<T>(zp), uint32_t(id))) p = 0.0f;
+                                    if (!in_kept_set(kqi, order_key<T>(zq), uint32_t(id))) q = 0.0f;
+                                  }
+                                  return fixed52(fminf(p, q));
+                                });
+        sum = warp_sum<uint64_t>(sum);
+        if ((tid & 31) == 0 && sum) atomicAdd(&as.cta[i], (unsigned long long)sum);
+      }
+      __syncthreads();
+      if (tid < K) st_cluster_u64(map_rank(smem_addr(&as.slots[rank][tid]), 0), as.cta[tid]);
+      hw_cluster_sync();   // every CTA's sums are in rank 0's slots
+      if (rank == 0 && tid < K) {
+        uint64_t tot = 0;
+        for (uint32_t r = 0; r < nranks; ++r) tot += as.slots[r][tid];
+        a.alpha[size_t(b) * K + tid] = float(double(tot) * 0x1p-52);
+      }
+    }
+  }
 }
 
 // ------------------------------------------------------------------ host side
@@ -667,10 +749,11 @@ static smp_status launch_verify(VerifyArgs a, cudaStream_t stream) {
   LaunchShape ls;   // one CTA per logit row, then one per batch row; no dynamic shared memory
   ls.pdl = true;
   cudaError_t err;
-  const void* pos = a.params ? reinterpret_cast<const void*>(&verify_pos_kernel<T, true>)
-                             : reinterpret_cast<const void*>(&verify_pos_kernel<T, false>);
-  const void* resolve = a.params ? reinterpret_cast<const void*>(&verify_resolve_kernel<T, true>)
-                                 : reinterpret_cast<const void*>(&verify_resolve_kernel<T, false>);
+  const bool knobs = a.params != nullptr || a.alpha != nullptr;   // the instances with per-row knobs
+  const void* pos = knobs ? reinterpret_cast<const void*>(&verify_pos_kernel<T, true>)
+                          : reinterpret_cast<const void*>(&verify_pos_kernel<T, false>);
+  const void* resolve = knobs ? reinterpret_cast<const void*>(&verify_resolve_kernel<T, true>)
+                              : reinterpret_cast<const void*>(&verify_resolve_kernel<T, false>);
   err = launch_cluster(pos, dim3(rows), dim3(kThreads), ls,
                        stream, &a);
   if (err != cudaSuccess) return fail_cuda(err);
@@ -696,8 +779,8 @@ extern "C" smp_status smp_spec_verify_params(const void* p_logits, const void* q
                                              const int32_t* draft_ids, int32_t batch, int32_t k,
                                              int32_t vocab, smp_dtype dtype, const smp_row_params* params,
                                              uint64_t seed, uint64_t offset, int32_t* out_accepted_len,
-                                             int32_t* out_ids, int32_t* status, void* workspace,
-                                             size_t workspace_bytes, void* stream) {
+                                             int32_t* out_ids, float* out_alpha, int32_t* status,
+                                             void* workspace, size_t workspace_bytes, void* stream) {
   using namespace smp;
   if (dtype != SMP_F32 && dtype != SMP_BF16) return SMP_ERR_DTYPE;
   if (!p_logits || !q_logits || !draft_ids || !out_accepted_len || !out_ids) return SMP_ERR_INVALID_ARG;
@@ -708,7 +791,8 @@ extern "C" smp_status smp_spec_verify_params(const void* p_logits, const void* q
   if (reinterpret_cast<uintptr_t>(p_logits) % elem || reinterpret_cast<uintptr_t>(q_logits) % elem)
     return SMP_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(draft_ids) % 4 || reinterpret_cast<uintptr_t>(out_ids) % 4 ||
-      reinterpret_cast<uintptr_t>(out_accepted_len) % 4 || reinterpret_cast<uintptr_t>(params) % 4)
+      reinterpret_cast<uintptr_t>(out_accepted_len) % 4 || reinterpret_cast<uintptr_t>(params) % 4 ||
+      reinterpret_cast<uintptr_t>(out_alpha) % 4)
     return SMP_ERR_INVALID_ARG;
   const size_t need = smp_spec_verify_workspace_bytes(batch, k);
   if (!workspace || workspace_bytes < need || reinterpret_cast<uintptr_t>(workspace) % 8)
@@ -732,6 +816,7 @@ extern "C" smp_status smp_spec_verify_params(const void* p_logits, const void* q
   a.status = status;
   a.ws = reinterpret_cast<PosStat*>(workspace);
   a.params = params;
+  a.alpha = out_alpha;
   if (dtype == SMP_F32) return launch_verify<float>(a, st);
   return launch_verify<uint16_t>(a, st);
 }
@@ -742,7 +827,7 @@ extern "C" smp_status smp_spec_verify(const void* p_logits, const void* q_logits
                                       int32_t* out_accepted_len, int32_t* out_ids, int32_t* status,
                                       void* workspace, size_t workspace_bytes, void* stream) {
   return smp_spec_verify_params(p_logits, q_logits, draft_ids, batch, k, vocab, dtype, nullptr, seed, offset,
-                                out_accepted_len, out_ids, status, workspace, workspace_bytes, stream);
+                                out_accepted_len, out_ids, nullptr, status, workspace, workspace_bytes, stream);
 }
 
 // ------------------------------------------------------------------ allocation-free variant

@@ -65,13 +65,15 @@ def test_host_validation_without_gpu(lib):
     assert need == 2 * 9 * 32
     assert lib.smp_spec_verify(fake, fake, fake, 2, 4, 8, 0, 0, 0, fake, fake, null, fake, need - 1, null) == 5
     # the per-row-knob entry: the same checks, and a misaligned params pointer
-    assert lib.smp_spec_verify_params(fake, fake, fake, 2, 0, 8, 0, fake, 0, 0, fake, fake, null, fake,
+    assert lib.smp_spec_verify_params(fake, fake, fake, 2, 0, 8, 0, fake, 0, 0, fake, fake, null, null, fake,
                                       1 << 20, null) == 1
     assert lib.smp_spec_verify_params(fake, fake, fake, 2, 4, 8, 0, ctypes.c_void_p(0x1002), 0, 0, fake, fake,
-                                      null, fake, 1 << 20, null) == 1
-    assert lib.smp_spec_verify_params(fake, fake, fake, 2, 4, 8, 9, fake, 0, 0, fake, fake, null, fake,
+                                      null, null, fake, 1 << 20, null) == 1
+    assert lib.smp_spec_verify_params(fake, fake, fake, 2, 4, 8, 0, fake, 0, 0, fake, fake,
+                                      ctypes.c_void_p(0x1001), null, fake, 1 << 20, null) == 1
+    assert lib.smp_spec_verify_params(fake, fake, fake, 2, 4, 8, 9, fake, 0, 0, fake, fake, null, null, fake,
                                       1 << 20, null) == 2
-    assert lib.smp_spec_verify_params(fake, fake, fake, 2, 4, 8, 0, null, 0, 0, fake, fake, null, null,
+    assert lib.smp_spec_verify_params(fake, fake, fake, 2, 4, 8, 0, null, 0, 0, fake, fake, null, null, null,
                                       1 << 20, null) == 5
     assert lib.smp_spec_verify_workspace_bytes(0, 4) == 0
     assert lib.smp_spec_verify_workspace_bytes(2, 17) == 0

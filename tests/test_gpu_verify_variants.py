@@ -228,3 +228,54 @@ def test_filtered_output_follows_filtered_target():
         target = p_tilde[:2] * reached.sum()
         stat = float(np.sum((counts[:2] - target) ** 2 / target))
         assert stat < 10.83, (pos, stat)   # chi-square, 1 degree of freedom, p = 0.001
+
+
+ALPHA_ATOL = 1e-5   # binary32 probabilities (Z within about 1e-6 relative), exact fixed-point sums
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("k,vocab", [(2, 300), (4, 32000)])
+def test_acceptance_rates_parity(dtype, k, vocab):
+    batch = 24
+    vb = workloads.verify_workload(batch=batch, k=k, vocab=vocab, dtype=dtype, seed_id=500 + k)
+    prm = workloads.make_params(batch)
+    for r in range(batch):
+        t, tk, tp, mp = FILTER_KNOBS[r % len(FILTER_KNOBS)]
+        prm[r] = (t, tk, tp, mp, 0)
+    prm["greedy"][5] = 1            # alpha undefined: NaN
+    prm["temperature"][7] = -1.0    # error row: NaN
+    drafts = drafts_from_filtered_q(vb.values("q"), prm)   # row 7 gets draft -1: its knobs are invalid anyway
+    p = device_logits(vb.p, dtype)
+    q = device_logits(vb.q, dtype)
+    d = torch.from_numpy(drafts).cuda()
+    alpha = torch.full((batch, k), -7.0, dtype=torch.float32, device="cuda")
+    acc, ids, status = binding.spec_verify_params(p, q, d, prm, 3, 1, out_alpha=alpha)
+    torch.cuda.synchronize()
+    want = over.spec_verify(vb.values("p"), vb.values("q"), drafts, 3, 1, params=prm, alpha=True)
+    compare_verify(want, acc.cpu().numpy(), ids.cpu().numpy()).check()
+    got = alpha.cpu().numpy()
+    for r in want:
+        w = np.array(r["alpha"])
+        if np.all(np.isnan(w)):
+            assert np.all(np.isnan(got[r["row"]])), r["row"]
+        else:
+            np.testing.assert_allclose(got[r["row"]], w, rtol=0, atol=ALPHA_ATOL, err_msg=str(r["row"]))
+    assert int(status.cpu()[0]) == binding.ROW_BAD_PARAMS
+
+
+def test_acceptance_rates_without_knobs_and_the_unchanged_draw():
+    # out_alpha with no knobs: alpha at T = 1; the accepted lengths and ids are
+    # those of the plain call
+    vb = workloads.verify_workload(batch=16, k=3, vocab=5003, dtype="f32", seed_id=61)
+    drafts = drafts_from_q(vb.values("q"), np.ones(16))
+    p = device_logits(vb.p, "f32")
+    q = device_logits(vb.q, "f32")
+    d = torch.from_numpy(drafts).cuda()
+    alpha = torch.empty((16, 3), dtype=torch.float32, device="cuda")
+    plain = binding.spec_verify(p, q, d, 9, 2)
+    withalpha = binding.spec_verify_params(p, q, d, None, 9, 2, out_alpha=alpha)
+    torch.cuda.synchronize()
+    assert torch.equal(plain[0], withalpha[0]) and torch.equal(plain[1], withalpha[1])
+    want = over.spec_verify(vb.values("p"), vb.values("q"), drafts, 9, 2, alpha=True)
+    np.testing.assert_allclose(alpha.cpu().numpy(), np.array([r["alpha"] for r in want]), rtol=0,
+                               atol=ALPHA_ATOL)

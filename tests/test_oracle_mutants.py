@@ -10,9 +10,11 @@ import numpy as np
 import pytest
 
 import oracle.philox as philox_mod
+import oracle.prepass as prepass_mod
 import oracle.sampler as sampler_mod
 import oracle.verify as verify_mod
 from tests import test_oracle_philox as t_philox
+from tests import test_oracle_prepass as t_prepass
 from tests import test_oracle_pins as t_pins
 from tests import test_oracle_properties as t_props
 from tests import test_oracle_verify_variants as t_variants
@@ -108,6 +110,16 @@ def _alpha_of_p_only(p_rows, q_rows, temperature=1.0, filters=None):
             for i in range(len(q_rows))]
 
 
+def _penalize_swapped(z, r, dtype="f32"):
+    z, r = np.float32(z), np.float32(r)
+    return np.float32(z * r) if z > 0 else np.float32(z / r)
+
+
+def _allowed_inverted(words, vocab):
+    ids = np.arange(vocab)
+    return ((np.asarray(words, dtype=np.uint32)[ids // 32] >> (ids % 32).astype(np.uint32)) & 1) == 0
+
+
 def _fd_no_renorm(original):
     def wrapped(row, temperature, top_k=0, top_p=1.0, min_p=0.0):
         p, keep, _, diag = original(row, temperature, top_k, top_p, min_p)
@@ -154,6 +166,11 @@ MUTANTS = [
     ("acceptance rate ignores q", verify_mod, "acceptance_rates", _alpha_of_p_only,
      [lambda: t_variants.test_acceptance_rate_three_token_example(load_golden),
       t_variants.test_acceptance_rate_is_one_minus_total_variation]),
+    ("penalty branches swapped", prepass_mod, "penalize", _penalize_swapped,
+     [t_prepass.test_penalty_branches_on_hand_values, t_prepass.test_penalty_lowers_every_score_for_r_above_one]),
+    ("mask inverted", prepass_mod, "allowed_mask", _allowed_inverted,
+     [t_prepass.test_masked_distribution_is_conditioned_on_the_allowed_set,
+      lambda: t_prepass.test_tiny_grammar_mask("[")]),
     ("renormalisation dropped", sampler_mod, "filtered_distribution",
      _fd_no_renorm(sampler_mod.filtered_distribution),
      [lambda: t_pins.test_exercise_39_1(load_golden), t_props.test_renormalisation_invariants]),

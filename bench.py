@@ -353,6 +353,29 @@ def run_gpu(args):
         ms = timed(g, 1)
         var_ms[name] = (ms, float(v_acc.float().mean().item()))   # accepted lengths of the last call
         del g
+    # Sampler with the logit pre-pass on the headline batch: repetition
+    # penalty over 64 recent tokens, with and without a constraint mask.
+    allowed_np, history_np, penalty_np = workloads.prepass_inputs(batch.values, seed=1, mask_density=(0.8, 1.0))
+    allowed_np[-1] = allowed_np[-2]   # no error row in the timed batch
+    allowed_dev = torch.from_numpy(allowed_np.view(np.int32)).to(dev)
+    history_dev = torch.from_numpy(history_np).to(dev)
+    penalty_dev = torch.from_numpy(penalty_np).to(dev)
+    sampler_variants = {}
+    for name, use_mask in (("penalty", False), ("penalty_and_mask", True)):
+        def pcall(i, use_mask=use_mask):
+            binding.sample_processed(logits[i % n_copies], params, seed, i, allowed_dev if use_mask else None,
+                                     history_dev, penalty_dev, out_ids, out_probs, status)
+        for i in range(max(args.warmup, 3)):
+            pcall(i)
+        torch.cuda.synchronize()
+        assert int(status.cpu()[0]) == 0
+        g = capture(pcall)
+        us = 1000.0 * timed(g, 1) / args.steps
+        del g
+        nbytes = sample_bytes + (allowed_np.nbytes if use_mask else 0) + history_np.nbytes + penalty_np.nbytes
+        sampler_variants[name] = {"us_per_call": us, "rows_per_s": job_rate(B, world, us * 1e-6),
+                                  "bytes_per_call": nbytes, "gbs": nbytes / (us * 1e-6) / 1e9}
+
     verify_variants = {}
     for name, (ms, accepted) in var_ms.items():
         us = 1000.0 * ms / args.steps
@@ -453,6 +476,7 @@ def run_gpu(args):
             "sampler_us_per_call": samp_us,
             "sample_kernel_us": kern_us,
             "hbm_gbs": achieved,
+            "sampler_variants": sampler_variants,
             "pct_of_measured_hbm": 100.0 * achieved / peak,
             "pct_of_8tbs_nominal": 100.0 * achieved / NOMINAL_HBM_GBS,
             "verify": {"tok_s": verify_tok_s, "us_per_call": ver_us, "mean_accepted": acc_mean,

@@ -39,6 +39,8 @@ extern "C" {
 #define SMP_MAX_VOCAB (1 << 19)
 /* Largest number of draft tokens per verify row. */
 #define SMP_MAX_DRAFT 16
+/* Longest window of recent tokens the repetition penalty looks at. */
+#define SMP_MAX_HISTORY 64
 
 typedef enum smp_dtype {
     SMP_F32 = 0,   /* IEEE binary32 logits */
@@ -121,6 +123,42 @@ smp_status smp_filter_debug(const void* logits, int32_t batch, int32_t vocab, sm
                             const smp_row_params* params, uint64_t seed, uint64_t offset,
                             int32_t* out_ids, float* out_probs, float* out_probs_full,
                             int32_t* out_kept, int32_t* status, void* stream);
+
+/*
+ * smp_sample_processed -- smp_sample after a logit pre-pass: a repetition
+ * penalty over recent tokens and a constraint mask.
+ *
+ *   repetition penalty  for each distinct token id i among the row's recent
+ *                tokens, z_i <- z_i / r if z_i > 0, else z_i * r ("Choosing
+ *                the next word", section "The repetition penalty"), applied
+ *                to the raw logits; the result is computed in binary32 and
+ *                kept in the logits' precision (bf16 logits: rounded to the
+ *                nearest bf16, ties to even).
+ *   constraint mask  tokens outside the allowed set get the logit -inf, so
+ *                the distribution is the model's conditioned on the allowed
+ *                set ("Decoding & Speculative Sampling", section 39.3).
+ * Then temperature, filters and the draw run exactly as in smp_sample.
+ *
+ *   allowed      device, [batch, ceil(vocab / 32)] uint32, or NULL (no mask):
+ *                bit (i mod 32) of word i / 32 set when token i is allowed.
+ *                A row with no allowed token has no finite logit: id -1 and
+ *                SMP_ROW_NONFINITE.
+ *   history      device, [batch, history_len] int32 recent token ids, or NULL;
+ *                ids outside [0, vocab) are padding, repeated ids count once.
+ *   history_len  0 .. SMP_MAX_HISTORY.
+ *   repetition_penalty  device, [batch] float r, or NULL (no penalty); r = 1
+ *                leaves the row unchanged; r must be finite and > 0, else the
+ *                row is an error row (SMP_ROW_BAD_PARAMS, greedy or not).
+ * Every other argument and the error behaviour are those of smp_sample.
+ * Every row takes the exact selection over global memory (the path smp_sample
+ * uses for top-p rows), one CTA per row: slower than smp_sample's streamed
+ * path.
+ */
+smp_status smp_sample_processed(const void* logits, int32_t batch, int32_t vocab, smp_dtype dtype,
+                                const smp_row_params* params, const uint32_t* allowed, const int32_t* history,
+                                int32_t history_len, const float* repetition_penalty, uint64_t seed,
+                                uint64_t offset, int32_t* out_ids, float* out_probs, int32_t* status,
+                                void* stream);
 
 /*
  * smp_spec_verify_workspace_bytes -- device workspace smp_spec_verify needs

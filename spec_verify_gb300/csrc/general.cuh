@@ -13,9 +13,9 @@
 
 // One row by the general path (see the top of this file).  `table` is the
 // 2^(j/64) table in shared memory.
-template <typename T>
+template <typename T, typename Xf = NoPrep>
 __device__ void general_row(GenShared& gs, const FloatPair* table, const SampleArgs& a, int b,
-                                 const smp_row_params& prm) {
+                            const smp_row_params& prm, const Xf& xf = Xf()) {
   const int tid = threadIdx.x;
   const int V = a.vocab;
   const T* row = reinterpret_cast<const T*>(a.logits) + size_t(b) * V;
@@ -25,7 +25,7 @@ __device__ void general_row(GenShared& gs, const FloatPair* table, const SampleA
   gen_sweep<T>(row, V, [&](int i, float z) {
     const uint64_t p = pack_key_id(order_key<T>(z), uint32_t(i));
     best = p > best ? p : best;
-  });
+  }, xf);
   best = block_max_u64(best, gs.red64);
   const uint32_t key_max = uint32_t(best >> 32);
   const uint32_t argmax = ~uint32_t(best);
@@ -52,7 +52,7 @@ __device__ void general_row(GenShared& gs, const FloatPair* table, const SampleA
     return;
   }
 
-  const KeptSet ks = gen_kept_set<T>(row, V, gs, table, prm, key_max);
+  const KeptSet ks = gen_kept_set<T>(row, V, gs, table, prm, key_max, xf);
   auto mass_of = [&](int i, float z) -> uint64_t { return kept_mass<T>(ks, table, i, z); };
   const uint64_t z_kept = ks.z_kept;
   const uint64_t len = ks.len;
@@ -60,18 +60,18 @@ __device__ void general_row(GenShared& gs, const FloatPair* table, const SampleA
   // t = floor(u * Z_S), u = Philox draw 0 of row b.
   const uint64_t u53 = uniform53(a.seed, a.offset, uint64_t(b), 0);
   const uint64_t t = uint64_t((u128(u53) * z_kept) >> 53);
-  const int tok = gen_walk<T, uint64_t>(row, V, t, gs, mass_of);
+  const int tok = gen_walk<T, uint64_t>(row, V, t, gs, mass_of, xf);
   if (tid == 0) {
     a.out_ids[b] = tok;
     if (a.out_probs)
-      a.out_probs[b] = tok >= 0 ? float(double(mass_of(tok, Elem<T>::widen(row[tok]))) / double(z_kept))
+      a.out_probs[b] = tok >= 0 ? float(double(mass_of(tok, xf(tok, Elem<T>::widen(row[tok])))) / double(z_kept))
                                 : __int_as_float(0x7FC00000);
     if (a.kept) a.kept[b] = int32_t(len);
   }
   if (a.full_probs) {
     const float zf = float(z_kept);
     for (int i = tid; i < V; i += kThreads) {
-      const uint64_t e = mass_of(i, Elem<T>::widen(row[i]));
+      const uint64_t e = mass_of(i, xf(i, Elem<T>::widen(row[i])));
       a.full_probs[size_t(b) * V + i] = e ? __fdiv_rn(float(e), zf) : 0.0f;
     }
   }

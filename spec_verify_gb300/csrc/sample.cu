@@ -798,6 +798,122 @@ __global__ void __launch_bounds__(kThreads, 2) sample_kernel(SampleArgs a) {
   }
 }
 
+// ------------------------------------------------------------------ logit pre-pass
+//
+// Repetition penalty ("Choosing the next word", section "The repetition
+// penalty": z_i <- z_i / r for z_i > 0, else z_i * r, for each distinct token
+// i among the row's recent tokens) and constraint mask ("Decoding &
+// Speculative Sampling", section 39.3: tokens outside the allowed set get
+// -inf), applied to every logit a pass of the general path reads.  The
+// penalised value is computed in binary32 and kept in the logits' precision.
+
+constexpr int kMaxHistory = SMP_MAX_HISTORY;
+constexpr int kUnitWords = SMP_MAX_VOCAB / 64 / 32;   // one bit per 64 ids
+
+struct PrepArgs {
+  const uint32_t* allowed;   // [batch, words] allowed-token bits, or nullptr
+  int words;                 // ceil(vocab / 32)
+  const int32_t* history;    // [batch, hist_len] recent token ids, or nullptr
+  int hist_len;
+  const float* penalty;      // [batch] factors r, or nullptr (no penalty)
+};
+
+// A row's distinct history ids, sorted, and one bit per unit of 64 ids that
+// holds one of them (most ids skip the search on that bit).
+struct PrepShared {
+  int32_t raw[kMaxHistory];
+  int32_t first[kMaxHistory];   // 1 at the first occurrence of a valid id
+  int32_t ids[kMaxHistory];
+  uint32_t unit_bits[kUnitWords];
+  int n;
+};
+
+// Nearest bf16 value of a binary32 number (ties to even); NaN and infinities kept.
+__device__ __forceinline__ float round_to_bf16(float x) {
+  uint32_t b = __float_as_uint(x);
+  if ((b & 0x7FFFFFFFu) > 0x7F800000u) return x;
+  b = (b + 0x7FFFu + ((b >> 16) & 1u)) & 0xFFFF0000u;
+  return __uint_as_float(b);
+}
+
+template <typename T>
+struct LogitPrep {
+  const uint32_t* allowed;   // this row's mask words, or nullptr
+  const PrepShared* ps;
+  float r;
+  __device__ __forceinline__ float operator()(int id, float z) const {
+    if (allowed && !((__ldg(allowed + (id >> 5)) >> (id & 31)) & 1u)) return -INFINITY;
+    if ((ps->unit_bits[id >> 11] >> ((id >> 6) & 31)) & 1u) {
+      int lo = 0, hi = ps->n - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (ps->ids[mid] < id) lo = mid + 1;
+        else hi = mid;
+      }
+      if (ps->ids[lo] == id) {
+        z = z > 0.0f ? __fdiv_rn(z, r) : __fmul_rn(z, r);
+        if (sizeof(T) == 2) z = round_to_bf16(z);
+      }
+    }
+    return z;
+  }
+};
+
+// Builds the row's PrepShared (history ids in [0, V), each once, sorted).
+__device__ __forceinline__ void build_prep(PrepShared& ps, const PrepArgs& pa, int row, int V, bool penalised) {
+  const int tid = threadIdx.x;
+  const int H = penalised && pa.history ? pa.hist_len : 0;
+  for (int w = tid; w < kUnitWords; w += kThreads) ps.unit_bits[w] = 0;
+  if (tid < kMaxHistory) {
+    int32_t id = -1;
+    if (tid < H) id = pa.history[size_t(row) * H + tid];
+    ps.raw[tid] = (id >= 0 && id < V) ? id : -1;
+  }
+  if (tid == 0) ps.n = 0;
+  cta_sync();
+  if (tid < kMaxHistory) {   // first occurrences
+    const int32_t id = ps.raw[tid];
+    bool first = id >= 0;
+    for (int s = 0; s < tid; ++s) first &= ps.raw[s] != id;
+    ps.first[tid] = first;
+  }
+  cta_sync();
+  if (tid < kMaxHistory && ps.first[tid]) {   // rank among the distinct ids
+    const int32_t id = ps.raw[tid];
+    int rank = 0;
+    for (int s = 0; s < kMaxHistory; ++s) rank += ps.first[s] && ps.raw[s] < id;
+    ps.ids[rank] = id;
+    atomicOr(&ps.unit_bits[id >> 11], 1u << ((id >> 6) & 31));
+    atomicAdd(&ps.n, 1);
+  }
+  cta_sync();
+}
+
+// One CTA per row (grid-strided): every row through the general path with
+// the pre-pass applied.
+template <typename T>
+__global__ void __launch_bounds__(kThreads, 2) prep_sample_kernel(SampleArgs a, PrepArgs pa) {
+  __shared__ FloatPair table[64];
+  __shared__ GenShared gen;
+  __shared__ PrepShared ps;
+  const int tid = threadIdx.x;
+  grid_dependency_wait();
+  allow_dependent_launch();
+  if (tid < 64) table[tid] = kExp2Table[tid];
+  for (int row = blockIdx.x; row < a.batch; row += gridDim.x) {
+    cta_sync();   // the previous row is done with the shared state
+    const smp_row_params prm = a.params[row];
+    const float r = pa.penalty ? pa.penalty[row] : 1.0f;
+    if (!(isfinite(r) && r > 0.0f)) {
+      if (tid == 0) write_error_row(a, row, kRowBadParams);
+      continue;
+    }
+    build_prep(ps, pa, row, a.vocab, r != 1.0f);
+    const LogitPrep<T> xf{pa.allowed ? pa.allowed + size_t(row) * pa.words : nullptr, &ps, r};
+    general_row<T>(gen, table, a, row, prm, xf);
+  }
+}
+
 // ------------------------------------------------------------------ host side
 
 template <typename T>
@@ -822,6 +938,36 @@ static smp_status launch_sample(const SampleArgs& args, cudaStream_t stream) {
             args.vocab, grid, per_sm, ls.smem);
   SampleArgs a = args;
   err = launch_cluster(kernel, dim3(grid), dim3(kThreads), ls, stream, &a);
+  if (err != cudaSuccess) return fail_cuda(err);
+  return SMP_OK;
+}
+
+template <typename T>
+static smp_status launch_prep_sample(const SampleArgs& args, const PrepArgs& pa, cudaStream_t stream) {
+  const int dev = current_device();
+  if (dev < 0) return fail_cuda(cudaGetLastError());
+  LaunchShape ls;
+  ls.pdl = true;
+  const void* kernel = reinterpret_cast<const void*>(&prep_sample_kernel<T>);
+  int per_sm = 0;
+  cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, 0);
+  if (err != cudaSuccess) return fail_cuda(err);
+  if (per_sm <= 0) return SMP_ERR_UNSUPPORTED;
+  const int resident = per_sm * device_sms(dev);
+  const int grid = args.batch < resident ? args.batch : resident;
+  SampleArgs a = args;
+  PrepArgs p = pa;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  void* params[2] = {&a, &p};
+  err = cudaLaunchKernelExC(&cfg, kernel, params);
   if (err != cudaSuccess) return fail_cuda(err);
   return SMP_OK;
 }
@@ -876,4 +1022,47 @@ extern "C" smp_status smp_filter_debug(const void* logits, int32_t batch, int32_
   if (!out_probs_full || !out_kept) return SMP_ERR_INVALID_ARG;
   return smp::sample_common(logits, batch, vocab, dtype, params, seed, offset, out_ids, out_probs,
                             out_probs_full, out_kept, status, stream);
+}
+
+extern "C" smp_status smp_sample_processed(const void* logits, int32_t batch, int32_t vocab, smp_dtype dtype,
+                                           const smp_row_params* params, const uint32_t* allowed,
+                                           const int32_t* history, int32_t history_len,
+                                           const float* repetition_penalty, uint64_t seed, uint64_t offset,
+                                           int32_t* out_ids, float* out_probs, int32_t* status, void* stream) {
+  using namespace smp;
+  if (dtype != SMP_F32 && dtype != SMP_BF16) return SMP_ERR_DTYPE;
+  if (!logits || !params || !out_ids) return SMP_ERR_INVALID_ARG;
+  if (batch <= 0 || vocab <= 0) return SMP_ERR_INVALID_ARG;
+  if (vocab > SMP_MAX_VOCAB) return SMP_ERR_UNSUPPORTED;
+  if (history_len < 0 || history_len > SMP_MAX_HISTORY || (history_len > 0 && !history))
+    return SMP_ERR_INVALID_ARG;
+  const int elem = dtype == SMP_F32 ? 4 : 2;
+  if (reinterpret_cast<uintptr_t>(logits) % elem) return SMP_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(params) | reinterpret_cast<uintptr_t>(out_ids) |
+       reinterpret_cast<uintptr_t>(out_probs) | reinterpret_cast<uintptr_t>(allowed) |
+       reinterpret_cast<uintptr_t>(history) | reinterpret_cast<uintptr_t>(repetition_penalty)) % 4)
+    return SMP_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (status) {
+    const smp_status rc = clear_status(status, st);
+    if (rc != SMP_OK) return rc;
+  }
+  SampleArgs a{};
+  a.logits = logits;
+  a.batch = batch;
+  a.vocab = vocab;
+  a.params = params;
+  a.seed = seed;
+  a.offset = offset;
+  a.out_ids = out_ids;
+  a.out_probs = out_probs;
+  a.status = status;
+  PrepArgs pa{};
+  pa.allowed = allowed;
+  pa.words = (vocab + 31) / 32;
+  pa.history = history_len > 0 ? history : nullptr;
+  pa.hist_len = history_len;
+  pa.penalty = repetition_penalty;
+  if (dtype == SMP_F32) return launch_prep_sample<float>(a, pa, st);
+  return launch_prep_sample<uint16_t>(a, pa, st);
 }

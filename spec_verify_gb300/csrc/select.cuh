@@ -112,9 +112,15 @@ struct GenShared {
   unsigned long long bc64[4];
 };
 
-// Sweep over every element of a row in no particular order: f(id, z).
-template <typename T, typename F>
-__device__ __forceinline__ void gen_sweep(const T* row, int V, F&& f) {
+// Per-element transform of a row's logits, applied to every value a pass
+// reads: xf(id, z) -> the logit the method sees.  NoPrep leaves it as is.
+struct NoPrep {
+  __device__ __forceinline__ float operator()(int, float z) const { return z; }
+};
+
+// Sweep over every element of a row in no particular order: f(id, xf(id, z)).
+template <typename T, typename F, typename Xf = NoPrep>
+__device__ __forceinline__ void gen_sweep(const T* row, int V, F&& f, const Xf& xf = Xf()) {
   using Vo = VecOps<T>;
   constexpr int kPer = Vo::kPer;
   const uintptr_t r0 = reinterpret_cast<uintptr_t>(row);
@@ -133,11 +139,14 @@ __device__ __forceinline__ void gen_sweep(const T* row, int V, F&& f) {
     for (int u = 0; u < kGenU; ++u)
       if (v0 + u < nvec) {
 #pragma unroll
-        for (int q = 0; q < kPer; ++q) f(head + (v0 + u) * kPer + q, Vo::elem(x[u], q));
+        for (int q = 0; q < kPer; ++q) {
+          const int id = head + (v0 + u) * kPer + q;
+          f(id, xf(id, Vo::elem(x[u], q)));
+        }
       }
   }
-  for (int i = threadIdx.x; i < head; i += kThreads) f(i, Elem<T>::widen(row[i]));
-  for (int i = tail0 + threadIdx.x; i < V; i += kThreads) f(i, Elem<T>::widen(row[i]));
+  for (int i = threadIdx.x; i < head; i += kThreads) f(i, xf(i, Elem<T>::widen(row[i])));
+  for (int i = tail0 + threadIdx.x; i < V; i += kThreads) f(i, xf(i, Elem<T>::widen(row[i])));
 }
 
 // Exclusive prefix over the CTA (thread order) of one value per thread, and the total.
@@ -164,8 +173,8 @@ __device__ __forceinline__ U gen_scan(U v, U* warp_tot, U* total) {
 // per thread, scanned over the CTA, and the thread whose interval holds the
 // target walks its elements.  Elements before and after the aligned middle
 // come first and last, walked by thread 0.
-template <typename T, typename U, typename G>
-__device__ int gen_walk(const T* row, int V, U target, GenShared& gs, G&& g) {
+template <typename T, typename U, typename G, typename Xf = NoPrep>
+__device__ int gen_walk(const T* row, int V, U target, GenShared& gs, G&& g, const Xf& xf = Xf()) {
   using Vo = VecOps<T>;
   constexpr int kPer = Vo::kPer;
   const uintptr_t r0 = reinterpret_cast<uintptr_t>(row);
@@ -183,7 +192,7 @@ __device__ int gen_walk(const T* row, int V, U target, GenShared& gs, G&& g) {
   if (threadIdx.x == 0) {
     U r = 0;
     for (int i = 0; i < head; ++i) {
-      r += g(i, Elem<T>::widen(row[i]));
+      r += g(i, xf(i, Elem<T>::widen(row[i])));
       if (r > target) {
         gs.bc32[4] = uint32_t(i);
         break;
@@ -205,7 +214,10 @@ __device__ int gen_walk(const T* row, int V, U target, GenShared& gs, G&& g) {
     for (int u = 0; u < kGenU; ++u)
       if (v0 + u < nvec) {
 #pragma unroll
-        for (int q = 0; q < kPer; ++q) mine += g(head + (v0 + u) * kPer + q, Vo::elem(x[u], q));
+        for (int q = 0; q < kPer; ++q) {
+          const int id = head + (v0 + u) * kPer + q;
+          mine += g(id, xf(id, Vo::elem(x[u], q)));
+        }
       }
     U total;
     const U before = run + gen_scan<U>(mine, warp_tot, &total);
@@ -217,7 +229,7 @@ __device__ int gen_walk(const T* row, int V, U target, GenShared& gs, G&& g) {
 #pragma unroll
         for (int q = 0; q < kPer; ++q) {
           const int id = head + (v0 + u) * kPer + q;
-          r += done ? U(0) : g(id, Vo::elem(xv, q));
+          r += done ? U(0) : g(id, xf(id, Vo::elem(xv, q)));
           if (!done && r > target) {
             gs.bc32[4] = uint32_t(id);
             done = true;
@@ -232,7 +244,7 @@ __device__ int gen_walk(const T* row, int V, U target, GenShared& gs, G&& g) {
   if (threadIdx.x == 0) {
     U r = run;
     for (int i = tail0; i < V; ++i) {
-      r += g(i, Elem<T>::widen(row[i]));
+      r += g(i, xf(i, Elem<T>::widen(row[i])));
       if (r > target) {
         gs.bc32[4] = uint32_t(i);
         break;
@@ -259,9 +271,10 @@ struct GenBoundary {
 // length k (counts only).  kMass = true: the shortest prefix whose mass
 // reaches the top-p target top_p * Z; the first level's mass total is Z,
 // returned in *z_total.
-template <typename T, bool kMass>
+template <typename T, bool kMass, typename Xf = NoPrep>
 __device__ GenBoundary gen_select(const T* row, int V, GenShared& gs, uint32_t k, float top_p,
-                                  const RowScale& rs, const FloatPair* table, uint64_t* z_total) {
+                                  const RowScale& rs, const FloatPair* table, uint64_t* z_total,
+                                  const Xf& xf = Xf()) {
   constexpr int kL = KeyTraits<T>::kLevels;
   constexpr int kBits = KeyTraits<T>::kBits;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -295,7 +308,7 @@ __device__ GenBoundary gen_select(const T* row, int V, GenShared& gs, uint32_t k
           atomicAdd(&gs.mass[warp][2][d], uint32_t(e >> 30));
         }
       }
-    });
+    }, xf);
     cta_sync();
     {   // one digit per thread: sum the warps' histograms
       uint32_t c = 0;
@@ -455,9 +468,9 @@ __device__ __forceinline__ uint64_t kept_mass(const KeptSet& ks, const FloatPair
 // of top-k and top-p, the tie member at the boundary (an id-order walk) and
 // Z_S (from the top-p histograms when top-p set the boundary, else a pass).
 // Every thread gets the result.
-template <typename T>
+template <typename T, typename Xf = NoPrep>
 __device__ KeptSet gen_kept_set(const T* row, int V, GenShared& gs, const FloatPair* table,
-                                const smp_row_params& prm, uint32_t key_max) {
+                                const smp_row_params& prm, uint32_t key_max, const Xf& xf = Xf()) {
   const int tid = threadIdx.x;
   KeptSet ks;
   ks.rs = make_row_scale(key_value<T>(key_max), prm.temperature);
@@ -471,17 +484,17 @@ __device__ KeptSet gen_kept_set(const T* row, int V, GenShared& gs, const FloatP
   if (minp) {
     key_min_p = minp_threshold_key<T>(gs.bc32, table, ks.rs, prm.temperature, prm.min_p, key_max);
     uint32_t c = 0;
-    gen_sweep<T>(row, V, [&](int, float z) { c += order_key<T>(z) >= key_min_p; });
+    gen_sweep<T>(row, V, [&](int, float z) { c += order_key<T>(z) >= key_min_p; }, xf);
     len_m = block_sum_u32(c, gs.scan32);
   }
   GenBoundary bk{}, bp{};
   uint64_t z_total = 0;
   if (topk) {
-    bk = gen_select<T, false>(row, V, gs, uint32_t(prm.top_k), 1.0f, ks.rs, table, &z_total);
+    bk = gen_select<T, false>(row, V, gs, uint32_t(prm.top_k), 1.0f, ks.rs, table, &z_total, xf);
     len_k = uint64_t(prm.top_k);
   }
   if (topp) {
-    bp = gen_select<T, true>(row, V, gs, 0, prm.top_p, ks.rs, table, &z_total);
+    bp = gen_select<T, true>(row, V, gs, 0, prm.top_p, ks.rs, table, &z_total, xf);
     len_p = uint64_t(bp.above) + bp.n;
   }
   uint64_t len = len_k < len_p ? len_k : len_p;
@@ -502,7 +515,7 @@ __device__ KeptSet gen_kept_set(const T* row, int V, GenShared& gs, const FloatP
       if (bd.n < bd.ties) {   // the id of the n-th member (id order) of the boundary's tie bucket
         const int id = gen_walk<T, uint32_t>(row, V, bd.n - 1, gs, [&](int, float z) -> uint32_t {
           return order_key<T>(z) == bd.key ? 1u : 0u;
-        });
+        }, xf);
         ks.id_cut = uint32_t(id);
       }
     }
@@ -513,7 +526,7 @@ __device__ KeptSet gen_kept_set(const T* row, int V, GenShared& gs, const FloatP
     ks.z_kept = z_total;
   } else {
     uint64_t zl = 0;
-    gen_sweep<T>(row, V, [&](int i, float z) { zl += kept_mass<T>(ks, table, i, z); });
+    gen_sweep<T>(row, V, [&](int i, float z) { zl += kept_mass<T>(ks, table, i, z); }, xf);
     zl = warp_sum<uint64_t>(zl);
     if ((tid & 31) == 0) gs.scan64[tid >> 5] = zl;
     cta_sync();

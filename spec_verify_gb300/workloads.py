@@ -218,3 +218,42 @@ def random_sampler_batch(batch, vocab, dtype="bf16", seed=0, kinds="mixed"):
     if dtype == "bf16":
         return Batch(f"random-{kinds}", "bf16", f32_to_bf16_bits(logits), prm)
     return Batch(f"random-{kinds}", "f32", logits, prm)
+
+
+def prepass_inputs(values, seed=0, history_len=64, mask_density=(0.3, 0.95)):
+    """Seeded inputs of the logit pre-pass for a [B, V] batch of logit values.
+
+    Returns (allowed [B, ceil(V/32)] uint32, history [B, H] int32, penalty [B]
+    float32).  Row densities of allowed tokens are drawn from mask_density;
+    row 0 allows one token only, and the last row of batches of 8 or more
+    allows none.  Histories hold some of the row's 32 highest-logit ids (so
+    that the penalty changes the outcome), random ids, repeats, and padding
+    (-1 and ids past V).  Penalties come from {1.0, 1.1, 1.3, 2.0, 0.8}.
+    """
+    values = np.asarray(values, dtype=np.float32)
+    batch, vocab = values.shape
+    rng = np.random.default_rng(70_000 + seed)
+    words = (vocab + 31) // 32
+    allowed = np.zeros((batch, words), dtype=np.uint32)
+    for b in range(batch):
+        dens = rng.uniform(*mask_density)
+        keep = rng.uniform(size=vocab) < dens
+        if b == 0:
+            keep[:] = False
+            keep[rng.integers(vocab)] = True
+        if batch >= 8 and b == batch - 1:
+            keep[:] = False
+        ids = np.flatnonzero(keep)
+        np.bitwise_or.at(allowed[b], ids // 32, (np.uint32(1) << (ids % 32).astype(np.uint32)))
+    history = np.full((batch, history_len), -1, dtype=np.int32)
+    for b in range(batch):
+        top = np.argsort(-values[b], kind="stable")[:32]
+        picks = list(rng.choice(top, size=min(12, top.size), replace=False))
+        picks += list(rng.integers(0, vocab, size=history_len // 2))
+        picks += picks[:4]                      # repeats
+        picks += [vocab + 3, -5]                # padding past either end
+        rng.shuffle(picks)
+        n = min(history_len, len(picks))
+        history[b, :n] = np.array(picks[:n], dtype=np.int64).astype(np.int32)
+    penalty = rng.choice(np.array([1.0, 1.1, 1.3, 2.0, 0.8], dtype=np.float32), size=batch)
+    return allowed, history, penalty

@@ -57,6 +57,12 @@ def test_host_validation_without_gpu(lib):
     assert lib.smp_sample(fake, 4, (1 << 19) + 1, 0, fake, 0, 0, fake, null, null, null) == 4
     assert lib.smp_sample(ctypes.c_void_p(0x1001), 4, 8, 1, fake, 0, 0, fake, null, null, null) == 1
     assert lib.smp_filter_debug(fake, 4, 8, 0, fake, 0, 0, fake, null, null, null, null, null) == 1
+    # pre-pass sampling: history length out of range, history missing, misaligned mask
+    assert lib.smp_sample_processed(fake, 4, 8, 0, fake, null, fake, 65, null, 0, 0, fake, null, null, null) == 1
+    assert lib.smp_sample_processed(fake, 4, 8, 0, fake, null, null, 4, null, 0, 0, fake, null, null, null) == 1
+    assert lib.smp_sample_processed(fake, 4, 8, 0, fake, ctypes.c_void_p(0x1002), null, 0, null, 0, 0, fake,
+                                    null, null, null) == 1
+    assert lib.smp_sample_processed(fake, 4, 8, 5, fake, null, null, 0, null, 0, 0, fake, null, null, null) == 2
     # verify: K out of range, workspace missing or too small
     assert lib.smp_spec_verify(fake, fake, fake, 2, 0, 8, 0, 0, 0, fake, fake, null, fake, 1 << 20, null) == 1
     assert lib.smp_spec_verify(fake, fake, fake, 2, 17, 8, 0, 0, 0, fake, fake, null, fake, 1 << 20, null) == 1

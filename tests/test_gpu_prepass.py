@@ -1,0 +1,142 @@
+"""CUDA sampler with the logit pre-pass (smp_sample_processed, through the C
+ABI) against the fp64 oracle: repetition penalty ("Choosing the next word",
+section "The repetition penalty") and constraint mask ("Decoding &
+Speculative Sampling", section 39.3)."""
+
+import numpy as np
+import pytest
+
+from oracle import prepass
+from oracle import sampler as osam
+from spec_verify_gb300 import binding, workloads
+from tests.parity import compare_sampler, device_logits
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    binding.load()
+
+
+def run(batch, allowed, history, penalty, seed=5, offset=2):
+    logits = device_logits(batch.data, batch.dtype)
+    to = lambda a, dt: None if a is None else torch.from_numpy(np.ascontiguousarray(a).view(dt)).cuda()
+    ids, probs, status = binding.sample_processed(logits, batch.params, seed, offset, to(allowed, np.int32),
+                                                  to(history, np.int32), to(penalty, np.float32))
+    torch.cuda.synchronize()
+    return ids.cpu().numpy(), probs.cpu().numpy(), int(status.cpu()[0])
+
+
+def expected_status(results):
+    st = 0
+    for r in results:
+        st |= r["status"]
+    return st
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("vocab", [1000, 32000, 50021])
+@pytest.mark.parametrize("parts", ["both", "mask", "penalty"])
+def test_prepass_parity(dtype, vocab, parts):
+    batch = workloads.random_sampler_batch(24, vocab, dtype=dtype, seed=vocab % 89, kinds="mixed")
+    allowed, history, penalty = workloads.prepass_inputs(batch.values, seed=vocab % 13)
+    if parts == "mask":
+        history = penalty = None
+    if parts == "penalty":
+        allowed = None
+    ids, probs, status = run(batch, allowed, history, penalty)
+    want = prepass.sample_processed(batch.values, batch.params, 5, 2, dtype=dtype, allowed=allowed,
+                                    history=history, penalty=penalty)
+    compare_sampler(want, ids, probs).check()
+    assert status == expected_status(want)
+    if parts != "penalty":
+        assert want[-1]["status"] == osam.ROW_NONFINITE          # the row with no allowed token
+
+
+def test_bad_penalty_rows():
+    batch = workloads.random_sampler_batch(6, 700, dtype="f32", seed=3, kinds="mixed")
+    _, history, _ = workloads.prepass_inputs(batch.values, seed=4)
+    penalty = np.array([1.2, 0.0, -1.0, np.nan, np.inf, 1.0], dtype=np.float32)
+    batch.params["greedy"][1] = 1    # greedy rows need a valid penalty as well
+    ids, probs, status = run(batch, None, history, penalty)
+    assert list(ids[1:5]) == [-1] * 4 and np.all(np.isnan(probs[1:5]))
+    want = prepass.sample_processed(batch.values, batch.params, 5, 2, history=history, penalty=penalty)
+    compare_sampler(want, ids, probs).check()
+    assert status & binding.ROW_BAD_PARAMS
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_no_prepass_equals_smp_sample(dtype):
+    # with no mask and no penalty the pre-pass path gives smp_sample's ids and
+    # probabilities exactly (both are exact; one streams, one reads rows again)
+    batch = workloads.random_sampler_batch(40, 20011, dtype=dtype, seed=8, kinds="mixed")
+    logits = device_logits(batch.data, dtype)
+    a = binding.sample(logits, batch.params, 9, 4)
+    b = binding.sample_processed(logits, batch.params, 9, 4)
+    torch.cuda.synchronize()
+    assert torch.equal(a[0], b[0])
+    assert torch.equal(a[1], b[1]) or torch.allclose(a[1], b[1], rtol=1e-6, equal_nan=True)
+    assert int(a[2].cpu()[0]) == int(b[2].cpu()[0])
+
+
+VOCAB = ["[", "]", ","] + [str(d) for d in range(10)] + ["a"]
+
+
+def grammar_words(prefix):
+    if not prefix:
+        ok = [t == "[" for t in VOCAB]
+    elif prefix[-1] in {"[", ","}:
+        ok = [t.isdigit() for t in VOCAB]
+    elif prefix[-1].isdigit():
+        ok = [t in {"]", ","} for t in VOCAB]
+    else:
+        ok = [False] * len(VOCAB)
+    w = 0
+    for i, a in enumerate(ok):
+        w |= int(a) << i
+    return np.array([w], dtype=np.uint32), np.array(ok)
+
+
+def test_tiny_grammar_generation():
+    # Listing 39.3's grammar '[' digit (',' digit)* ']' drives the mask step by
+    # step; every sampled string is in the language
+    rows = 64
+    rng = np.random.default_rng(11)
+    prefixes = [""] * rows
+    for step in range(12):
+        z = rng.normal(0, 2, (rows, len(VOCAB))).astype(np.float32)
+        words = np.stack([grammar_words(p)[0] for p in prefixes])
+        logits = torch.from_numpy(z).cuda()
+        prm = workloads.make_params(rows, temperature=1.0)
+        ids, _, _ = binding.sample_processed(logits, prm, 1, step,
+                                             torch.from_numpy(words.view(np.int32)).cuda())
+        ids = ids.cpu().numpy()
+        for r in range(rows):
+            ok = grammar_words(prefixes[r])[1]
+            if not ok.any():
+                assert ids[r] == -1
+                continue
+            assert ok[ids[r]]
+            prefixes[r] += VOCAB[ids[r]]
+    for p in prefixes:
+        assert p.startswith("[")
+        body = p[1:].rstrip("]")
+        assert all(c.isdigit() or c == "," for c in body)
+        assert ",," not in p and "[," not in p
+
+
+def test_large_vocab_with_penalty_sampled_rows():
+    # the headline batch (B 256, V 128256 bf16, mixed knobs) with a penalty
+    # and a mask, checked on a sample of rows the oracle recomputes
+    batch = workloads.sampler_workload("large_vocab")
+    allowed, history, penalty = workloads.prepass_inputs(batch.values, seed=1, mask_density=(0.8, 1.0))
+    ids, probs, status = run(batch, allowed, history, penalty, seed=0, offset=0)
+    rows = list(range(0, 256, 9)) + [255]
+    want = prepass.sample_processed(batch.values, batch.params, 0, 0, dtype="bf16", allowed=allowed,
+                                    history=history, penalty=penalty, rows=rows)
+    compare_sampler(want, ids, probs).check()

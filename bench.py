@@ -376,6 +376,24 @@ def run_gpu(args):
         sampler_variants[name] = {"us_per_call": us, "rows_per_s": job_rate(B, world, us * 1e-6),
                                   "bytes_per_call": nbytes, "gbs": nbytes / (us * 1e-6) / 1e9}
 
+    # The same through the in-place pre-pass: smp_logit_prepass, then
+    # smp_sample (the copies are modified in place; the penalty compounds
+    # over replays on the same copy, which changes no byte count).
+    for name, use_mask in (("inplace_penalty_then_sample", False), ("inplace_penalty_and_mask_then_sample", True)):
+        def icall(i, use_mask=use_mask):
+            binding.logit_prepass(logits[i % n_copies], allowed_dev if use_mask else None, history_dev,
+                                  penalty_dev, status)
+            binding.sample(logits[i % n_copies], params, seed, i, out_ids, out_probs, status)
+        for i in range(max(args.warmup, 3)):
+            icall(i)
+        torch.cuda.synchronize()
+        g = capture(icall)
+        us = 1000.0 * timed(g, 1) / args.steps
+        del g
+        nbytes = sample_bytes + (allowed_np.nbytes if use_mask else 0) + history_np.nbytes + penalty_np.nbytes
+        sampler_variants[name] = {"us_per_call": us, "rows_per_s": job_rate(B, world, us * 1e-6),
+                                  "bytes_per_call": nbytes, "gbs": nbytes / (us * 1e-6) / 1e9}
+
     verify_variants = {}
     for name, (ms, accepted) in var_ms.items():
         us = 1000.0 * ms / args.steps

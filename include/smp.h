@@ -161,6 +161,31 @@ smp_status smp_sample_processed(const void* logits, int32_t batch, int32_t vocab
                                 void* stream);
 
 /*
+ * smp_logit_prepass -- the pre-pass of smp_sample_processed written into the
+ * logits in place, so that smp_sample (or a verifier call) then reads the
+ * processed logits in its own single pass.  The cheap way to sample with a
+ * repetition penalty and a constraint mask when the logits may be modified.
+ *
+ *   logits       device, [batch, vocab] contiguous, dtype elements, read and
+ *                written: disallowed tokens become -inf, each distinct
+ *                allowed history id gets z / r (z > 0) or z * r (z <= 0),
+ *                computed in binary32 and stored in the logits' precision
+ *                (bf16: nearest, ties to even).  Nothing else is written.
+ *   allowed, history, history_len, repetition_penalty  as for
+ *                smp_sample_processed.
+ *   status       device int32 or NULL: cleared, then SMP_ROW_BAD_PARAMS for
+ *                rows whose factor r is not finite and > 0.  Such rows are
+ *                filled with NaN, so that a following smp_sample gives them
+ *                id -1 and SMP_ROW_NONFINITE.
+ * Cost: the mask words are read (vocab / 8 bytes per row) and only changed
+ * elements are written; a row without a mask and without a penalty is not
+ * touched.
+ */
+smp_status smp_logit_prepass(void* logits, int32_t batch, int32_t vocab, smp_dtype dtype, const uint32_t* allowed,
+                             const int32_t* history, int32_t history_len, const float* repetition_penalty,
+                             int32_t* status, void* stream);
+
+/*
  * smp_spec_verify_workspace_bytes -- device workspace smp_spec_verify needs
  * for a batch of `batch` rows with `k` drafts (0 if the sizes are invalid).
  */

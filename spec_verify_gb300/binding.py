@@ -25,7 +25,8 @@ ROW_TIMEOUT = 4
 ROW_BAD_DRAFT = 8
 
 # Symbols declared in include/smp.h.
-EXPORTS = ("smp_sample", "smp_filter_debug", "smp_sample_processed", "smp_spec_verify_workspace_bytes",
+EXPORTS = ("smp_sample", "smp_filter_debug", "smp_sample_processed", "smp_logit_prepass",
+           "smp_spec_verify_workspace_bytes",
            "smp_spec_verify", "smp_spec_verify_params", "smp_spec_verify_static", "smp_status_string",
            "smp_last_cuda_error",
            "smp_abi_version")
@@ -60,6 +61,8 @@ def load():
     lib.smp_filter_debug.restype = i32
     lib.smp_sample_processed.argtypes = [vp, i32, i32, i32, vp, vp, vp, i32, vp, u64, u64, vp, vp, vp, vp]
     lib.smp_sample_processed.restype = i32
+    lib.smp_logit_prepass.argtypes = [vp, i32, i32, i32, vp, vp, i32, vp, vp, vp]
+    lib.smp_logit_prepass.restype = i32
     lib.smp_spec_verify_workspace_bytes.argtypes = [i32, i32]
     lib.smp_spec_verify_workspace_bytes.restype = sz
     lib.smp_spec_verify.argtypes = [vp, vp, vp, i32, i32, i32, i32, u64, u64, vp, vp, vp, vp, sz, vp]
@@ -175,6 +178,30 @@ def sample_processed(logits, params, seed=0, offset=0, allowed=None, history=Non
                                     _ptr(history), hlen, _ptr(penalty), seed, offset, _ptr(out_ids),
                                     _ptr(out_probs), _ptr(status), _stream(stream)))
     return out_ids, out_probs, status
+
+
+def logit_prepass(logits, allowed=None, history=None, penalty=None, status=None, stream=None):
+    """smp_logit_prepass: the repetition penalty and the constraint mask
+    written into `logits` (a contiguous [B, V] float32/bfloat16 CUDA tensor)
+    in place.  Arguments as for sample_processed.  Returns status."""
+    torch = _torch()
+    lib = load()
+    if logits.dim() != 2 or not logits.is_cuda or not logits.is_contiguous():
+        raise SmpError("logits must be a contiguous [B, V] CUDA tensor")
+    batch, vocab = logits.shape
+    dev = logits.device
+    for t, shape in ((allowed, (batch, (vocab + 31) // 32)), (penalty, (batch,))):
+        if t is not None and (tuple(t.shape) != shape or not t.is_cuda or not t.is_contiguous()):
+            raise SmpError(f"expected a contiguous CUDA tensor of shape {shape}")
+    hlen = 0
+    if history is not None:
+        if history.dim() != 2 or history.shape[0] != batch or history.dtype != torch.int32:
+            raise SmpError("history must be an int32 [B, H] CUDA tensor")
+        hlen = int(history.shape[1])
+    status = status if status is not None else torch.empty(1, dtype=torch.int32, device=dev)
+    _check(lib.smp_logit_prepass(_ptr(logits), batch, vocab, _dtype_code(logits), _ptr(allowed), _ptr(history),
+                                 hlen, _ptr(penalty), _ptr(status), _stream(stream)))
+    return status
 
 
 def filter_debug(logits, params, seed=0, offset=0, stream=None):

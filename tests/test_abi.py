@@ -63,6 +63,10 @@ def test_host_validation_without_gpu(lib):
     assert lib.smp_sample_processed(fake, 4, 8, 0, fake, ctypes.c_void_p(0x1002), null, 0, null, 0, 0, fake,
                                     null, null, null) == 1
     assert lib.smp_sample_processed(fake, 4, 8, 5, fake, null, null, 0, null, 0, 0, fake, null, null, null) == 2
+    assert lib.smp_logit_prepass(null, 4, 8, 0, null, null, 0, null, null, null) == 1
+    assert lib.smp_logit_prepass(fake, 4, 8, 0, null, fake, 65, null, null, null) == 1
+    assert lib.smp_logit_prepass(fake, 4, 8, 3, null, null, 0, null, null, null) == 2
+    assert lib.smp_logit_prepass(ctypes.c_void_p(0x1001), 4, 8, 1, null, null, 0, null, null, null) == 1
     # verify: K out of range, workspace missing or too small
     assert lib.smp_spec_verify(fake, fake, fake, 2, 0, 8, 0, 0, 0, fake, fake, null, fake, 1 << 20, null) == 1
     assert lib.smp_spec_verify(fake, fake, fake, 2, 17, 8, 0, 0, 0, fake, fake, null, fake, 1 << 20, null) == 1

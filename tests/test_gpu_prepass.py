@@ -140,3 +140,55 @@ def test_large_vocab_with_penalty_sampled_rows():
     want = prepass.sample_processed(batch.values, batch.params, 0, 0, dtype="bf16", allowed=allowed,
                                     history=history, penalty=penalty, rows=rows)
     compare_sampler(want, ids, probs).check()
+
+
+# ------------------------------------------------------------------ in place (smp_logit_prepass)
+
+
+def storage_bits(values, dtype):
+    v = np.ascontiguousarray(values, dtype=np.float32).view(np.uint32)
+    return (v >> 16).astype(np.uint16) if dtype == "bf16" else v
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("vocab", [31, 1000, 32000, 50021])
+def test_inplace_prepass_is_bit_exact(dtype, vocab):
+    batch = workloads.random_sampler_batch(12, vocab, dtype=dtype, seed=vocab % 31, kinds="mixed")
+    allowed, history, penalty = workloads.prepass_inputs(batch.values, seed=vocab % 7)
+    penalty[3] = 0.0                      # invalid: the row becomes NaN
+    logits = device_logits(batch.data, dtype)
+    to = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a).view(dt)).cuda()
+    status = binding.logit_prepass(logits, to(allowed, np.int32), to(history, np.int32), to(penalty, np.float32))
+    torch.cuda.synchronize()
+    assert int(status.cpu()[0]) == binding.ROW_BAD_PARAMS
+    got = logits.cpu().view(torch.int16 if dtype == "bf16" else torch.int32).numpy()
+    got = got.view(np.uint16 if dtype == "bf16" else np.uint32)
+    for b in range(12):
+        if b == 3:
+            vals = got[b].astype(np.uint32) << 16 if dtype == "bf16" else got[b]
+            assert np.all(np.isnan(vals.view(np.float32)))
+            continue
+        want = prepass.prepare_row(batch.values[b], dtype, allowed[b], history[b], penalty[b])
+        assert np.array_equal(got[b], storage_bits(want, dtype)), b
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_inplace_prepass_then_sample(dtype):
+    batch = workloads.random_sampler_batch(32, 20011, dtype=dtype, seed=21, kinds="mixed")
+    allowed, history, penalty = workloads.prepass_inputs(batch.values, seed=22)
+    logits = device_logits(batch.data, dtype)
+    to = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a).view(dt)).cuda()
+    binding.logit_prepass(logits, to(allowed, np.int32), to(history, np.int32), to(penalty, np.float32))
+    ids, probs, status = binding.sample(logits, batch.params, 6, 1)
+    torch.cuda.synchronize()
+    want = prepass.sample_processed(batch.values, batch.params, 6, 1, dtype=dtype, allowed=allowed,
+                                    history=history, penalty=penalty)
+    compare_sampler(want, ids.cpu().numpy(), probs.cpu().numpy()).check()
+    # the row with no allowed token has no finite logit
+    assert int(status.cpu()[0]) == binding.ROW_NONFINITE
+    # and the out-of-place call gives the same ids
+    fresh = device_logits(batch.data, dtype)
+    ids2, _, _ = binding.sample_processed(fresh, batch.params, 6, 1, to(allowed, np.int32),
+                                          to(history, np.int32), to(penalty, np.float32))
+    torch.cuda.synchronize()
+    assert torch.equal(ids, ids2)

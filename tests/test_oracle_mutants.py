@@ -9,10 +9,12 @@ then fail; if none does, that part of the oracle is not pinned.
 import numpy as np
 import pytest
 
+import oracle.beam as beam_mod
 import oracle.philox as philox_mod
 import oracle.prepass as prepass_mod
 import oracle.sampler as sampler_mod
 import oracle.verify as verify_mod
+from tests import test_oracle_beam as t_beam
 from tests import test_oracle_philox as t_philox
 from tests import test_oracle_prepass as t_prepass
 from tests import test_oracle_pins as t_pins
@@ -120,6 +122,15 @@ def _allowed_inverted(words, vocab):
     return ((np.asarray(words, dtype=np.uint32)[ids // 32] >> (ids % 32).astype(np.uint32)) & 1) == 0
 
 
+def _candidates_without_beam_score(logits, scores):
+    return beam_mod.__dict__["_original_candidates"](logits, np.zeros(len(scores)))
+
+
+def _log_softmax_no_norm(row):
+    z = sampler_mod.logits_to_f64(row)
+    return z - np.max(z)
+
+
 def _fd_no_renorm(original):
     def wrapped(row, temperature, top_k=0, top_p=1.0, min_p=0.0):
         p, keep, _, diag = original(row, temperature, top_k, top_p, min_p)
@@ -171,10 +182,17 @@ MUTANTS = [
     ("mask inverted", prepass_mod, "allowed_mask", _allowed_inverted,
      [t_prepass.test_masked_distribution_is_conditioned_on_the_allowed_set,
       lambda: t_prepass.test_tiny_grammar_mask("[")]),
+    ("beam score ignored", beam_mod, "candidates", _candidates_without_beam_score,
+     [t_beam.test_two_step_example_beats_greedy, t_beam.test_brute_force_against_log_softmax]),
+    ("log-softmax without the log-sum", beam_mod, "log_softmax64", _log_softmax_no_norm,
+     [t_beam.test_two_step_example_beats_greedy, t_beam.test_brute_force_against_log_softmax]),
     ("renormalisation dropped", sampler_mod, "filtered_distribution",
      _fd_no_renorm(sampler_mod.filtered_distribution),
      [lambda: t_pins.test_exercise_39_1(load_golden), t_props.test_renormalisation_invariants]),
 ]
+
+
+beam_mod._original_candidates = beam_mod.candidates
 
 
 @pytest.mark.parametrize("name,module,attr,mutant,pins", MUTANTS, ids=[m[0] for m in MUTANTS])

@@ -394,6 +394,36 @@ def run_gpu(args):
         sampler_variants[name] = {"us_per_call": us, "rows_per_s": job_rate(B, world, us * 1e-6),
                                   "bytes_per_call": nbytes, "gbs": nbytes / (us * 1e-6) / 1e9}
 
+    # One beam-search step: 8 requests x 4 beams over the large vocabulary
+    # (bf16, Zipf-headed logits), the 4 best candidates of each request.
+    bG, bW, bwidth = 8, 4, 4
+    brng = np.random.default_rng(3000)
+    bz = workloads.f32_to_bf16_bits(workloads.zipf_logits_f32(brng, bG * bW, V)).reshape(bG, bW, V)
+    b_bytes = bz.nbytes
+    b_copies = max(4, math.ceil(4 * l2 / b_bytes))
+    b_host = torch.from_numpy(bz.view(np.int16)).view(torch.bfloat16)
+    b_dev = [b_host.to(dev) for _ in range(b_copies)]
+    b_scores = torch.from_numpy(-brng.uniform(0, 12, (bG, bW))).to(dev)
+    b_ws = torch.empty(max(8, int(binding.load().smp_beam_topk_workspace_bytes(bG, bW, bwidth))),
+                       dtype=torch.uint8, device=dev)
+    b_par = torch.empty(bG, bwidth, dtype=torch.int32, device=dev)
+    b_tok = torch.empty(bG, bwidth, dtype=torch.int32, device=dev)
+    b_sc = torch.empty(bG, bwidth, dtype=torch.float64, device=dev)
+
+    def bcall(i):
+        binding.beam_topk(b_dev[i % b_copies], b_scores, bwidth, b_ws, b_par, b_tok, b_sc, status)
+    for i in range(max(args.warmup, 3)):
+        bcall(i)
+    torch.cuda.synchronize()
+    assert int(status.cpu()[0]) == 0
+    g = capture(bcall)
+    b_us = 1000.0 * timed(g, 1) / args.steps
+    del g
+    beam_line = {"workload": f"{bG} requests x {bW} beams x V={V} bf16 (Zipf-headed), width {bwidth}",
+                 "us_per_call": b_us, "steps_per_s": world / (b_us * 1e-6), "bytes_per_call": b_bytes,
+                 "gbs": b_bytes / (b_us * 1e-6) / 1e9,
+                 "l2": f"inputs rotate over {b_copies} copies ({b_copies * b_bytes / 1e6:.0f} MB)"}
+
     verify_variants = {}
     for name, (ms, accepted) in var_ms.items():
         us = 1000.0 * ms / args.steps
@@ -495,6 +525,7 @@ def run_gpu(args):
             "sample_kernel_us": kern_us,
             "hbm_gbs": achieved,
             "sampler_variants": sampler_variants,
+            "beam_step": beam_line,
             "pct_of_measured_hbm": 100.0 * achieved / peak,
             "pct_of_8tbs_nominal": 100.0 * achieved / NOMINAL_HBM_GBS,
             "verify": {"tok_s": verify_tok_s, "us_per_call": ver_us, "mean_accepted": acc_mean,

@@ -41,6 +41,8 @@ extern "C" {
 #define SMP_MAX_DRAFT 16
 /* Longest window of recent tokens the repetition penalty looks at. */
 #define SMP_MAX_HISTORY 64
+/* Most beams per group, and most candidates kept per group, of a beam step. */
+#define SMP_MAX_BEAM_WIDTH 32
 
 typedef enum smp_dtype {
     SMP_F32 = 0,   /* IEEE binary32 logits */
@@ -272,6 +274,43 @@ smp_status smp_spec_verify_params(const void* p_logits, const void* q_logits, co
                                   const smp_row_params* params, uint64_t seed, uint64_t offset,
                                   int32_t* out_accepted_len, int32_t* out_ids, float* out_alpha,
                                   int32_t* status, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * smp_beam_topk_workspace_bytes -- device workspace smp_beam_topk needs (0 if
+ * the sizes are invalid).
+ */
+size_t smp_beam_topk_workspace_bytes(int32_t groups, int32_t beams, int32_t width);
+
+/*
+ * smp_beam_topk -- the candidate selection of one beam-search step ("Decoding
+ * & Speculative Sampling", section 39.1, eq. 39.1 and Listing 39.1;
+ * "Efficient Inference & Compression", section "Beam search").  For each
+ * group (one request), every beam b is extended by every token t with score
+ * s_b + log p_b(t), p_b = softmax(logits[g, b]) (temperature 1, no filters),
+ * and the `width` best candidates of the group's beams x vocab are returned,
+ * best first; equal scores keep the lower flat index b * vocab + t first (the
+ * listing's stable sort).
+ *
+ *   logits       device, [groups, beams, vocab] contiguous, dtype elements.
+ *   beam_scores  device, [groups, beams] double: s_b (log-probabilities of the
+ *                prefixes); -inf marks a dead beam, NaN makes an error group.
+ *   groups 1 ..; beams, width 1 .. SMP_MAX_BEAM_WIDTH; vocab 1 .. SMP_MAX_VOCAB.
+ *   out_parent, out_token  device, [groups, width] int32: the beam each kept
+ *                candidate extends and its token; out_score [groups, width]
+ *                double: its score.  Ranks past beams x vocab, and every rank
+ *                of an error group, are -1 / NaN.
+ *   status       device int32 or NULL: SMP_ROW_NONFINITE (a beam with no
+ *                finite logit), SMP_ROW_BAD_PARAMS (a NaN beam score).
+ *   workspace    device buffer of smp_beam_topk_workspace_bytes(groups,
+ *                beams, width) bytes, 8-byte aligned; caller-owned scratch.
+ * log p is computed as z - m - ln Z with Z a sum of binary32 exponentials in
+ * fixed point (relative error below about 1e-6), so scores match an fp64
+ * log-softmax within about 1e-6; candidates closer than that may swap.
+ */
+smp_status smp_beam_topk(const void* logits, const double* beam_scores, int32_t groups, int32_t beams,
+                         int32_t vocab, int32_t width, smp_dtype dtype, int32_t* out_parent, int32_t* out_token,
+                         double* out_score, int32_t* status, void* workspace, size_t workspace_bytes,
+                         void* stream);
 
 /*
  * Size of the device array that smp_spec_verify_static uses as its workspace

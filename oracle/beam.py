@@ -72,7 +72,7 @@ def select_group(logits, scores, width):
     cand = candidates(logits, scores)
     cand.sort(key=lambda c: c[1])                  # appended order: flat index
     cand.sort(key=lambda c: c[0], reverse=True)    # stable: equal scores keep it
-    for j in range(width):
+    for j in range(min(width, len(cand))):      # ranks past beams x V stay -1 / NaN
         s, flat = cand[j]
         res["parent"][j] = flat // V
         res["token"][j] = flat % V

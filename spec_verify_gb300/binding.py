@@ -26,7 +26,7 @@ ROW_BAD_DRAFT = 8
 
 # Symbols declared in include/smp.h.
 EXPORTS = ("smp_sample", "smp_filter_debug", "smp_sample_processed", "smp_logit_prepass",
-           "smp_spec_verify_workspace_bytes",
+           "smp_beam_topk_workspace_bytes", "smp_beam_topk", "smp_spec_verify_workspace_bytes",
            "smp_spec_verify", "smp_spec_verify_params", "smp_spec_verify_static", "smp_status_string",
            "smp_last_cuda_error",
            "smp_abi_version")
@@ -63,6 +63,10 @@ def load():
     lib.smp_sample_processed.restype = i32
     lib.smp_logit_prepass.argtypes = [vp, i32, i32, i32, vp, vp, i32, vp, vp, vp]
     lib.smp_logit_prepass.restype = i32
+    lib.smp_beam_topk_workspace_bytes.argtypes = [i32, i32, i32]
+    lib.smp_beam_topk_workspace_bytes.restype = sz
+    lib.smp_beam_topk.argtypes = [vp, vp, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, sz, vp]
+    lib.smp_beam_topk.restype = i32
     lib.smp_spec_verify_workspace_bytes.argtypes = [i32, i32]
     lib.smp_spec_verify_workspace_bytes.restype = sz
     lib.smp_spec_verify.argtypes = [vp, vp, vp, i32, i32, i32, i32, u64, u64, vp, vp, vp, vp, sz, vp]
@@ -308,3 +312,31 @@ def spec_verify_static(p_logits, q_logits, draft_ids, seed=0, offset=0, out_acce
                                       _dtype_code(p_logits), seed, offset, _ptr(out_accepted),
                                       _ptr(out_ids), _ptr(status), _stream(stream)))
     return out_accepted, out_ids, status
+
+
+def beam_topk(logits, beam_scores, width=None, workspace=None, out_parent=None, out_token=None, out_score=None,
+              status=None, stream=None):
+    """smp_beam_topk on logits [G, W, V] (float32/bfloat16) and beam_scores
+    [G, W] (float64) CUDA tensors; width defaults to W.  Returns (parent
+    int32 [G, width], token int32 [G, width], score float64 [G, width],
+    status int32 [1])."""
+    torch = _torch()
+    lib = load()
+    if logits.dim() != 3 or not logits.is_cuda or not logits.is_contiguous():
+        raise SmpError("logits must be a contiguous [G, W, V] CUDA tensor")
+    groups, beams, vocab = logits.shape
+    if tuple(beam_scores.shape) != (groups, beams) or beam_scores.dtype != torch.float64 or not beam_scores.is_cuda:
+        raise SmpError("beam_scores must be a float64 [G, W] CUDA tensor")
+    width = beams if width is None else int(width)
+    dev = logits.device
+    need = int(lib.smp_beam_topk_workspace_bytes(groups, beams, width))
+    if workspace is None:
+        workspace = torch.empty(max(need, 8), dtype=torch.uint8, device=dev)
+    out_parent = out_parent if out_parent is not None else torch.empty(groups, width, dtype=torch.int32, device=dev)
+    out_token = out_token if out_token is not None else torch.empty(groups, width, dtype=torch.int32, device=dev)
+    out_score = out_score if out_score is not None else torch.empty(groups, width, dtype=torch.float64, device=dev)
+    status = status if status is not None else torch.empty(1, dtype=torch.int32, device=dev)
+    _check(lib.smp_beam_topk(_ptr(logits), _ptr(beam_scores), groups, beams, vocab, width, _dtype_code(logits),
+                             _ptr(out_parent), _ptr(out_token), _ptr(out_score), _ptr(status), _ptr(workspace),
+                             workspace.numel(), _stream(stream)))
+    return out_parent, out_token, out_score, status

@@ -21,7 +21,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libsmp.so")
 
-SOURCES = ["api.cu", "sample.cu", "verify.cu", "prepass.cu"]
+SOURCES = ["api.cu", "sample.cu", "verify.cu", "prepass.cu", "beam.cu"]
 HEADERS = ["common.cuh", "row_ops.cuh", "select.cuh", "general.cuh", "launch.h", "exp_table.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",

@@ -1,0 +1,262 @@
+// One beam-search step's candidate selection ("Decoding & Speculative
+// Sampling", section 39.1, eq. 39.1 and Listing 39.1; "Efficient Inference &
+// Compression", section "Beam search"): every beam b of a group is extended
+// by every token t with score s_b + log p_b(t), and the `width` best of the
+// group's beams x V candidates survive, ordered by score (equal scores: lower
+// flat index b * V + t first).
+//
+// Two kernels on the caller's stream:
+//   beam_row_kernel    one CTA per beam row: the row maximum m, the mass
+//                      sum Z (binary32 exponentials, fixed-point sums), and
+//                      the row's `width` best tokens by (logit desc, id asc),
+//                      found by the sampler's exact count radix selection;
+//   beam_merge_kernel  one CTA per group: the scores s_b + (z - m_b - ln Z_b)
+//                      in fp64 of the beams' listed tokens, and each
+//                      candidate's rank in the group by comparison with all
+//                      the others; the first `width` are written.
+// Only a row's best `width` tokens can be among its group's best `width`
+// candidates, because within a beam the score order is the logit order.
+#include <cuda_runtime.h>
+
+#include <climits>
+
+#include "launch.h"
+#include "row_ops.cuh"
+#include "smp.h"
+
+namespace smp {
+
+#include "select.cuh"
+
+// Per beam row in the workspace: its header, then `width` (id, logit) pairs
+// sorted by (logit desc, id asc).
+struct BeamRowHead {
+  double c;        // -m - ln Z (the row's log-softmax offset)
+  int32_t flags;   // kRowNonFinite
+  int32_t n;       // candidates listed: min(width, vocab)
+};
+struct BeamCand {
+  int32_t id;
+  float z;
+};
+
+struct BeamArgs {
+  const void* logits;   // [groups, beams, vocab]
+  const double* scores; // [groups, beams]
+  int groups;
+  int beams;
+  int vocab;
+  int width;
+  int32_t* out_parent;  // [groups, width]
+  int32_t* out_token;
+  double* out_score;
+  int32_t* status;
+  unsigned char* ws;
+};
+
+__host__ __device__ __forceinline__ size_t beam_row_bytes(int width) {
+  return sizeof(BeamRowHead) + size_t(width) * sizeof(BeamCand);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads, 2) beam_row_kernel(BeamArgs a) {
+  __shared__ FloatPair table[64];
+  __shared__ GenShared gs;
+  __shared__ unsigned long long members[SMP_MAX_BEAM_WIDTH];   // (key << 32) | ~id
+  __shared__ int n_members;
+  const int tid = threadIdx.x;
+  const int rowi = int(blockIdx.x);
+  const int V = a.vocab;
+  grid_dependency_wait();
+  allow_dependent_launch();
+  if (tid < 64) table[tid] = kExp2Table[tid];
+  if (tid == 0) n_members = 0;
+  const T* row = reinterpret_cast<const T*>(a.logits) + size_t(rowi) * V;
+  BeamRowHead* head = reinterpret_cast<BeamRowHead*>(a.ws + size_t(rowi) * beam_row_bytes(a.width));
+  BeamCand* cand = reinterpret_cast<BeamCand*>(head + 1);
+
+  // The row maximum (as an order key), then Z = sum exp(z - m) in binary32
+  // per thread, turned into 44-bit fixed point once per thread and summed
+  // exactly.
+  uint32_t kmax = 0;
+  gen_sweep<T>(row, V, [&](int, float z) { kmax = max(kmax, order_key<T>(z)); });
+  kmax = uint32_t(block_max_u64(uint64_t(kmax), gs.red64));
+  if (!key_finite<T>(kmax)) {
+    if (tid == 0) {
+      head->c = 0.0;
+      head->flags = kRowNonFinite;
+      head->n = 0;
+    }
+    return;
+  }
+  const float m = key_value<T>(kmax);
+  const RowScale rs = make_row_scale_unit(m);
+  float st = 0.0f;
+  gen_sweep<T>(row, V, [&](int, float z) { st += exp_fast(z, rs); });
+  uint64_t zf = __float2ull_rn(__fmul_rn(st, float(kFixedOne)));
+  zf = warp_sum<uint64_t>(zf);
+  if ((tid & 31) == 0) gs.scan64[tid >> 5] = zf;
+  cta_sync();
+  uint64_t ztot = 0;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) ztot += gs.scan64[w];
+  cta_sync();
+
+  // The row's `width` best tokens: the kept set of top-k = width.
+  smp_row_params prm;
+  prm.temperature = 1.0f;
+  prm.top_k = a.width;
+  prm.top_p = 1.0f;
+  prm.min_p = 0.0f;
+  prm.greedy = 0;
+  const KeptSet ks = gen_kept_set<T>(row, V, gs, table, prm, kmax);
+  gen_sweep<T>(row, V, [&](int i, float z) {
+    const uint32_t k = order_key<T>(z);
+    if (in_kept_set(ks, k, uint32_t(i))) {
+      const int slot = atomicAdd(&n_members, 1);
+      if (slot < SMP_MAX_BEAM_WIDTH) members[slot] = pack_key_id(k, uint32_t(i));
+    }
+  });
+  cta_sync();
+  const int n = min(n_members, min(a.width, V));
+  // Sorted by (key desc, id asc): the packed values in decreasing order.
+  if (tid < n) {
+    const unsigned long long mine = members[tid];
+    int rank = 0;
+    for (int j = 0; j < n; ++j) rank += members[j] > mine;
+    const uint32_t id = ~uint32_t(mine);
+    cand[rank].id = int32_t(id);
+    cand[rank].z = Elem<T>::widen(row[id]);
+  }
+  if (tid == 0) {
+    head->c = -double(m) - log(double(ztot) * (1.0 / double(kFixedOne)));
+    head->flags = 0;
+    head->n = n;
+  }
+}
+
+// One CTA per group: every listed candidate (b, j) gets its score
+// s_b + (z + c_b) in fp64 and its flat index b * V + id; its rank is the
+// number of listed candidates before it in the order (score desc, flat asc),
+// a strict total order, so the first `width` ranks are filled exactly once.
+__global__ void __launch_bounds__(kThreads) beam_merge_kernel(BeamArgs a) {
+  constexpr int kMaxCand = SMP_MAX_BEAM_WIDTH * SMP_MAX_BEAM_WIDTH;
+  __shared__ double cs[kMaxCand];
+  __shared__ int32_t cf[kMaxCand];   // flat index, or -1 for an empty slot
+  __shared__ int bad;
+  const int g = int(blockIdx.x);
+  const int W = a.beams, width = a.width, V = a.vocab;
+  const int tid = threadIdx.x;
+  grid_dependency_wait();
+  allow_dependent_launch();
+  auto head_of = [&](int b) {
+    return reinterpret_cast<const BeamRowHead*>(a.ws + size_t(g * W + b) * beam_row_bytes(width));
+  };
+  if (tid == 0) {
+    int f = 0;
+    for (int b = 0; b < W; ++b) {
+      f |= head_of(b)->flags;
+      if (isnan(a.scores[size_t(g) * W + b])) f |= kRowBadParams;
+    }
+    bad = f;
+    if (f && a.status) atomicOr(a.status, f);
+  }
+  // ranks nobody fills (fewer candidates than width, or an error group) stay -1 / NaN
+  for (int r = tid; r < width; r += kThreads) {
+    a.out_parent[size_t(g) * width + r] = -1;
+    a.out_token[size_t(g) * width + r] = -1;
+    a.out_score[size_t(g) * width + r] = __longlong_as_double(0x7FF8000000000000ll);
+  }
+  __syncthreads();
+  if (bad) return;
+  const int n = W * width;
+  for (int c = tid; c < n; c += kThreads) {
+    const int b = c / width, j = c % width;
+    const BeamRowHead* hb = head_of(b);
+    cf[c] = -1;
+    cs[c] = 0.0;
+    if (j < hb->n) {
+      const BeamCand* lb = reinterpret_cast<const BeamCand*>(hb + 1);
+      cs[c] = a.scores[size_t(g) * W + b] + (double(lb[j].z) + hb->c);
+      cf[c] = b * V + lb[j].id;
+    }
+  }
+  __syncthreads();
+  for (int c = tid; c < n; c += kThreads) {
+    const int f = cf[c];
+    if (f < 0) continue;
+    const double s = cs[c];
+    int rank = 0;
+    for (int d = 0; d < n && rank < width; ++d) {
+      const int fd = cf[d];
+      rank += fd >= 0 && (cs[d] > s || (cs[d] == s && fd < f));
+    }
+    if (rank < width) {
+      a.out_parent[size_t(g) * width + rank] = f / V;
+      a.out_token[size_t(g) * width + rank] = f % V;
+      a.out_score[size_t(g) * width + rank] = s;
+    }
+  }
+}
+
+template <typename T>
+static smp_status launch_beam(const BeamArgs& args, cudaStream_t stream) {
+  BeamArgs a = args;
+  LaunchShape ls;
+  ls.pdl = true;
+  cudaError_t err = launch_cluster(reinterpret_cast<const void*>(&beam_row_kernel<T>),
+                                   dim3(unsigned(a.groups * a.beams)), dim3(kThreads), ls, stream, &a);
+  if (err != cudaSuccess) return fail_cuda(err);
+  err = launch_cluster(reinterpret_cast<const void*>(&beam_merge_kernel), dim3(unsigned(a.groups)), dim3(kThreads),
+                       ls, stream, &a);
+  if (err != cudaSuccess) return fail_cuda(err);
+  return SMP_OK;
+}
+
+}  // namespace smp
+
+extern "C" size_t smp_beam_topk_workspace_bytes(int32_t groups, int32_t beams, int32_t width) {
+  if (groups <= 0 || beams <= 0 || width <= 0 || width > SMP_MAX_BEAM_WIDTH || beams > SMP_MAX_BEAM_WIDTH ||
+      int64_t(groups) * beams > (1 << 24))
+    return 0;
+  return size_t(groups) * size_t(beams) * smp::beam_row_bytes(width);
+}
+
+extern "C" smp_status smp_beam_topk(const void* logits, const double* beam_scores, int32_t groups, int32_t beams,
+                                    int32_t vocab, int32_t width, smp_dtype dtype, int32_t* out_parent,
+                                    int32_t* out_token, double* out_score, int32_t* status, void* workspace,
+                                    size_t workspace_bytes, void* stream) {
+  using namespace smp;
+  if (dtype != SMP_F32 && dtype != SMP_BF16) return SMP_ERR_DTYPE;
+  if (!logits || !beam_scores || !out_parent || !out_token || !out_score) return SMP_ERR_INVALID_ARG;
+  if (vocab <= 0 || int64_t(beams) * vocab > INT_MAX) return SMP_ERR_INVALID_ARG;
+  const size_t need = smp_beam_topk_workspace_bytes(groups, beams, width);
+  if (need == 0) return SMP_ERR_INVALID_ARG;
+  if (vocab > SMP_MAX_VOCAB) return SMP_ERR_UNSUPPORTED;
+  const int elem = dtype == SMP_F32 ? 4 : 2;
+  if (reinterpret_cast<uintptr_t>(logits) % elem || reinterpret_cast<uintptr_t>(beam_scores) % 8 ||
+      reinterpret_cast<uintptr_t>(out_score) % 8 ||
+      (reinterpret_cast<uintptr_t>(out_parent) | reinterpret_cast<uintptr_t>(out_token) |
+       reinterpret_cast<uintptr_t>(status)) % 4)
+    return SMP_ERR_INVALID_ARG;
+  if (!workspace || workspace_bytes < need || reinterpret_cast<uintptr_t>(workspace) % 8) return SMP_ERR_WORKSPACE;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (status) {
+    const smp_status rc = clear_status(status, st);
+    if (rc != SMP_OK) return rc;
+  }
+  BeamArgs a{};
+  a.logits = logits;
+  a.scores = beam_scores;
+  a.groups = groups;
+  a.beams = beams;
+  a.vocab = vocab;
+  a.width = width;
+  a.out_parent = out_parent;
+  a.out_token = out_token;
+  a.out_score = out_score;
+  a.status = status;
+  a.ws = reinterpret_cast<unsigned char*>(workspace);
+  if (dtype == SMP_F32) return launch_beam<float>(a, st);
+  return launch_beam<uint16_t>(a, st);
+}

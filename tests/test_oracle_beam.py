@@ -89,3 +89,10 @@ def test_error_groups():
     z[1] = -np.inf
     r = beam.select_group(z, np.array([0.0, 0.0]), 2)
     assert r["status"] == beam.GROUP_NONFINITE and r["token"] == [-1, -1]
+
+
+def test_width_past_the_candidates():
+    z = np.array([[0.0, 1.0]], dtype=np.float32)
+    got = beam.select_group(z, np.array([0.0]), 4)
+    assert got["token"] == [1, 0, -1, -1] and got["parent"] == [0, 0, -1, -1]
+    assert math.isnan(got["score"][2]) and math.isnan(got["score"][3])

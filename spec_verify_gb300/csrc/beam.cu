@@ -6,18 +6,21 @@
 // flat index b * V + t first).
 //
 // Two kernels on the caller's stream:
-//   beam_row_kernel    one CTA per beam row: the row maximum m, the mass
-//                      sum Z (binary32 exponentials, fixed-point sums), and
-//                      the row's `width` best tokens by (logit desc, id asc),
-//                      found by the sampler's exact count radix selection;
-//   beam_merge_kernel  one CTA per group: the scores s_b + (z - m_b - ln Z_b)
-//                      in fp64 of the beams' listed tokens, and each
-//                      candidate's rank in the group by comparison with all
-//                      the others; the first `width` are written.
+//   beam_row_kernel    one CTA per slice of a beam row: the slice maximum,
+//                      its mass sum (binary32 exponentials, fixed-point
+//                      sums), and its `width` best tokens by (logit desc,
+//                      id asc), found by the sampler's exact count radix
+//                      selection;
+//   beam_merge_kernel  one CTA per group: each beam's m and Z from its
+//                      slices, the scores s_b + (z - m_b - ln Z_b) in fp64 of
+//                      the listed tokens, and each candidate's rank in the
+//                      group by comparison with all the others; the first
+//                      `width` are written.
 // Only a row's best `width` tokens can be among its group's best `width`
 // candidates, because within a beam the score order is the logit order.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <climits>
 
 #include "launch.h"
@@ -28,12 +31,20 @@ namespace smp {
 
 #include "select.cuh"
 
-// Per beam row in the workspace: its header, then `width` (id, logit) pairs
-// sorted by (logit desc, id asc).
-struct BeamRowHead {
-  double c;        // -m - ln Z (the row's log-softmax offset)
-  int32_t flags;   // kRowNonFinite
-  int32_t n;       // candidates listed: min(width, vocab)
+// Each beam row is cut into S slices of about V / S ids, one CTA per slice,
+// so that a few rows still spread over the GPU.  Per slice in the workspace:
+// its header, then `width` (id, logit) pairs, its best tokens by (logit desc,
+// id asc).  The union of a row's slice lists holds the row's best `width`.
+constexpr int kBeamMaxSlices = 16;
+constexpr int kBeamMaxCand = SMP_MAX_BEAM_WIDTH * SMP_MAX_BEAM_WIDTH;   // candidates one merge CTA ranks
+constexpr int kSliceEmpty = 1 << 8;   // a slice with no finite logit (not an error by itself)
+
+struct BeamSliceHead {
+  float m;         // the slice's maximum logit
+  int32_t flags;   // kSliceEmpty, or kRowNonFinite (+inf in the slice)
+  uint64_t z;      // sum of exp(z - m) over the slice, 44-bit fixed point
+  int32_t n;       // candidates listed
+  int32_t pad;
 };
 struct BeamCand {
   int32_t id;
@@ -47,6 +58,8 @@ struct BeamArgs {
   int beams;
   int vocab;
   int width;
+  int slices;           // S
+  int slice_len;        // ids per slice (a multiple of 8)
   int32_t* out_parent;  // [groups, width]
   int32_t* out_token;
   double* out_score;
@@ -54,37 +67,50 @@ struct BeamArgs {
   unsigned char* ws;
 };
 
-__host__ __device__ __forceinline__ size_t beam_row_bytes(int width) {
-  return sizeof(BeamRowHead) + size_t(width) * sizeof(BeamCand);
+__host__ __device__ __forceinline__ size_t beam_slice_bytes(int width) {
+  return sizeof(BeamSliceHead) + size_t(width) * sizeof(BeamCand);
 }
 
 template <typename T>
 __global__ void __launch_bounds__(kThreads, 2) beam_row_kernel(BeamArgs a) {
   __shared__ FloatPair table[64];
   __shared__ GenShared gs;
-  __shared__ unsigned long long members[SMP_MAX_BEAM_WIDTH];   // (key << 32) | ~id
+  __shared__ unsigned long long members[SMP_MAX_BEAM_WIDTH];   // (key << 32) | ~local id
   __shared__ int n_members;
   const int tid = threadIdx.x;
-  const int rowi = int(blockIdx.x);
-  const int V = a.vocab;
+  const int rowi = int(blockIdx.x) / a.slices;
+  const int slice = int(blockIdx.x) % a.slices;
   grid_dependency_wait();
   allow_dependent_launch();
   if (tid < 64) table[tid] = kExp2Table[tid];
   if (tid == 0) n_members = 0;
-  const T* row = reinterpret_cast<const T*>(a.logits) + size_t(rowi) * V;
-  BeamRowHead* head = reinterpret_cast<BeamRowHead*>(a.ws + size_t(rowi) * beam_row_bytes(a.width));
+  const int lo = slice * a.slice_len;
+  const int len = max(0, min(a.vocab, lo + a.slice_len) - lo);
+  const T* row = reinterpret_cast<const T*>(a.logits) + size_t(rowi) * a.vocab + lo;
+  BeamSliceHead* head = reinterpret_cast<BeamSliceHead*>(a.ws + size_t(blockIdx.x) * beam_slice_bytes(a.width));
   BeamCand* cand = reinterpret_cast<BeamCand*>(head + 1);
+  if (len == 0) {
+    if (tid == 0) {
+      head->m = -INFINITY;
+      head->flags = kSliceEmpty;
+      head->z = 0;
+      head->n = 0;
+    }
+    return;
+  }
 
-  // The row maximum (as an order key), then Z = sum exp(z - m) in binary32
+  // The slice maximum (as an order key), then Z = sum exp(z - m) in binary32
   // per thread, turned into 44-bit fixed point once per thread and summed
   // exactly.
   uint32_t kmax = 0;
-  gen_sweep<T>(row, V, [&](int, float z) { kmax = max(kmax, order_key<T>(z)); });
+  gen_sweep<T>(row, len, [&](int, float z) { kmax = max(kmax, order_key<T>(z)); });
   kmax = uint32_t(block_max_u64(uint64_t(kmax), gs.red64));
-  if (!key_finite<T>(kmax)) {
+  if (!key_finite<T>(kmax)) {   // all -inf / NaN, or +inf present
     if (tid == 0) {
-      head->c = 0.0;
-      head->flags = kRowNonFinite;
+      const bool pinf = kmax == order_key<T>(INFINITY);
+      head->m = -INFINITY;
+      head->flags = pinf ? kRowNonFinite : kSliceEmpty;
+      head->z = 0;
       head->n = 0;
     }
     return;
@@ -92,7 +118,7 @@ __global__ void __launch_bounds__(kThreads, 2) beam_row_kernel(BeamArgs a) {
   const float m = key_value<T>(kmax);
   const RowScale rs = make_row_scale_unit(m);
   float st = 0.0f;
-  gen_sweep<T>(row, V, [&](int, float z) { st += exp_fast(z, rs); });
+  gen_sweep<T>(row, len, [&](int, float z) { st += exp_fast(z, rs); });
   uint64_t zf = __float2ull_rn(__fmul_rn(st, float(kFixedOne)));
   zf = warp_sum<uint64_t>(zf);
   if ((tid & 31) == 0) gs.scan64[tid >> 5] = zf;
@@ -102,15 +128,15 @@ __global__ void __launch_bounds__(kThreads, 2) beam_row_kernel(BeamArgs a) {
   for (int w = 0; w < kWarps; ++w) ztot += gs.scan64[w];
   cta_sync();
 
-  // The row's `width` best tokens: the kept set of top-k = width.
+  // The slice's `width` best tokens: the kept set of top-k = width.
   smp_row_params prm;
   prm.temperature = 1.0f;
   prm.top_k = a.width;
   prm.top_p = 1.0f;
   prm.min_p = 0.0f;
   prm.greedy = 0;
-  const KeptSet ks = gen_kept_set<T>(row, V, gs, table, prm, kmax);
-  gen_sweep<T>(row, V, [&](int i, float z) {
+  const KeptSet ks = gen_kept_set<T>(row, len, gs, table, prm, kmax);
+  gen_sweep<T>(row, len, [&](int i, float z) {
     const uint32_t k = order_key<T>(z);
     if (in_kept_set(ks, k, uint32_t(i))) {
       const int slot = atomicAdd(&n_members, 1);
@@ -118,48 +144,67 @@ __global__ void __launch_bounds__(kThreads, 2) beam_row_kernel(BeamArgs a) {
     }
   });
   cta_sync();
-  const int n = min(n_members, min(a.width, V));
+  const int n = min(n_members, min(a.width, len));
   // Sorted by (key desc, id asc): the packed values in decreasing order.
   if (tid < n) {
     const unsigned long long mine = members[tid];
     int rank = 0;
     for (int j = 0; j < n; ++j) rank += members[j] > mine;
     const uint32_t id = ~uint32_t(mine);
-    cand[rank].id = int32_t(id);
+    cand[rank].id = lo + int32_t(id);
     cand[rank].z = Elem<T>::widen(row[id]);
   }
   if (tid == 0) {
-    head->c = -double(m) - log(double(ztot) * (1.0 / double(kFixedOne)));
+    head->m = m;
     head->flags = 0;
+    head->z = ztot;
     head->n = n;
   }
 }
 
-// One CTA per group: every listed candidate (b, j) gets its score
-// s_b + (z + c_b) in fp64 and its flat index b * V + id; its rank is the
-// number of listed candidates before it in the order (score desc, flat asc),
-// a strict total order, so the first `width` ranks are filled exactly once.
+// One CTA per group.  Per beam: m = the slices' maximum, Z = sum over slices
+// of Z_s exp(m_s - m) in fp64, c = -m - ln Z.  Every listed candidate gets its
+// score s_b + (z + c_b) and its flat index b * V + id; its rank is the number
+// of listed candidates before it in the order (score desc, flat asc), a
+// strict total order, so the first `width` ranks are filled exactly once.
 __global__ void __launch_bounds__(kThreads) beam_merge_kernel(BeamArgs a) {
-  constexpr int kMaxCand = SMP_MAX_BEAM_WIDTH * SMP_MAX_BEAM_WIDTH;
-  __shared__ double cs[kMaxCand];
-  __shared__ int32_t cf[kMaxCand];   // flat index, or -1 for an empty slot
+  __shared__ double cs[kBeamMaxCand];
+  __shared__ int32_t cf[kBeamMaxCand];   // flat index, or -1 for an empty slot
+  __shared__ double beam_c[SMP_MAX_BEAM_WIDTH];
   __shared__ int bad;
   const int g = int(blockIdx.x);
-  const int W = a.beams, width = a.width, V = a.vocab;
+  const int W = a.beams, width = a.width, V = a.vocab, S = a.slices;
   const int tid = threadIdx.x;
   grid_dependency_wait();
   allow_dependent_launch();
-  auto head_of = [&](int b) {
-    return reinterpret_cast<const BeamRowHead*>(a.ws + size_t(g * W + b) * beam_row_bytes(width));
+  auto head_of = [&](int b, int s) {
+    return reinterpret_cast<const BeamSliceHead*>(a.ws + (size_t(g * W + b) * S + s) * beam_slice_bytes(width));
   };
-  if (tid == 0) {
-    int f = 0;
-    for (int b = 0; b < W; ++b) {
-      f |= head_of(b)->flags;
-      if (isnan(a.scores[size_t(g) * W + b])) f |= kRowBadParams;
+  if (tid == 0) bad = 0;
+  __syncthreads();
+  if (tid < W) {
+    const int b = tid;
+    int f = isnan(a.scores[size_t(g) * W + b]) ? kRowBadParams : 0;
+    float m = -INFINITY;
+    bool any = false;
+    for (int s = 0; s < S; ++s) {
+      const BeamSliceHead* h = head_of(b, s);
+      f |= h->flags & kRowNonFinite;
+      if (!(h->flags & kSliceEmpty) && !(h->flags & kRowNonFinite)) {
+        any = true;
+        m = fmaxf(m, h->m);
+      }
     }
-    bad = f;
-    if (f && a.status) atomicOr(a.status, f);
+    if (!any) f |= kRowNonFinite;
+    double z = 0.0;
+    if (!f)
+      for (int s = 0; s < S; ++s) {
+        const BeamSliceHead* h = head_of(b, s);
+        if (h->flags) continue;
+        z += double(h->z) * (1.0 / double(kFixedOne)) * exp(double(h->m) - double(m));
+      }
+    beam_c[b] = f ? 0.0 : -double(m) - log(z);
+    if (f) atomicOr(&bad, f);
   }
   // ranks nobody fills (fewer candidates than width, or an error group) stay -1 / NaN
   for (int r = tid; r < width; r += kThreads) {
@@ -168,33 +213,37 @@ __global__ void __launch_bounds__(kThreads) beam_merge_kernel(BeamArgs a) {
     a.out_score[size_t(g) * width + r] = __longlong_as_double(0x7FF8000000000000ll);
   }
   __syncthreads();
-  if (bad) return;
-  const int n = W * width;
+  if (bad) {
+    if (tid == 0 && a.status) atomicOr(a.status, bad);
+    return;
+  }
+  const int per_beam = S * width;
+  const int n = W * per_beam;
   for (int c = tid; c < n; c += kThreads) {
-    const int b = c / width, j = c % width;
-    const BeamRowHead* hb = head_of(b);
+    const int b = c / per_beam, s = (c % per_beam) / width, j = c % width;
+    const BeamSliceHead* h = head_of(b, s);
     cf[c] = -1;
     cs[c] = 0.0;
-    if (j < hb->n) {
-      const BeamCand* lb = reinterpret_cast<const BeamCand*>(hb + 1);
-      cs[c] = a.scores[size_t(g) * W + b] + (double(lb[j].z) + hb->c);
-      cf[c] = b * V + lb[j].id;
+    if (j < h->n) {
+      const BeamCand* l = reinterpret_cast<const BeamCand*>(h + 1);
+      cs[c] = a.scores[size_t(g) * W + b] + (double(l[j].z) + beam_c[b]);
+      cf[c] = b * V + l[j].id;
     }
   }
   __syncthreads();
   for (int c = tid; c < n; c += kThreads) {
     const int f = cf[c];
     if (f < 0) continue;
-    const double s = cs[c];
+    const double sc = cs[c];
     int rank = 0;
     for (int d = 0; d < n && rank < width; ++d) {
       const int fd = cf[d];
-      rank += fd >= 0 && (cs[d] > s || (cs[d] == s && fd < f));
+      rank += fd >= 0 && (cs[d] > sc || (cs[d] == sc && fd < f));
     }
     if (rank < width) {
       a.out_parent[size_t(g) * width + rank] = f / V;
       a.out_token[size_t(g) * width + rank] = f % V;
-      a.out_score[size_t(g) * width + rank] = s;
+      a.out_score[size_t(g) * width + rank] = sc;
     }
   }
 }
@@ -202,10 +251,23 @@ __global__ void __launch_bounds__(kThreads) beam_merge_kernel(BeamArgs a) {
 template <typename T>
 static smp_status launch_beam(const BeamArgs& args, cudaStream_t stream) {
   BeamArgs a = args;
+  const int dev = current_device();
+  if (dev < 0) return fail_cuda(cudaGetLastError());
+  // Slices: enough CTAs for about two per SM, at most kBeamMaxSlices, at
+  // least 2048 ids each, and no more candidates per group than one merge CTA
+  // ranks.
+  const int64_t rows = int64_t(a.groups) * a.beams;
+  int S = int((2 * int64_t(device_sms(dev)) + rows - 1) / rows);
+  S = std::min(S, kBeamMaxSlices);
+  S = std::min(S, kBeamMaxCand / (a.beams * a.width));
+  S = std::min(S, (a.vocab + 2047) / 2048);
+  S = std::max(S, 1);
+  a.slices = S;
+  a.slice_len = ((a.vocab + S - 1) / S + 7) / 8 * 8;
   LaunchShape ls;
   ls.pdl = true;
   cudaError_t err = launch_cluster(reinterpret_cast<const void*>(&beam_row_kernel<T>),
-                                   dim3(unsigned(a.groups * a.beams)), dim3(kThreads), ls, stream, &a);
+                                   dim3(unsigned(rows * S)), dim3(kThreads), ls, stream, &a);
   if (err != cudaSuccess) return fail_cuda(err);
   err = launch_cluster(reinterpret_cast<const void*>(&beam_merge_kernel), dim3(unsigned(a.groups)), dim3(kThreads),
                        ls, stream, &a);
@@ -219,7 +281,7 @@ extern "C" size_t smp_beam_topk_workspace_bytes(int32_t groups, int32_t beams, i
   if (groups <= 0 || beams <= 0 || width <= 0 || width > SMP_MAX_BEAM_WIDTH || beams > SMP_MAX_BEAM_WIDTH ||
       int64_t(groups) * beams > (1 << 24))
     return 0;
-  return size_t(groups) * size_t(beams) * smp::beam_row_bytes(width);
+  return size_t(groups) * size_t(beams) * smp::kBeamMaxSlices * smp::beam_slice_bytes(width);
 }
 
 extern "C" smp_status smp_beam_topk(const void* logits, const double* beam_scores, int32_t groups, int32_t beams,

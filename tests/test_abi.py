@@ -63,7 +63,7 @@ def test_host_validation_without_gpu(lib):
     assert lib.smp_sample_processed(fake, 4, 8, 0, fake, ctypes.c_void_p(0x1002), null, 0, null, 0, 0, fake,
                                     null, null, null) == 1
     assert lib.smp_sample_processed(fake, 4, 8, 5, fake, null, null, 0, null, 0, 0, fake, null, null, null) == 2
-    assert lib.smp_beam_topk_workspace_bytes(2, 4, 4) == 2 * 4 * (16 + 4 * 8)
+    assert lib.smp_beam_topk_workspace_bytes(2, 4, 4) == 2 * 4 * 16 * (24 + 4 * 8)   # 16 slices at most
     assert lib.smp_beam_topk_workspace_bytes(2, 33, 4) == 0
     assert lib.smp_beam_topk_workspace_bytes(2, 4, 0) == 0
     assert lib.smp_beam_topk(null, fake, 2, 4, 100, 4, 0, fake, fake, fake, null, fake, 1 << 20, null) == 1

@@ -77,6 +77,21 @@ def test_beam_parity(dtype, beams, width, vocab):
     compare(want, parent, token, score)
 
 
+def test_infinities_and_nan_slices():
+    # +inf anywhere makes the beam's row non-finite; a slice of only NaN or
+    # -inf is not an error when the rest of the row is finite
+    data, values, scores = beam_batch(3, 2, 20000, "f32", seed=9)
+    data[0, 1, 17000] = np.inf
+    data[1, 0, :9000] = np.nan
+    data[2, 1, 5000:] = -np.inf
+    values = data
+    parent, token, score, status = run(data, "f32", scores, 2)
+    assert status == binding.ROW_NONFINITE
+    assert np.all(parent[0] == -1)
+    want = obeam.beam_step(values, scores, 2, groups=[1, 2])
+    compare(want, parent, token, score)
+
+
 def test_ties_within_a_beam_follow_the_flat_index():
     # one beam, integer logits: equal logits give equal scores by the same
     # formula on both sides, so the lower token id must come first, exactly

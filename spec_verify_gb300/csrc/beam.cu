@@ -9,8 +9,9 @@
 //   beam_row_kernel    one CTA per slice of a beam row: the slice maximum,
 //                      its mass sum (binary32 exponentials, fixed-point
 //                      sums), and its `width` best tokens by (logit desc,
-//                      id asc), found by the sampler's exact count radix
-//                      selection;
+//                      id asc): the elements at or above the width-th
+//                      largest thread maximum, ranked exactly (the sampler's
+//                      radix selection when too many tie there);
 //   beam_merge_kernel  one CTA per group: each beam's m and Z from its
 //                      slices, the scores s_b + (z - m_b - ln Z_b) in fp64 of
 //                      the listed tokens, and each candidate's rank in the
@@ -36,6 +37,7 @@ namespace smp {
 // its header, then `width` (id, logit) pairs, its best tokens by (logit desc,
 // id asc).  The union of a row's slice lists holds the row's best `width`.
 constexpr int kBeamMaxSlices = 16;
+constexpr int kBeamU = 8;   // 16-byte loads in flight per thread in the slice passes
 constexpr int kBeamMaxCand = SMP_MAX_BEAM_WIDTH * SMP_MAX_BEAM_WIDTH;   // candidates one merge CTA ranks
 constexpr int kSliceEmpty = 1 << 8;   // a slice with no finite logit (not an error by itself)
 
@@ -71,6 +73,35 @@ __host__ __device__ __forceinline__ size_t beam_slice_bytes(int width) {
   return sizeof(BeamSliceHead) + size_t(width) * sizeof(BeamCand);
 }
 
+// A pass over a row slice with kU 16-byte vectors in flight per thread (the
+// selection passes keep one): f(id, z) over every element, in no particular order.
+template <typename T, int kU, typename F>
+__device__ __forceinline__ void gen_sweep_wide(const T* row, int V, F&& f) {
+  using Vo = VecOps<T>;
+  constexpr int kPer = Vo::kPer;
+  const uintptr_t r0 = reinterpret_cast<uintptr_t>(row);
+  const uintptr_t a0 = (r0 + 15) & ~uintptr_t(15), a1 = (r0 + size_t(V) * sizeof(T)) & ~uintptr_t(15);
+  const bool mid = a1 > a0;
+  const int head = mid ? int((a0 - r0) / sizeof(T)) : V;
+  const int tail0 = mid ? int((a1 - r0) / sizeof(T)) : V;
+  const int nvec = mid ? int((a1 - a0) / 16) : 0;
+  const uint4* vp = reinterpret_cast<const uint4*>(a0);
+  for (int v0 = threadIdx.x; v0 < nvec; v0 += kThreads * kU) {
+    uint4 x[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u)
+      if (v0 + u * kThreads < nvec) x[u] = __ldg(vp + v0 + u * kThreads);
+#pragma unroll
+    for (int u = 0; u < kU; ++u)
+      if (v0 + u * kThreads < nvec) {
+#pragma unroll
+        for (int q = 0; q < kPer; ++q) f(head + (v0 + u * kThreads) * kPer + q, Vo::elem(x[u], q));
+      }
+  }
+  for (int i = threadIdx.x; i < head; i += kThreads) f(i, Elem<T>::widen(row[i]));
+  for (int i = tail0 + threadIdx.x; i < V; i += kThreads) f(i, Elem<T>::widen(row[i]));
+}
+
 template <typename T>
 __global__ void __launch_bounds__(kThreads, 2) beam_row_kernel(BeamArgs a) {
   __shared__ FloatPair table[64];
@@ -102,9 +133,9 @@ __global__ void __launch_bounds__(kThreads, 2) beam_row_kernel(BeamArgs a) {
   // The slice maximum (as an order key), then Z = sum exp(z - m) in binary32
   // per thread, turned into 44-bit fixed point once per thread and summed
   // exactly.
-  uint32_t kmax = 0;
-  gen_sweep<T>(row, len, [&](int, float z) { kmax = max(kmax, order_key<T>(z)); });
-  kmax = uint32_t(block_max_u64(uint64_t(kmax), gs.red64));
+  uint32_t kmine = 0;   // this thread's maximum key
+  gen_sweep_wide<T, kBeamU>(row, len, [&](int, float z) { kmine = max(kmine, order_key<T>(z)); });
+  const uint32_t kmax = uint32_t(block_max_u64(uint64_t(kmine), gs.red64));
   if (!key_finite<T>(kmax)) {   // all -inf / NaN, or +inf present
     if (tid == 0) {
       const bool pinf = kmax == order_key<T>(INFINITY);
@@ -118,47 +149,85 @@ __global__ void __launch_bounds__(kThreads, 2) beam_row_kernel(BeamArgs a) {
   const float m = key_value<T>(kmax);
   const RowScale rs = make_row_scale_unit(m);
   float st = 0.0f;
-  gen_sweep<T>(row, len, [&](int, float z) { st += exp_fast(z, rs); });
+  gen_sweep_wide<T, kBeamU>(row, len, [&](int, float z) { st += exp_fast(z, rs); });
   uint64_t zf = __float2ull_rn(__fmul_rn(st, float(kFixedOne)));
   zf = warp_sum<uint64_t>(zf);
   if ((tid & 31) == 0) gs.scan64[tid >> 5] = zf;
+
+  // The slice's `width` best tokens by (key desc, id asc).  theta = the
+  // width-th largest of the threads' maxima: at least `width` elements reach
+  // it, so every one of the best `width` does.  The elements >= theta are
+  // listed and ranked exactly; if there are too many (many equal logits),
+  // the exact radix selection of the sampler finds the boundary instead.
+  uint32_t* tkeys = &gs.cnt[0][0];   // kThreads thread maxima
+  tkeys[tid] = kmine;
   cta_sync();
   uint64_t ztot = 0;
 #pragma unroll
   for (int w = 0; w < kWarps; ++w) ztot += gs.scan64[w];
+  const int kw = min(a.width, len);
+  {
+    int rank = 0;   // threads ordered by (key desc, thread asc)
+    for (int j = 0; j < kThreads; ++j) {
+      const uint32_t o = tkeys[j];
+      rank += o > kmine || (o == kmine && j < tid);
+    }
+    if (rank == kw - 1) gs.bc32[0] = kmine;
+  }
   cta_sync();
-
-  // The slice's `width` best tokens: the kept set of top-k = width.
-  smp_row_params prm;
-  prm.temperature = 1.0f;
-  prm.top_k = a.width;
-  prm.top_p = 1.0f;
-  prm.min_p = 0.0f;
-  prm.greedy = 0;
-  const KeptSet ks = gen_kept_set<T>(row, len, gs, table, prm, kmax);
-  gen_sweep<T>(row, len, [&](int i, float z) {
-    const uint32_t k = order_key<T>(z);
-    if (in_kept_set(ks, k, uint32_t(i))) {
+  const uint32_t theta = gs.bc32[0];
+  unsigned long long* list = reinterpret_cast<unsigned long long*>(&gs.mass[0][0][0]);   // kBeamList entries
+  constexpr int kBeamList = int(sizeof(gs.mass) / sizeof(unsigned long long));
+  if (tid == 0) n_members = 0;
+  cta_sync();
+  gen_sweep_wide<T, kBeamU>(row, len, [&](int i, float z) {
+    const uint32_t k = order_key<T>(isnan(z) ? -INFINITY : z);   // NaN counts as -inf
+    if (k >= theta) {
       const int slot = atomicAdd(&n_members, 1);
-      if (slot < SMP_MAX_BEAM_WIDTH) members[slot] = pack_key_id(k, uint32_t(i));
+      if (slot < kBeamList) list[slot] = pack_key_id(k, uint32_t(i));
     }
   });
   cta_sync();
-  const int n = min(n_members, min(a.width, len));
-  // Sorted by (key desc, id asc): the packed values in decreasing order.
-  if (tid < n) {
-    const unsigned long long mine = members[tid];
+  int nl = n_members;
+  if (nl > kBeamList) {   // too many at or above theta: exact radix selection of the boundary
+    smp_row_params prm;
+    prm.temperature = 1.0f;
+    prm.top_k = a.width;
+    prm.top_p = 1.0f;
+    prm.min_p = 0.0f;
+    prm.greedy = 0;
+    cta_sync();
+    const KeptSet ks = gen_kept_set<T>(row, len, gs, table, prm, kmax);
+    if (tid == 0) n_members = 0;
+    cta_sync();
+    gen_sweep<T>(row, len, [&](int i, float z) {
+      const uint32_t k = order_key<T>(isnan(z) ? -INFINITY : z);
+      if (in_kept_set(ks, k, uint32_t(i))) {
+        const int slot = atomicAdd(&n_members, 1);
+        if (slot < SMP_MAX_BEAM_WIDTH) members[slot] = pack_key_id(k, uint32_t(i));
+      }
+    });
+    cta_sync();
+    nl = min(n_members, SMP_MAX_BEAM_WIDTH);
+    list = members;
+  }
+  // The listed values ranked in decreasing order; the first kw are kept.
+  for (int c = tid; c < nl; c += kThreads) {
+    const unsigned long long mine = list[c];
     int rank = 0;
-    for (int j = 0; j < n; ++j) rank += members[j] > mine;
-    const uint32_t id = ~uint32_t(mine);
-    cand[rank].id = lo + int32_t(id);
-    cand[rank].z = Elem<T>::widen(row[id]);
+    for (int j = 0; j < nl && rank < kw; ++j) rank += list[j] > mine;
+    if (rank < kw) {
+      const uint32_t id = ~uint32_t(mine);
+      const float z = Elem<T>::widen(row[id]);
+      cand[rank].id = lo + int32_t(id);
+      cand[rank].z = isnan(z) ? -INFINITY : z;
+    }
   }
   if (tid == 0) {
     head->m = m;
     head->flags = 0;
     head->z = ztot;
-    head->n = n;
+    head->n = min(kw, nl);
   }
 }
 

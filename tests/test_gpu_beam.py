@@ -92,6 +92,31 @@ def test_infinities_and_nan_slices():
     compare(want, parent, token, score)
 
 
+def test_fewer_finite_logits_than_width():
+    # NaN counts as -inf: with fewer finite logits than the width, the rest
+    # of the kept candidates score -inf in flat-index order
+    z = np.full((2, 2, 3000), -np.inf, dtype=np.float32)
+    z[:, :, 10] = 1.0
+    z[:, 0, 20] = 0.5
+    z[0, 1, 100:140] = np.nan
+    scores = np.array([[0.0, -1.0], [-2.0, 0.0]])
+    parent, token, score, status = run(z, "f32", scores, 6)
+    assert status == 0
+    want = obeam.beam_step(z, scores, 6)
+    compare(want, parent, token, score, exact=True)
+
+
+def test_flat_rows_take_the_radix_path():
+    # every logit equal: all of a slice ties at the threshold, more than the
+    # list holds, so the exact radix selection picks the lowest ids
+    z = np.zeros((2, 3, 40000), dtype=np.float32)
+    z[1, 2, 39999] = 0.25
+    scores = np.array([[0.0, -0.5, -0.25], [-1.0, -1.0, -1.0]])
+    parent, token, score, status = run(z, "f32", scores, 8)
+    want = obeam.beam_step(z, scores, 8)
+    compare(want, parent, token, score, exact=True)
+
+
 def test_ties_within_a_beam_follow_the_flat_index():
     # one beam, integer logits: equal logits give equal scores by the same
     # formula on both sides, so the lower token id must come first, exactly

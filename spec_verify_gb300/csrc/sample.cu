@@ -32,6 +32,7 @@ namespace smp {
 
 constexpr int kBufBytes = 32768;                       // one TMA copy: a batch of the row
 constexpr int kBufs = 2;                               // batches in flight per CTA (double buffering)
+constexpr int kPrefetchBatches = 8;                    // batches of the first row prefetched into L2
 constexpr int kSubBytes = kBufBytes / kWarps;          // the part of a batch one warp processes
 constexpr int kVecPerLane = kSubBytes / 16 / 32;       // 16-byte vectors per lane and batch
 static_assert(kVecPerLane == 8, "a lane's unit is one 128-byte line, read in XOR-swizzled order");
@@ -515,6 +516,20 @@ __global__ void __launch_bounds__(kThreads, 2) sample_kernel(SampleArgs a) {
   if (tid == 0) {
     for (int i = 0; i < kBufs; ++i) mbar_init(&ss.full[i], 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  // The first batches of the CTA's first row are prefetched into L2 before
+  // the dependency wait: a prefetch is a hint that changes no memory, and L2
+  // is the point of coherence, so writes the previous kernel makes to these
+  // bytes still reach the copies below.  In a chain of launches the prefetch
+  // overlaps the previous launch's row ends, when HBM is otherwise idle.
+  if (tid == 0 && int(blockIdx.x) < B) {
+    const RowGeom g = row_geom<T>(a, blockIdx.x);
+    const int nb = min(g.nchunks, kPrefetchBatches);
+    for (int bt = 0; bt < nb; ++bt) {
+      const uintptr_t src = g.a0 + uintptr_t(bt) * kBufBytes;
+      const uint32_t bytes = uint32_t(min(uintptr_t(kBufBytes), g.a1 - src));
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+    }
   }
   // Inputs may come from the previous kernel on the stream (programmatic launch).
   grid_dependency_wait();

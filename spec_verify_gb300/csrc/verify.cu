@@ -92,6 +92,8 @@ __device__ __forceinline__ const T* logit_row(const VerifyArgs& a, int b, int j)
 }
 
 constexpr int kPosUnroll = 16;   // 16-byte loads in flight per thread in verify_pos_kernel
+constexpr uintptr_t kPosPrefetchChunk = 32768;        // one L2 prefetch request
+constexpr uintptr_t kPosPrefetchBytes = 256 * 1024;   // most of a row prefetched before the wait
 
 __device__ __forceinline__ uint4 load_stream(const uint4* p) {
   uint4 x;
@@ -216,6 +218,20 @@ __global__ void __launch_bounds__(kThreads, 2) verify_pos_kernel(VerifyArgs a) {
   const int b = pr / rows_per_b;
   const int j = pr % rows_per_b;
   const int Vn = a.vocab;
+  // The row's aligned middle (up to kPosPrefetchBytes) is prefetched into L2
+  // before the dependency wait: a prefetch changes no memory and L2 is the
+  // point of coherence, so the previous kernel's writes still reach the loads
+  // below; in a chain of calls it overlaps the previous call's resolve
+  // kernel, which leaves HBM idle.
+  if (tid == 0) {
+    const T* prow = logit_row<T>(a, b, j);
+    const uintptr_t p0 = (reinterpret_cast<uintptr_t>(prow) + 15) & ~uintptr_t(15);
+    const uintptr_t p1 = (reinterpret_cast<uintptr_t>(prow) + size_t(Vn) * sizeof(T)) & ~uintptr_t(15);
+    for (uintptr_t src = p0; src < p1 && src < p0 + kPosPrefetchBytes; src += kPosPrefetchChunk) {
+      const uint32_t bytes = uint32_t(min(uintptr_t(kPosPrefetchChunk), p1 - src));
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+    }
+  }
   grid_dependency_wait();
   allow_dependent_launch();
   const RowMode md = row_mode<kParams>(a, b);

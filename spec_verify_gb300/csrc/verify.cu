@@ -234,6 +234,9 @@ __global__ void __launch_bounds__(kThreads, 2) verify_pos_kernel(VerifyArgs a) {
   }
   grid_dependency_wait();
   allow_dependent_launch();
+  // The status word is cleared here: only the resolve kernel, which waits
+  // for this kernel to finish, ORs flags into it.
+  if (blockIdx.x == 0 && tid == 0 && a.status) *a.status = 0;
   const RowMode md = row_mode<kParams>(a, b);
   if (md.bad || (md.greedy && j > a.k)) {
     // An error row's statistics carry the flag; greedy rows read no q row.
@@ -814,10 +817,6 @@ extern "C" smp_status smp_spec_verify_params(const void* p_logits, const void* q
   if (!workspace || workspace_bytes < need || reinterpret_cast<uintptr_t>(workspace) % 8)
     return SMP_ERR_WORKSPACE;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  if (status) {
-    const smp_status rc = clear_status(status, st);
-    if (rc != SMP_OK) return rc;
-  }
   VerifyArgs a{};
   a.p = p_logits;
   a.q = q_logits;

@@ -44,6 +44,17 @@ constexpr int kFastTopK = 128;    // top-k rows up to this k take the candidate 
 // rows (never a result: results are token ids >= 0, or -1).
 constexpr int32_t kHandOff = int32_t(0x80000000u);
 
+constexpr int kMaxHistory = SMP_MAX_HISTORY;
+constexpr int kUnitWords = SMP_MAX_VOCAB / 64 / 32;   // one bit per 64 ids
+
+struct PrepArgs {
+  const uint32_t* allowed;   // [batch, words] allowed-token bits, or nullptr
+  int words;                 // ceil(vocab / 32)
+  const int32_t* history;    // [batch, hist_len] recent token ids, or nullptr
+  int hist_len;
+  const float* penalty;      // [batch] factors r, or nullptr (no penalty)
+};
+
 struct SampleArgs {
   const void* logits;
   int batch;
@@ -56,6 +67,7 @@ struct SampleArgs {
   int32_t* status;
   float* full_probs;   // debug: [B, V] p~ or NULL
   int32_t* kept;       // debug: [B] |S| or NULL
+  PrepArgs prep;       // logit pre-pass (the kernel instance with kPrep only)
 };
 
 // Candidate path: greedy, or valid knobs without top-p and with min-p or a small top-k.
@@ -132,6 +144,208 @@ __device__ __forceinline__ void write_error_row(const SampleArgs& a, int b, int 
 // ------------------------------------------------------------------ general path
 
 #include "general.cuh"
+
+// ------------------------------------------------------------------ logit pre-pass
+//
+// Repetition penalty ("Choosing the next word", section "The repetition
+// penalty": z_i <- z_i / r for z_i > 0, else z_i * r, for each distinct token
+// i among the row's recent tokens) and constraint mask ("Decoding &
+// Speculative Sampling", section 39.3: tokens outside the allowed set get
+// -inf), applied to every logit the kernel instance with kPrep reads: the
+// streamed vectors, the segments read again, the row's edges and the general
+// path's passes.  The penalised value is computed in binary32 and kept in the
+// logits' precision.
+
+// A row's distinct history ids, sorted, and one bit per unit of 64 ids that
+// holds one of them (most ids skip the search on that bit).
+struct PrepShared {
+  int32_t raw[kMaxHistory];
+  int32_t first[kMaxHistory];   // 1 at the first occurrence of a valid id
+  int32_t ids[kMaxHistory];
+  uint32_t unit_bits[kUnitWords];
+  int n;
+};
+
+// Nearest bf16 value of a binary32 number (ties to even); NaN and infinities kept.
+__device__ __forceinline__ float round_to_bf16(float x) {
+  uint32_t b = __float_as_uint(x);
+  if ((b & 0x7FFFFFFFu) > 0x7F800000u) return x;
+  b = (b + 0x7FFFu + ((b >> 16) & 1u)) & 0xFFFF0000u;
+  return __uint_as_float(b);
+}
+
+template <typename T>
+struct LogitPrep {
+  const uint32_t* allowed;   // this row's mask words, or nullptr
+  const PrepShared* ps;
+  float r;
+  __device__ __forceinline__ float operator()(int id, float z) const {
+    if (allowed && !((__ldg(allowed + (id >> 5)) >> (id & 31)) & 1u)) return -INFINITY;
+    if ((ps->unit_bits[id >> 11] >> ((id >> 6) & 31)) & 1u) {
+      int lo = 0, hi = ps->n - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (ps->ids[mid] < id) lo = mid + 1;
+        else hi = mid;
+      }
+      if (ps->ids[lo] == id) {
+        z = z > 0.0f ? __fdiv_rn(z, r) : __fmul_rn(z, r);
+        if (sizeof(T) == 2) z = round_to_bf16(z);
+      }
+    }
+    return z;
+  }
+};
+
+__device__ __forceinline__ bool penalty_ok(const SampleArgs& a, int row) {
+  if (a.prep.penalty == nullptr) return true;
+  const float r = a.prep.penalty[row];
+  return isfinite(r) && r > 0.0f;
+}
+
+// Whether the 64-id block holding `id` (id < V) holds a history id.
+__device__ __forceinline__ bool hist_block(const PrepShared& ps, uint32_t id) {
+  return (ps.unit_bits[id >> 11] >> ((id >> 6) & 31)) & 1u;
+}
+
+// The allowed bits of the 32 ids from `id` (bit q: id + q), id < V; bits
+// past the mask's last word count as allowed.
+__device__ __forceinline__ uint32_t allowed_bits32(const uint32_t* w, int words, uint32_t id) {
+  if (w == nullptr) return 0xFFFFFFFFu;
+  const uint32_t k = id >> 5, sft = id & 31;
+  const uint64_t lo = __ldg(w + k);
+  const uint64_t hi = int(k) + 1 < words ? __ldg(w + k + 1) : 0xFFFFFFFFull;
+  return uint32_t(((hi << 32) | lo) >> sft);
+}
+
+// The pre-pass state of a lane's unit (kVecPerLane vectors from token uid0):
+// its mask bits and whether its ids may hold a history id.
+struct UnitPrep {
+  uint32_t w0, w1;   // allowed bits of ids uid0 .. +31 and +32 .. +63
+  bool hist;
+};
+
+template <typename T>
+__device__ __forceinline__ UnitPrep unit_prep(const uint32_t* mrow, int words, int V, uint32_t uid0,
+                                              const PrepShared& ps) {
+  constexpr int kIds = kVecPerLane * VecOps<T>::kPer;   // 32 (fp32) or 64 (bf16)
+  UnitPrep u;
+  u.w0 = allowed_bits32(mrow, words, uid0);
+  u.w1 = (kIds > 32 && int(uid0) + 32 < V) ? allowed_bits32(mrow, words, uid0 + 32) : 0xFFFFFFFFu;
+  u.hist = ps.n > 0 && (hist_block(ps, uid0) || hist_block(ps, uint32_t(min(int(uid0) + kIds - 1, V - 1))));
+  return u;
+}
+
+// Mask bits of vector jj (0 .. kVecPerLane-1) of a unit.
+template <typename T>
+__device__ __forceinline__ uint32_t unit_bits_of(const UnitPrep& u, int jj) {
+  constexpr int kPer = VecOps<T>::kPer;
+  const int off = jj * kPer;
+  return off < 32 ? (u.w0 >> off) : (u.w1 >> (off - 32));
+}
+
+__device__ __forceinline__ PrepShared& prep_shared();
+
+// First index of the sorted history ids at or past `id`.
+__device__ __forceinline__ int hist_lower_bound(const PrepShared& ps, int id) {
+  int lo = 0, hi = ps.n;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (ps.ids[mid] < id) lo = mid + 1;
+    else hi = mid;
+  }
+  return lo;
+}
+
+// The pre-pass on nv vectors of one unit (in place, shared or local memory),
+// the first at token uid0, visited in the order j ^ swz (the ring's bank
+// swizzle).  The history ids inside the unit are found by two binary
+// searches; each vector then checks those few ids.  Out of line: most units
+// need nothing, and the streaming loop keeps its code small.
+template <typename T>
+__device__ __noinline__ void prep_unit(uint4* v, int nv, int swz, uint32_t uid0, uint32_t w0, uint32_t w1, bool hist,
+                                       float r) {
+  using Vo = VecOps<T>;
+  constexpr int kPer = Vo::kPer;
+  constexpr uint32_t kFull = (1u << kPer) - 1u;
+  const PrepShared& ps = prep_shared();
+  const UnitPrep up{w0, w1, hist};
+  int h0 = 0, h1 = 0;
+  if (hist) {
+    h0 = hist_lower_bound(ps, int(uid0));
+    h1 = hist_lower_bound(ps, int(uid0) + nv * kPer);
+  }
+  for (int j = 0; j < kVecPerLane; ++j) {
+    const int jj = j ^ swz;
+    if (jj >= nv) continue;
+    const uint32_t bits = unit_bits_of<T>(up, jj);
+    const int vid0 = int(uid0) + jj * kPer;
+    bool pen = false;
+    for (int t = h0; t < h1; ++t) pen |= ps.ids[t] >= vid0 && ps.ids[t] < vid0 + kPer;
+    if (!pen && (bits & kFull) == kFull) continue;
+    uint4 x = v[jj];
+    uint32_t w[4] = {x.x, x.y, x.z, x.w};
+    for (int t = h0; pen && t < h1; ++t) {
+      const int q = ps.ids[t] - vid0;
+      if (q < 0 || q >= kPer) continue;
+#pragma unroll
+      for (int qq = 0; qq < kPer; ++qq)
+        if (qq == q) {
+          float z = Vo::elem(make_uint4(w[0], w[1], w[2], w[3]), qq);
+          z = z > 0.0f ? __fdiv_rn(z, r) : __fmul_rn(z, r);
+          if (sizeof(T) == 2) {
+            const uint32_t hb = __float_as_uint(round_to_bf16(z)) >> 16;
+            w[qq >> 1] = (qq & 1) ? ((w[qq >> 1] & 0x0000FFFFu) | (hb << 16)) : ((w[qq >> 1] & 0xFFFF0000u) | hb);
+          } else {
+            w[qq] = __float_as_uint(z);
+          }
+        }
+    }
+#pragma unroll
+    for (int q = 0; q < kPer; ++q)
+      if (!((bits >> q) & 1u)) {
+        if (sizeof(T) == 2) w[q >> 1] = (q & 1) ? ((w[q >> 1] & 0x0000FFFFu) | 0xFF800000u) : ((w[q >> 1] & 0xFFFF0000u) | 0xFF80u);
+        else w[q] = 0xFF800000u;
+      }
+    v[jj] = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+// Builds the row's PrepShared (history ids in [0, V), each once, sorted).
+__device__ __forceinline__ PrepShared& prep_shared() {
+  __shared__ PrepShared ps;
+  return ps;
+}
+
+__device__ __forceinline__ void build_prep(PrepShared& ps, const PrepArgs& pa, int row, int V, bool penalised) {
+  const int tid = threadIdx.x;
+  const int H = penalised && pa.history ? pa.hist_len : 0;
+  for (int w = tid; w < kUnitWords; w += kThreads) ps.unit_bits[w] = 0;
+  if (tid < kMaxHistory) {
+    int32_t id = -1;
+    if (tid < H) id = pa.history[size_t(row) * H + tid];
+    ps.raw[tid] = (id >= 0 && id < V) ? id : -1;
+  }
+  if (tid == 0) ps.n = 0;
+  cta_sync();
+  if (tid < kMaxHistory) {   // first occurrences
+    const int32_t id = ps.raw[tid];
+    bool first = id >= 0;
+    for (int s = 0; s < tid; ++s) first &= ps.raw[s] != id;
+    ps.first[tid] = first;
+  }
+  cta_sync();
+  if (tid < kMaxHistory && ps.first[tid]) {   // rank among the distinct ids
+    const int32_t id = ps.raw[tid];
+    int rank = 0;
+    for (int s = 0; s < kMaxHistory; ++s) rank += ps.first[s] && ps.raw[s] < id;
+    ps.ids[rank] = id;
+    atomicOr(&ps.unit_bits[id >> 11], 1u << ((id >> 6) & 31));
+    atomicAdd(&ps.n, 1);
+  }
+  cta_sync();
+}
+
 
 // ------------------------------------------------------------------ candidate path
 
@@ -321,7 +535,7 @@ __device__ __forceinline__ bool parts_at_least(const ExpParts& e, float x) {
 // candidates hold every element at or above a lower bound of the kept set's
 // boundary; row_max is the row's largest logit.  Returns false if the row
 // needs the general path.
-template <typename T>
+template <typename T, bool kPrep>
 __device__ bool finalize_candidates(StreamShared& ss, CandShared& cs, const FloatPair* table, const SampleArgs& a, int b,
                                     const smp_row_params& prm, float row_max) {
   const int tid = threadIdx.x, lane = tid & 31;
@@ -360,7 +574,10 @@ __device__ bool finalize_candidates(StreamShared& ss, CandShared& cs, const Floa
     ids = cs.f_id;
   }
   // Fewer candidates than k: some of the top k are NaN (ranked as -inf).
-  if (topk && n < prm.top_k) return false;
+  // With the pre-pass the candidates exclude -inf (masked tokens), so fewer
+  // than k means every finite token is a candidate, and the rest of the top
+  // k have zero mass: the candidates decide the draw alone.
+  if (!kPrep && topk && n < prm.top_k) return false;
 
   // Membership of the kept set S, one candidate per thread.
   const bool have = tid < n;
@@ -455,7 +672,7 @@ __device__ bool finalize_candidates(StreamShared& ss, CandShared& cs, const Floa
 // candidate-path rows are done, so that none of its state is live across it.
 
 // Cursor over the batches of this CTA's candidate-path rows (thread 0 only).
-template <typename T>
+template <typename T, bool kPrep>
 struct BatchCursor {
   int row;
   int batch;
@@ -484,7 +701,8 @@ struct BatchCursor {
       nbatch = 0;
       if (row < a.batch) {
         const smp_row_params prm = a.params[row];
-        nbatch = row_is_fast(prm, a.vocab) ? row_geom<T>(a, row).nchunks : 0;
+        const bool fast = row_is_fast(prm, a.vocab) && (!kPrep || penalty_ok(a, row));
+        nbatch = fast ? row_geom<T>(a, row).nchunks : 0;
       }
     }
   }
@@ -500,7 +718,10 @@ struct BatchCursor {
   }
 };
 
-template <typename T>
+// kPrep: the instance of smp_sample_processed, which applies the logit
+// pre-pass to every value it reads; without it the kernel carries none of
+// that code.
+template <typename T, bool kPrep>
 __global__ void __launch_bounds__(kThreads, 2) sample_kernel(SampleArgs a) {
   extern __shared__ __align__(128) unsigned char ring[];
   __shared__ StreamShared ss;
@@ -512,7 +733,7 @@ __global__ void __launch_bounds__(kThreads, 2) sample_kernel(SampleArgs a) {
   const int warp = tid >> 5, lane = tid & 31;
   const int B = a.batch;
   const int Vn = a.vocab;
-  BatchCursor<T> cur;
+  BatchCursor<T, kPrep> cur;
   if (tid == 0) {
     for (int i = 0; i < kBufs; ++i) mbar_init(&ss.full[i], 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -550,7 +771,7 @@ __global__ void __launch_bounds__(kThreads, 2) sample_kernel(SampleArgs a) {
     const smp_row_params prm = a.params[row];
     const RowGeom geo = row_geom<T>(a, row);
     const bool first = row == int(blockIdx.x);
-    const bool fast = row_is_fast(prm, Vn);
+    const bool fast = row_is_fast(prm, Vn) && (!kPrep || penalty_ok(a, row));
     const T* rowp = reinterpret_cast<const T*>(geo.r0);
     if (!fast) {
       if (first && geo.nchunks > 0) {
@@ -597,6 +818,19 @@ __global__ void __launch_bounds__(kThreads, 2) sample_kernel(SampleArgs a) {
       ss.zsum = 0;
     }
     cta_sync();
+    // The row's pre-pass state (kPrep): its mask words, its distinct history
+    // ids and its factor; xf applies the pre-pass to one element.
+    const uint32_t* mrow = nullptr;
+    float prep_r = 1.0f;
+    if constexpr (kPrep) {
+      mrow = a.prep.allowed ? a.prep.allowed + size_t(row) * a.prep.words : nullptr;
+      prep_r = a.prep.penalty ? a.prep.penalty[row] : 1.0f;
+      build_prep(prep_shared(), a.prep, row, Vn, prep_r != 1.0f);
+    }
+    auto xf = [&](uint32_t id, float z) -> float {
+      if constexpr (kPrep) return LogitPrep<T>{mrow, &prep_shared(), prep_r}(int(id), z);
+      return z;
+    };
     const uint32_t id_base = uint32_t((geo.a0 - reinterpret_cast<uintptr_t>(geo.r0)) / sizeof(T));
     const int v0 = warp * (kSubBytes / 16);            // this warp's first vector in every batch
     const int seg_len = (geo.nchunks + kSegs - 1) / kSegs;   // batches per segment
@@ -620,6 +854,36 @@ __global__ void __launch_bounds__(kThreads, 2) sample_kernel(SampleArgs a) {
       // kVecPerLane, read in the order j ^ (lane % 8) so that the 32 lanes of
       // a step touch all banks evenly.
       uint32_t pm = V::neg_inf();
+      if constexpr (kPrep) {
+        const PrepShared& ps = prep_shared();
+        if (ps.n > 0) {
+          // The penalty, in place in the ring: thread t takes history id t if
+          // it lies in this batch; one barrier before the lanes read.
+          if (tid < ps.n) {
+            const uint32_t bid0 = id_base + uint32_t(bt) * (kBufBytes / sizeof(T));
+            const uint32_t e = uint32_t(ps.ids[tid]) - bid0;
+            if (uint32_t(ps.ids[tid]) >= bid0 && e < uint32_t(bvec) * uint32_t(kPer)) {
+              T* slot = reinterpret_cast<T*>(ring + size_t(bi) * kBufBytes) + e;
+              float z = Elem<T>::widen(*slot);
+              z = z > 0.0f ? __fdiv_rn(z, prep_r) : __fmul_rn(z, prep_r);
+              if (sizeof(T) == 2) *reinterpret_cast<uint16_t*>(slot) = uint16_t(__float_as_uint(round_to_bf16(z)) >> 16);
+              else *reinterpret_cast<float*>(slot) = z;
+            }
+          }
+          cta_sync();
+        }
+        // The mask on the lane's unit, in place in the ring (only this lane
+        // reads it), when its mask bits are not all set.
+        if (mrow && lane * kVecPerLane < nvec) {
+          const uint32_t uid0 = id0 + uint32_t(lane * kVecPerLane * kPer);
+          const uint32_t w0 = allowed_bits32(mrow, a.prep.words, uid0);
+          const uint32_t w1 = (kVecPerLane * kPer > 32 && int(uid0) + 32 < Vn)
+                                  ? allowed_bits32(mrow, a.prep.words, uid0 + 32) : 0xFFFFFFFFu;
+          if ((w0 & w1) != 0xFFFFFFFFu)
+            prep_unit<T>(const_cast<uint4*>(vec) + lane * kVecPerLane, min(kVecPerLane, nvec - lane * kVecPerLane),
+                         lane & (kVecPerLane - 1), uid0, w0, w1, false, prep_r);
+        }
+      }
 #pragma unroll
       for (int j = 0; j < kVecPerLane; ++j) {
         const int v = lane * kVecPerLane + (j ^ (lane & (kVecPerLane - 1)));
@@ -672,11 +936,11 @@ __global__ void __launch_bounds__(kThreads, 2) sample_kernel(SampleArgs a) {
       // Elements outside the aligned middle; then the CTA-wide (max, lowest id).
       uint64_t best = pack_key_id(key_of_bits(__float_as_uint(best_z)), best_id);
       for (int i = tid; i < geo.head; i += kThreads) {
-        const uint64_t p = pack_key_id(key_of_bits(__float_as_uint(Elem<T>::widen(rowp[i]))), uint32_t(i));
+        const uint64_t p = pack_key_id(key_of_bits(__float_as_uint(xf(i, Elem<T>::widen(rowp[i])))), uint32_t(i));
         best = p > best ? p : best;
       }
       for (int i = geo.tail0 + tid; i < Vn; i += kThreads) {
-        const uint64_t p = pack_key_id(key_of_bits(__float_as_uint(Elem<T>::widen(rowp[i]))), uint32_t(i));
+        const uint64_t p = pack_key_id(key_of_bits(__float_as_uint(xf(i, Elem<T>::widen(rowp[i])))), uint32_t(i));
         best = p > best ? p : best;
       }
       best = block_max_u64(best, ss.red64);
@@ -705,8 +969,8 @@ __global__ void __launch_bounds__(kThreads, 2) sample_kernel(SampleArgs a) {
     const bool edges = geo.head > 0 || geo.tail0 < Vn;
     if (edges) {
       float emax = -INFINITY;
-      for (int i = tid; i < geo.head; i += kThreads) emax = fmaxf(emax, Elem<T>::widen(rowp[i]));
-      for (int i = geo.tail0 + tid; i < Vn; i += kThreads) emax = fmaxf(emax, Elem<T>::widen(rowp[i]));
+      for (int i = tid; i < geo.head; i += kThreads) emax = fmaxf(emax, xf(i, Elem<T>::widen(rowp[i])));
+      for (int i = geo.tail0 + tid; i < Vn; i += kThreads) emax = fmaxf(emax, xf(i, Elem<T>::widen(rowp[i])));
       run_max = fmaxf(run_max, block_max_f(emax, ss.red));
     }
     // A lower bound theta of the kept set's boundary: min-p's at the row
@@ -722,6 +986,10 @@ __global__ void __launch_bounds__(kThreads, 2) sample_kernel(SampleArgs a) {
       cta_sync();
       theta = fmaxf(theta, kth_largest_list<T>(cs.cand_val, kThreads, prm.top_k, cs.hist, ss.bc));
     }
+    // With the pre-pass, masked tokens (-inf, zero mass) are never
+    // candidates, so that a row with few allowed tokens stays on this path.
+    if constexpr (kPrep)
+      if (!isnan(theta)) theta = fmaxf(theta, __uint_as_float(0xFF7FFFFFu));   // the lowest finite float
     // Candidates: every element >= theta, from the segments whose maximum
     // reaches it (read again from global memory, normally still in L2) and
     // from the edges.
@@ -763,21 +1031,29 @@ __global__ void __launch_bounds__(kThreads, 2) sample_kernel(SampleArgs a) {
             const int v = ol * kVecPerLane + j;
             xv[j] = v < nvec ? __ldg(gv + v) : make_uint4(V::neg_inf(), V::neg_inf(), V::neg_inf(), V::neg_inf());
           }
+          if constexpr (kPrep) {
+            if (ol * kVecPerLane < nvec) {
+              const uint32_t uid0 = id0 + uint32_t(ol * kVecPerLane * kPer);
+              const UnitPrep up = unit_prep<T>(mrow, a.prep.words, Vn, uid0, prep_shared());
+              if (up.hist || (up.w0 & up.w1) != 0xFFFFFFFFu)
+                prep_unit<T>(xv, min(kVecPerLane, nvec - ol * kVecPerLane), 0, uid0, up.w0, up.w1, up.hist, prep_r);
+            }
+          }
           push_unit<T>(ss, cs, xv, min(kVecPerLane, max(0, nvec - ol * kVecPerLane)),
                        id0 + uint32_t(ol * kVecPerLane * kPer), theta);
         }
       }
       for (int i = tid; i < geo.head; i += kThreads) {
-        const float z = Elem<T>::widen(rowp[i]);
+        const float z = xf(i, Elem<T>::widen(rowp[i]));
         if (z >= theta) push_candidate(ss, cs, uint32_t(i), z);
       }
       for (int i = geo.tail0 + tid; i < Vn; i += kThreads) {
-        const float z = Elem<T>::widen(rowp[i]);
+        const float z = xf(i, Elem<T>::widen(rowp[i]));
         if (z >= theta) push_candidate(ss, cs, uint32_t(i), z);
       }
     }
     cta_sync();
-    if (!finalize_candidates<T>(ss, cs, table, a, row, prm, run_max) && tid == 0) {
+    if (!finalize_candidates<T, kPrep>(ss, cs, table, a, row, prm, run_max) && tid == 0) {
       a.out_ids[row] = kHandOff;
       ++ss.handoffs;
     }
@@ -809,129 +1085,25 @@ __global__ void __launch_bounds__(kThreads, 2) sample_kernel(SampleArgs a) {
     // result replaces it only after later barriers.
     if (load_volatile(a.out_ids + r) != kHandOff) continue;
     const smp_row_params prm = a.params[r];
-    general_row<T>(gen, table, a, r, prm);
-  }
-}
-
-// ------------------------------------------------------------------ logit pre-pass
-//
-// Repetition penalty ("Choosing the next word", section "The repetition
-// penalty": z_i <- z_i / r for z_i > 0, else z_i * r, for each distinct token
-// i among the row's recent tokens) and constraint mask ("Decoding &
-// Speculative Sampling", section 39.3: tokens outside the allowed set get
-// -inf), applied to every logit a pass of the general path reads.  The
-// penalised value is computed in binary32 and kept in the logits' precision.
-
-constexpr int kMaxHistory = SMP_MAX_HISTORY;
-constexpr int kUnitWords = SMP_MAX_VOCAB / 64 / 32;   // one bit per 64 ids
-
-struct PrepArgs {
-  const uint32_t* allowed;   // [batch, words] allowed-token bits, or nullptr
-  int words;                 // ceil(vocab / 32)
-  const int32_t* history;    // [batch, hist_len] recent token ids, or nullptr
-  int hist_len;
-  const float* penalty;      // [batch] factors r, or nullptr (no penalty)
-};
-
-// A row's distinct history ids, sorted, and one bit per unit of 64 ids that
-// holds one of them (most ids skip the search on that bit).
-struct PrepShared {
-  int32_t raw[kMaxHistory];
-  int32_t first[kMaxHistory];   // 1 at the first occurrence of a valid id
-  int32_t ids[kMaxHistory];
-  uint32_t unit_bits[kUnitWords];
-  int n;
-};
-
-// Nearest bf16 value of a binary32 number (ties to even); NaN and infinities kept.
-__device__ __forceinline__ float round_to_bf16(float x) {
-  uint32_t b = __float_as_uint(x);
-  if ((b & 0x7FFFFFFFu) > 0x7F800000u) return x;
-  b = (b + 0x7FFFu + ((b >> 16) & 1u)) & 0xFFFF0000u;
-  return __uint_as_float(b);
-}
-
-template <typename T>
-struct LogitPrep {
-  const uint32_t* allowed;   // this row's mask words, or nullptr
-  const PrepShared* ps;
-  float r;
-  __device__ __forceinline__ float operator()(int id, float z) const {
-    if (allowed && !((__ldg(allowed + (id >> 5)) >> (id & 31)) & 1u)) return -INFINITY;
-    if ((ps->unit_bits[id >> 11] >> ((id >> 6) & 31)) & 1u) {
-      int lo = 0, hi = ps->n - 1;
-      while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        if (ps->ids[mid] < id) lo = mid + 1;
-        else hi = mid;
+    if constexpr (kPrep) {
+      if (!penalty_ok(a, r)) {   // an invalid factor: an error row (after every thread read the mark)
+        cta_sync();
+        if (tid == 0) write_error_row(a, r, kRowBadParams);
+        continue;
       }
-      if (ps->ids[lo] == id) {
-        z = z > 0.0f ? __fdiv_rn(z, r) : __fmul_rn(z, r);
-        if (sizeof(T) == 2) z = round_to_bf16(z);
-      }
+      const float rr = a.prep.penalty ? a.prep.penalty[r] : 1.0f;
+      build_prep(prep_shared(), a.prep, r, Vn, rr != 1.0f);
+      const uint32_t* mr = a.prep.allowed ? a.prep.allowed + size_t(r) * a.prep.words : nullptr;
+      general_row<T>(gen, table, a, r, prm, LogitPrep<T>{mr, &prep_shared(), rr});
+    } else {
+      general_row<T>(gen, table, a, r, prm);
     }
-    return z;
-  }
-};
-
-// Builds the row's PrepShared (history ids in [0, V), each once, sorted).
-__device__ __forceinline__ void build_prep(PrepShared& ps, const PrepArgs& pa, int row, int V, bool penalised) {
-  const int tid = threadIdx.x;
-  const int H = penalised && pa.history ? pa.hist_len : 0;
-  for (int w = tid; w < kUnitWords; w += kThreads) ps.unit_bits[w] = 0;
-  if (tid < kMaxHistory) {
-    int32_t id = -1;
-    if (tid < H) id = pa.history[size_t(row) * H + tid];
-    ps.raw[tid] = (id >= 0 && id < V) ? id : -1;
-  }
-  if (tid == 0) ps.n = 0;
-  cta_sync();
-  if (tid < kMaxHistory) {   // first occurrences
-    const int32_t id = ps.raw[tid];
-    bool first = id >= 0;
-    for (int s = 0; s < tid; ++s) first &= ps.raw[s] != id;
-    ps.first[tid] = first;
-  }
-  cta_sync();
-  if (tid < kMaxHistory && ps.first[tid]) {   // rank among the distinct ids
-    const int32_t id = ps.raw[tid];
-    int rank = 0;
-    for (int s = 0; s < kMaxHistory; ++s) rank += ps.first[s] && ps.raw[s] < id;
-    ps.ids[rank] = id;
-    atomicOr(&ps.unit_bits[id >> 11], 1u << ((id >> 6) & 31));
-    atomicAdd(&ps.n, 1);
-  }
-  cta_sync();
-}
-
-// One CTA per row (grid-strided): every row through the general path with
-// the pre-pass applied.
-template <typename T>
-__global__ void __launch_bounds__(kThreads, 2) prep_sample_kernel(SampleArgs a, PrepArgs pa) {
-  __shared__ FloatPair table[64];
-  __shared__ GenShared gen;
-  __shared__ PrepShared ps;
-  const int tid = threadIdx.x;
-  grid_dependency_wait();
-  allow_dependent_launch();
-  if (tid < 64) table[tid] = kExp2Table[tid];
-  for (int row = blockIdx.x; row < a.batch; row += gridDim.x) {
-    cta_sync();   // the previous row is done with the shared state
-    const smp_row_params prm = a.params[row];
-    const float r = pa.penalty ? pa.penalty[row] : 1.0f;
-    if (!(isfinite(r) && r > 0.0f)) {
-      if (tid == 0) write_error_row(a, row, kRowBadParams);
-      continue;
-    }
-    build_prep(ps, pa, row, a.vocab, r != 1.0f);
-    const LogitPrep<T> xf{pa.allowed ? pa.allowed + size_t(row) * pa.words : nullptr, &ps, r};
-    general_row<T>(gen, table, a, row, prm, xf);
   }
 }
 
 // ------------------------------------------------------------------ host side
 
-template <typename T>
+template <typename T, bool kPrep = false>
 static smp_status launch_sample(const SampleArgs& args, cudaStream_t stream) {
   const int dev = current_device();
   if (dev < 0) return fail_cuda(cudaGetLastError());
@@ -939,7 +1111,7 @@ static smp_status launch_sample(const SampleArgs& args, cudaStream_t stream) {
   ls.cluster = 1;
   ls.smem = size_t(kBufs) * kBufBytes;
   ls.pdl = true;
-  const void* kernel = reinterpret_cast<const void*>(&sample_kernel<T>);
+  const void* kernel = reinterpret_cast<const void*>(&sample_kernel<T, kPrep>);
   cudaError_t err = prepare_kernel(kernel, dev, ls);
   if (err != cudaSuccess) return fail_cuda(err);
   int per_sm = 0;
@@ -953,36 +1125,6 @@ static smp_status launch_sample(const SampleArgs& args, cudaStream_t stream) {
             args.vocab, grid, per_sm, ls.smem);
   SampleArgs a = args;
   err = launch_cluster(kernel, dim3(grid), dim3(kThreads), ls, stream, &a);
-  if (err != cudaSuccess) return fail_cuda(err);
-  return SMP_OK;
-}
-
-template <typename T>
-static smp_status launch_prep_sample(const SampleArgs& args, const PrepArgs& pa, cudaStream_t stream) {
-  const int dev = current_device();
-  if (dev < 0) return fail_cuda(cudaGetLastError());
-  LaunchShape ls;
-  ls.pdl = true;
-  const void* kernel = reinterpret_cast<const void*>(&prep_sample_kernel<T>);
-  int per_sm = 0;
-  cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, 0);
-  if (err != cudaSuccess) return fail_cuda(err);
-  if (per_sm <= 0) return SMP_ERR_UNSUPPORTED;
-  const int resident = per_sm * device_sms(dev);
-  const int grid = args.batch < resident ? args.batch : resident;
-  SampleArgs a = args;
-  PrepArgs p = pa;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kThreads);
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  void* params[2] = {&a, &p};
-  err = cudaLaunchKernelExC(&cfg, kernel, params);
   if (err != cudaSuccess) return fail_cuda(err);
   return SMP_OK;
 }
@@ -1072,12 +1214,11 @@ extern "C" smp_status smp_sample_processed(const void* logits, int32_t batch, in
   a.out_ids = out_ids;
   a.out_probs = out_probs;
   a.status = status;
-  PrepArgs pa{};
-  pa.allowed = allowed;
-  pa.words = (vocab + 31) / 32;
-  pa.history = history_len > 0 ? history : nullptr;
-  pa.hist_len = history_len;
-  pa.penalty = repetition_penalty;
-  if (dtype == SMP_F32) return launch_prep_sample<float>(a, pa, st);
-  return launch_prep_sample<uint16_t>(a, pa, st);
+  a.prep.allowed = allowed;
+  a.prep.words = (vocab + 31) / 32;
+  a.prep.history = history_len > 0 ? history : nullptr;
+  a.prep.hist_len = history_len;
+  a.prep.penalty = repetition_penalty;
+  if (dtype == SMP_F32) return launch_sample<float, true>(a, st);
+  return launch_sample<uint16_t, true>(a, st);
 }

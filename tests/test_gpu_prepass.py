@@ -58,6 +58,25 @@ def test_prepass_parity(dtype, vocab, parts):
         assert want[-1]["status"] == osam.ROW_NONFINITE          # the row with no allowed token
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_sparse_mask_with_top_k(dtype):
+    # a grammar-like mask (a handful of allowed tokens) under top-k 40 and
+    # min-p: fewer finite logits than k, so the masked tokens pad the top k
+    batch = workloads.random_sampler_batch(16, 32000, dtype=dtype, seed=77, kinds="topk")
+    batch.params["top_k"] = 40
+    batch.params["min_p"][::2] = 0.05
+    rng = np.random.default_rng(78)
+    words = (32000 + 31) // 32
+    allowed = np.zeros((16, words), dtype=np.uint32)
+    for b in range(16):
+        ids = rng.choice(32000, size=1 + b, replace=False)
+        np.bitwise_or.at(allowed[b], ids // 32, (np.uint32(1) << (ids % 32).astype(np.uint32)))
+    ids, probs, status = run(batch, allowed, None, None)
+    want = prepass.sample_processed(batch.values, batch.params, 5, 2, dtype=dtype, allowed=allowed)
+    compare_sampler(want, ids, probs).check()
+    assert status == 0
+
+
 def test_bad_penalty_rows():
     batch = workloads.random_sampler_batch(6, 700, dtype="f32", seed=3, kinds="mixed")
     _, history, _ = workloads.prepass_inputs(batch.values, seed=4)

@@ -152,9 +152,10 @@ smp_status smp_filter_debug(const void* logits, int32_t batch, int32_t vocab, sm
  *                leaves the row unchanged; r must be finite and > 0, else the
  *                row is an error row (SMP_ROW_BAD_PARAMS, greedy or not).
  * Every other argument and the error behaviour are those of smp_sample.
- * Every row takes the exact selection over global memory (the path smp_sample
- * uses for top-p rows), one CTA per row: slower than smp_sample's streamed
- * path.
+ * The pre-pass runs inside smp_sample's own single pass over the logits
+ * (each value is transformed as it is read), so the cost over smp_sample is
+ * the mask words (vocab / 8 bytes per row) and the transform of the units
+ * that hold a disallowed token or a history id.
  */
 smp_status smp_sample_processed(const void* logits, int32_t batch, int32_t vocab, smp_dtype dtype,
                                 const smp_row_params* params, const uint32_t* allowed, const int32_t* history,
@@ -164,9 +165,10 @@ smp_status smp_sample_processed(const void* logits, int32_t batch, int32_t vocab
 
 /*
  * smp_logit_prepass -- the pre-pass of smp_sample_processed written into the
- * logits in place, so that smp_sample (or a verifier call) then reads the
- * processed logits in its own single pass.  The cheap way to sample with a
- * repetition penalty and a constraint mask when the logits may be modified.
+ * logits in place, so that smp_sample, or a verifier call, then reads the
+ * processed logits.  For callers whose later steps all need the processed
+ * logits (the verifier has no pre-pass of its own); to sample once,
+ * smp_sample_processed is faster.
  *
  *   logits       device, [batch, vocab] contiguous, dtype elements, read and
  *                written: disallowed tokens become -inf, each distinct

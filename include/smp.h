@@ -4,7 +4,7 @@
  *
  * Every entry point is asynchronous on the caller's CUDA stream, allocates
  * nothing, and reads and writes only the caller-owned device buffers it is
- * given.  Host-detectable errors (a NULL pointer, a size out of range, an
+ * given (smp_spec_verify_static also its own fixed scratch array).  Host-detectable errors (a NULL pointer, a size out of range, an
  * unknown dtype) return a status code before anything is launched.  Problems
  * that belong to one row (bad knobs, no finite logit, a draft id out of range,
  * a wait that ran out of time) give that row the id -1 and OR a flag

@@ -250,29 +250,36 @@ __global__ void __launch_bounds__(kThreads) beam_merge_kernel(BeamArgs a) {
     return reinterpret_cast<const BeamSliceHead*>(a.ws + (size_t(g * W + b) * S + s) * beam_slice_bytes(width));
   };
   if (tid == 0) bad = 0;
+  // The slice headers, one load per thread and all in flight at once, staged
+  // in the candidate arrays (free until the candidates are built): Z_s in
+  // cs[c], m_s in cs[half + c], the flags in cf[c] (W * S <= half).
+  constexpr int kHalf = kBeamMaxCand / 2;
+  for (int c = tid; c < W * S; c += kThreads) {
+    const BeamSliceHead* h = head_of(c / S, c % S);
+    cs[c] = double(h->z) * (1.0 / double(kFixedOne));
+    cs[kHalf + c] = double(h->m);
+    cf[c] = h->flags;
+  }
   __syncthreads();
   if (tid < W) {
     const int b = tid;
     int f = isnan(a.scores[size_t(g) * W + b]) ? kRowBadParams : 0;
-    float m = -INFINITY;
+    double m = -INFINITY;
     bool any = false;
     for (int s = 0; s < S; ++s) {
-      const BeamSliceHead* h = head_of(b, s);
-      f |= h->flags & kRowNonFinite;
-      if (!(h->flags & kSliceEmpty) && !(h->flags & kRowNonFinite)) {
+      const int fl = cf[b * S + s];
+      f |= fl & kRowNonFinite;
+      if (!fl) {
         any = true;
-        m = fmaxf(m, h->m);
+        m = fmax(m, cs[kHalf + b * S + s]);
       }
     }
     if (!any) f |= kRowNonFinite;
     double z = 0.0;
     if (!f)
-      for (int s = 0; s < S; ++s) {
-        const BeamSliceHead* h = head_of(b, s);
-        if (h->flags) continue;
-        z += double(h->z) * (1.0 / double(kFixedOne)) * exp(double(h->m) - double(m));
-      }
-    beam_c[b] = f ? 0.0 : -double(m) - log(z);
+      for (int s = 0; s < S; ++s)
+        if (!cf[b * S + s]) z += cs[b * S + s] * exp(cs[kHalf + b * S + s] - m);
+    beam_c[b] = f ? 0.0 : -m - log(z);
     if (f) atomicOr(&bad, f);
   }
   // ranks nobody fills (fewer candidates than width, or an error group) stay -1 / NaN

@@ -211,3 +211,16 @@ def test_inplace_prepass_then_sample(dtype):
                                           to(history, np.int32), to(penalty, np.float32))
     torch.cuda.synchronize()
     assert torch.equal(ids, ids2)
+
+
+def test_more_rows_than_resident_ctas_with_prepass():
+    # more rows than CTAs that fit on the GPU: each CTA takes several rows,
+    # and its copies run ahead into the next row while the pre-pass state is
+    # rebuilt per row
+    batch = workloads.random_sampler_batch(700, 3001, dtype="bf16", seed=91, kinds="mixed")
+    allowed, history, penalty = workloads.prepass_inputs(batch.values, seed=92)
+    ids, probs, status = run(batch, allowed, history, penalty)
+    rows = list(range(0, 700, 7)) + [699]
+    want = prepass.sample_processed(batch.values, batch.params, 5, 2, dtype="bf16", allowed=allowed,
+                                    history=history, penalty=penalty, rows=rows)
+    compare_sampler(want, ids, probs).check()

@@ -100,7 +100,7 @@ def grammar_allowed(prefix):
     return np.zeros(len(VOCAB), dtype=bool)
 
 
-@pytest.mark.parametrize("prefix", ["", "[", "[7", "[7,", "[7,3]"])
+@pytest.mark.parametrize("prefix", ["", "[", "[7", "[7,", "[7,3]", "[3", "[3,"])   # Exercise 39.4's prefixes too
 def test_tiny_grammar_mask(prefix):
     from spec_verify_gb300 import workloads
     rows = 300
@@ -135,3 +135,13 @@ def test_penalty_and_mask_order_and_bad_penalty():
     for bad in (0.0, -1.0, np.nan, np.inf):
         r = prepass.sample_processed(z, prm, 0, 0, history=hist, penalty=np.array([bad]))[0]
         assert r["token"] == -1 and r["status"] == osam.ROW_BAD_PARAMS
+
+
+@pytest.mark.parametrize("prefix, allowed_tokens", [
+    ("[", set("0123456789")), ("[3", {"]", ","}), ("[3,", set("0123456789")), ("", {"["}),
+])
+def test_exercise_39_4_allowed_next_tokens(prefix, allowed_tokens):
+    # "Decoding & Speculative Sampling", Exercise 39.4: the grammar [ d (, d)* ]
+    # allows these next tokens after each prefix
+    got = {VOCAB[i] for i in np.flatnonzero(grammar_allowed(prefix))}
+    assert got == allowed_tokens

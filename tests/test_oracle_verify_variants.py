@@ -306,3 +306,16 @@ def test_acceptance_rate_filtered_and_undefined_rows():
     res = over.spec_verify(P, Q, np.zeros((rows, 1), dtype=np.int32), 0, 0, params=prm, alpha=True)
     assert abs(res[0]["alpha"][0] - 3 / 7) < 1e-7      # float32 logits; sum min((4/7, 3/7, 0, 0), (3/7, 0, 4/7, 0))
     assert np.isnan(res[1]["alpha"][0]) and np.isnan(res[2]["alpha"][0])
+
+
+def test_exercise_39_2_residual_mass_is_one_minus_acceptance():
+    # "Decoding & Speculative Sampling", Exercise 39.2: for normalised p and q,
+    # sum_x max(0, p(x) - q(x)) = 1 - sum_x min(p(x), q(x)); the rejection path
+    # therefore carries exactly the residual mass
+    b, k, v = 5, 3, 40
+    p, q = batch(b, k, v, seed=31)
+    for r in range(b):
+        alphas = over.acceptance_rates(p[r], q[r], 0.8)
+        for i in range(k):
+            pi, qi = over.softmax64(p[r, i], 0.8), over.softmax64(q[r, i], 0.8)
+            assert abs(np.sum(np.maximum(0.0, pi - qi)) - (1.0 - alphas[i])) < 1e-12

@@ -11,8 +11,11 @@ arithmetic.
 Modules:
     philox   -- Philox4x64-10 and the uniform construction
     sampler  -- temperature, top-k, top-p, min-p, eq. 39.2, the id-order draw
-    verify   -- accept test (eq. 39.3), residual (eq. 39.4), bonus token
+    verify   -- accept test (eq. 39.3), residual (eq. 39.4), bonus token;
+                temperature, filters and greedy verification; acceptance rates
+    prepass  -- repetition penalty and constraint mask before sampling
+    beam     -- one beam-search step's candidate selection (eq. 39.1)
 """
 
-from . import philox, sampler, verify  # noqa: F401
+from . import beam, philox, prepass, sampler, verify  # noqa: F401
 from .sampler import ROW_BAD_PARAMS, ROW_NONFINITE, ROW_OK  # noqa: F401

@@ -1,4 +1,4 @@
-"""Benchmark of the sampler and the speculative verifier on one GB300.
+"""Benchmark of the sampler and the speculative verifier on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl smp|reference]
 
@@ -6,16 +6,26 @@ One step = one smp_sample call on the large-vocabulary batch (B=256,
 V=128256, bf16 Zipf-headed logits; half the rows min-p 0.1, a quarter greedy,
 a quarter T=0.7 with top-k 40) followed by one smp_spec_verify call on the
 verify batch (B=32, K=4, V=32000, fp32).  Inputs are resident in HBM and
-rotate over enough copies that every call reads logits that are not in L2.
-The K timed steps are replayed from a CUDA graph and timed with CUDA events.
+rotate over enough copies that no call finds its logits in L2.  The K steps
+are captured in one CUDA graph; the graph is replayed at least 10 times, each
+replay timed with CUDA events on the launching stream between a barrier and a
+device synchronisation, and the median replay (the best beside it) gives the
+per-call time.
+
+With N GPUs (torchrun, one process per GPU) the job is one batch of N x 256
+rows split by rows: rank r takes rows [256 r, 256 (r + 1)) and passes 256 r as
+the row base of its Philox counters, so the tokens do not depend on the split
+and no collective runs on the data path (weak scaling); the time is the
+maximum over ranks.
 
 `value` is sampled rows per second of sampler time; the verifier's emitted
-tokens per second, the roofline of the sampler kernel, an end-to-end number
-through host buffers, the clocks seen during the timed region and the oracle's
-own rate on the host cores are reported beside it, on one JSON line.
+tokens per second, the roofline of the sampler kernel, the general-path
+workloads (the mixed batch and the wide-nucleus batch), an end-to-end number
+through host buffers, the clocks seen during the timed region and the
+oracle's own rate on the host cores are reported beside it, on one JSON line.
 
 --impl reference times the fp64 oracle instead, on bounded samples of the
-same workload, on the host cores.
+same workload, on all host cores.
 """
 
 import argparse
@@ -27,7 +37,6 @@ import statistics
 import subprocess
 import sys
 import tempfile
-import threading
 import time
 
 import numpy as np
@@ -43,10 +52,12 @@ WORKLOAD_DESC = ("large_vocab: B=256, V=128256, bf16 logits log(Zipf s=1.1) over
                  "permutation + N(0, 0.5^2); rows b%4 in {0,1}: min_p=0.1 T=1, b%4==2: greedy, "
                  "b%4==3: T=0.7 top_k=40; Philox seed 0")
 VERIFY_DESC = "verify: B=32, K=4, V=32000, fp32; q = G[:, :4], p = G + N(0,1), G ~ N(0, 2^2)"
+DTYPE = "bf16 logits; exp in double-float (pairs of binary32); u64 fixed-point masses, exact integer sums"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "sample_kernel_large_vocab.md")
+PROFILE_JSON = os.path.join(ROOT, "profiles", "sample_kernel_large_vocab.json")
 KERNEL_SOURCES = ["common.cuh", "row_ops.cuh", "select.cuh", "general.cuh", "sample.cu", "exp_table.h"]
+MIN_REPLAYS = 10
 
 
 def dist_env():
@@ -54,6 +65,14 @@ def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return rank, world, local
+
+
+def row_block(rows, rank, world):
+    """The contiguous block [lo, hi) of a batch of `rows` rows that rank
+    `rank` of `world` takes (sizes differ by at most one)."""
+    base, extra = divmod(rows, world)
+    lo = rank * base + min(rank, extra)
+    return lo, lo + base + (1 if rank < extra else 0)
 
 
 def max_over_ranks(value, device=None):
@@ -92,23 +111,20 @@ def kernel_source_sha():
     return h.hexdigest()[:16]
 
 
-def profiled_traffic():
-    """DRAM bytes per launch from the committed ncu summary, if it matches the source."""
+def profiled_traffic(path=PROFILE_JSON):
+    """DRAM bytes per launch of sample_kernel from the committed ncu capture
+    (profiles/*.json, written with the capture), or None when the kernel
+    sources have changed since the counters were taken."""
     try:
-        with open(PROFILE_SUMMARY) as fh:
-            text = fh.read()
-    except OSError:
+        with open(path) as fh:
+            data = json.load(fh)
+    except (OSError, ValueError):
         return None
-    fields = {}
-    for line in text.splitlines():
-        if line.startswith("- ") and ":" in line:
-            k, v = line[2:].split(":", 1)
-            fields[k.strip()] = v.strip().strip("`")
-    if fields.get("source_sha") != kernel_source_sha():
+    if data.get("source_sha") != kernel_source_sha():
         return None
     try:
-        return float(fields["dram_bytes_per_launch"])
-    except (KeyError, ValueError):
+        return float(data["dram_bytes_per_launch"])
+    except (KeyError, TypeError, ValueError):
         return None
 
 
@@ -166,56 +182,80 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
-def oracle_rate(batch, seconds, start_row=0):
-    """Rows per second of the fp64 oracle on this process's host core."""
-    from oracle import sampler as osam
-    done = 0
-    t0 = time.perf_counter()
-    rows = []
-    b = start_row
-    while time.perf_counter() - t0 < seconds or done == 0:
-        osam.sample(batch.values, batch.params, batch.seed, batch.offset, rows=[b])
-        rows.append(b)
-        done += 1
-        b = (b + 1) % batch.data.shape[0]
-    elapsed = time.perf_counter() - t0
-    return done / elapsed, done, elapsed
+# ---------------------------------------------------------------- the oracle on the host cores
+
+def cpu_baseline(batch, seconds):
+    """The fp64 oracle on all host cores and on one core (spawned worker
+    processes, so nothing of the GPU process competes with them), each over
+    whole passes of the batch sized to about `seconds`.  Returns the
+    cpu_baseline object of the JSON line."""
+    from oracle import pool
+    B = batch.data.shape[0]
+    cores = pool.default_procs()
+    probe, _, _ = pool.sampler_rate(batch.values, batch.params, batch.seed, batch.offset, range(B), 1)
+    passes_1 = max(1, int(round(seconds * probe / B)))
+    passes_all = max(1, int(round(seconds * probe * cores / B)))
+    rate_1, n_1, s_1 = pool.sampler_rate(batch.values, batch.params, batch.seed, batch.offset,
+                                         list(range(B)) * passes_1, 1)
+    rate_all, n_all, s_all = pool.sampler_rate(batch.values, batch.params, batch.seed, batch.offset,
+                                               list(range(B)) * passes_all, cores)
+    return {"value": rate_all, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": (f"{n_all} rows ({passes_all} passes over the {WORKLOAD} batch) in {s_all:.1f} s on "
+                       f"{cores} worker processes, one per core; {n_1} rows in {s_1:.1f} s on one; fp64 numpy "
+                       f"oracle"),
+            "cores_all": cores, "rows_per_s_all": rate_all, "rows_per_s_1": rate_1}
 
 
 def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
+    import multiprocessing as mp
+
+    from oracle import pool
     from spec_verify_gb300 import workloads
     batch = workloads.sampler_workload(WORKLOAD)
-    rows_per_step = 4
-    from oracle import sampler as osam
+    B = batch.data.shape[0]
+    cores = pool.default_procs()
+    rows_per_step = 4 * cores
+    handles, specs = pool._share({"values": batch.values, "params": batch.params})
+    try:
+        ctx = mp.get_context("spawn")
+        with ctx.Pool(processes=cores, initializer=pool._attach, initargs=(specs,)) as workers:
+            def step(i):
+                base = (i * rows_per_step) % B
+                rows = [(base + j) % B for j in range(rows_per_step)]
+                chunks = [rows[j::cores] for j in range(cores)]
+                workers.map(pool._timed_sample_chunk, [(c, batch.seed, batch.offset) for c in chunks],
+                            chunksize=1)
 
-    def step(i):
-        base = (i * rows_per_step) % batch.data.shape[0]
-        osam.sample(batch.values, batch.params, batch.seed, batch.offset,
-                    rows=list(range(base, base + rows_per_step)))
-
-    for i in range(args.warmup):
-        step(i)
-    t0 = time.perf_counter()
-    for i in range(args.steps):
-        step(args.warmup + i)
-    elapsed = time.perf_counter() - t0
+            for i in range(args.warmup):
+                step(i)
+            t0 = time.perf_counter()
+            for i in range(args.steps):
+                step(args.warmup + i)
+            elapsed = time.perf_counter() - t0
+    finally:
+        for h in handles:
+            h.close()
+            h.unlink()
     value = rows_per_step * args.steps / elapsed
-    sample = f"{rows_per_step} rows of the {WORKLOAD} batch per step, fp64 numpy oracle, one core"
+    sample = (f"{rows_per_step} rows of the {WORKLOAD} batch per step (cycling through it), fp64 numpy oracle "
+              f"on {cores} worker processes, one per host core")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1000.0 * elapsed / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": WORKLOAD_DESC, "rows_per_step": rows_per_step},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
     return 0
 
+
+# ---------------------------------------------------------------- the GPU arm
 
 def run_gpu(args):
     import torch
@@ -226,6 +266,9 @@ def run_gpu(args):
     from spec_verify_gb300 import workloads
 
     rank, world, local = dist_env()
+    if world != args.gpus:
+        raise SystemExit(f"--gpus {args.gpus} but WORLD_SIZE={world}: launch one process per GPU with "
+                         f"torchrun --nproc-per-node {args.gpus}")
     if world > 1:
         dist.init_process_group("nccl")
     torch.cuda.set_device(local)
@@ -238,123 +281,178 @@ def run_gpu(args):
             dist.barrier()
         torch.cuda.synchronize()
 
+    steps = args.steps
+    replays = max(MIN_REPLAYS, args.replays)
+
     # ---------------- inputs, resident in HBM, rotated past L2
     batch = workloads.sampler_workload(WORKLOAD)
     B, V = batch.data.shape
+    row_base, _ = row_block(world * B, rank, world)     # this rank's rows of the N x B job
     l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 129 * 2**20))
     sample_bytes = batch.data.nbytes
-    n_copies = max(4, math.ceil(4 * l2 / sample_bytes))
+
+    def copies(nbytes):
+        return max(4, math.ceil(4 * l2 / nbytes))
+
+    n_copies = copies(sample_bytes)
     host = torch.from_numpy(batch.data.view(np.int16)).view(torch.bfloat16)
     logits = [host.to(dev) for _ in range(n_copies)]
     params = binding.params_to_device(batch.params, dev)
     out_ids = torch.empty(B, dtype=torch.int32, device=dev)
     out_probs = torch.empty(B, dtype=torch.float32, device=dev)
     status = torch.empty(1, dtype=torch.int32, device=dev)
-    seed = rank   # each rank samples its own rows (weak scaling, no collective)
+    seed = batch.seed
 
     vb = workloads.verify_workload()
     vB, vK, vV = vb.shape
+    v_base, _ = row_block(world * vB, rank, world)
     v_bytes = vb.p.nbytes + vb.q.nbytes
-    v_copies = max(4, math.ceil(4 * l2 / v_bytes))
+    v_copies = copies(v_bytes)
     p_dev = [torch.from_numpy(vb.p).to(dev) for _ in range(v_copies)]
     q_dev = [torch.from_numpy(vb.q).to(dev) for _ in range(v_copies)]
     d, _, _ = binding.sample(q_dev[0].view(vB * vK, vV), workloads.make_params(vB * vK), vb.draft_seed,
                              vb.draft_offset)
     drafts = d.view(vB, vK).contiguous()
-    ws = torch.empty(binding.spec_verify_workspace_bytes(vB, vK), dtype=torch.uint8, device=dev)
+    ws = torch.zeros(binding.spec_verify_workspace_bytes(vB, vK), dtype=torch.uint8, device=dev)
     v_acc = torch.empty(vB, dtype=torch.int32, device=dev)
     v_ids = torch.empty(vB, vK + 1, dtype=torch.int32, device=dev)
     v_status = torch.empty(1, dtype=torch.int32, device=dev)
 
     def sampler_call(i):
-        binding.sample(logits[i % n_copies], params, seed, i, out_ids, out_probs, status)
+        binding.sample_rows(logits[i % n_copies], params, seed, i, row_base, out_ids=out_ids, out_probs=out_probs,
+                            status=status)
 
     def sampler_kernel_only(i):   # no status word: sample_kernel alone, for the roofline
-        binding.sample(logits[i % n_copies], params, seed, i, out_ids, out_probs, False)
+        binding.sample_rows(logits[i % n_copies], params, seed, i, row_base, out_ids=out_ids, out_probs=out_probs,
+                            status=False)
+
+    def sampler_warm_l2(i):       # one copy, resident in L2 after the first call
+        binding.sample_rows(logits[0], params, seed, i, row_base, out_ids=out_ids, out_probs=out_probs,
+                            status=False)
 
     def verify_call(i):
-        binding.spec_verify(p_dev[i % v_copies], q_dev[i % v_copies], drafts, seed, i, ws, v_acc, v_ids,
-                            v_status)
-
-    # Verifier variants on the same batch: temperature, greedy, filters (each
-    # with drafts drawn from q under the same knobs, by the CUDA sampler).
-    variant_knobs = {"temperature_0.8": dict(temperature=0.8), "greedy": dict(greedy=1),
-                     "top_k40_top_p0.9_T0.8": dict(temperature=0.8, top_k=40, top_p=0.9),
-                     "alpha_T1": dict()}   # T = 1, and the acceptance rates of every position
-    v_alpha = torch.empty(vB, vK, dtype=torch.float32, device=dev)
-    variants = {}
-
-    def variant_call(name):
-        vprm, vdrafts, _ = variants[name]
-
-        def call(i):
-            binding.spec_verify_params(p_dev[i % v_copies], q_dev[i % v_copies], vdrafts, vprm, seed, i, ws,
-                                       v_acc, v_ids, v_status, out_alpha=v_alpha if name == "alpha_T1" else None)
-        return call
+        binding.spec_verify_rows(p_dev[i % v_copies], q_dev[i % v_copies], drafts, None, vb.seed, i, v_base,
+                                 workspace=ws, out_accepted=v_acc, out_ids=v_ids, status=v_status)
 
     # warm-up (also sets kernel attributes before any capture)
-    for i in range(max(args.warmup, 3)):
+    for i in range(args.warmup):
         sampler_call(i)
         verify_call(i)
     torch.cuda.synchronize()
     assert int(status.cpu()[0]) == 0 and int(v_status.cpu()[0]) == 0
 
-    def capture(fn):
+    def capture(fn, n=steps):
         g = torch.cuda.CUDAGraph()
         s = torch.cuda.Stream()
         s.wait_stream(torch.cuda.current_stream())
         with torch.cuda.stream(s):
             with torch.cuda.graph(g, stream=s):
-                for i in range(args.steps):
+                for i in range(n):
                     fn(i)
         torch.cuda.current_stream().wait_stream(s)
         return g
 
+    def timed(graph, calls=steps):
+        """Per-call microseconds of a graph of `calls` calls: (median, best)
+        over `replays` replays, each between a barrier and a synchronize,
+        maximum over ranks."""
+        graph.replay()               # warm replay
+        stream = torch.cuda.current_stream()
+        times = []
+        for _ in range(replays):
+            barrier()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            graph.replay()
+            e1.record(stream)
+            barrier()
+            times.append(max_over_ranks(e0.elapsed_time(e1), dev))
+        return 1000.0 * statistics.median(times) / calls, 1000.0 * min(times) / calls
+
     g_step = capture(lambda i: (sampler_call(i), verify_call(i)))
     g_samp = capture(sampler_call)
     g_kern = capture(sampler_kernel_only)
+    g_warm = capture(sampler_warm_l2)
     g_ver = capture(verify_call)
 
-    def timed(graph, reps):
-        for _ in range(reps):       # warm replays
-            graph.replay()
-        barrier()
-        stream = torch.cuda.current_stream()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        graph.replay()
-        e1.record(stream)
-        barrier()
-        return max_over_ranks(e0.elapsed_time(e1), dev)
-
     with ClockSampler(local) as clocks:
-        step_ms = timed(g_step, max(1, args.warmup // max(1, args.steps)))
-        samp_ms = timed(g_samp, 1)
-        kern_ms = timed(g_kern, 1)
-        ver_ms = timed(g_ver, 1)
+        step_us, step_best = timed(g_step)
+        samp_us, samp_best = timed(g_samp)
+        kern_us, kern_best = timed(g_kern)
+        warm_us, warm_best = timed(g_warm)
+        ver_us, ver_best = timed(g_ver)
     clock_info = clocks.summary()
     acc_mean = float(v_acc.float().mean().item())   # accepted lengths of the plain verifier's last call
+    del g_step, g_samp, g_kern, g_warm, g_ver
 
-    # Verifier variants, set up and timed after the headline graphs.
+    def graph_line(fn, nbytes, units, calls=steps):
+        for i in range(args.warmup):
+            fn(i)
+        torch.cuda.synchronize()
+        g = capture(fn, calls)
+        med, best = timed(g, calls)
+        del g
+        return {"us_per_call": med, "us_best": best, "units_per_s": job_rate(units, world, med * 1e-6),
+                "bytes_per_call": nbytes, "gbs": nbytes / (med * 1e-6) / 1e9}
+
+    peak, peak_kind = measured_peaks()
+
+    # ---------------- the general path: the mixed batch and the wide nucleus
+    general = {}
+    for name in ("mixed", "flat_nucleus"):
+        gb = workloads.sampler_workload(name)
+        gB, gV = gb.data.shape
+        g_host = torch.from_numpy(gb.data.view(np.int16)).view(torch.bfloat16)
+        g_n = copies(gb.data.nbytes)
+        g_dev = [g_host.to(dev) for _ in range(g_n)]
+        g_prm = binding.params_to_device(gb.params, dev)
+        g_ids = torch.empty(gB, dtype=torch.int32, device=dev)
+        g_probs = torch.empty(gB, dtype=torch.float32, device=dev)
+        g_base, _ = row_block(world * gB, rank, world)
+
+        def gcall(i, g_dev=g_dev, g_prm=g_prm, g_ids=g_ids, g_probs=g_probs, g_base=g_base, g_n=g_n):
+            binding.sample_rows(g_dev[i % g_n], g_prm, gb.seed, i, g_base, out_ids=g_ids, out_probs=g_probs,
+                                status=status)
+
+        nbytes = gB * (gV * 2 + 28)
+        line = graph_line(gcall, nbytes, gB, calls=min(steps, 50))
+        assert int(status.cpu()[0]) == 0
+        line["rows_per_s"] = line.pop("units_per_s")
+        line["frac_of_measured_hbm"] = line["gbs"] / peak
+        line["workload"] = f"{name}: B={gB}, V={gV}, bf16"
+        line["l2"] = f"inputs rotate over {g_n} copies ({g_n * gb.data.nbytes / 1e6:.0f} MB)"
+        general[name] = line
+        del g_dev
+        torch.cuda.empty_cache()
+
+    # ---------------- verifier variants on the same batch
+    variant_knobs = {"temperature_0.8": dict(temperature=0.8), "greedy": dict(greedy=1),
+                     "top_k40_top_p0.9_T0.8": dict(temperature=0.8, top_k=40, top_p=0.9),
+                     "alpha_T1": dict()}   # T = 1, and the acceptance rates of every position
+    v_alpha = torch.empty(vB, vK, dtype=torch.float32, device=dev)
+    verify_variants = {}
     for name, knobs in variant_knobs.items():
         vprm = binding.params_to_device(workloads.make_params(vB, **knobs), dev)
         dprm = workloads.make_params(vB * vK, **knobs)
         dv, _, _ = binding.sample(q_dev[0].view(vB * vK, vV), dprm, vb.draft_seed, vb.draft_offset)
-        variants[name] = (vprm, dv.view(vB, vK).contiguous(), knobs)
-    var_ms = {}
-    for name in variants:
-        call = variant_call(name)
-        for i in range(max(args.warmup, 3)):
-            call(i)
-        torch.cuda.synchronize()
+        vdrafts = dv.view(vB, vK).contiguous()
+
+        def vcall(i, vprm=vprm, vdrafts=vdrafts, name=name):
+            binding.spec_verify_rows(p_dev[i % v_copies], q_dev[i % v_copies], vdrafts, vprm, vb.seed, i, v_base,
+                                     workspace=ws, out_accepted=v_acc, out_ids=v_ids, status=v_status,
+                                     out_alpha=v_alpha if name == "alpha_T1" else None)
+
+        nbytes = vb.p.nbytes if "greedy" in name else v_bytes   # greedy reads no draft row
+        line = graph_line(vcall, nbytes, vB)
         assert int(v_status.cpu()[0]) == 0
-        g = capture(call)
-        ms = timed(g, 1)
-        var_ms[name] = (ms, float(v_acc.float().mean().item()))   # accepted lengths of the last call
-        del g
-    # Sampler with the logit pre-pass on the headline batch: repetition
-    # penalty over 64 recent tokens, with and without a constraint mask.
+        accepted = float(v_acc.float().mean().item())
+        line.pop("units_per_s")
+        line.update({"mean_accepted": accepted, "tok_s": world * vB * (accepted + 1.0) / (line["us_per_call"] * 1e-6),
+                     "knobs": knobs})
+        verify_variants[name] = line
+
+    # ---------------- sampler with the logit pre-pass on the headline batch
     allowed_np, history_np, penalty_np = workloads.prepass_inputs(batch.values, seed=1, mask_density=(0.8, 1.0))
     allowed_np[-1] = allowed_np[-2]   # no error row in the timed batch
     allowed_dev = torch.from_numpy(allowed_np.view(np.int32)).to(dev)
@@ -363,19 +461,14 @@ def run_gpu(args):
     sampler_variants = {}
     for name, use_mask in (("penalty", False), ("penalty_and_mask", True)):
         def pcall(i, use_mask=use_mask):
-            binding.sample_processed(logits[i % n_copies], params, seed, i, allowed_dev if use_mask else None,
-                                     history_dev, penalty_dev, out_ids, out_probs, status)
-        for i in range(max(args.warmup, 3)):
-            pcall(i)
-        torch.cuda.synchronize()
-        assert int(status.cpu()[0]) == 0
-        g = capture(pcall)
-        us = 1000.0 * timed(g, 1) / args.steps
-        del g
+            binding.sample_rows(logits[i % n_copies], params, seed, i, row_base,
+                                allowed=allowed_dev if use_mask else None, history=history_dev,
+                                penalty=penalty_dev, out_ids=out_ids, out_probs=out_probs, status=status)
         nbytes = sample_bytes + (allowed_np.nbytes if use_mask else 0) + history_np.nbytes + penalty_np.nbytes
-        sampler_variants[name] = {"us_per_call": us, "rows_per_s": job_rate(B, world, us * 1e-6),
-                                  "bytes_per_call": nbytes, "gbs": nbytes / (us * 1e-6) / 1e9}
-
+        line = graph_line(pcall, nbytes, B)
+        assert int(status.cpu()[0]) == 0
+        line["rows_per_s"] = line.pop("units_per_s")
+        sampler_variants[name] = line
     # The same through the in-place pre-pass: smp_logit_prepass, then
     # smp_sample (the copies are modified in place; the penalty compounds
     # over replays on the same copy, which changes no byte count).
@@ -383,24 +476,19 @@ def run_gpu(args):
         def icall(i, use_mask=use_mask):
             binding.logit_prepass(logits[i % n_copies], allowed_dev if use_mask else None, history_dev,
                                   penalty_dev, status)
-            binding.sample(logits[i % n_copies], params, seed, i, out_ids, out_probs, status)
-        for i in range(max(args.warmup, 3)):
-            icall(i)
-        torch.cuda.synchronize()
-        g = capture(icall)
-        us = 1000.0 * timed(g, 1) / args.steps
-        del g
+            binding.sample_rows(logits[i % n_copies], params, seed, i, row_base, out_ids=out_ids,
+                                out_probs=out_probs, status=status)
         nbytes = sample_bytes + (allowed_np.nbytes if use_mask else 0) + history_np.nbytes + penalty_np.nbytes
-        sampler_variants[name] = {"us_per_call": us, "rows_per_s": job_rate(B, world, us * 1e-6),
-                                  "bytes_per_call": nbytes, "gbs": nbytes / (us * 1e-6) / 1e9}
+        line = graph_line(icall, nbytes, B)
+        line["rows_per_s"] = line.pop("units_per_s")
+        sampler_variants[name] = line
 
-    # One beam-search step: 8 requests x 4 beams over the large vocabulary
-    # (bf16, Zipf-headed logits), the 4 best candidates of each request.
+    # ---------------- one beam-search step: 8 requests x 4 beams over the large vocabulary
     bG, bW, bwidth = 8, 4, 4
     brng = np.random.default_rng(3000)
     bz = workloads.f32_to_bf16_bits(workloads.zipf_logits_f32(brng, bG * bW, V)).reshape(bG, bW, V)
     b_bytes = bz.nbytes
-    b_copies = max(4, math.ceil(4 * l2 / b_bytes))
+    b_copies = copies(b_bytes)
     b_host = torch.from_numpy(bz.view(np.int16)).view(torch.bfloat16)
     b_dev = [b_host.to(dev) for _ in range(b_copies)]
     b_scores = torch.from_numpy(-brng.uniform(0, 12, (bG, bW))).to(dev)
@@ -412,44 +500,26 @@ def run_gpu(args):
 
     def bcall(i):
         binding.beam_topk(b_dev[i % b_copies], b_scores, bwidth, b_ws, b_par, b_tok, b_sc, status)
-    for i in range(max(args.warmup, 3)):
-        bcall(i)
-    torch.cuda.synchronize()
+    beam_line = graph_line(bcall, b_bytes, 1)
     assert int(status.cpu()[0]) == 0
-    g = capture(bcall)
-    b_us = 1000.0 * timed(g, 1) / args.steps
-    del g
-    beam_line = {"workload": f"{bG} requests x {bW} beams x V={V} bf16 (Zipf-headed), width {bwidth}",
-                 "us_per_call": b_us, "steps_per_s": world / (b_us * 1e-6), "bytes_per_call": b_bytes,
-                 "gbs": b_bytes / (b_us * 1e-6) / 1e9,
-                 "l2": f"inputs rotate over {b_copies} copies ({b_copies * b_bytes / 1e6:.0f} MB)"}
+    beam_line["steps_per_s"] = beam_line.pop("units_per_s")
+    beam_line["workload"] = f"{bG} requests x {bW} beams x V={V} bf16 (Zipf-headed), width {bwidth}"
+    beam_line["l2"] = f"inputs rotate over {b_copies} copies ({b_copies * b_bytes / 1e6:.0f} MB)"
+    del b_dev
 
-    verify_variants = {}
-    for name, (ms, accepted) in var_ms.items():
-        us = 1000.0 * ms / args.steps
-        nbytes = vb.p.nbytes if "greedy" in name else v_bytes   # greedy reads no draft row
-        verify_variants[name] = {"us_per_call": us, "mean_accepted": accepted,
-                                 "tok_s": world * vB * (accepted + 1.0) / (us * 1e-6),
-                                 "bytes_per_call": nbytes, "gbs": nbytes / (us * 1e-6) / 1e9,
-                                 "knobs": variants[name][2]}
-
-    # per step: clear_status_kernel + sample_kernel, verify_pos_kernel (which clears the
-    # verifier's status word) + verify_resolve_kernel
-    gpu_launches = args.steps * 4
-    samp_us = 1000.0 * samp_ms / args.steps
-    kern_us = 1000.0 * kern_ms / args.steps
-    ver_us = 1000.0 * ver_ms / args.steps
+    # per step: clear_status_kernel + sample_kernel, then the verifier's kernels
+    gpu_launches = steps * (2 + binding.VERIFY_LAUNCHES)
     rows_per_s = job_rate(B, world, samp_us * 1e-6)
     verify_tok_s = world * vB * (acc_mean + 1.0) / (ver_us * 1e-6)
 
     # roofline of the sampler kernel: logits read once, ids + probs written, params read
     alg_bytes = B * V * 2 + B * 8 + B * 20
     achieved = alg_bytes / (kern_us * 1e-6) / 1e9
-    peak, peak_kind = measured_peaks()
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "traffic": profiled_traffic(),
-                "kernel": "sample_kernel", "kernel_us_per_launch": kern_us,
-                "timing": "K back-to-back sample_kernel launches (no status word) in one CUDA graph",
+                "kernel": "sample_kernel", "kernel_us_per_launch": kern_us, "kernel_us_best": kern_best,
+                "timing": (f"K back-to-back sample_kernel launches (no status word) in one CUDA graph, median of "
+                           f"{replays} replays"),
                 "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)",
                 "algorithmic_bytes_per_launch": alg_bytes}
 
@@ -469,7 +539,7 @@ def run_gpu(args):
     freed = [torch.cuda.Event() for _ in range(2)]
     for ev in freed:
         ev.record(compute)
-    e2e_steps = max(3, args.steps)
+    e2e_steps = max(3, steps)
 
     def e2e_step(i):
         k = i % 2
@@ -479,7 +549,8 @@ def run_gpu(args):
             dev_params[k].copy_(params_host, non_blocking=True)
             copied[k].record(copy_stream)
         compute.wait_event(copied[k])
-        binding.sample(dev_in[k], dev_params[k], seed, i, out_ids, out_probs, status)
+        binding.sample_rows(dev_in[k], dev_params[k], seed, i, row_base, out_ids=out_ids, out_probs=out_probs,
+                            status=status)
         freed[k].record(compute)
         ids_host.copy_(out_ids, non_blocking=True)
         probs_host.copy_(out_probs, non_blocking=True)
@@ -487,7 +558,6 @@ def run_gpu(args):
     for i in range(3):
         e2e_step(i)
     barrier()
-    t0 = time.perf_counter()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record()
@@ -500,39 +570,45 @@ def run_gpu(args):
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), dev)
     e2e = {"value": job_rate(B * e2e_steps, world, e2e_ms * 1e-3), "unit": UNIT,
            "h2d_bytes_per_step": sample_bytes + batch.params.nbytes, "d2h_bytes_per_step": B * 8,
-           "what": "pinned host logits+params -> device copy (own stream, two buffers: overlaps the previous step's call), smp_sample, ids+probs -> host, per step"}
+           "what": ("pinned host logits+params -> device copy (own stream, two buffers: overlaps the previous "
+                    "step's call), smp_sample_rows, ids+probs -> host, per step")}
 
     # ---------------- oracle on the host cores (rank 0, N = 1 only)
-    cpu_baseline = None
+    cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        rate, rows_done, secs = oracle_rate(batch, args.cpu_seconds)
-        cpu_baseline = {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
-                        "sample": f"{rows_done} rows of the {WORKLOAD} batch in {secs:.1f} s, fp64 numpy oracle"}
+        cpu = cpu_baseline(batch, args.cpu_seconds)
 
     if rank == 0:
         line = {
             "metric": METRIC, "value": rows_per_s, "unit": UNIT, "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms / args.steps,
+            "steps": steps, "warmup": args.warmup, "ms_per_step": step_us / 1000.0,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "u64", "data": "synthetic",
+            "dtype": DTYPE, "data": "synthetic",
             "config": {"workload": WORKLOAD_DESC, "batch": B, "vocab": V, "logits_dtype": "bf16",
                        "verify_workload": VERIFY_DESC,
                        "l2": f"inputs rotate over {n_copies} sampler copies ({n_copies * sample_bytes / 1e6:.0f} MB) "
                              f"and {v_copies} verify copies; L2 {l2 / 1e6:.0f} MB",
-                       "timing": "K steps captured in one CUDA graph, CUDA events on the launching stream",
-                       "parallelism": f"dp{world} (rows independent, no collective)"},
-            "sampler_us_per_call": samp_us,
-            "sample_kernel_us": kern_us,
+                       "timing": (f"K steps captured in one CUDA graph, replayed {replays} times, CUDA events on "
+                                  f"the launching stream; median replay (best beside it)"),
+                       "parallelism": (f"dp{world}: a batch of {world} x {B} rows split by rows, rank r at row base "
+                                       f"{B} r (no collective)")},
+            "ms_per_step_best": step_best / 1000.0,
+            "sampler_us_per_call": samp_us, "sampler_us_best": samp_best,
+            "sample_kernel_us": kern_us, "sample_kernel_us_best": kern_best,
+            "warm_l2": {"us_per_call": warm_us, "us_best": warm_best,
+                        "what": "sample_kernel on one copy of the batch (L2-resident after the first call)"},
             "hbm_gbs": achieved,
-            "sampler_variants": sampler_variants,
-            "beam_step": beam_line,
             "pct_of_measured_hbm": 100.0 * achieved / peak,
             "pct_of_8tbs_nominal": 100.0 * achieved / NOMINAL_HBM_GBS,
-            "verify": {"tok_s": verify_tok_s, "us_per_call": ver_us, "mean_accepted": acc_mean,
+            "general_path": general,
+            "sampler_variants": sampler_variants,
+            "beam_step": beam_line,
+            "verify": {"tok_s": verify_tok_s, "us_per_call": ver_us, "us_best": ver_best, "mean_accepted": acc_mean,
                        "bytes_per_call": v_bytes, "gbs": v_bytes / (ver_us * 1e-6) / 1e9,
+                       "frac_of_measured_hbm": v_bytes / (ver_us * 1e-6) / 1e9 / peak,
                        "variants": verify_variants},
             "roofline": roofline,
-            "cpu_baseline": cpu_baseline,
+            "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": gpu_launches,
             "clocks": clock_info,
@@ -546,14 +622,17 @@ def run_gpu(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--replays", type=int, default=MIN_REPLAYS, help=f"graph replays timed (at least {MIN_REPLAYS})")
     ap.add_argument("--impl", choices=["smp", "reference"], default="smp")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.gpus < 1:
+        ap.error("--gpus must be at least 1")
     if args.impl == "reference":
         return run_reference(args)
     return run_gpu(args)

@@ -22,6 +22,24 @@
  * double-float exponential (relative error below 2^-44), and sums them
  * exactly in integers.  Masses below 2^-45 of the row maximum (more than
  * about 31 T below the top logit) are zero.
+ *
+ * Sharding: rows are independent, so a batch split across GPUs (or across
+ * calls) gives the same tokens as one call when each part passes the global
+ * index of its first row as row_base (smp_sample_rows, smp_spec_verify_rows):
+ * the Philox counter holds row_base + row.  The other entry points use
+ * row_base = 0.
+ *
+ * Two departures from the first sketch of this interface, kept on purpose:
+ *   - the verifier takes a caller-owned workspace (smp_spec_verify_workspace_bytes):
+ *     its per-position statistics are written by one kernel and read by the
+ *     next, which shared memory cannot carry between launches; callers that
+ *     cannot allocate use smp_spec_verify_static;
+ *   - status codes 4 and 5 are SMP_ERR_UNSUPPORTED (a vocabulary beyond
+ *     SMP_MAX_VOCAB) and SMP_ERR_WORKSPACE (a missing or short workspace),
+ *     host-side conditions of this interface; the device conditions the sketch
+ *     gave codes to (a wait that ran out of time, a bad row) are reported per
+ *     row through the SMP_ROW_* flags of the status word instead, since they
+ *     are only known after the call has returned.
  */
 #ifndef SMP_H
 #define SMP_H
@@ -33,7 +51,7 @@
 extern "C" {
 #endif
 
-#define SMP_ABI_VERSION 2
+#define SMP_ABI_VERSION 3
 
 /* Largest vocabulary the kernels accept (rows are kept in on-chip memory). */
 #define SMP_MAX_VOCAB (1 << 19)
@@ -61,8 +79,10 @@ typedef enum smp_dtype {
  *                top_p < 0 or NaN is invalid.
  *   min_p        keep p_i >= min_p * max_j p_j ("Inference: Sampling, the KV
  *                Cache, Speculative Decoding and int8", section "Picking the
- *                next token"); active for 0 < min_p < 1, off for 0 and >= 1;
- *                min_p < 0 or NaN is invalid.
+ *                next token"); active for 0 < min_p < 1 only, which is the
+ *                range in which that section's own code applies the filter:
+ *                0 and every value >= 1 switch it off (so min_p = 1 does not
+ *                keep just the tied arg-max set); min_p < 0 or NaN is invalid.
  *   greedy       non-zero: take the arg-max (lowest id on ties), knobs ignored.
  * The filters are applied to the same post-temperature distribution and their
  * kept sets intersected, then renormalised (eq. 39.2).
@@ -162,6 +182,20 @@ smp_status smp_sample_processed(const void* logits, int32_t batch, int32_t vocab
                                 int32_t history_len, const float* repetition_penalty, uint64_t seed,
                                 uint64_t offset, int32_t* out_ids, float* out_probs, int32_t* status,
                                 void* stream);
+
+/*
+ * smp_sample_rows -- smp_sample_processed for a part of a larger batch: the
+ * Philox counter of row b is row_base + b, so splitting a batch into parts
+ * (over GPUs or calls) and passing each part's first global row index gives
+ * exactly the tokens of one call on the whole batch.  allowed, history and
+ * repetition_penalty may all be NULL (no pre-pass: the call is smp_sample
+ * with a row base).  Every other argument and the error behaviour are those
+ * of smp_sample_processed.
+ */
+smp_status smp_sample_rows(const void* logits, int32_t batch, int32_t vocab, smp_dtype dtype,
+                           const smp_row_params* params, const uint32_t* allowed, const int32_t* history,
+                           int32_t history_len, const float* repetition_penalty, uint64_t seed, uint64_t offset,
+                           uint64_t row_base, int32_t* out_ids, float* out_probs, int32_t* status, void* stream);
 
 /*
  * smp_logit_prepass -- the pre-pass of smp_sample_processed written into the
@@ -278,6 +312,20 @@ smp_status smp_spec_verify_params(const void* p_logits, const void* q_logits, co
                                   int32_t* status, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * smp_spec_verify_rows -- smp_spec_verify_params for a part of a larger batch:
+ * the uniforms of batch row b are drawn at Philox counter row row_base + b
+ * (draws 0..k), so parts verified separately with their first global row
+ * index give exactly the result of one call on the whole batch.  Every other
+ * argument, the workspace and the error behaviour are those of
+ * smp_spec_verify_params.
+ */
+smp_status smp_spec_verify_rows(const void* p_logits, const void* q_logits, const int32_t* draft_ids,
+                                int32_t batch, int32_t k, int32_t vocab, smp_dtype dtype,
+                                const smp_row_params* params, uint64_t seed, uint64_t offset, uint64_t row_base,
+                                int32_t* out_accepted_len, int32_t* out_ids, float* out_alpha, int32_t* status,
+                                void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * smp_beam_topk_workspace_bytes -- device workspace smp_beam_topk needs (0 if
  * the sizes are invalid).
  */
@@ -338,7 +386,11 @@ smp_status smp_beam_topk(const void* logits, const double* beam_scores, int32_t 
  *     before anything is launched.
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture on the device.
+ *     before any stream capture on the device.  The address is kept for the
+ *     rest of the process, which assumes one CUDA context per device (the
+ *     primary context) for the process lifetime: after cudaDeviceReset, or
+ *     with another context made current on that device, the kept address no
+ *     longer names the array and this entry point must not be called.
  *   - Every call on a device uses the same array and leaves its contents
  *     behind.  Each call writes every entry it reads before reading it, so
  *     nothing needs to start at zero, but calls that can overlap on the GPU

@@ -15,7 +15,9 @@ Modules:
                 temperature, filters and greedy verification; acceptance rates
     prepass  -- repetition penalty and constraint mask before sampling
     beam     -- one beam-search step's candidate selection (eq. 39.1)
+    pool     -- runs the per-row functions above over a batch on several
+                host cores (worker processes; no arithmetic of its own)
 """
 
-from . import beam, philox, prepass, sampler, verify  # noqa: F401
+from . import beam, philox, pool, prepass, sampler, verify  # noqa: F401
 from .sampler import ROW_BAD_PARAMS, ROW_NONFINITE, ROW_OK  # noqa: F401

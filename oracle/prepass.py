@@ -89,11 +89,13 @@ def prepare_row(row, dtype="f32", allowed_words=None, history=None, penalty=1.0)
 
 
 def sample_processed(logits, params, seed, offset, dtype="f32", allowed=None, history=None, penalty=None,
-                     rows=None):
+                     rows=None, row_base=0):
     """oracle.sampler.sample on pre-processed rows.
 
     allowed: [B, ceil(V / 32)] uint32 or None; history: [B, H] int or None;
-    penalty: [B] float or None (no penalty).  Returns per-row result dicts.
+    penalty: [B] float or None (no penalty); row_base: global index of row 0
+    (the uniform of row b is drawn at counter row row_base + b).  Returns
+    per-row result dicts.
     """
     logits = np.asarray(logits)
     if rows is None:
@@ -101,7 +103,7 @@ def sample_processed(logits, params, seed, offset, dtype="f32", allowed=None, hi
     results = []
     for b in rows:
         prm = params[b]
-        u = philox.uniform(seed, offset, int(b), 0)
+        u = philox.uniform(seed, offset, int(row_base) + int(b), 0)
         r = 1.0 if penalty is None else float(penalty[b])
         if not penalty_valid(r):
             res = {"token": -1, "prob": math.nan, "status": ROW_BAD_PARAMS, "kept": 0,

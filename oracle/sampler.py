@@ -201,7 +201,7 @@ def sample_row(row, temperature, top_k, top_p, min_p, greedy, u):
     return out
 
 
-def sample(logits, params, seed, offset, rows=None):
+def sample(logits, params, seed, offset, rows=None, row_base=0):
     """Run sample_row over a [B, V] batch.
 
     logits: array [B, V] of float32 values (bf16 logits widened exactly).
@@ -209,6 +209,9 @@ def sample(logits, params, seed, offset, rows=None):
             greedy (one record per row).
     rows:   optional subset of row indices (the Philox counter uses the row's
             own index, so any subset gives the same per-row results).
+    row_base: global index of row 0 when the batch is one part of a larger
+            batch: row b draws its uniform at counter row row_base + b, so a
+            batch split into parts gives the tokens of the whole.
     Returns a list of per-row result dicts in the order of `rows`.
     """
     logits = np.asarray(logits)
@@ -217,7 +220,7 @@ def sample(logits, params, seed, offset, rows=None):
     results = []
     for b in rows:
         prm = params[b]
-        u = philox.uniform(seed, offset, int(b), 0)
+        u = philox.uniform(seed, offset, int(row_base) + int(b), 0)
         res = sample_row(logits[b], prm["temperature"], prm["top_k"],
                          prm["top_p"], prm["min_p"], prm["greedy"], u)
         res["row"] = int(b)

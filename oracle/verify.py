@@ -199,14 +199,15 @@ def row_mode(prm, vocab):
 
 
 def spec_verify(p_logits, q_logits, draft_ids, seed, offset, rows=None, temperature=1.0, greedy=False,
-                params=None, alpha=False):
+                params=None, alpha=False, row_base=0):
     """Run verify_row over a batch (temperature and greedy for all its rows,
     or per row from `params`, one record per batch row, see row_mode).
     alpha: also return each row's acceptance rates ("alpha", K values; NaN
     for greedy and error rows, which compare no distributions).
 
     p_logits: [B, K+1, V]; q_logits: [B, K, V]; draft_ids: [B, K].
-    Uniform for batch row b, draw d: philox.uniform(seed, offset, b, d).
+    Uniform for batch row b, draw d: philox.uniform(seed, offset, row_base + b, d)
+    (row_base: global index of row 0 when the batch is one part of a larger one).
     Returns a list of per-row dicts (with "row") in the order of `rows`.
     """
     p_logits = np.asarray(p_logits)
@@ -217,7 +218,7 @@ def spec_verify(p_logits, q_logits, draft_ids, seed, offset, rows=None, temperat
         rows = range(p_logits.shape[0])
     results = []
     for b in rows:
-        us = [philox.uniform(seed, offset, int(b), d) for d in range(k + 1)]
+        us = [philox.uniform(seed, offset, int(row_base) + int(b), d) for d in range(k + 1)]
         if params is not None:
             status, t_row, g_row, f_row = row_mode(params[b], p_logits.shape[-1])
             if status != ROW_OK:

@@ -25,13 +25,15 @@ ROW_TIMEOUT = 4
 ROW_BAD_DRAFT = 8
 
 # Symbols declared in include/smp.h.
-EXPORTS = ("smp_sample", "smp_filter_debug", "smp_sample_processed", "smp_logit_prepass",
+EXPORTS = ("smp_sample", "smp_filter_debug", "smp_sample_processed", "smp_sample_rows", "smp_logit_prepass",
            "smp_beam_topk_workspace_bytes", "smp_beam_topk", "smp_spec_verify_workspace_bytes",
-           "smp_spec_verify", "smp_spec_verify_params", "smp_spec_verify_static", "smp_status_string",
-           "smp_last_cuda_error",
-           "smp_abi_version")
+           "smp_spec_verify", "smp_spec_verify_params", "smp_spec_verify_rows", "smp_spec_verify_static",
+           "smp_status_string", "smp_last_cuda_error", "smp_abi_version")
 
 STATIC_VERIFY_SCRATCH_BYTES = 1 << 20
+
+# Kernels one verifier call launches (the position kernel, then the resolve kernel).
+VERIFY_LAUNCHES = 2
 
 _lib = None
 
@@ -61,6 +63,8 @@ def load():
     lib.smp_filter_debug.restype = i32
     lib.smp_sample_processed.argtypes = [vp, i32, i32, i32, vp, vp, vp, i32, vp, u64, u64, vp, vp, vp, vp]
     lib.smp_sample_processed.restype = i32
+    lib.smp_sample_rows.argtypes = [vp, i32, i32, i32, vp, vp, vp, i32, vp, u64, u64, u64, vp, vp, vp, vp]
+    lib.smp_sample_rows.restype = i32
     lib.smp_logit_prepass.argtypes = [vp, i32, i32, i32, vp, vp, i32, vp, vp, vp]
     lib.smp_logit_prepass.restype = i32
     lib.smp_beam_topk_workspace_bytes.argtypes = [i32, i32, i32]
@@ -74,6 +78,9 @@ def load():
     lib.smp_spec_verify_params.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, u64, u64, vp, vp, vp, vp, vp, sz,
                                            vp]
     lib.smp_spec_verify_params.restype = i32
+    lib.smp_spec_verify_rows.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, u64, u64, u64, vp, vp, vp, vp, vp,
+                                         sz, vp]
+    lib.smp_spec_verify_rows.restype = i32
     lib.smp_spec_verify_static.argtypes = [vp, vp, vp, i32, i32, i32, i32, u64, u64, vp, vp, vp, vp]
     lib.smp_spec_verify_static.restype = i32
     lib.smp_status_string.argtypes = [i32]
@@ -181,6 +188,39 @@ def sample_processed(logits, params, seed=0, offset=0, allowed=None, history=Non
     _check(lib.smp_sample_processed(_ptr(logits), batch, vocab, _dtype_code(logits), _ptr(prm), _ptr(allowed),
                                     _ptr(history), hlen, _ptr(penalty), seed, offset, _ptr(out_ids),
                                     _ptr(out_probs), _ptr(status), _stream(stream)))
+    return out_ids, out_probs, status
+
+
+def sample_rows(logits, params, seed=0, offset=0, row_base=0, allowed=None, history=None, penalty=None,
+                out_ids=None, out_probs=None, status=None, stream=None):
+    """smp_sample_rows: sample_processed for a part of a larger batch whose
+    first row has the global index row_base (the Philox counter of row b is
+    row_base + b).  The pre-pass inputs may all be None.  Returns (ids,
+    probs, status)."""
+    torch = _torch()
+    lib = load()
+    if logits.dim() != 2 or not logits.is_cuda or not logits.is_contiguous():
+        raise SmpError("logits must be a contiguous [B, V] CUDA tensor")
+    batch, vocab = logits.shape
+    dev = logits.device
+    prm = params_to_device(params, dev)
+    for t, shape in ((allowed, (batch, (vocab + 31) // 32)), (penalty, (batch,))):
+        if t is not None and (tuple(t.shape) != shape or not t.is_cuda or not t.is_contiguous()):
+            raise SmpError(f"expected a contiguous CUDA tensor of shape {shape}")
+    hlen = 0
+    if history is not None:
+        if history.dim() != 2 or history.shape[0] != batch or history.dtype != torch.int32:
+            raise SmpError("history must be an int32 [B, H] CUDA tensor")
+        hlen = int(history.shape[1])
+    out_ids = out_ids if out_ids is not None else torch.empty(batch, dtype=torch.int32, device=dev)
+    out_probs = out_probs if out_probs is not None else torch.empty(batch, dtype=torch.float32, device=dev)
+    if status is False:
+        status = None
+    elif status is None:
+        status = torch.empty(1, dtype=torch.int32, device=dev)
+    _check(lib.smp_sample_rows(_ptr(logits), batch, vocab, _dtype_code(logits), _ptr(prm), _ptr(allowed),
+                               _ptr(history), hlen, _ptr(penalty), seed, offset, int(row_base), _ptr(out_ids),
+                               _ptr(out_probs), _ptr(status), _stream(stream)))
     return out_ids, out_probs, status
 
 
@@ -292,6 +332,24 @@ def spec_verify_params(p_logits, q_logits, draft_ids, params, seed=0, offset=0, 
                                       _dtype_code(p_logits), _ptr(prm), seed, offset, _ptr(out_accepted),
                                       _ptr(out_ids), _ptr(out_alpha), _ptr(status), _ptr(workspace),
                                       workspace.numel(), _stream(stream)))
+    return out_accepted, out_ids, status
+
+
+def spec_verify_rows(p_logits, q_logits, draft_ids, params=None, seed=0, offset=0, row_base=0, workspace=None,
+                     out_accepted=None, out_ids=None, status=None, stream=None, out_alpha=None):
+    """smp_spec_verify_rows: spec_verify_params for a part of a larger batch
+    whose first row has the global index row_base.  Returns (accepted_len,
+    ids, status)."""
+    lib = load()
+    batch, k, vocab = _verify_shapes(p_logits, q_logits, draft_ids)
+    dev = p_logits.device
+    prm = params_to_device(params, dev) if params is not None else None
+    workspace, out_accepted, out_ids, status = _verify_outputs(batch, k, dev, workspace, out_accepted,
+                                                               out_ids, status)
+    _check(lib.smp_spec_verify_rows(_ptr(p_logits), _ptr(q_logits), _ptr(draft_ids), batch, k, vocab,
+                                    _dtype_code(p_logits), _ptr(prm), seed, offset, int(row_base), _ptr(out_accepted),
+                                    _ptr(out_ids), _ptr(out_alpha), _ptr(status), _ptr(workspace),
+                                    workspace.numel(), _stream(stream)))
     return out_accepted, out_ids, status
 
 

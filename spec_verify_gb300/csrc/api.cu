@@ -64,6 +64,16 @@ int forced_cluster() {
 
 bool verbose() { return getenv("SMP_VERBOSE") != nullptr; }
 
+uint64_t wait_limit_ns() {
+  const char* v = getenv("SMP_WAIT_LIMIT_NS");
+  if (v && *v) {
+    char* end = nullptr;
+    const unsigned long long n = strtoull(v, &end, 10);
+    if (end && *end == '\0') return uint64_t(n);
+  }
+  return 2000000000ull;
+}
+
 cudaError_t prepare_kernel(const void* kernel, int dev, const LaunchShape& ls) {
   static std::mutex mu;
   static std::map<std::pair<const void*, int>, std::pair<size_t, int>> done;

@@ -58,7 +58,7 @@ __device__ void general_row(GenShared& gs, const FloatPair* table, const SampleA
   const uint64_t len = ks.len;
   // The draw: the first kept token (id order) whose running mass exceeds
   // t = floor(u * Z_S), u = Philox draw 0 of row b.
-  const uint64_t u53 = uniform53(a.seed, a.offset, uint64_t(b), 0);
+  const uint64_t u53 = uniform53(a.seed, a.offset, a.row_base + uint64_t(b), 0);
   const uint64_t t = uint64_t((u128(u53) * z_kept) >> 53);
   const int tok = gen_walk<T, uint64_t>(row, V, t, gs, mass_of, xf);
   if (tid == 0) {

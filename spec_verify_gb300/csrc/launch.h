@@ -49,6 +49,12 @@ int forced_cluster();
 // printed to stderr.
 bool verbose();
 
+// Time limit, in nanoseconds, of one bounded device wait: the environment
+// variable SMP_WAIT_LIMIT_NS when it holds a number (0 gives up at the first
+// poll that finds the awaited data missing, which lets a test see the
+// expiry path on normal inputs), else 2 s.
+uint64_t wait_limit_ns();
+
 // Sets the dynamic shared memory limit and, for clusters above 8, the
 // non-portable cluster size attribute of `kernel` (once per device and size).
 cudaError_t prepare_kernel(const void* kernel, int dev, const LaunchShape& ls);

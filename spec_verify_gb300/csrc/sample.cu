@@ -68,6 +68,8 @@ struct SampleArgs {
   float* full_probs;   // debug: [B, V] p~ or NULL
   int32_t* kept;       // debug: [B] |S| or NULL
   PrepArgs prep;       // logit pre-pass (the kernel instance with kPrep only)
+  uint64_t row_base;   // global index of row 0 (the Philox counter uses row_base + row)
+  uint64_t wait_limit_ns;   // time limit of one wait for a TMA batch
 };
 
 // Candidate path: greedy, or valid knobs without top-p and with min-p or a small top-k.
@@ -113,8 +115,9 @@ __device__ __forceinline__ void tma_load(void* dst, const void* src, uint32_t by
         : "memory");
 }
 
-// Wait (every thread) for a TMA phase; false after the time limit.
-__device__ __forceinline__ bool wait_full(uint64_t* bar, uint32_t parity) {
+// Wait (every thread) for a TMA phase; false after `limit_ns` (a limit of 0
+// gives up at the first poll that finds the phase incomplete).
+__device__ __forceinline__ bool wait_full(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 0;; ++it) {
     uint32_t done;
@@ -126,7 +129,8 @@ __device__ __forceinline__ bool wait_full(uint64_t* bar, uint32_t parity) {
         : "r"(smem_addr(bar)), "r"(parity)
         : "memory");
     if (done) return true;
-    if ((it & 255u) == 255u && global_timer_ns() - t0 > kWaitLimitNs) return false;
+    if (limit_ns == 0) return false;
+    if ((it & 255u) == 255u && global_timer_ns() - t0 > limit_ns) return false;
   }
 }
 
@@ -781,7 +785,7 @@ __global__ void __launch_bounds__(kThreads, 2) sample_kernel(SampleArgs a) {
           cur.known(false);
           for (int s = 0; s < spec; ++s) {
             const uint32_t k = consumed + uint32_t(s);
-            if (!wait_full(&ss.full[k % kBufs], (k / kBufs) & 1)) {
+            if (!wait_full(&ss.full[k % kBufs], (k / kBufs) & 1, a.wait_limit_ns)) {
               ss.timeout = 1;
               break;
             }
@@ -810,7 +814,7 @@ __global__ void __launch_bounds__(kThreads, 2) sample_kernel(SampleArgs a) {
     }
     if (!greedy && tid == kThreads - 1) {
       // Row constants of the draw, off the critical path of the stream.
-      ss.u53 = uniform53(a.seed, a.offset, uint64_t(row), 0);
+      ss.u53 = uniform53(a.seed, a.offset, a.row_base + uint64_t(row), 0);
       const RowScale r0 = make_row_scale(0.0f, prm.temperature);
       ss.c_hi = r0.c_hi;
       ss.c_lo = r0.c_lo;
@@ -841,7 +845,7 @@ __global__ void __launch_bounds__(kThreads, 2) sample_kernel(SampleArgs a) {
 
     for (int bt = 0; bt < geo.nchunks; ++bt) {
       const uint32_t bi = consumed % kBufs;
-      if (!wait_full(&ss.full[bi], (consumed / kBufs) & 1)) ss.timeout = 1;
+      if (!wait_full(&ss.full[bi], (consumed / kBufs) & 1, a.wait_limit_ns)) ss.timeout = 1;
       // This warp's part of the batch.
       const uintptr_t bstart = geo.a0 + uintptr_t(bt) * kBufBytes;
       const int bvec = int(min(uintptr_t(kBufBytes), geo.a1 - bstart) / 16);
@@ -923,11 +927,13 @@ __global__ void __launch_bounds__(kThreads, 2) sample_kernel(SampleArgs a) {
       }
       if (lane == 0 && wkey) atomicMax(&ss.maxkey, wkey);
       cta_sync();   // the buffer is free
-      ++consumed;
       if (ss.timeout) {
+        // This batch's copy may still be in flight: `consumed` stays on it,
+        // so that the clean-up below waits for it too.
         alive = false;
         break;
       }
+      ++consumed;
       if (tid == 0) cur.issue(a, ring + size_t(bi) * kBufBytes, &ss.full[bi]);
     }
     if (!alive) break;
@@ -1063,10 +1069,12 @@ __global__ void __launch_bounds__(kThreads, 2) sample_kernel(SampleArgs a) {
   // row: every thread must see the same marks and count before it branches.
   cta_sync();
   if (!alive) {
-    // A wait ran out of time: let the copies in flight land, and give the
-    // rows from that one on, and the marked rows, the error result.
+    // A wait ran out of time: let the copies in flight land (with the
+    // default limit, whatever the call's: the CTA must not exit while a copy
+    // still writes its shared memory), and give the rows from that one on,
+    // and the marked rows, the error result.
     if (tid == 0)
-      for (uint32_t k = consumed; k < cur.issued; ++k) wait_full(&ss.full[k % kBufs], (k / kBufs) & 1);
+      for (uint32_t k = consumed; k < cur.issued; ++k) wait_full(&ss.full[k % kBufs], (k / kBufs) & 1, kWaitLimitNs);
     for (int r = blockIdx.x; r < B; r += gridDim.x) {
       if (r < row && load_volatile(a.out_ids + r) != kHandOff) continue;
       cta_sync();
@@ -1129,64 +1137,13 @@ static smp_status launch_sample(const SampleArgs& args, cudaStream_t stream) {
   return SMP_OK;
 }
 
-static smp_status sample_common(const void* logits, int32_t batch, int32_t vocab, smp_dtype dtype,
-                                const smp_row_params* params, uint64_t seed, uint64_t offset,
-                                int32_t* out_ids, float* out_probs, float* full, int32_t* kept,
-                                int32_t* status, void* stream) {
-  if (dtype != SMP_F32 && dtype != SMP_BF16) return SMP_ERR_DTYPE;
-  if (!logits || !params || !out_ids) return SMP_ERR_INVALID_ARG;
-  if (batch <= 0 || vocab <= 0) return SMP_ERR_INVALID_ARG;
-  if (vocab > SMP_MAX_VOCAB) return SMP_ERR_UNSUPPORTED;
-  const int elem = dtype == SMP_F32 ? 4 : 2;
-  if (reinterpret_cast<uintptr_t>(logits) % elem) return SMP_ERR_INVALID_ARG;
-  if (reinterpret_cast<uintptr_t>(params) % 4 || reinterpret_cast<uintptr_t>(out_ids) % 4)
-    return SMP_ERR_INVALID_ARG;
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  if (status) {
-    const smp_status rc = clear_status(status, st);
-    if (rc != SMP_OK) return rc;
-  }
-  SampleArgs a{};
-  a.logits = logits;
-  a.batch = batch;
-  a.vocab = vocab;
-  a.params = params;
-  a.seed = seed;
-  a.offset = offset;
-  a.out_ids = out_ids;
-  a.out_probs = out_probs;
-  a.status = status;
-  a.full_probs = full;
-  a.kept = kept;
-  if (dtype == SMP_F32) return launch_sample<float>(a, st);
-  return launch_sample<uint16_t>(a, st);
-}
-
-}  // namespace smp
-
-extern "C" smp_status smp_sample(const void* logits, int32_t batch, int32_t vocab, smp_dtype dtype,
-                                 const smp_row_params* params, uint64_t seed, uint64_t offset,
-                                 int32_t* out_ids, float* out_probs, int32_t* status, void* stream) {
-  return smp::sample_common(logits, batch, vocab, dtype, params, seed, offset, out_ids, out_probs,
-                            nullptr, nullptr, status, stream);
-}
-
-extern "C" smp_status smp_filter_debug(const void* logits, int32_t batch, int32_t vocab,
-                                       smp_dtype dtype, const smp_row_params* params, uint64_t seed,
-                                       uint64_t offset, int32_t* out_ids, float* out_probs,
-                                       float* out_probs_full, int32_t* out_kept, int32_t* status,
-                                       void* stream) {
-  if (!out_probs_full || !out_kept) return SMP_ERR_INVALID_ARG;
-  return smp::sample_common(logits, batch, vocab, dtype, params, seed, offset, out_ids, out_probs,
-                            out_probs_full, out_kept, status, stream);
-}
-
-extern "C" smp_status smp_sample_processed(const void* logits, int32_t batch, int32_t vocab, smp_dtype dtype,
-                                           const smp_row_params* params, const uint32_t* allowed,
-                                           const int32_t* history, int32_t history_len,
-                                           const float* repetition_penalty, uint64_t seed, uint64_t offset,
-                                           int32_t* out_ids, float* out_probs, int32_t* status, void* stream) {
-  using namespace smp;
+// Every sampler entry point: argument checks, then the status clear and the
+// kernel instance (with the logit pre-pass when any of its inputs is given).
+static smp_status sample_entry(const void* logits, int32_t batch, int32_t vocab, smp_dtype dtype,
+                               const smp_row_params* params, const uint32_t* allowed, const int32_t* history,
+                               int32_t history_len, const float* penalty, uint64_t seed, uint64_t offset,
+                               uint64_t row_base, int32_t* out_ids, float* out_probs, float* full, int32_t* kept,
+                               int32_t* status, void* stream) {
   if (dtype != SMP_F32 && dtype != SMP_BF16) return SMP_ERR_DTYPE;
   if (!logits || !params || !out_ids) return SMP_ERR_INVALID_ARG;
   if (batch <= 0 || vocab <= 0) return SMP_ERR_INVALID_ARG;
@@ -1197,7 +1154,8 @@ extern "C" smp_status smp_sample_processed(const void* logits, int32_t batch, in
   if (reinterpret_cast<uintptr_t>(logits) % elem) return SMP_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(params) | reinterpret_cast<uintptr_t>(out_ids) |
        reinterpret_cast<uintptr_t>(out_probs) | reinterpret_cast<uintptr_t>(allowed) |
-       reinterpret_cast<uintptr_t>(history) | reinterpret_cast<uintptr_t>(repetition_penalty)) % 4)
+       reinterpret_cast<uintptr_t>(history) | reinterpret_cast<uintptr_t>(penalty) |
+       reinterpret_cast<uintptr_t>(full) | reinterpret_cast<uintptr_t>(kept)) % 4)
     return SMP_ERR_INVALID_ARG;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (status) {
@@ -1211,14 +1169,56 @@ extern "C" smp_status smp_sample_processed(const void* logits, int32_t batch, in
   a.params = params;
   a.seed = seed;
   a.offset = offset;
+  a.row_base = row_base;
+  a.wait_limit_ns = wait_limit_ns();
   a.out_ids = out_ids;
   a.out_probs = out_probs;
   a.status = status;
+  a.full_probs = full;
+  a.kept = kept;
   a.prep.allowed = allowed;
   a.prep.words = (vocab + 31) / 32;
   a.prep.history = history_len > 0 ? history : nullptr;
   a.prep.hist_len = history_len;
-  a.prep.penalty = repetition_penalty;
-  if (dtype == SMP_F32) return launch_sample<float, true>(a, st);
-  return launch_sample<uint16_t, true>(a, st);
+  a.prep.penalty = penalty;
+  const bool prep = allowed || history_len > 0 || penalty;
+  if (prep) return dtype == SMP_F32 ? launch_sample<float, true>(a, st) : launch_sample<uint16_t, true>(a, st);
+  return dtype == SMP_F32 ? launch_sample<float>(a, st) : launch_sample<uint16_t>(a, st);
+}
+
+}  // namespace smp
+
+extern "C" smp_status smp_sample(const void* logits, int32_t batch, int32_t vocab, smp_dtype dtype,
+                                 const smp_row_params* params, uint64_t seed, uint64_t offset,
+                                 int32_t* out_ids, float* out_probs, int32_t* status, void* stream) {
+  return smp::sample_entry(logits, batch, vocab, dtype, params, nullptr, nullptr, 0, nullptr, seed, offset, 0,
+                           out_ids, out_probs, nullptr, nullptr, status, stream);
+}
+
+extern "C" smp_status smp_filter_debug(const void* logits, int32_t batch, int32_t vocab,
+                                       smp_dtype dtype, const smp_row_params* params, uint64_t seed,
+                                       uint64_t offset, int32_t* out_ids, float* out_probs,
+                                       float* out_probs_full, int32_t* out_kept, int32_t* status,
+                                       void* stream) {
+  if (!out_probs_full || !out_kept) return SMP_ERR_INVALID_ARG;
+  return smp::sample_entry(logits, batch, vocab, dtype, params, nullptr, nullptr, 0, nullptr, seed, offset, 0,
+                           out_ids, out_probs, out_probs_full, out_kept, status, stream);
+}
+
+extern "C" smp_status smp_sample_processed(const void* logits, int32_t batch, int32_t vocab, smp_dtype dtype,
+                                           const smp_row_params* params, const uint32_t* allowed,
+                                           const int32_t* history, int32_t history_len,
+                                           const float* repetition_penalty, uint64_t seed, uint64_t offset,
+                                           int32_t* out_ids, float* out_probs, int32_t* status, void* stream) {
+  return smp::sample_entry(logits, batch, vocab, dtype, params, allowed, history, history_len, repetition_penalty,
+                           seed, offset, 0, out_ids, out_probs, nullptr, nullptr, status, stream);
+}
+
+extern "C" smp_status smp_sample_rows(const void* logits, int32_t batch, int32_t vocab, smp_dtype dtype,
+                                      const smp_row_params* params, const uint32_t* allowed, const int32_t* history,
+                                      int32_t history_len, const float* repetition_penalty, uint64_t seed,
+                                      uint64_t offset, uint64_t row_base, int32_t* out_ids, float* out_probs,
+                                      int32_t* status, void* stream) {
+  return smp::sample_entry(logits, batch, vocab, dtype, params, allowed, history, history_len, repetition_penalty,
+                           seed, offset, row_base, out_ids, out_probs, nullptr, nullptr, status, stream);
 }

@@ -56,6 +56,7 @@ struct VerifyArgs {
   PosStat* ws;
   const smp_row_params* params;   // [batch] or nullptr (T = 1 on every row)
   float* alpha;                   // [batch, k] acceptance rates, or nullptr
+  uint64_t row_base;              // global index of batch row 0 (Philox counter row)
 };
 
 // How batch row b is verified: temperature T > 0 with or without filters,
@@ -476,8 +477,9 @@ __global__ void __launch_bounds__(kResolveThreads, 2) verify_resolve_kernel(Veri
   const int rows_per_b = 2 * K + 1;
   const PosStat* st = a.ws + size_t(b) * rows_per_b;
   // The uniforms depend on nothing the position kernel writes: drawn while it runs.
-  const uint64_t u_acc = threadIdx.x < K ? uniform53(a.seed, a.offset, uint64_t(b), uint64_t(threadIdx.x)) : 0ull;
-  const uint64_t u53 = uniform53(a.seed, a.offset, uint64_t(b), uint64_t(K));
+  const uint64_t grow = a.row_base + uint64_t(b);
+  const uint64_t u_acc = threadIdx.x < K ? uniform53(a.seed, a.offset, grow, uint64_t(threadIdx.x)) : 0ull;
+  const uint64_t u53 = uniform53(a.seed, a.offset, grow, uint64_t(K));
   hw_cluster_sync();        // every CTA of the cluster has started (remote stores below)
   grid_dependency_wait();   // the position statistics come from verify_pos_kernel
   allow_dependent_launch();
@@ -794,13 +796,14 @@ extern "C" size_t smp_spec_verify_workspace_bytes(int32_t batch, int32_t k) {
   return size_t(batch) * size_t(2 * k + 1) * sizeof(smp::PosStat);
 }
 
-extern "C" smp_status smp_spec_verify_params(const void* p_logits, const void* q_logits,
-                                             const int32_t* draft_ids, int32_t batch, int32_t k,
-                                             int32_t vocab, smp_dtype dtype, const smp_row_params* params,
-                                             uint64_t seed, uint64_t offset, int32_t* out_accepted_len,
-                                             int32_t* out_ids, float* out_alpha, int32_t* status,
-                                             void* workspace, size_t workspace_bytes, void* stream) {
-  using namespace smp;
+namespace smp {
+
+// Every verifier entry point: argument checks, then the two kernels.
+static smp_status verify_entry(const void* p_logits, const void* q_logits, const int32_t* draft_ids, int32_t batch,
+                               int32_t k, int32_t vocab, smp_dtype dtype, const smp_row_params* params, uint64_t seed,
+                               uint64_t offset, uint64_t row_base, int32_t* out_accepted_len, int32_t* out_ids,
+                               float* out_alpha, int32_t* status, void* workspace, size_t workspace_bytes,
+                               void* stream) {
   if (dtype != SMP_F32 && dtype != SMP_BF16) return SMP_ERR_DTYPE;
   if (!p_logits || !q_logits || !draft_ids || !out_accepted_len || !out_ids) return SMP_ERR_INVALID_ARG;
   if (batch <= 0 || batch > (1 << 20) || k < 1 || k > SMP_MAX_DRAFT || vocab <= 0)
@@ -811,7 +814,7 @@ extern "C" smp_status smp_spec_verify_params(const void* p_logits, const void* q
     return SMP_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(draft_ids) % 4 || reinterpret_cast<uintptr_t>(out_ids) % 4 ||
       reinterpret_cast<uintptr_t>(out_accepted_len) % 4 || reinterpret_cast<uintptr_t>(params) % 4 ||
-      reinterpret_cast<uintptr_t>(out_alpha) % 4)
+      reinterpret_cast<uintptr_t>(out_alpha) % 4 || reinterpret_cast<uintptr_t>(status) % 4)
     return SMP_ERR_INVALID_ARG;
   const size_t need = smp_spec_verify_workspace_bytes(batch, k);
   if (!workspace || workspace_bytes < need || reinterpret_cast<uintptr_t>(workspace) % 8)
@@ -826,6 +829,7 @@ extern "C" smp_status smp_spec_verify_params(const void* p_logits, const void* q
   a.vocab = vocab;
   a.seed = seed;
   a.offset = offset;
+  a.row_base = row_base;
   a.accepted = out_accepted_len;
   a.ids = out_ids;
   a.status = status;
@@ -834,6 +838,28 @@ extern "C" smp_status smp_spec_verify_params(const void* p_logits, const void* q
   a.alpha = out_alpha;
   if (dtype == SMP_F32) return launch_verify<float>(a, st);
   return launch_verify<uint16_t>(a, st);
+}
+
+}  // namespace smp
+
+extern "C" smp_status smp_spec_verify_params(const void* p_logits, const void* q_logits,
+                                             const int32_t* draft_ids, int32_t batch, int32_t k,
+                                             int32_t vocab, smp_dtype dtype, const smp_row_params* params,
+                                             uint64_t seed, uint64_t offset, int32_t* out_accepted_len,
+                                             int32_t* out_ids, float* out_alpha, int32_t* status,
+                                             void* workspace, size_t workspace_bytes, void* stream) {
+  return smp::verify_entry(p_logits, q_logits, draft_ids, batch, k, vocab, dtype, params, seed, offset, 0,
+                           out_accepted_len, out_ids, out_alpha, status, workspace, workspace_bytes, stream);
+}
+
+extern "C" smp_status smp_spec_verify_rows(const void* p_logits, const void* q_logits, const int32_t* draft_ids,
+                                           int32_t batch, int32_t k, int32_t vocab, smp_dtype dtype,
+                                           const smp_row_params* params, uint64_t seed, uint64_t offset,
+                                           uint64_t row_base, int32_t* out_accepted_len, int32_t* out_ids,
+                                           float* out_alpha, int32_t* status, void* workspace,
+                                           size_t workspace_bytes, void* stream) {
+  return smp::verify_entry(p_logits, q_logits, draft_ids, batch, k, vocab, dtype, params, seed, offset, row_base,
+                           out_accepted_len, out_ids, out_alpha, status, workspace, workspace_bytes, stream);
 }
 
 extern "C" smp_status smp_spec_verify(const void* p_logits, const void* q_logits,

@@ -41,7 +41,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_version_and_strings(lib):
-    assert lib.smp_abi_version() == 2
+    assert lib.smp_abi_version() == 3
     for code in range(6):
         assert lib.smp_status_string(code).decode().startswith(binding.STATUS_NAMES[code])
 
@@ -63,6 +63,12 @@ def test_host_validation_without_gpu(lib):
     assert lib.smp_sample_processed(fake, 4, 8, 0, fake, ctypes.c_void_p(0x1002), null, 0, null, 0, 0, fake,
                                     null, null, null) == 1
     assert lib.smp_sample_processed(fake, 4, 8, 5, fake, null, null, 0, null, 0, 0, fake, null, null, null) == 2
+    # a part of a larger batch: the same checks as the pre-pass entry
+    assert lib.smp_sample_rows(null, 4, 8, 0, fake, null, null, 0, null, 0, 0, 64, fake, null, null, null) == 1
+    assert lib.smp_sample_rows(fake, 4, 8, 0, fake, null, fake, 65, null, 0, 0, 64, fake, null, null, null) == 1
+    assert lib.smp_sample_rows(fake, 4, 8, 6, fake, null, null, 0, null, 0, 0, 64, fake, null, null, null) == 2
+    assert lib.smp_sample_rows(fake, 4, 8, 0, fake, null, null, 0, null, 0, 0, 64, fake,
+                               ctypes.c_void_p(0x1002), null, null) == 1
     assert lib.smp_beam_topk_workspace_bytes(2, 4, 4) == 2 * 4 * 16 * (24 + 4 * 8)   # 16 slices at most
     assert lib.smp_beam_topk_workspace_bytes(2, 33, 4) == 0
     assert lib.smp_beam_topk_workspace_bytes(2, 4, 0) == 0
@@ -93,6 +99,10 @@ def test_host_validation_without_gpu(lib):
                                       1 << 20, null) == 2
     assert lib.smp_spec_verify_params(fake, fake, fake, 2, 4, 8, 0, null, 0, 0, fake, fake, null, null, null,
                                       1 << 20, null) == 5
+    assert lib.smp_spec_verify_rows(fake, fake, fake, 2, 17, 8, 0, null, 0, 0, 32, fake, fake, null, null, fake,
+                                    1 << 20, null) == 1
+    assert lib.smp_spec_verify_rows(fake, fake, fake, 2, 4, 8, 0, null, 0, 0, 32, fake, fake, null, null, null,
+                                    1 << 20, null) == 5
     assert lib.smp_spec_verify_workspace_bytes(0, 4) == 0
     assert lib.smp_spec_verify_workspace_bytes(2, 17) == 0
 

@@ -3,6 +3,7 @@
 import numpy as np
 import pytest
 
+from oracle import pool as opool
 from oracle import sampler as osam
 from oracle import verify as over
 from spec_verify_gb300 import binding, workloads
@@ -44,6 +45,58 @@ def test_verify_workload_parity():
     compare_verify(want, acc, ids).check()
     # both paths (rejection and bonus) are exercised by this workload
     assert any(r["accepted"] < 4 for r in want)
+
+
+def test_verify_parity_over_1e5_rows():
+    # The verify workload's 32 batch rows verified as 3125 parts of a
+    # 100,000-row batch (row bases 0, 32, 64, ...): the logits repeat, the
+    # uniforms of every part are new.  At most 1e-4 of the rows may differ,
+    # and only where the oracle's margin is inside the 1e-6 band.
+    vb = workloads.verify_workload()
+    B, K, V = vb.shape
+    drafts = oracle_drafts(vb.values("q"), vb.draft_seed, vb.draft_offset)
+    p = device_logits(vb.p, vb.dtype)
+    q = device_logits(vb.q, vb.dtype)
+    d = torch.from_numpy(drafts).cuda()
+    tiles = 3125
+    ws = torch.zeros(binding.spec_verify_workspace_bytes(B, K), dtype=torch.uint8, device="cuda")
+    acc = torch.empty(tiles, B, dtype=torch.int32, device="cuda")
+    ids = torch.empty(tiles, B, K + 1, dtype=torch.int32, device="cuda")
+    status = torch.empty(tiles, dtype=torch.int32, device="cuda")
+    for t in range(tiles):
+        binding.spec_verify_rows(p, q, d, None, vb.seed, vb.offset, row_base=t * B, workspace=ws,
+                                 out_accepted=acc[t], out_ids=ids[t], status=status[t:t + 1])
+    torch.cuda.synchronize()
+    assert int(status.abs().max().item()) == 0
+    want = opool.spec_verify_tiled(vb.values("p"), vb.values("q"), drafts, vb.seed, vb.offset,
+                                   [t * B for t in range(tiles)])
+    for r in want:
+        r["row"] = r["row_base"] + r["row"]
+    verdict = compare_verify(want, acc.view(-1).cpu().numpy(), ids.view(-1, K + 1).cpu().numpy())
+    verdict.check()
+    assert verdict.compared == tiles * B
+
+
+def test_verify_row_base_split_equals_whole():
+    vb = workloads.verify_workload(batch=24, k=3, vocab=4099, dtype="bf16", seed_id=211)
+    drafts = oracle_drafts(vb.values("q"), 1, 0)
+    p = device_logits(vb.p, vb.dtype)
+    q = device_logits(vb.q, vb.dtype)
+    d = torch.from_numpy(drafts).cuda()
+    prm = workloads.make_params(24, temperature=0.9)
+    prm["top_p"][::3] = 0.9
+    prm["greedy"][5] = 1
+    whole = binding.spec_verify_params(p, q, d, prm, 3, 4)
+    parts = [binding.spec_verify_rows(p[lo:hi].contiguous(), q[lo:hi].contiguous(), d[lo:hi].contiguous(),
+                                      prm[lo:hi], 3, 4, row_base=lo) for lo, hi in ((0, 10), (10, 24))]
+    torch.cuda.synchronize()
+    assert torch.equal(torch.cat([x[0] for x in parts]), whole[0])
+    assert torch.equal(torch.cat([x[1] for x in parts]), whole[1])
+    want = over.spec_verify(vb.values("p")[10:], vb.values("q")[10:], drafts[10:], 3, 4, params=prm[10:],
+                            row_base=10)
+    for r in want:
+        r["row"] += 10
+    compare_verify(want, whole[0].cpu().numpy(), whole[1].cpu().numpy()).check()
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])

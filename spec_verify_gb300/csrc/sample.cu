@@ -115,9 +115,21 @@ __device__ __forceinline__ void tma_load(void* dst, const void* src, uint32_t by
         : "memory");
 }
 
-// Wait (every thread) for a TMA phase; false after `limit_ns` (a limit of 0
-// gives up at the first poll that finds the phase incomplete).
+// Wait (every thread) for a TMA phase; false after `limit_ns`.  A limit of
+// 0 tests the phase once without waiting (mbarrier.try_wait may suspend the
+// thread until the phase completes, so it is not used for that test).
 __device__ __forceinline__ bool wait_full(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  if (limit_ns == 0) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+  }
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 0;; ++it) {
     uint32_t done;
@@ -129,7 +141,6 @@ __device__ __forceinline__ bool wait_full(uint64_t* bar, uint32_t parity, uint64
         : "r"(smem_addr(bar)), "r"(parity)
         : "memory");
     if (done) return true;
-    if (limit_ns == 0) return false;
     if ((it & 255u) == 255u && global_timer_ns() - t0 > limit_ns) return false;
   }
 }

@@ -20,6 +20,7 @@
 #include <cuda_runtime.h>
 
 #include <climits>
+#include <stdlib.h>
 #include <mutex>
 #include <type_traits>
 
@@ -57,6 +58,7 @@ struct VerifyArgs {
   const smp_row_params* params;   // [batch] or nullptr (T = 1 on every row)
   float* alpha;                   // [batch, k] acceptance rates, or nullptr
   uint64_t row_base;              // global index of batch row 0 (Philox counter row)
+  int exact_accept;               // decide every accept test on exact Z (tests of that path)
 };
 
 // How batch row b is verified: temperature T > 0 with or without filters,
@@ -93,6 +95,10 @@ __device__ __forceinline__ const T* logit_row(const VerifyArgs& a, int b, int j)
 }
 
 constexpr int kPosUnroll = 16;   // 16-byte loads in flight per thread in verify_pos_kernel
+// ex2.approx.ftz.f32: largest relative error 1.46e-7, measured on GB300 over
+// every binary32 input in [-126, 1] whose result is normal; with a margin:
+constexpr double kEx2Err = 1.7e-7;
+constexpr double kArgErr = 0.6931471805599453 * 0x1p-23;   // per unit |y|: y = (z - m) c rounded twice
 constexpr uintptr_t kPosPrefetchChunk = 32768;        // one L2 prefetch request
 constexpr uintptr_t kPosPrefetchBytes = 256 * 1024;   // most of a row prefetched before the wait
 
@@ -460,7 +466,12 @@ __device__ __forceinline__ uint64_t fixed52(float r) {
 // draw, and warp 0 of its CTA walks it.
 template <typename T, bool kParams>
 __global__ void __launch_bounds__(kResolveThreads, 2) verify_resolve_kernel(VerifyArgs a) {
-  __shared__ int32_t decision[2];   // first rejection j, row flags
+  __shared__ int32_t decision[3];   // first rejection j, row flags, an undecided test
+  __shared__ uint64_t ez_zp[SMP_MAX_DRAFT], ez_zq[SMP_MAX_DRAFT];   // exact Z of retested positions
+  __shared__ int ez_have[SMP_MAX_DRAFT];
+  __shared__ uint64_t ez_wq[kResolveWarps];
+  __shared__ uint64_t ez_slots[2][kResolveMaxCluster];
+  __shared__ FloatPair table[64];   // 2^(j/64) for the exact retest's exponentials
   __shared__ float inv_z[2];        // 2^F / Z of the drawn row's p and q (binary32)
   __shared__ float row_m[2];        // the drawn row's p and q maxima
   __shared__ uint32_t kept_desc[4]; // the drawn row's p and q kept sets (key, id) when filtered
@@ -484,6 +495,7 @@ __global__ void __launch_bounds__(kResolveThreads, 2) verify_resolve_kernel(Veri
   grid_dependency_wait();   // the position statistics come from verify_pos_kernel
   allow_dependent_launch();
   const RowMode md = row_mode<kParams>(a, b);
+  if (tid < 64) table[tid] = kExp2Table[tid];
 
   // Greedy verification (and error rows): lane i compares draft i with the
   // target's arg-max of position i; the first mismatch j emits the arg-max of
@@ -511,61 +523,135 @@ __global__ void __launch_bounds__(kResolveThreads, 2) verify_resolve_kernel(Veri
     return;
   }
 
+  // Thread g of the cluster owns ids [c0, c1): a whole number of 16-byte
+  // groups of the row (rows whose base is not 16-byte aligned fall back to
+  // element loads).
+  constexpr int kPer = 16 / int(sizeof(T));
+  const int nthreads = int(nranks) * kResolveThreads;
+  const int per = (V + nthreads - 1) / nthreads;
+  const int chunk = (per + kPer - 1) / kPer * kPer;
+  const int g = int(rank) * kResolveThreads + tid;
+  const int c0 = min(V, g * chunk), c1 = min(V, c0 + chunk);
+
+  // Worst-case relative error of the position kernel's Z (unfiltered rows):
+  // every exponential is ex2.approx (largest relative error 1.46e-7, measured
+  // over every binary32 input in [-126, 1] on GB300; kEx2Err with a margin),
+  // applied once per element, once per rescaling of a thread's running sum
+  // (at most one per group of kPosUnroll vectors, plus one for the row's
+  // edges) and once to scale the thread's sum to the row maximum; the
+  // rounding of each argument y = (z - m) log2(e) / T, relative to y, whose
+  // mean |y| under the row's distribution is at most log2(V) (it equals the
+  // entropy H(p) minus log2 Z, Z >= 1), twice for the shifts to new maxima;
+  // the binary32 sums (a tree over a group, then one addition per group and
+  // one product per rescaling).
+  const int groups = (V * int(sizeof(T)) / 16 + kThreads * kPosUnroll - 1) / (kThreads * kPosUnroll) + 1;
+  const float z_err = md.filtered ? 0.0f
+                                  : float(groups + 2) * float(kEx2Err) + 2.0f * float(kArgErr) * log2f(float(V)) +
+                                        float(2 * groups + 9) * 0x1p-24f + 1e-10f;
+
   // Accept tests u_i < p_i(x) / max(q_i(x), 1e-300), one lane per position
   // (K <= 32), as the product form u_i * max(q, 1e-300) < p with
   // p = ex_p / (Z_p 2^-F), q = ex_q / (Z_q 2^-F); the first failing position
-  // is the rejection.  Every CTA of the cluster decides alike.
+  // is the rejection.  A test whose two sides are closer than the error of
+  // the fast Z allows is decided again on Z recomputed exactly (double-float
+  // exponentials summed as integers over the cluster).  Every CTA of the
+  // cluster decides alike.
+  PosStat P{}, Q{};
   if (tid < 32) {
-    // Lane i holds the statistics of p row i (i <= K) and q row i (i < K):
-    // all the rows' flags, its accept test, and, for the drawn row, the
-    // maxima and reciprocals the draw needs.
-    const int i = tid;
-    PosStat P{}, Q{};
-    if (i <= K) P = st[i];
-    if (i < K) Q = st[K + 1 + i];
-    int fl = (i <= K ? P.flags : 0) | (i < K ? Q.flags : 0);
-    for (int o = 16; o; o >>= 1) fl |= __shfl_xor_sync(0xFFFFFFFFu, fl, o);
-    bool reject = false;
-    if (!fl && i < K) {
-      const double zp = double(P.z) * (1.0 / double(kFixedOne));
-      const double zq = double(Q.z) * (1.0 / double(kFixedOne));
-      const double u = double(u_acc) * 0x1p-53;
-      // u * max(ex_q / zq, 1e-300) < ex_p / zp, multiplied through by zp * zq > 0
-      const double lhs = Q.ex > 0.0 ? u * Q.ex * zp : u * 1e-300 * zp * zq;
-      reject = !(lhs < P.ex * zq);
-    }
-    const uint32_t rej = __ballot_sync(0xFFFFFFFFu, reject);
-    const int jr = rej ? __ffs(rej) - 1 : K;
-    if (tid == 0) {
-      decision[0] = jr;
-      decision[1] = fl;
-    }
-    // The reciprocals of the drawn row's Z, once, in binary32 (within an ulp
-    // of 2^F / Z; FP64 is slow on this part).
-    if (i == jr && !fl) {
-      row_m[0] = P.m;
-      inv_z[0] = __fdiv_rn(float(kFixedOne), __ull2float_rn(P.z));
-      row_m[1] = jr < K ? Q.m : P.m;
-      inv_z[1] = jr < K ? __fdiv_rn(float(kFixedOne), __ull2float_rn(Q.z)) : inv_z[0];
-      kept_desc[0] = P.kkey;
-      kept_desc[1] = P.kid;
-      kept_desc[2] = jr < K ? Q.kkey : P.kkey;
-      kept_desc[3] = jr < K ? Q.kid : P.kid;
-    }
-    if constexpr (kParams) {
-      if (a.alpha && i < K && !fl) {
-        AlphaShared& as = alpha_shared();
-        as.m[0][i] = P.m;
-        as.m[1][i] = Q.m;
-        as.inv_z[0][i] = __fdiv_rn(float(kFixedOne), __ull2float_rn(P.z));
-        as.inv_z[1][i] = __fdiv_rn(float(kFixedOne), __ull2float_rn(Q.z));
-        as.kept[0][i] = P.kkey;
-        as.kept[1][i] = P.kid;
-        as.kept[2][i] = Q.kkey;
-        as.kept[3][i] = Q.kid;
-        as.cta[i] = 0;
+    if (tid <= K) P = st[tid];
+    if (tid < K) Q = st[K + 1 + tid];
+    if (tid < K) ez_have[tid] = 0;
+  }
+  for (int iter = 0; iter <= K; ++iter) {
+    if (tid < 32) {
+      const int i = tid;
+      int fl = (i <= K ? P.flags : 0) | (i < K ? Q.flags : 0);
+      for (int o = 16; o; o >>= 1) fl |= __shfl_xor_sync(0xFFFFFFFFu, fl, o);
+      bool reject = false, unsure = false;
+      if (!fl && i < K) {
+        const bool exact = ez_have[i] != 0;
+        const double zp = double(exact ? ez_zp[i] : P.z) * (1.0 / double(kFixedOne));
+        const double zq = double(exact ? ez_zq[i] : Q.z) * (1.0 / double(kFixedOne));
+        const double u = double(u_acc) * 0x1p-53;
+        // u * max(ex_q / zq, 1e-300) < ex_p / zp, multiplied through by zp * zq > 0
+        const double lhs = Q.ex > 0.0 ? u * Q.ex * zp : u * 1e-300 * zp * zq;
+        const double rhs = P.ex * zq;
+        reject = !(lhs < rhs);
+        unsure = !exact && (a.exact_accept || fabs(lhs - rhs) <= double(2.0f * z_err + 1e-12f) * fmax(lhs, rhs));
+      }
+      const uint32_t hit = __ballot_sync(0xFFFFFFFFu, reject || unsure);
+      const int jr = hit ? __ffs(hit) - 1 : K;
+      const bool jr_unsure = __shfl_sync(0xFFFFFFFFu, unsure ? 1 : 0, jr < 32 ? jr : 0) != 0;
+      const bool undecided = !fl && jr < K && jr_unsure;
+      if (tid == 0) {
+        decision[0] = jr;
+        decision[1] = fl;
+        decision[2] = undecided ? 1 : 0;
+      }
+      if (!undecided) {
+        // For the drawn row, the maxima and reciprocals of Z the draw needs,
+        // once, in binary32 (within an ulp of 2^F / Z; FP64 is slow on this
+        // part); the acceptance rates' per-position state.
+        if (i == jr && !fl) {
+          row_m[0] = P.m;
+          inv_z[0] = __fdiv_rn(float(kFixedOne), __ull2float_rn(P.z));
+          row_m[1] = jr < K ? Q.m : P.m;
+          inv_z[1] = jr < K ? __fdiv_rn(float(kFixedOne), __ull2float_rn(Q.z)) : inv_z[0];
+          kept_desc[0] = P.kkey;
+          kept_desc[1] = P.kid;
+          kept_desc[2] = jr < K ? Q.kkey : P.kkey;
+          kept_desc[3] = jr < K ? Q.kid : P.kid;
+        }
+        if constexpr (kParams) {
+          if (a.alpha && i < K && !fl) {
+            AlphaShared& as = alpha_shared();
+            as.m[0][i] = P.m;
+            as.m[1][i] = Q.m;
+            as.inv_z[0][i] = __fdiv_rn(float(kFixedOne), __ull2float_rn(P.z));
+            as.inv_z[1][i] = __fdiv_rn(float(kFixedOne), __ull2float_rn(Q.z));
+            as.kept[0][i] = P.kkey;
+            as.kept[1][i] = P.kid;
+            as.kept[2][i] = Q.kkey;
+            as.kept[3][i] = Q.kid;
+            as.cta[i] = 0;
+          }
+        }
       }
     }
+    __syncthreads();
+    if (!decision[2]) break;
+    // Exact Z of the undecided position's p and q rows.
+    const int pos = decision[0];
+    const RowScale sp = make_row_scale(st[pos].m, md.temperature);
+    const RowScale sq = make_row_scale(st[K + 1 + pos].m, md.temperature);
+    const T* pr = logit_row<T>(a, b, pos);
+    const T* qr = logit_row<T>(a, b, K + 1 + pos);
+    uint64_t ep = 0, eq = 0;
+    for (int i = c0; i < c1; ++i) {
+      ep += mass_fixed(Elem<T>::widen(pr[i]), sp, table);
+      eq += mass_fixed(Elem<T>::widen(qr[i]), sq, table);
+    }
+    uint64_t tp = 0, tq = 0, cta_p = 0, cta_q = 0;
+    ep = warp_sum<uint64_t>(ep);
+    eq = warp_sum<uint64_t>(eq);
+    if ((tid & 31) == 0) {
+      warp_tot[tid >> 5] = ep;
+      ez_wq[tid >> 5] = eq;
+    }
+    __syncthreads();
+    for (int w = 0; w < kResolveWarps; ++w) {
+      cta_p += warp_tot[w];
+      cta_q += ez_wq[w];
+    }
+    __syncthreads();
+    cluster_prefix(cta_p, ez_slots[0], cta_bc, &tp);
+    cluster_prefix(cta_q, ez_slots[1], cta_bc, &tq);
+    if (tid == 0) {
+      ez_zp[pos] = tp;
+      ez_zq[pos] = tq;
+      ez_have[pos] = 1;
+    }
+    __syncthreads();
   }
   __syncthreads();
   const int jrej = decision[0];
@@ -586,15 +672,6 @@ __global__ void __launch_bounds__(kResolveThreads, 2) verify_resolve_kernel(Veri
   const T* qrow = residual ? logit_row<T>(a, b, K + 1 + jrej) : prow;
   const RowScale rp = make_row_scale(row_m[0], md.temperature);
   const RowScale rq = make_row_scale(row_m[1], md.temperature);
-  // Thread g owns ids [c0, c1): a whole number of 16-byte groups of the row
-  // (rows whose base is not 16-byte aligned fall back to element loads).
-  constexpr int kPer = 16 / int(sizeof(T));
-  const int nthreads = int(nranks) * kResolveThreads;
-  const int per = (V + nthreads - 1) / nthreads;
-  const int chunk = (per + kPer - 1) / kPer * kPer;
-  const int g = int(rank) * kResolveThreads + tid;
-  const int c0 = min(V, g * chunk), c1 = min(V, c0 + chunk);
-
   // Weights in fixed point with 52 fraction bits: max(0, p - q) with
   // p = e_p / Z_p and q = e_q / Z_q in binary32 (eq. 39.4), or e_p / Z_p for a
   // draw from p.  r * 2^52 is the binary32 r exactly for r >= 2^-28 (below,
@@ -830,6 +907,7 @@ static smp_status verify_entry(const void* p_logits, const void* q_logits, const
   a.seed = seed;
   a.offset = offset;
   a.row_base = row_base;
+  a.exact_accept = getenv("SMP_VERIFY_EXACT_ACCEPT") != nullptr;
   a.accepted = out_accepted_len;
   a.ids = out_ids;
   a.status = status;

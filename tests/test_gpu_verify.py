@@ -172,3 +172,21 @@ def test_verify_results_do_not_depend_on_cluster_size(monkeypatch):
         assert np.array_equal(ids, outs[0][1])
     want = over.spec_verify(vb.values("p"), vb.values("q"), drafts, 4, 9)
     compare_verify(want, outs[0][0], outs[0][1]).check()
+
+
+def test_exact_accept_retest_gives_the_same_results(monkeypatch):
+    # An accept test whose two sides lie within the fast Z's error bound is
+    # decided again on Z recomputed exactly; SMP_VERIFY_EXACT_ACCEPT sends
+    # every test down that path.  Both paths must give the oracle's results,
+    # and the same ones wherever the fast path was certain (everywhere here).
+    for dtype, k, vocab, seed_id in (("f32", 4, 32000, 17), ("bf16", 3, 4099, 18)):
+        vb = workloads.verify_workload(batch=16, k=k, vocab=vocab, dtype=dtype, seed_id=seed_id)
+        drafts = oracle_drafts(vb.values("q"), 1, 0)
+        fast = run_verify(vb.p, vb.q, dtype, drafts, 2, 5)
+        monkeypatch.setenv("SMP_VERIFY_EXACT_ACCEPT", "1")
+        exact = run_verify(vb.p, vb.q, dtype, drafts, 2, 5)
+        monkeypatch.delenv("SMP_VERIFY_EXACT_ACCEPT")
+        assert fast[2] == exact[2] == 0
+        assert np.array_equal(fast[0], exact[0]) and np.array_equal(fast[1], exact[1])
+        want = over.spec_verify(vb.values("p"), vb.values("q"), drafts, 2, 5)
+        compare_verify(want, exact[0], exact[1]).check()

@@ -56,7 +56,7 @@ DTYPE = "bf16 logits; exp in double-float (pairs of binary32); u64 fixed-point m
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 PROFILE_JSON = os.path.join(ROOT, "profiles", "sample_kernel_large_vocab.json")
-KERNEL_SOURCES = ["common.cuh", "row_ops.cuh", "select.cuh", "general.cuh", "sample.cu", "exp_table.h", "tma.cuh"]
+KERNEL_SOURCES = ["common.cuh", "row_ops.cuh", "select.cuh", "general.cuh", "sample.cu", "exp_table.h", "tma.cuh", "general_bf16.cuh"]
 MIN_REPLAYS = 10
 
 

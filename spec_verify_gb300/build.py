@@ -22,7 +22,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libsmp.so")
 
 SOURCES = ["api.cu", "sample.cu", "verify.cu", "prepass.cu", "beam.cu"]
-HEADERS = ["common.cuh", "row_ops.cuh", "select.cuh", "general.cuh", "launch.h", "exp_table.h", "tma.cuh"]
+HEADERS = ["common.cuh", "row_ops.cuh", "select.cuh", "general.cuh", "launch.h", "exp_table.h", "tma.cuh", "general_bf16.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]

@@ -109,6 +109,7 @@ __device__ __forceinline__ void write_error_row(const SampleArgs& a, int b, int 
 // ------------------------------------------------------------------ general path
 
 #include "general.cuh"
+#include "general_bf16.cuh"
 
 // ------------------------------------------------------------------ logit pre-pass
 //
@@ -1063,9 +1064,14 @@ __global__ void __launch_bounds__(kThreads, 2) sample_kernel(SampleArgs a) {
       const float rr = a.prep.penalty ? a.prep.penalty[r] : 1.0f;
       build_prep(prep_shared(), a.prep, r, Vn, rr != 1.0f);
       const uint32_t* mr = a.prep.allowed ? a.prep.allowed + size_t(r) * a.prep.words : nullptr;
-      general_row<T>(gen, table, a, r, prm, LogitPrep<T>{mr, &prep_shared(), rr});
+      const LogitPrep<T> xf{mr, &prep_shared(), rr};
+      bool done = false;
+      if constexpr (sizeof(T) == 2) done = key_table_row(*reinterpret_cast<KeyTable*>(ring), table, a, r, prm, xf);
+      if (!done) general_row<T>(gen, table, a, r, prm, xf);
     } else {
-      general_row<T>(gen, table, a, r, prm);
+      bool done = false;
+      if constexpr (sizeof(T) == 2) done = key_table_row(*reinterpret_cast<KeyTable*>(ring), table, a, r, prm);
+      if (!done) general_row<T>(gen, table, a, r, prm);
     }
   }
 }

@@ -191,24 +191,36 @@ __device__ __forceinline__ void kt_list(KeyTable& kt, uint32_t h, uint32_t id) {
 // The first position where the running count (kMass false: reaches `need`)
 // or the running mass (kMass true: reaches the top-p target) is reached, in
 // every thread, with the count and mass before it.  Each thread covers `spt`
-// consecutive positions; (pc, pw) are its exclusive prefixes over the CTA.
+// <= 32 consecutive positions; (pc, pw) are its exclusive prefixes over the
+// CTA.  The thread whose run holds the crossing hands it to warp 0, whose
+// lanes take one position each.
 template <bool kMass>
 __device__ __forceinline__ int kt_locate(KeyTable& kt, int npos, int spt, uint32_t pc, uint64_t pw, uint32_t tc,
                                          uint64_t tw, uint32_t need, const MassTarget& target, uint32_t sp_count,
                                          uint64_t sp_mass, uint32_t* c_before, uint64_t* w_before) {
   const int tid = threadIdx.x;
-  if (tid == 0) kt.bc32[4] = 0xFFFFFFFFu;
+  if (tid == 0) {
+    kt.bc32[4] = 0xFFFFFFFFu;
+    kt.bc32[6] = 0xFFFFFFFFu;
+  }
   cta_sync();
   const bool reach_end = kMass ? (target.trivial || mass_reaches(pw + tw, target)) : (pc + tc >= need);
   const bool reach_start = kMass ? (target.trivial || mass_reaches(pw, target)) : (pc >= need);
   if (reach_end && !reach_start && tc + tw > 0) {   // exactly one thread
-    uint32_t c = pc;
-    uint64_t w = pw;
-    const int gp = kt.npb * 128;
-    for (int p = tid * spt; p < min(npos, (tid + 1) * spt); ++p) {
-      uint32_t pcnt;
-      uint64_t pm;
-      if (p == gp) {
+    kt.bc32[4] = uint32_t(tid);
+    kt.bc32[5] = pc;
+    kt.bc64[0] = pw;
+  }
+  cta_sync();
+  const uint32_t owner = kt.bc32[4];
+  if (tid < 32 && owner != 0xFFFFFFFFu) {
+    const int lane = tid;
+    const int p = int(owner) * spt + lane;
+    const bool valid = lane < spt && p < npos;
+    uint32_t pcnt = 0;
+    uint64_t pm = 0;
+    if (valid) {
+      if (p == kt.npb * 128) {
         pcnt = sp_count;
         pm = sp_mass;
       } else {
@@ -216,23 +228,41 @@ __device__ __forceinline__ int kt_locate(KeyTable& kt, int npos, int spt, uint32
         pcnt = kt.cnt[s];
         pm = uint64_t(pcnt) * kt.mass[s];
       }
-      const bool hit = kMass ? (pcnt > 0 && (target.trivial || mass_reaches(w + pm, target))) : (c + pcnt >= need);
-      if (hit) {
-        kt.bc32[4] = uint32_t(p);
-        kt.bc32[5] = c;
-        kt.bc64[0] = w;
-        break;
-      }
-      c += pcnt;
-      w += pm;
+    }
+    const uint32_t cb = kt.bc32[5] + warp_inclusive_scan<uint32_t>(pcnt) - pcnt;
+    const uint64_t wb = kt.bc64[0] + warp_inclusive_scan<uint64_t>(pm) - pm;
+    const bool hit =
+        valid && (kMass ? (pcnt > 0 && (target.trivial || mass_reaches(wb + pm, target))) : (cb + pcnt >= need));
+    const uint32_t bal = __ballot_sync(0xFFFFFFFFu, hit);
+    if (bal && lane == __ffs(bal) - 1) {
+      kt.bc32[6] = uint32_t(p);
+      kt.bc32[7] = cb;
+      kt.bc64[1] = wb;
     }
   }
   cta_sync();
-  const int pos = int(kt.bc32[4]);
-  *c_before = kt.bc32[5];
-  *w_before = kt.bc64[0];
+  const int pos = int(kt.bc32[6]);
+  *c_before = kt.bc32[7];
+  *w_before = kt.bc64[1];
   cta_sync();
   return pos;
+}
+
+// The smallest n in [1, cnt] with ((w + n e) << sh) >= rhs, or cnt: a float
+// estimate of the quotient, corrected by exact products (n < 2^31).
+__device__ __forceinline__ uint32_t kt_tokens_to_reach(uint64_t w, uint64_t e, uint32_t cnt, const MassTarget& t) {
+  if (t.trivial || e == 0) return 1;
+  const u128 have = u128(w) << t.sh;
+  if (t.rhs <= have) return 1;
+  const u128 need = t.rhs - have;
+  const u128 step = u128(e) << t.sh;
+  auto to_f = [](u128 x) { return __fmaf_rn(kt_u64_to_f(uint64_t(x >> 64)), 0x1p64f, kt_u64_to_f(uint64_t(x))); };
+  float qf = ceilf(__fdiv_rn(to_f(need), to_f(step)));
+  qf = fminf(fmaxf(qf, 1.0f), float(cnt));
+  uint32_t q = uint32_t(qf);
+  while (q < cnt && u128(q) * step < need) ++q;
+  while (q > 1 && u128(q - 1) * step >= need) --q;
+  return q;
 }
 
 // One row of the general path (see the top of this file).  Returns false,
@@ -385,8 +415,18 @@ __device__ bool key_table_row(KeyTable& kt, const FloatPair* table, const Sample
   const RowScale rs = make_row_scale(m, prm.temperature);
   const int nslots = (kt.npb + kt.nnb) * 128;
   const uint32_t sp_n = kt.sp_n;
-  for (int s = tid; s < nslots; s += kThreads)
-    kt.mass[s] = kt.cnt[s] ? mass_fixed(__uint_as_float(kt_bits_of_slot(kt, s) << 16), rs, table) : 0ull;
+  // (two slots per thread and step: two independent exponentials in flight)
+  for (int s0 = tid; s0 < nslots; s0 += 2 * kThreads) {
+    const int s1 = min(s0 + kThreads, nslots - 1);
+    const uint32_t c0 = kt.cnt[s0], c1 = kt.cnt[s1];
+    uint64_t e0 = 0, e1 = 0;
+    if (c0 | c1) {
+      e0 = mass_fixed(__uint_as_float(kt_bits_of_slot(kt, s0) << 16), rs, table);
+      e1 = mass_fixed(__uint_as_float(kt_bits_of_slot(kt, s1) << 16), rs, table);
+    }
+    kt.mass[s0] = c0 ? e0 : 0ull;
+    if (s0 + kThreads < nslots) kt.mass[s1] = c1 ? e1 : 0ull;
+  }
   for (int s = kKtSlots + tid; s < kKtAll; s += kThreads) kt.mass[s] = 0;
   // the listed tokens: E, and their rank in id order
   uint64_t spe = 0;
@@ -518,7 +558,7 @@ __device__ bool key_table_row(KeyTable& kt, const FloatPair* table, const Sample
       uint64_t wb;
       const int pos = kt_locate<false>(kt, npos, spt, pc, pw, tc, tw, uint32_t(prm.top_k), none, sp_n, sp_mass, &cb,
                                        &wb);
-      if (!boundary(pos, cb, wb, uint32_t(prm.top_k) - cb)) return false;
+      if (pos < 0 || !boundary(pos, cb, wb, uint32_t(prm.top_k) - cb)) return false;
     }
   }
   if (topp) {
@@ -526,22 +566,11 @@ __device__ bool key_table_row(KeyTable& kt, const FloatPair* table, const Sample
     uint32_t cb;
     uint64_t wb;
     const int pos = kt_locate<true>(kt, npos, spt, pc, pw, tc, tw, 0, target, sp_n, sp_mass, &cb, &wb);
-    if (pos == gp) return false;
+    if (pos < 0 || pos == gp) return false;
     const int s = kt_slot_of_pos(kt, pos);
     // the crossing inside the value's tokens: the smallest n >= 1 with
     // (mass before + n E) * 2^sh >= top_p * Z (all of them at most)
-    const uint64_t e = kt.mass[s];
-    uint32_t n = 1;
-    if (!target.trivial && e > 0) {
-      const u128 have = u128(wb) << target.sh;
-      if (target.rhs > have) {
-        const u128 need = target.rhs - have;
-        const u128 step = u128(e) << target.sh;
-        const u128 q = (need + step - 1) / step;
-        n = q > u128(kt.cnt[s]) ? kt.cnt[s] : uint32_t(q);
-        if (n == 0) n = 1;
-      }
-    }
+    const uint32_t n = kt_tokens_to_reach(wb, kt.mass[s], kt.cnt[s], target);
     if (uint64_t(cb) + n < len) boundary(pos, cb, wb, n);
   }
   const bool gap_kept = pos_cut > gp && sp_n > 0;   // the listed tokens are kept (all or none)

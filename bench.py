@@ -619,6 +619,42 @@ def run_gpu(args):
     return 0
 
 
+def run_case(args):
+    """One sampler workload by plain calls (no graph), for profilers: W
+    untimed calls, then K calls timed together with CUDA events; prints one
+    JSON line with the per-call time."""
+    import numpy as np
+    import torch
+    from spec_verify_gb300 import binding, workloads
+    binding.load()
+    gb = workloads.sampler_workload(args.case)
+    B, V = gb.data.shape
+    if gb.dtype == "bf16":
+        x = torch.from_numpy(gb.data.view(np.int16)).view(torch.bfloat16).cuda()
+    else:
+        x = torch.from_numpy(gb.data).cuda()
+    prm = binding.params_to_device(gb.params, x.device)
+    ids = torch.empty(B, dtype=torch.int32, device=x.device)
+    probs = torch.empty(B, dtype=torch.float32, device=x.device)
+    status = torch.empty(1, dtype=torch.int32, device=x.device)
+    for i in range(args.warmup):
+        binding.sample_rows(x, prm, gb.seed, i, 0, out_ids=ids, out_probs=probs, status=status)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(args.steps):
+        binding.sample_rows(x, prm, gb.seed, args.warmup + i, 0, out_ids=ids, out_probs=probs, status=status)
+    e1.record()
+    torch.cuda.synchronize()
+    if int(status.cpu()[0]) != 0:
+        raise SystemExit(f"status {int(status.cpu()[0])}")
+    print(json.dumps({"case": args.case, "batch": B, "vocab": V, "dtype": gb.dtype, "calls": args.steps,
+                      "us_per_call": 1000.0 * e0.elapsed_time(e1) / args.steps,
+                      "l2": "one input copy, reused by every call"}))
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -628,6 +664,8 @@ def main():
     ap.add_argument("--impl", choices=["smp", "reference"], default="smp")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--case", choices=["basic", "mixed", "large_vocab", "flat_nucleus"],
+                    help="only time plain sampler calls on this workload (for profilers)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -635,6 +673,8 @@ def main():
         ap.error("--gpus must be at least 1")
     if args.impl == "reference":
         return run_reference(args)
+    if args.case:
+        return run_case(args)
     return run_gpu(args)
 
 

@@ -360,7 +360,10 @@ __device__ bool key_table_row(KeyTable& kt, const FloatPair* table, const Sample
     if constexpr (kRaw) {
       // pairs of bf16 values; fill vectors past the row count in counters
       // outside the window
-      uint32_t seen = 0;   // OR of the offsets: bit 15 when a listed binade occurred
+      // every offset of the round first, then the atomics: an atomic may not
+      // pass a later table load (the compiler cannot tell them apart), so
+      // interleaving them would serialise two shared-memory latencies per pair
+      uint32_t off[kKtU1 * 8];
 #pragma unroll
       for (int u = 0; u < kKtU1; ++u) {
         vmax2 = Vo::max2(vmax2, Vo::vmax(x[u]));
@@ -368,12 +371,15 @@ __device__ bool key_table_row(KeyTable& kt, const FloatPair* table, const Sample
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const uint32_t w = w4[k];
-          const uint32_t o0 = kt.lut[(w >> 7) & 0x1FFu] + ((w & 0x7Fu) << 2);
-          const uint32_t o1 = kt.lut[w >> 23] + ((w >> 14) & 0x1FCu);
-          atomicAdd(reinterpret_cast<uint32_t*>(cntb + o0), 1u);
-          atomicAdd(reinterpret_cast<uint32_t*>(cntb + o1), 1u);
-          seen |= o0 | o1;
+          off[u * 8 + 2 * k] = kt.lut[(w >> 7) & 0x1FFu] + ((w & 0x7Fu) << 2);
+          off[u * 8 + 2 * k + 1] = kt.lut[w >> 23] + ((w >> 14) & 0x1FCu);
         }
+      }
+      uint32_t seen = 0;   // OR of the offsets: bit 15 when a listed binade occurred
+#pragma unroll
+      for (int j = 0; j < kKtU1 * 8; ++j) {
+        atomicAdd(reinterpret_cast<uint32_t*>(cntb + off[j]), 1u);
+        seen |= off[j];
       }
       if (seen & kKtGapOff) {   // rare: list this round's small magnitudes
         for (int u = 0; u < kKtU1; ++u) {
@@ -591,7 +597,8 @@ __device__ bool key_table_row(KeyTable& kt, const FloatPair* table, const Sample
   cta_sync();
 
   // ---------------- pass 2: the draw, in token-id order
-  // t = floor(u Z_S), u = Philox draw 0 of the row; a token is kept when its
+  // t = floor(u Z_S), u = Philox draw 0 of the row; the token is the first
+  // kept one (id order) whose running mass passes t; a token is kept when its
   // value comes before the boundary, or is the boundary value and it is among
   // the first n_cut such tokens.  Rounds of kThreads * kKtU2 vectors, thread t
   // its kKtU2 consecutive ones; per round each thread's kept mass (the
@@ -623,31 +630,43 @@ __device__ bool key_table_row(KeyTable& kt, const FloatPair* table, const Sample
     if (kt_listed_binade(kt, h)) return listed_mass(id);
     return mass_at(kt.lut[h >> 7] + ((h & 0x7Fu) << 3));
   };
+  // The walk runs from whichever end of the row is nearer the draw.  Walking
+  // backwards is the forward walk over the reversed ids with
+  // t_b = Z_S - 1 - t: the token is the first (reversed) whose running mass
+  // passes t_b, and of the boundary value's tokens the last n_cut (id order)
+  // are kept.  kept(r): boundary tokens kept among the first r in walk order.
+  const bool bwd = t >= z_kept - t;
+  const uint64_t t_walk = bwd ? z_kept - 1 - t : t;
+  const uint32_t cnt_cut = pos_cut < npos ? kt.cnt[kt_slot_of_pos(kt, pos_cut)] : 0u;
+  const uint32_t skip = cnt_cut - n_cut;
+  auto kept = [&](uint32_t r) -> uint32_t { return bwd ? (r > skip ? r - skip : 0u) : min(r, n_cut); };
   // walking: the running mass r and boundary count rc over one token
   auto step = [&](uint64_t ent, uint64_t& r, uint32_t& rc) {
     if (ent == kKtCutMark) {
-      r += rc < n_cut ? e_cut : 0ull;
+      r += kept(rc + 1) > kept(rc) ? e_cut : 0ull;
       ++rc;
     } else {
       r += ent;
     }
   };
-  uint64_t run = 0;      // kept mass before this round
+  // the row's edges in walk order (ids before and after the aligned middle)
+  auto walk_edge = [&](bool first, uint64_t& r, uint32_t& rc) -> int {
+    const bool lead = first != bwd;   // the head walked forwards, or the tail backwards
+    const int n = lead ? head : V - tail0;
+    for (int j = 0; j < n; ++j) {
+      const int i = lead ? (bwd ? head - 1 - j : j) : (bwd ? V - 1 - j : tail0 + j);
+      step(entry(edge_pattern(i), uint32_t(i)), r, rc);
+      if (r > t_walk) return i;
+    }
+    return -1;
+  };
+  uint64_t run = 0;      // kept mass before this round (walk order)
   uint32_t run_cut = 0;  // boundary tokens before this round
   int tok = -1;
-  if (tid == 0) kt.bc32[4] = 0xFFFFFFFFu;
-  // the edges first (ids before the aligned middle), by thread 0, then the
-  // middle's rounds, then the ids after it
   if (tid == 0) {
     uint64_t r = 0;
     uint32_t rc = 0;
-    for (int i = 0; i < head; ++i) {
-      step(entry(edge_pattern(i), uint32_t(i)), r, rc);
-      if (r > t) {
-        kt.bc32[4] = uint32_t(i);
-        break;
-      }
-    }
+    kt.bc32[4] = uint32_t(walk_edge(true, r, rc));
     kt.bc64[2] = r;
     kt.bc32[5] = rc;
   }
@@ -656,12 +675,14 @@ __device__ bool key_table_row(KeyTable& kt, const FloatPair* table, const Sample
   run = kt.bc64[2];
   run_cut = kt.bc32[5];
   const int warp = tid >> 5, lane = tid & 31;
-  for (int base = 0, rnd = 0; tok < 0 && base < nvec; base += kThreads * kKtU2, rnd ^= 1) {
-    const int v0 = base + tid * kKtU2;
+  constexpr int kRound = kThreads * kKtU2;
+  for (int base = 0, rnd = 0; tok < 0 && base < nvec; base += kRound, rnd ^= 1) {
+    // this thread's kKtU2 vectors: the tid-th chunk of the round in walk order
+    const int v0 = bwd ? nvec - base - (tid + 1) * kKtU2 : base + tid * kKtU2;
     uint4 xv[kKtU2];
 #pragma unroll
     for (int u = 0; u < kKtU2; ++u)
-      xv[u] = v0 + u < nvec ? __ldg(vp + v0 + u) : make_uint4(kKtFill, kKtFill, kKtFill, kKtFill);
+      xv[u] = v0 + u >= 0 && v0 + u < nvec ? __ldg(vp + v0 + u) : make_uint4(kKtFill, kKtFill, kKtFill, kKtFill);
     uint64_t se = 0;
     if constexpr (kRaw) {
 #pragma unroll
@@ -678,7 +699,7 @@ __device__ bool key_table_row(KeyTable& kt, const FloatPair* table, const Sample
     } else {
 #pragma unroll
       for (int u = 0; u < kKtU2; ++u)
-        if (v0 + u < nvec) {
+        if (v0 + u >= 0 && v0 + u < nvec) {
           const uint32_t id0 = uint32_t(head + (v0 + u) * kPer);
 #pragma unroll
           for (int q = 0; q < kPer; ++q) {
@@ -687,8 +708,9 @@ __device__ bool key_table_row(KeyTable& kt, const FloatPair* table, const Sample
           }
         }
     }
-    if (nsp > 0 && v0 < nvec) {   // the listed tokens among this thread's ids
-      const uint32_t lo = uint32_t(head + v0 * kPer), hi = uint32_t(head + min(v0 + kKtU2, nvec) * kPer);
+    const int va = max(v0, 0), vb = min(v0 + kKtU2, nvec);
+    if (nsp > 0 && va < vb) {   // the listed tokens among this thread's ids
+      const uint32_t lo = uint32_t(head + va * kPer), hi = uint32_t(head + vb * kPer);
       se += kt.gpre[listed_below(hi)] - kt.gpre[listed_below(lo)];
     }
     const uint32_t sc = uint32_t(se >> 56);
@@ -714,33 +736,37 @@ __device__ bool key_table_row(KeyTable& kt, const FloatPair* table, const Sample
       tot_c += wc;
       tot_e += we;
     }
-    const uint64_t round_mass = tot_e + uint64_t(min(run_cut + tot_c, n_cut) - min(run_cut, n_cut)) * e_cut;
-    if (run + round_mass > t) {   // the draw falls in this round (every thread alike)
+    const uint64_t round_mass = tot_e + uint64_t(kept(run_cut + tot_c) - kept(run_cut)) * e_cut;
+    if (run + round_mass > t_walk) {   // the draw falls in this round (every thread alike)
       // kept boundary tokens before this thread and in it
       const uint32_t cut_before = run_cut + bc;
-      const uint32_t keep_before = min(cut_before, n_cut);
-      const uint32_t keep_mine = min(cut_before + sc, n_cut) - keep_before;
-      const uint64_t before = run + be + uint64_t(keep_before - min(run_cut, n_cut)) * e_cut;
-      const uint64_t mine = se + uint64_t(keep_mine) * e_cut;
-      const uint32_t hit = __ballot_sync(0xFFFFFFFFu, mine > 0 && before <= t && t - before < mine);
-      if (hit) {   // this warp walks the crossing thread's ids: lane l the l-th pair
+      const uint64_t before = run + be + uint64_t(kept(cut_before) - kept(run_cut)) * e_cut;
+      const uint64_t mine = se + uint64_t(kept(cut_before + sc) - kept(cut_before)) * e_cut;
+      const uint32_t hit = __ballot_sync(0xFFFFFFFFu, mine > 0 && before <= t_walk && t_walk - before < mine);
+      if (hit) {
+        // this warp walks the crossing thread's ids: lane l the l-th pair in
+        // walk order (backwards: the pairs from the last, high id first)
         const int src = __ffs(hit) - 1;
         const int cv0 = __shfl_sync(0xFFFFFFFFu, v0, src);
         const uint64_t cb = shfl_u64(before, src);
         const uint32_t ccut = __shfl_sync(0xFFFFFFFFu, cut_before, src);
-        const int v = cv0 + (lane >> 2);
-        const uint32_t w = v < nvec ? __ldg(reinterpret_cast<const uint32_t*>(vp + v) + (lane & 3)) : kKtFill;
-        const uint32_t id0 = uint32_t(head + v * kPer + 2 * (lane & 3));
-        const uint64_t e0 = v < nvec ? entry(transform(w & 0xFFFFu, id0), id0) : 0ull;
-        const uint64_t e1 = v < nvec ? entry(transform(w >> 16, id0 + 1), id0 + 1) : 0ull;
+        const int pr = bwd ? 31 - lane : lane;
+        const int v = cv0 + (pr >> 2);
+        const bool valid = v >= 0 && v < nvec;
+        const uint32_t w = valid ? __ldg(reinterpret_cast<const uint32_t*>(vp + v) + (pr & 3)) : kKtFill;
+        const uint32_t id_lo = uint32_t(head + v * kPer + 2 * (pr & 3));
+        const uint32_t id0 = bwd ? id_lo + 1 : id_lo, id1 = bwd ? id_lo : id_lo + 1;
+        const uint32_t h0 = bwd ? (w >> 16) : (w & 0xFFFFu), h1 = bwd ? (w & 0xFFFFu) : (w >> 16);
+        const uint64_t e0 = valid ? entry(transform(h0, id0), id0) : 0ull;
+        const uint64_t e1 = valid ? entry(transform(h1, id1), id1) : 0ull;
         const uint32_t c0 = e0 == kKtCutMark, c1 = e1 == kKtCutMark;
         const uint32_t rank0 = ccut + warp_inclusive_scan<uint32_t>(c0 + c1) - (c0 + c1);
-        const uint64_t m0 = c0 ? (rank0 < n_cut ? e_cut : 0ull) : e0;
-        const uint64_t m1 = c1 ? (rank0 + c0 < n_cut ? e_cut : 0ull) : e1;
+        const uint64_t m0 = c0 ? (kept(rank0 + 1) > kept(rank0) ? e_cut : 0ull) : e0;
+        const uint64_t m1 = c1 ? (kept(rank0 + c0 + 1) > kept(rank0 + c0) ? e_cut : 0ull) : e1;
         const uint64_t r0 = cb + warp_inclusive_scan<uint64_t>(m0 + m1) - m1;
         const uint64_t r1 = r0 + m1;
-        const uint32_t found = __ballot_sync(0xFFFFFFFFu, r1 > t);
-        if (found && lane == __ffs(found) - 1) kt.bc32[4] = r0 > t ? id0 : id0 + 1;
+        const uint32_t found = __ballot_sync(0xFFFFFFFFu, r1 > t_walk);
+        if (found && lane == __ffs(found) - 1) kt.bc32[4] = r0 > t_walk ? id0 : id1;
       }
       cta_sync();
       tok = int(kt.bc32[4]);
@@ -752,13 +778,7 @@ __device__ bool key_table_row(KeyTable& kt, const FloatPair* table, const Sample
   if (tok < 0 && tid == 0) {
     uint64_t r = run;
     uint32_t rc = run_cut;
-    for (int i = tail0; i < V; ++i) {
-      step(entry(edge_pattern(i), uint32_t(i)), r, rc);
-      if (r > t) {
-        kt.bc32[4] = uint32_t(i);
-        break;
-      }
-    }
+    kt.bc32[4] = uint32_t(walk_edge(false, r, rc));
   }
   cta_sync();
   tok = int(kt.bc32[4]);

@@ -306,16 +306,16 @@ __device__ bool key_table_row(KeyTable& kt, const FloatPair* table, const Sample
   };
 
   // ---------------- pass 1: the maximum and the per-value counts
-  for (int i = tid; i < kKtAll; i += kThreads) kt.cnt[i] = 0;
-  if (tid == 0) kt.sp_n = 0;
   // the first round's vectors (coalesced: thread t takes t + 256 u) give the
-  // window's anchor
+  // window's anchor; the counters are cleared while they load
   uint4 x[kKtU1];
 #pragma unroll
   for (int u = 0; u < kKtU1; ++u) {
     const int v = tid + u * kThreads;
     x[u] = v < nvec ? __ldg(vp + v) : make_uint4(kKtFill, kKtFill, kKtFill, kKtFill);
   }
+  for (int i = tid; i < kKtAll; i += kThreads) kt.cnt[i] = 0;
+  if (tid == 0) kt.sp_n = 0;
   uint32_t he = kKtFill & 0xFFFFu;   // this thread's edge element (ids before and after the aligned middle)
   int ie = -1;
   if (tid < 16 && tid < head) ie = tid;
@@ -421,17 +421,20 @@ __device__ bool key_table_row(KeyTable& kt, const FloatPair* table, const Sample
   const RowScale rs = make_row_scale(m, prm.temperature);
   const int nslots = (kt.npb + kt.nnb) * 128;
   const uint32_t sp_n = kt.sp_n;
-  // (two slots per thread and step: two independent exponentials in flight)
-  for (int s0 = tid; s0 < nslots; s0 += 2 * kThreads) {
-    const int s1 = min(s0 + kThreads, nslots - 1);
-    const uint32_t c0 = kt.cnt[s0], c1 = kt.cnt[s1];
-    uint64_t e0 = 0, e1 = 0;
-    if (c0 | c1) {
-      e0 = mass_fixed(__uint_as_float(kt_bits_of_slot(kt, s0) << 16), rs, table);
-      e1 = mass_fixed(__uint_as_float(kt_bits_of_slot(kt, s1) << 16), rs, table);
+  // (four slots per thread and step: four independent exponentials in flight)
+  for (int s0 = tid; s0 < nslots; s0 += 4 * kThreads) {
+    uint32_t c[4];
+    uint64_t e[4] = {0, 0, 0, 0};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) c[j] = s0 + j * kThreads < nslots ? kt.cnt[s0 + j * kThreads] : 0u;
+    if (c[0] | c[1] | c[2] | c[3]) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        e[j] = mass_fixed(__uint_as_float(kt_bits_of_slot(kt, min(s0 + j * kThreads, nslots - 1)) << 16), rs, table);
     }
-    kt.mass[s0] = c0 ? e0 : 0ull;
-    if (s0 + kThreads < nslots) kt.mass[s1] = c1 ? e1 : 0ull;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (s0 + j * kThreads < nslots) kt.mass[s0 + j * kThreads] = c[j] ? e[j] : 0ull;
   }
   for (int s = kKtSlots + tid; s < kKtAll; s += kThreads) kt.mass[s] = 0;
   // the listed tokens: E, and their rank in id order
@@ -443,35 +446,57 @@ __device__ bool key_table_row(KeyTable& kt, const FloatPair* table, const Sample
     spe = mass_fixed(key_value<uint16_t>(uint32_t(ent >> 32)), rs, table);
     for (uint32_t j = 0; j < sp_n; ++j) sp_rank += uint32_t(kt.sparse[j]) < sp_id ? 1u : 0u;
   }
-  uint64_t sp_mass;
-  (void)gen_scan<uint64_t>(spe, reinterpret_cast<uint64_t*>(kt.scan64[0]), &sp_mass);
-  // (gen_scan's barriers: every read of the list is done)
+  cta_sync();   // the masses are in place
+  // per-thread runs of positions, their counts and masses (the list's
+  // position apart), and the list's masses: one CTA scan of the three
+  const int gp = kt.npb * 128;
+  const int npos = nslots + 1;
+  const int spt = (npos + kThreads - 1) / kThreads;
+  const int p_lo = tid * spt, p_hi = min(npos, (tid + 1) * spt);
+  uint32_t tc = 0;
+  uint64_t tw = 0;
+#pragma unroll 4
+  for (int p = p_lo; p < p_hi; ++p) {
+    if (p != gp) {
+      const int sl = kt_slot_of_pos(kt, p);
+      const uint32_t c = kt.cnt[sl];
+      tc += c;
+      tw += uint64_t(c) * kt.mass[sl];
+    }
+  }
+  const bool own_gp = gp >= p_lo && gp < p_hi;
+  if (own_gp) tc += sp_n;
+  const uint32_t ic = warp_inclusive_scan<uint32_t>(tc);
+  const uint64_t iw = warp_inclusive_scan<uint64_t>(tw);
+  const uint64_t is = warp_inclusive_scan<uint64_t>(spe);
+  if ((tid & 31) == 31) {
+    kt.scan32[0][tid >> 5] = ic;
+    kt.scan64[0][tid >> 5] = iw;
+    kt.scan64[1][tid >> 5] = is;
+  }
+  cta_sync();   // (also: every read of the unsorted list is done)
+  uint32_t pc = ic - tc, total_c = 0;
+  uint64_t pw = iw - tw, z_total = 0, sp_mass = 0;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    if (w < (tid >> 5)) {
+      pc += kt.scan32[0][w];
+      pw += kt.scan64[0][w];
+    }
+    total_c += kt.scan32[0][w];
+    z_total += kt.scan64[0][w];
+    sp_mass += kt.scan64[1][w];
+  }
+  // the list's mass sits at position gp
+  if (own_gp) tw += sp_mass;
+  if (p_lo > gp) pw += sp_mass;
+  z_total += sp_mass;
   if (tid < int(sp_n)) {
     kt.gid[sp_rank] = sp_id;
     kt.gpre[sp_rank + 1] = spe;   // prefix sums below, once the masses are in place
   }
-  // per-thread runs of positions, their counts and masses, scanned
-  const int gp = kt.npb * 128;
-  const int npos = nslots + 1;
-  const int spt = (npos + kThreads - 1) / kThreads;
-  uint32_t tc = 0;
-  uint64_t tw = 0;
-  for (int p = tid * spt; p < min(npos, (tid + 1) * spt); ++p) {
-    if (p == gp) {
-      tc += sp_n;
-      tw += sp_mass;
-    } else {
-      const int s = kt_slot_of_pos(kt, p);
-      const uint32_t c = kt.cnt[s];
-      tc += c;
-      tw += uint64_t(c) * kt.mass[s];
-    }
-  }
-  uint32_t total_c;
-  uint64_t z_total;
-  const uint32_t pc = gen_scan<uint32_t>(tc, kt.scan32[0], &total_c);
-  const uint64_t pw = gen_scan<uint64_t>(tw, reinterpret_cast<uint64_t*>(kt.scan64[0]), &z_total);
-  // (barriers above: the sorted masses are in place) the list's prefix sums, by warp 0
+  cta_sync();
+  // the list's prefix sums, by warp 0
   if (tid < 32) {
     constexpr int kPerLane = kKtSparse / 32;
     uint64_t v[kPerLane], sum = 0;

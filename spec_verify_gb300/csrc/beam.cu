@@ -130,11 +130,57 @@ __global__ void __launch_bounds__(kThreads, 2) beam_row_kernel(BeamArgs a) {
     return;
   }
 
-  // The slice maximum (as an order key), then Z = sum exp(z - m) in binary32
-  // per thread, turned into 44-bit fixed point once per thread and summed
-  // exactly.
-  uint32_t kmine = 0;   // this thread's maximum key
-  gen_sweep_wide<T, kBeamU>(row, len, [&](int, float z) { kmine = max(kmine, order_key<T>(z)); });
+  // One pass for the slice maximum and Z = sum exp(z - m): each thread keeps
+  // a running maximum tm and the binary32 sum st of exp(z - tm) over its
+  // elements, rescaled when a group of kBeamU vectors raises tm; its share,
+  // scaled to the slice maximum, is turned into 44-bit fixed point once and
+  // summed exactly.  NaN counts as -inf (the packed maxima skip it, and its
+  // exponential is 0).
+  using Vo = VecOps<T>;
+  constexpr int kPer = Vo::kPer;
+  const RowScale unit = make_row_scale_unit(0.0f);
+  float tm = -INFINITY, st = 0.0f;
+  auto raise_to = [&](float g) {   // g > tm
+    st = tm > -INFINITY ? __fmul_rn(st, exp_fast(tm, RowScale{g, unit.c_hi, unit.c_lo})) : 0.0f;
+    tm = g;
+  };
+  {
+    const uintptr_t r0 = reinterpret_cast<uintptr_t>(row);
+    const uintptr_t a0 = (r0 + 15) & ~uintptr_t(15), a1 = (r0 + size_t(len) * sizeof(T)) & ~uintptr_t(15);
+    const bool mid = a1 > a0;
+    const int head = mid ? int((a0 - r0) / sizeof(T)) : len;
+    const int tail0 = mid ? int((a1 - r0) / sizeof(T)) : len;
+    const int nvec = mid ? int((a1 - a0) / 16) : 0;
+    const uint4* vp = reinterpret_cast<const uint4*>(a0);
+    const uint32_t ninf = Vo::neg_inf();
+    for (int v0 = tid; v0 < nvec; v0 += kThreads * kBeamU) {
+      uint4 x[kBeamU];
+      uint32_t pm = ninf;
+#pragma unroll
+      for (int u = 0; u < kBeamU; ++u) {
+        x[u] = v0 + u * kThreads < nvec ? __ldg(vp + v0 + u * kThreads) : make_uint4(ninf, ninf, ninf, ninf);
+        pm = Vo::max2(pm, Vo::vmax(x[u]));
+      }
+      const float gmx = Vo::finish(pm);
+      if (gmx > tm) raise_to(gmx);
+      if (tm > -INFINITY) {
+        const RowScale rt{tm, unit.c_hi, unit.c_lo};
+        float acc = 0.0f;
+#pragma unroll
+        for (int u = 0; u < kBeamU; ++u)
+#pragma unroll
+          for (int q = 0; q < kPer; ++q) acc += exp_fast(Vo::elem(x[u], q), rt);
+        st += acc;
+      }
+    }
+    auto edge = [&](float z) {
+      if (z > tm) raise_to(z);
+      if (tm > -INFINITY) st += exp_fast(z, RowScale{tm, unit.c_hi, unit.c_lo});
+    };
+    for (int i = tid; i < head; i += kThreads) edge(Elem<T>::widen(row[i]));
+    for (int i = tail0 + tid; i < len; i += kThreads) edge(Elem<T>::widen(row[i]));
+  }
+  const uint32_t kmine = order_key<T>(tm);   // this thread's maximum key
   const uint32_t kmax = uint32_t(block_max_u64(uint64_t(kmine), gs.red64));
   if (!key_finite<T>(kmax)) {   // all -inf / NaN, or +inf present
     if (tid == 0) {
@@ -148,9 +194,8 @@ __global__ void __launch_bounds__(kThreads, 2) beam_row_kernel(BeamArgs a) {
   }
   const float m = key_value<T>(kmax);
   const RowScale rs = make_row_scale_unit(m);
-  float st = 0.0f;
-  gen_sweep_wide<T, kBeamU>(row, len, [&](int, float z) { st += exp_fast(z, rs); });
-  uint64_t zf = __float2ull_rn(__fmul_rn(st, float(kFixedOne)));
+  const float share = tm > -INFINITY ? __fmul_rn(st, exp_fast(tm, rs)) : 0.0f;
+  uint64_t zf = __float2ull_rn(__fmul_rn(share, float(kFixedOne)));
   zf = warp_sum<uint64_t>(zf);
   if ((tid & 31) == 0) gs.scan64[tid >> 5] = zf;
 
@@ -159,20 +204,51 @@ __global__ void __launch_bounds__(kThreads, 2) beam_row_kernel(BeamArgs a) {
   // it, so every one of the best `width` does.  The elements >= theta are
   // listed and ranked exactly; if there are too many (many equal logits),
   // the exact radix selection of the sampler finds the boundary instead.
-  uint32_t* tkeys = &gs.cnt[0][0];   // kThreads thread maxima
-  tkeys[tid] = kmine;
+  // theta = the kw-th largest of the threads' maxima (a multiset): each warp
+  // lists its kw largest lane maxima by repeated warp maxima, then warp 0 takes
+  // the kw-th largest of the warps' lists the same way.  Real keys are above 0.
+  const int kw = min(a.width, len);
+  const int lane = tid & 31, warp = tid >> 5;
+  uint32_t* wtop = &gs.cnt[0][0];   // kWarps * kw keys
+  {
+    bool in = true;
+    for (int r = 0; r < kw; ++r) {
+      const uint32_t mx = __reduce_max_sync(0xFFFFFFFFu, in ? kmine : 0u);
+      const uint32_t who = __ballot_sync(0xFFFFFFFFu, in && kmine == mx);
+      if (lane == __ffs(who) - 1) in = false;
+      if (lane == 0) wtop[warp * kw + r] = mx;
+    }
+  }
   cta_sync();
   uint64_t ztot = 0;
 #pragma unroll
   for (int w = 0; w < kWarps; ++w) ztot += gs.scan64[w];
-  const int kw = min(a.width, len);
-  {
-    int rank = 0;   // threads ordered by (key desc, thread asc)
-    for (int j = 0; j < kThreads; ++j) {
-      const uint32_t o = tkeys[j];
-      rank += o > kmine || (o == kmine && j < tid);
+  if (warp == 0) {
+    constexpr int kPerLane = kWarps * SMP_MAX_BEAM_WIDTH / 32;
+    const int total = kWarps * kw;
+    uint32_t v[kPerLane];
+    uint32_t act = 0;   // bit j: v[j] still in the multiset
+#pragma unroll
+    for (int j = 0; j < kPerLane; ++j) {
+      const int idx = lane + 32 * j;
+      v[j] = idx < total ? wtop[idx] : 0u;
+      act |= (idx < total ? 1u : 0u) << j;
     }
-    if (rank == kw - 1) gs.bc32[0] = kmine;
+    uint32_t kth = 0;
+    for (int r = 0; r < kw; ++r) {
+      uint32_t lm = 0;
+      int lj = -1;
+#pragma unroll
+      for (int j = 0; j < kPerLane; ++j)
+        if (((act >> j) & 1u) && (lj < 0 || v[j] > lm)) {
+          lm = v[j];
+          lj = j;
+        }
+      kth = __reduce_max_sync(0xFFFFFFFFu, lj >= 0 ? lm : 0u);
+      const uint32_t who = __ballot_sync(0xFFFFFFFFu, lj >= 0 && lm == kth);
+      if (lane == __ffs(who) - 1) act &= ~(1u << lj);
+    }
+    if (lane == 0) gs.bc32[0] = kth;
   }
   cta_sync();
   const uint32_t theta = gs.bc32[0];
@@ -306,20 +382,34 @@ __global__ void __launch_bounds__(kThreads) beam_merge_kernel(BeamArgs a) {
       cf[c] = b * V + l[j].id;
     }
   }
+  // The scores as order keys in place (the fp64 bits with the sign folded
+  // in, -0 as +0), so that the rank loop compares integers: fp64 comparisons
+  // run on the narrow fp64 pipe of this part.
+  auto to_key = [](double x) -> unsigned long long {
+    const unsigned long long b = (unsigned long long)__double_as_longlong(x == 0.0 ? 0.0 : x);
+    return (b >> 63) ? ~b : (b | 0x8000000000000000ull);
+  };
+  auto from_key = [](unsigned long long k) -> double {
+    return __longlong_as_double((long long)((k >> 63) ? (k & 0x7FFFFFFFFFFFFFFFull) : ~k));
+  };
+  unsigned long long* ck = reinterpret_cast<unsigned long long*>(cs);
+  __syncthreads();
+  for (int c = tid; c < n; c += kThreads) ck[c] = to_key(cs[c]);
   __syncthreads();
   for (int c = tid; c < n; c += kThreads) {
     const int f = cf[c];
     if (f < 0) continue;
-    const double sc = cs[c];
+    const unsigned long long kc = ck[c];
     int rank = 0;
     for (int d = 0; d < n && rank < width; ++d) {
       const int fd = cf[d];
-      rank += fd >= 0 && (cs[d] > sc || (cs[d] == sc && fd < f));
+      const unsigned long long kd = ck[d];
+      rank += fd >= 0 && (kd > kc || (kd == kc && fd < f));
     }
     if (rank < width) {
       a.out_parent[size_t(g) * width + rank] = f / V;
       a.out_token[size_t(g) * width + rank] = f % V;
-      a.out_score[size_t(g) * width + rank] = sc;
+      a.out_score[size_t(g) * width + rank] = from_key(kc);
     }
   }
 }

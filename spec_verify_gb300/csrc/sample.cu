@@ -807,7 +807,6 @@ __global__ void __launch_bounds__(kThreads, 2) sample_kernel(SampleArgs a) {
 
     for (int bt = 0; bt < geo.nchunks; ++bt) {
       const uint32_t bi = consumed % kBufs;
-      if (!wait_full(&ss.full[bi], (consumed / kBufs) & 1, a.wait_limit_ns)) ss.timeout = 1;
       // This warp's part of the batch.
       const uintptr_t bstart = geo.a0 + uintptr_t(bt) * kBufBytes;
       const int bvec = int(min(uintptr_t(kBufBytes), geo.a1 - bstart) / 16);
@@ -815,6 +814,17 @@ __global__ void __launch_bounds__(kThreads, 2) sample_kernel(SampleArgs a) {
       const uint4* vec = reinterpret_cast<const uint4*>(ring + size_t(bi) * kBufBytes) + v0;
       const T* part = reinterpret_cast<const T*>(vec);
       const uint32_t id0 = id_base + uint32_t(bt) * (kBufBytes / sizeof(T)) + uint32_t(v0 * kPer);
+      // The mask bits of the lane's unit, requested before the wait for the
+      // batch so that their latency overlaps it.
+      uint32_t mw0 = 0xFFFFFFFFu, mw1 = 0xFFFFFFFFu;
+      if constexpr (kPrep) {
+        if (mrow && lane * kVecPerLane < nvec) {
+          const uint32_t uid0 = id0 + uint32_t(lane * kVecPerLane * kPer);
+          mw0 = allowed_bits32(mrow, a.prep.words, uid0);
+          if (kVecPerLane * kPer > 32 && int(uid0) + 32 < Vn) mw1 = allowed_bits32(mrow, a.prep.words, uid0 + 32);
+        }
+      }
+      if (!wait_full(&ss.full[bi], (consumed / kBufs) & 1, a.wait_limit_ns)) ss.timeout = 1;
       // The lane's batch maximum: one packed maximum over its unit, the
       // kVecPerLane consecutive vectors (one 128-byte line) from lane *
       // kVecPerLane, read in the order j ^ (lane % 8) so that the 32 lanes of
@@ -840,15 +850,9 @@ __global__ void __launch_bounds__(kThreads, 2) sample_kernel(SampleArgs a) {
         }
         // The mask on the lane's unit, in place in the ring (only this lane
         // reads it), when its mask bits are not all set.
-        if (mrow && lane * kVecPerLane < nvec) {
-          const uint32_t uid0 = id0 + uint32_t(lane * kVecPerLane * kPer);
-          const uint32_t w0 = allowed_bits32(mrow, a.prep.words, uid0);
-          const uint32_t w1 = (kVecPerLane * kPer > 32 && int(uid0) + 32 < Vn)
-                                  ? allowed_bits32(mrow, a.prep.words, uid0 + 32) : 0xFFFFFFFFu;
-          if ((w0 & w1) != 0xFFFFFFFFu)
-            prep_unit<T>(const_cast<uint4*>(vec) + lane * kVecPerLane, min(kVecPerLane, nvec - lane * kVecPerLane),
-                         lane & (kVecPerLane - 1), uid0, w0, w1, false, prep_r);
-        }
+        if (mrow && lane * kVecPerLane < nvec && (mw0 & mw1) != 0xFFFFFFFFu)
+          prep_unit<T>(const_cast<uint4*>(vec) + lane * kVecPerLane, min(kVecPerLane, nvec - lane * kVecPerLane),
+                       lane & (kVecPerLane - 1), id0 + uint32_t(lane * kVecPerLane * kPer), mw0, mw1, false, prep_r);
       }
 #pragma unroll
       for (int j = 0; j < kVecPerLane; ++j) {

@@ -52,7 +52,10 @@ WORKLOAD_DESC = ("large_vocab: B=256, V=128256, bf16 logits log(Zipf s=1.1) over
                  "permutation + N(0, 0.5^2); rows b%4 in {0,1}: min_p=0.1 T=1, b%4==2: greedy, "
                  "b%4==3: T=0.7 top_k=40; Philox seed 0")
 VERIFY_DESC = "verify: B=32, K=4, V=32000, fp32; q = G[:, :4], p = G + N(0,1), G ~ N(0, 2^2)"
-DTYPE = "bf16 logits; exp in double-float (pairs of binary32); u64 fixed-point masses, exact integer sums"
+# The path's arithmetic: binary32 (exponentials as double-float pairs of
+# binary32, comparisons); masses are summed as exact u64 integers.
+DTYPE = "f32"
+ARITHMETIC = "bf16 logits; exp in double-float (pairs of binary32); u64 fixed-point masses, exact integer sums"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 PROFILE_JSON = os.path.join(ROOT, "profiles", "sample_kernel_large_vocab.json")
@@ -590,6 +593,7 @@ def run_gpu(args):
                              f"and {v_copies} verify copies; L2 {l2 / 1e6:.0f} MB",
                        "timing": (f"K steps captured in one CUDA graph, replayed {replays} times, CUDA events on "
                                   f"the launching stream; median replay (best beside it)"),
+                       "arithmetic": ARITHMETIC,
                        "parallelism": (f"dp{world}: a batch of {world} x {B} rows split by rows, rank r at row base "
                                        f"{B} r (no collective)")},
             "ms_per_step_best": step_best / 1000.0,

@@ -124,7 +124,7 @@ __device__ __forceinline__ void write_error_row(const SampleArgs& a, int b, int 
 
 // A row's distinct history ids, sorted, and one bit per unit of 64 ids that
 // holds one of them (most ids skip the search on that bit).
-struct PrepShared {
+struct __align__(16) PrepShared {
   int32_t raw[kMaxHistory];
   int32_t first[kMaxHistory];   // 1 at the first occurrence of a valid id
   int32_t ids[kMaxHistory];
@@ -223,59 +223,75 @@ __device__ __forceinline__ int hist_lower_bound(const PrepShared& ps, int id) {
   return lo;
 }
 
-// The pre-pass on nv vectors of one unit (in place, shared or local memory),
-// the first at token uid0, visited in the order j ^ swz (the ring's bank
-// swizzle).  The history ids inside the unit are found by two binary
-// searches; each vector then checks those few ids.  Out of line: most units
-// need nothing, and the streaming loop keeps its code small.
+// The constraint mask on one vector: each 32-bit word becomes
+// (word & keep) | (-inf & ~keep), keep expanding the vector's mask bits
+// (bit q: element q allowed) to its elements.
 template <typename T>
-__device__ __noinline__ void prep_unit(uint4* v, int nv, int swz, uint32_t uid0, uint32_t w0, uint32_t w1, bool hist,
-                                       float r) {
-  using Vo = VecOps<T>;
-  constexpr int kPer = Vo::kPer;
-  constexpr uint32_t kFull = (1u << kPer) - 1u;
-  const PrepShared& ps = prep_shared();
-  const UnitPrep up{w0, w1, hist};
-  int h0 = 0, h1 = 0;
-  if (hist) {
-    h0 = hist_lower_bound(ps, int(uid0));
-    h1 = hist_lower_bound(ps, int(uid0) + nv * kPer);
+__device__ __forceinline__ uint4 mask_vec(const uint4& x, uint32_t bits) {
+  uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    uint32_t keep;
+    if (sizeof(T) == 2)
+      keep = (((bits >> (2 * k)) & 1u) ? 0x0000FFFFu : 0u) | (((bits >> (2 * k + 1)) & 1u) ? 0xFFFF0000u : 0u);
+    else
+      keep = ((bits >> k) & 1u) ? 0xFFFFFFFFu : 0u;
+    const uint32_t ninf = sizeof(T) == 2 ? 0xFF80FF80u : 0xFF800000u;
+    w[k] = (w[k] & keep) | (ninf & ~keep);
   }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// The mask on a unit held in registers (its first nv vectors).
+template <typename T>
+__device__ __forceinline__ void mask_regs(uint4 (&xv)[kVecPerLane], int nv, uint32_t w0, uint32_t w1) {
+  constexpr uint32_t kFull = (1u << VecOps<T>::kPer) - 1u;
+  const UnitPrep up{w0, w1, false};
+#pragma unroll
   for (int j = 0; j < kVecPerLane; ++j) {
-    const int jj = j ^ swz;
-    if (jj >= nv) continue;
-    const uint32_t bits = unit_bits_of<T>(up, jj);
-    const int vid0 = int(uid0) + jj * kPer;
-    bool pen = false;
-    for (int t = h0; t < h1; ++t) pen |= ps.ids[t] >= vid0 && ps.ids[t] < vid0 + kPer;
-    if (!pen && (bits & kFull) == kFull) continue;
-    uint4 x = v[jj];
-    uint32_t w[4] = {x.x, x.y, x.z, x.w};
-    for (int t = h0; pen && t < h1; ++t) {
-      const int q = ps.ids[t] - vid0;
-      if (q < 0 || q >= kPer) continue;
-#pragma unroll
-      for (int qq = 0; qq < kPer; ++qq)
-        if (qq == q) {
-          float z = Vo::elem(make_uint4(w[0], w[1], w[2], w[3]), qq);
-          z = z > 0.0f ? __fdiv_rn(z, r) : __fmul_rn(z, r);
-          if (sizeof(T) == 2) {
-            const uint32_t hb = __float_as_uint(round_to_bf16(z)) >> 16;
-            w[qq >> 1] = (qq & 1) ? ((w[qq >> 1] & 0x0000FFFFu) | (hb << 16)) : ((w[qq >> 1] & 0xFFFF0000u) | hb);
-          } else {
-            w[qq] = __float_as_uint(z);
-          }
-        }
-    }
-#pragma unroll
-    for (int q = 0; q < kPer; ++q)
-      if (!((bits >> q) & 1u)) {
-        if (sizeof(T) == 2) w[q >> 1] = (q & 1) ? ((w[q >> 1] & 0x0000FFFFu) | 0xFF800000u) : ((w[q >> 1] & 0xFFFF0000u) | 0xFF80u);
-        else w[q] = 0xFF800000u;
-      }
-    v[jj] = make_uint4(w[0], w[1], w[2], w[3]);
+    const uint32_t bits = unit_bits_of<T>(up, j) & kFull;
+    if (j < nv && bits != kFull) xv[j] = mask_vec<T>(xv[j], bits);
   }
 }
+
+// The repetition penalty (a history id of the unit) and then the mask on a
+// unit held in registers: element q of vector j is id uid0 + j kPer + q.
+// The history ids inside the unit come from two binary searches; each of
+// them is applied by a compare with every element (units with history ids
+// are few).
+template <typename T>
+__device__ __forceinline__ void prep_regs(uint4 (&xv)[kVecPerLane], int nv, uint32_t uid0, uint32_t w0, uint32_t w1,
+                                          float r) {
+  using Vo = VecOps<T>;
+  constexpr int kPer = Vo::kPer;
+  const PrepShared& ps = prep_shared();
+  const int h0 = hist_lower_bound(ps, int(uid0));
+  const int h1 = hist_lower_bound(ps, int(uid0) + nv * kPer);
+  for (int t = h0; t < h1; ++t) {
+    const int o = ps.ids[t] - int(uid0);
+    const int jo = o / kPer, q = o % kPer;
+    // element q of a vector: word q / (kPer / 4), half (bf16) q % 2
+    const int wi = sizeof(T) == 2 ? (q >> 1) : q;
+#pragma unroll
+    for (int j = 0; j < kVecPerLane; ++j)
+      if (j == jo) {
+        uint32_t w[4] = {xv[j].x, xv[j].y, xv[j].z, xv[j].w};
+        const uint32_t word = wi == 0 ? w[0] : wi == 1 ? w[1] : wi == 2 ? w[2] : w[3];
+        float z = sizeof(T) == 2 ? __uint_as_float((q & 1) ? (word & 0xFFFF0000u) : (word << 16)) : __uint_as_float(word);
+        z = z > 0.0f ? __fdiv_rn(z, r) : __fmul_rn(z, r);
+        uint32_t nw;
+        if (sizeof(T) == 2) {
+          const uint32_t hb = __float_as_uint(round_to_bf16(z)) >> 16;
+          nw = (q & 1) ? ((word & 0x0000FFFFu) | (hb << 16)) : ((word & 0xFFFF0000u) | hb);
+        } else {
+          nw = __float_as_uint(z);
+        }
+        xv[j] = make_uint4(wi == 0 ? nw : w[0], wi == 1 ? nw : w[1], wi == 2 ? nw : w[2], wi == 3 ? nw : w[3]);
+      }
+  }
+  if ((w0 & w1) != 0xFFFFFFFFu) mask_regs<T>(xv, nv, w0, w1);
+}
+
 
 // Builds the row's PrepShared (history ids in [0, V), each once, sorted).
 __device__ __forceinline__ PrepShared& prep_shared() {
@@ -294,17 +310,30 @@ __device__ __forceinline__ void build_prep(PrepShared& ps, const PrepArgs& pa, i
   }
   if (tid == 0) ps.n = 0;
   cta_sync();
+  // (the loops below read the 64 entries four at a time, every load issued
+  // at once)
+  const int4* raw4 = reinterpret_cast<const int4*>(ps.raw);
   if (tid < kMaxHistory) {   // first occurrences
     const int32_t id = ps.raw[tid];
     bool first = id >= 0;
-    for (int s = 0; s < tid; ++s) first &= ps.raw[s] != id;
+#pragma unroll
+    for (int s = 0; s < kMaxHistory / 4; ++s) {
+      const int4 q = raw4[s];
+      first &= !((4 * s < tid && q.x == id) || (4 * s + 1 < tid && q.y == id) ||
+                 (4 * s + 2 < tid && q.z == id) || (4 * s + 3 < tid && q.w == id));
+    }
     ps.first[tid] = first;
   }
   cta_sync();
   if (tid < kMaxHistory && ps.first[tid]) {   // rank among the distinct ids
     const int32_t id = ps.raw[tid];
+    const int4* first4 = reinterpret_cast<const int4*>(ps.first);
     int rank = 0;
-    for (int s = 0; s < kMaxHistory; ++s) rank += ps.first[s] && ps.raw[s] < id;
+#pragma unroll
+    for (int s = 0; s < kMaxHistory / 4; ++s) {
+      const int4 q = raw4[s], f = first4[s];
+      rank += (f.x && q.x < id) + (f.y && q.y < id) + (f.z && q.z < id) + (f.w && q.w < id);
+    }
     ps.ids[rank] = id;
     atomicOr(&ps.unit_bits[id >> 11], 1u << ((id >> 6) & 31));
     atomicAdd(&ps.n, 1);
@@ -804,6 +833,34 @@ __global__ void __launch_bounds__(kThreads, 2) sample_kernel(SampleArgs a) {
     uint32_t best_id = 0xFFFFFFFFu;
     float seg_max = -INFINITY;     // other rows: this lane's maximum over the current segment
     float lane_row_max = -INFINITY;   // ... and over the row
+    // The raw mask words of this lane's unit in batch bt2 (the fused
+    // pre-pass with a mask), combined when the batch is processed.
+    struct MaskRaw {
+      uint32_t a, b, c, sft;
+      bool on, w1;
+    };
+    auto mask_load = [&](int bt2) -> MaskRaw {
+      MaskRaw m{0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0u, false, false};
+      if constexpr (kPrep) {
+        const uintptr_t bst = geo.a0 + uintptr_t(bt2) * kBufBytes;
+        const int bv = int(min(uintptr_t(kBufBytes), geo.a1 - bst) / 16);
+        const int nv2 = max(0, min(bv - v0, kSubBytes / 16));
+        if (mrow && lane * kVecPerLane < nv2) {
+          const uint32_t uid0 = id_base + uint32_t(bt2) * (kBufBytes / sizeof(T)) + uint32_t(v0 * kPer) +
+                                uint32_t(lane * kVecPerLane * kPer);
+          const uint32_t k = uid0 >> 5;
+          const int words = a.prep.words;
+          m.on = true;
+          m.sft = uid0 & 31u;
+          m.w1 = kVecPerLane * kPer > 32 && int(uid0) + 32 < Vn;
+          m.a = __ldg(mrow + k);
+          m.b = int(k) + 1 < words ? __ldg(mrow + k + 1) : 0xFFFFFFFFu;
+          m.c = m.w1 && int(k) + 2 < words ? __ldg(mrow + k + 2) : 0xFFFFFFFFu;
+        }
+      }
+      return m;
+    };
+    MaskRaw mnext = mask_load(0);
 
     for (int bt = 0; bt < geo.nchunks; ++bt) {
       const uint32_t bi = consumed % kBufs;
@@ -814,15 +871,16 @@ __global__ void __launch_bounds__(kThreads, 2) sample_kernel(SampleArgs a) {
       const uint4* vec = reinterpret_cast<const uint4*>(ring + size_t(bi) * kBufBytes) + v0;
       const T* part = reinterpret_cast<const T*>(vec);
       const uint32_t id0 = id_base + uint32_t(bt) * (kBufBytes / sizeof(T)) + uint32_t(v0 * kPer);
-      // The mask bits of the lane's unit, requested before the wait for the
-      // batch so that their latency overlaps it.
+      // The mask bits of the lane's unit: its words were requested one batch
+      // ahead (and the next batch's are requested now), so that their latency
+      // overlaps a whole batch.
       uint32_t mw0 = 0xFFFFFFFFu, mw1 = 0xFFFFFFFFu;
       if constexpr (kPrep) {
-        if (mrow && lane * kVecPerLane < nvec) {
-          const uint32_t uid0 = id0 + uint32_t(lane * kVecPerLane * kPer);
-          mw0 = allowed_bits32(mrow, a.prep.words, uid0);
-          if (kVecPerLane * kPer > 32 && int(uid0) + 32 < Vn) mw1 = allowed_bits32(mrow, a.prep.words, uid0 + 32);
+        if (mnext.on) {
+          mw0 = uint32_t(((uint64_t(mnext.b) << 32) | mnext.a) >> mnext.sft);
+          if (mnext.w1) mw1 = uint32_t(((uint64_t(mnext.c) << 32) | mnext.b) >> mnext.sft);
         }
+        if (bt + 1 < geo.nchunks) mnext = mask_load(bt + 1);
       }
       if (!wait_full(&ss.full[bi], (consumed / kBufs) & 1, a.wait_limit_ns)) ss.timeout = 1;
       // The lane's batch maximum: one packed maximum over its unit, the
@@ -848,16 +906,26 @@ __global__ void __launch_bounds__(kThreads, 2) sample_kernel(SampleArgs a) {
           }
           cta_sync();
         }
-        // The mask on the lane's unit, in place in the ring (only this lane
-        // reads it), when its mask bits are not all set.
-        if (mrow && lane * kVecPerLane < nvec && (mw0 & mw1) != 0xFFFFFFFFu)
-          prep_unit<T>(const_cast<uint4*>(vec) + lane * kVecPerLane, min(kVecPerLane, nvec - lane * kVecPerLane),
-                       lane & (kVecPerLane - 1), id0 + uint32_t(lane * kVecPerLane * kPer), mw0, mw1, false, prep_r);
       }
+      // (with a mask: each vector masked in registers as it is read, and
+      // written back to the ring when one of its bits is clear)
+      bool masking = false;
+      if constexpr (kPrep) masking = mrow && (mw0 & mw1) != 0xFFFFFFFFu;
 #pragma unroll
       for (int j = 0; j < kVecPerLane; ++j) {
-        const int v = lane * kVecPerLane + (j ^ (lane & (kVecPerLane - 1)));
-        if (v < nvec) pm = V::max2(pm, V::vmax(vec[v]));
+        const int jj = j ^ (lane & (kVecPerLane - 1));
+        const int v = lane * kVecPerLane + jj;
+        if (v < nvec) {
+          uint4 x = vec[v];
+          if constexpr (kPrep) {
+            const uint32_t bits = unit_bits_of<T>(UnitPrep{mw0, mw1, false}, jj) & ((1u << kPer) - 1u);
+            if (masking && bits != (1u << kPer) - 1u) {
+              x = mask_vec<T>(x, bits);
+              const_cast<uint4*>(vec)[v] = x;
+            }
+          }
+          pm = V::max2(pm, V::vmax(x));
+        }
       }
       const float lane_max = V::finish(pm);
       const uint32_t lane_key = lane_max > -INFINITY ? key_of_bits(__float_as_uint(lane_max)) : 0u;
@@ -1007,8 +1075,10 @@ __global__ void __launch_bounds__(kThreads, 2) sample_kernel(SampleArgs a) {
             if (ol * kVecPerLane < nvec) {
               const uint32_t uid0 = id0 + uint32_t(ol * kVecPerLane * kPer);
               const UnitPrep up = unit_prep<T>(mrow, a.prep.words, Vn, uid0, prep_shared());
-              if (up.hist || (up.w0 & up.w1) != 0xFFFFFFFFu)
-                prep_unit<T>(xv, min(kVecPerLane, nvec - ol * kVecPerLane), 0, uid0, up.w0, up.w1, up.hist, prep_r);
+              if (up.hist)
+                prep_regs<T>(xv, min(kVecPerLane, nvec - ol * kVecPerLane), uid0, up.w0, up.w1, prep_r);
+              else if ((up.w0 & up.w1) != 0xFFFFFFFFu)
+                mask_regs<T>(xv, min(kVecPerLane, nvec - ol * kVecPerLane), up.w0, up.w1);
             }
           }
           push_unit<T>(ss, cs, xv, min(kVecPerLane, max(0, nvec - ol * kVecPerLane)),

@@ -73,35 +73,6 @@ __host__ __device__ __forceinline__ size_t beam_slice_bytes(int width) {
   return sizeof(BeamSliceHead) + size_t(width) * sizeof(BeamCand);
 }
 
-// A pass over a row slice with kU 16-byte vectors in flight per thread (the
-// selection passes keep one): f(id, z) over every element, in no particular order.
-template <typename T, int kU, typename F>
-__device__ __forceinline__ void gen_sweep_wide(const T* row, int V, F&& f) {
-  using Vo = VecOps<T>;
-  constexpr int kPer = Vo::kPer;
-  const uintptr_t r0 = reinterpret_cast<uintptr_t>(row);
-  const uintptr_t a0 = (r0 + 15) & ~uintptr_t(15), a1 = (r0 + size_t(V) * sizeof(T)) & ~uintptr_t(15);
-  const bool mid = a1 > a0;
-  const int head = mid ? int((a0 - r0) / sizeof(T)) : V;
-  const int tail0 = mid ? int((a1 - r0) / sizeof(T)) : V;
-  const int nvec = mid ? int((a1 - a0) / 16) : 0;
-  const uint4* vp = reinterpret_cast<const uint4*>(a0);
-  for (int v0 = threadIdx.x; v0 < nvec; v0 += kThreads * kU) {
-    uint4 x[kU];
-#pragma unroll
-    for (int u = 0; u < kU; ++u)
-      if (v0 + u * kThreads < nvec) x[u] = __ldg(vp + v0 + u * kThreads);
-#pragma unroll
-    for (int u = 0; u < kU; ++u)
-      if (v0 + u * kThreads < nvec) {
-#pragma unroll
-        for (int q = 0; q < kPer; ++q) f(head + (v0 + u * kThreads) * kPer + q, Vo::elem(x[u], q));
-      }
-  }
-  for (int i = threadIdx.x; i < head; i += kThreads) f(i, Elem<T>::widen(row[i]));
-  for (int i = tail0 + threadIdx.x; i < V; i += kThreads) f(i, Elem<T>::widen(row[i]));
-}
-
 template <typename T>
 __global__ void __launch_bounds__(kThreads, 2) beam_row_kernel(BeamArgs a) {
   __shared__ FloatPair table[64];
@@ -256,7 +227,7 @@ __global__ void __launch_bounds__(kThreads, 2) beam_row_kernel(BeamArgs a) {
   constexpr int kBeamList = int(sizeof(gs.mass) / sizeof(unsigned long long));
   if (tid == 0) n_members = 0;
   cta_sync();
-  gen_sweep_wide<T, kBeamU>(row, len, [&](int i, float z) {
+  gen_sweep<T, kBeamU>(row, len, [&](int i, float z) {
     const uint32_t k = order_key<T>(isnan(z) ? -INFINITY : z);   // NaN counts as -inf
     if (k >= theta) {
       const int slot = atomicAdd(&n_members, 1);

@@ -6,10 +6,35 @@
 //
 // The kept set, the shortest of the enabled prefixes of the order (logit
 // descending, id ascending), comes from gen_kept_set (select.cuh), by radix
-// selection over order keys.  Included by sample.cu
+// selection over order keys, or, for top-k up to kTopKMax, from
+// gen_kept_set_topk's ranked candidate list, which the draw then reads in
+// place of a walk over the row.  Included by sample.cu
 // inside namespace smp, after the sampler's argument block and row helpers
 // it uses.
 #pragma once
+
+// The draw over a kept set held as a list (topk_list and topk_mass, len
+// entries in rank order): the token whose interval [run, run + E) of the
+// running mass in id order holds t.  Each of the first len threads sums the
+// masses of the listed tokens with lower ids.
+__device__ __forceinline__ int topk_draw(GenShared& gs, uint32_t len, uint64_t t) {
+  const unsigned long long* list = topk_list(gs);
+  const unsigned long long* lmass = topk_mass(gs);
+  const int tid = threadIdx.x;
+  if (tid == 0) gs.bc32[4] = 0xFFFFFFFFu;
+  cta_sync();
+  if (uint32_t(tid) < len) {
+    const uint32_t id = ~uint32_t(list[tid]);
+    const uint64_t e = lmass[tid];
+    uint64_t run = 0;
+    for (uint32_t j = 0; j < len; ++j) run += ~uint32_t(list[j]) < id ? lmass[j] : 0ull;
+    if (e > 0 && run <= t && t - run < e) gs.bc32[4] = id;
+  }
+  cta_sync();
+  const uint32_t tok = gs.bc32[4];
+  cta_sync();
+  return tok == 0xFFFFFFFFu ? -1 : int(tok);
+}
 
 // One row by the general path (see the top of this file).  `table` is the
 // 2^(j/64) table in shared memory.
@@ -22,10 +47,11 @@ __device__ void general_row(GenShared& gs, const FloatPair* table, const SampleA
 
   // The maximum and the lowest id holding it.
   uint64_t best = 0;
-  gen_sweep<T>(row, V, [&](int i, float z) {
+  gen_sweep<T, light_pass_vectors<Xf>()>(row, V, [&](int i, float z) {
     const uint64_t p = pack_key_id(order_key<T>(z), uint32_t(i));
     best = p > best ? p : best;
   }, xf);
+  const uint32_t thread_key_max = uint32_t(best >> 32);
   best = block_max_u64(best, gs.red64);
   const uint32_t key_max = uint32_t(best >> 32);
   const uint32_t argmax = ~uint32_t(best);
@@ -52,7 +78,10 @@ __device__ void general_row(GenShared& gs, const FloatPair* table, const SampleA
     return;
   }
 
-  const KeptSet ks = gen_kept_set<T>(row, V, gs, table, prm, key_max, xf);
+  KeptSet ks;
+  const bool listed = topk_bounded(prm, V) &&
+                      gen_kept_set_topk<T>(row, V, gs, table, prm, key_max, thread_key_max, &ks, xf);
+  if (!listed) ks = gen_kept_set<T>(row, V, gs, table, prm, key_max, xf);
   auto mass_of = [&](int i, float z) -> uint64_t { return kept_mass<T>(ks, table, i, z); };
   const uint64_t z_kept = ks.z_kept;
   const uint64_t len = ks.len;
@@ -60,7 +89,7 @@ __device__ void general_row(GenShared& gs, const FloatPair* table, const SampleA
   // t = floor(u * Z_S), u = Philox draw 0 of row b.
   const uint64_t u53 = uniform53(a.seed, a.offset, a.row_base + uint64_t(b), 0);
   const uint64_t t = uint64_t((u128(u53) * z_kept) >> 53);
-  const int tok = gen_walk<T, uint64_t>(row, V, t, gs, mass_of, xf);
+  const int tok = listed ? topk_draw(gs, uint32_t(len), t) : gen_walk<T, uint64_t>(row, V, t, gs, mass_of, xf);
   if (tid == 0) {
     a.out_ids[b] = tok;
     if (a.out_probs)

@@ -14,8 +14,11 @@
 //    candidates at the end of the row.
 //
 //  * general path -- top-p rows, unfiltered sampling, large k, or a candidate
-//    overflow: exact radix selection over logit keys with 64-bit fixed-point
-//    masses (row_ops.cuh), run by the row's CTA over global memory.
+//    overflow, run by the row's CTA over global memory: for bf16 rows the
+//    per-value count table (general_bf16.cuh); else, with top-k up to
+//    kTopKMax, a ranked candidate list (select.cuh); else exact radix
+//    selection over logit keys; 64-bit fixed-point masses throughout
+//    (row_ops.cuh).
 //
 // All decisions use exact integers (keys, fixed-point masses), so results do
 // not depend on how rows are scheduled.
@@ -412,58 +415,6 @@ __device__ __forceinline__ RowGeom row_geom(const SampleArgs& a, int row) {
   return g;
 }
 
-
-// The k-th largest of vals[0..n) (1 <= k <= n), exactly, as a float: radix
-// selection over the order keys with 8-bit digits (two levels for bf16
-// values, four for binary32), one shared 256-bin histogram per level.
-template <typename T>
-__device__ float kth_largest_list(const float* vals, int n, int k, uint32_t* hist, uint32_t* bcast) {
-  constexpr int kLevels = KeyTraits<T>::kBits == 16 ? 2 : 4;
-  uint32_t prefix = 0;
-  uint32_t need = uint32_t(k);
-  for (int lvl = 0; lvl < kLevels; ++lvl) {
-    const int shift = 24 - 8 * lvl;
-    hist[threadIdx.x] = 0;
-    cta_sync();
-    for (int i = threadIdx.x; i < n; i += kThreads) {
-      const uint32_t key = key_of_bits(__float_as_uint(vals[i]));
-      if (lvl == 0 || (key >> (shift + 8)) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
-    }
-    cta_sync();
-    if (threadIdx.x < 32) {
-      // digits 255..0 in lane order: lane l covers 255 - 8l .. 248 - 8l
-      uint32_t c[8], sum = 0;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        c[j] = hist[255 - (threadIdx.x * 8 + j)];
-        sum += c[j];
-      }
-      const uint32_t incl = warp_inclusive_scan<uint32_t>(sum);
-      uint32_t run = incl - sum;
-      int found = -1;
-      uint32_t above = 0;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        if (found < 0 && run + c[j] >= need) {
-          found = 255 - (threadIdx.x * 8 + j);
-          above = run;
-        }
-        run += c[j];
-      }
-      const uint32_t hits = __ballot_sync(0xFFFFFFFFu, found >= 0);
-      const int src = hits ? __ffs(hits) - 1 : 0;
-      if (threadIdx.x == src) {
-        bcast[0] = uint32_t(found < 0 ? 0 : found);
-        bcast[1] = above;
-      }
-    }
-    cta_sync();
-    prefix = (prefix << 8) | bcast[0];
-    need -= bcast[1];
-    cta_sync();
-  }
-  return value_of_key(kLevels == 2 ? (prefix << 16) | ((prefix & 0x8000u) ? 0u : 0xFFFFu) : prefix);
-}
 
 __device__ __forceinline__ void push_candidate(StreamShared& ss, CandShared& cs, uint32_t id, float z) {
   const uint32_t slot = atomicAdd(&ss.cand_n, 1u);

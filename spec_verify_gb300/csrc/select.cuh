@@ -119,7 +119,8 @@ struct NoPrep {
 };
 
 // Sweep over every element of a row in no particular order: f(id, xf(id, z)).
-template <typename T, typename F, typename Xf = NoPrep>
+// kU vectors per thread in flight (more for light f).
+template <typename T, int kU = kGenU, typename F, typename Xf = NoPrep>
 __device__ __forceinline__ void gen_sweep(const T* row, int V, F&& f, const Xf& xf = Xf()) {
   using Vo = VecOps<T>;
   constexpr int kPer = Vo::kPer;
@@ -130,20 +131,25 @@ __device__ __forceinline__ void gen_sweep(const T* row, int V, F&& f, const Xf& 
   const int tail0 = mid ? int((a1 - r0) / sizeof(T)) : V;
   const int nvec = mid ? int((a1 - a0) / 16) : 0;
   const uint4* vp = reinterpret_cast<const uint4*>(a0);
-  for (int v0 = threadIdx.x * kGenU; v0 < nvec; v0 += kThreads * kGenU) {
-    uint4 x[kGenU];
+  // vector base + u * kThreads + t for thread t: each load instruction coalesced
+  for (int base = 0; base < nvec; base += kThreads * kU) {
+    uint4 x[kU];
 #pragma unroll
-    for (int u = 0; u < kGenU; ++u)
-      if (v0 + u < nvec) x[u] = __ldg(vp + v0 + u);
+    for (int u = 0; u < kU; ++u) {
+      const int v = base + u * kThreads + int(threadIdx.x);
+      if (v < nvec) x[u] = __ldg(vp + v);
+    }
 #pragma unroll
-    for (int u = 0; u < kGenU; ++u)
-      if (v0 + u < nvec) {
+    for (int u = 0; u < kU; ++u) {
+      const int v = base + u * kThreads + int(threadIdx.x);
+      if (v < nvec) {
 #pragma unroll
         for (int q = 0; q < kPer; ++q) {
-          const int id = head + (v0 + u) * kPer + q;
+          const int id = head + v * kPer + q;
           f(id, xf(id, Vo::elem(x[u], q)));
         }
       }
+    }
   }
   for (int i = threadIdx.x; i < head; i += kThreads) f(i, xf(i, Elem<T>::widen(row[i])));
   for (int i = tail0 + threadIdx.x; i < V; i += kThreads) f(i, xf(i, Elem<T>::widen(row[i])));
@@ -433,6 +439,69 @@ __device__ GenBoundary gen_select(const T* row, int V, GenShared& gs, uint32_t k
   return out;
 }
 
+// ------------------------------------------------------------------ k-th largest of a short list
+
+// The k-th largest (1 <= k <= n) of n keys key_at(0 .. n-1), exactly: radix
+// selection over their top 8 * kLevels bits with 8-bit digits, one shared
+// 256-bin histogram per level.  Returns those bits, right-aligned.
+template <int kLevels, typename KeyAt>
+__device__ uint32_t kth_largest_key(int n, uint32_t k, KeyAt&& key_at, uint32_t* hist, uint32_t* bcast) {
+  uint32_t prefix = 0;
+  uint32_t need = k;
+  for (int lvl = 0; lvl < kLevels; ++lvl) {
+    const int shift = 24 - 8 * lvl;
+    hist[threadIdx.x] = 0;
+    cta_sync();
+    for (int i = threadIdx.x; i < n; i += kThreads) {
+      const uint32_t key = key_at(i);
+      if (lvl == 0 || (key >> (shift + 8)) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+    }
+    cta_sync();
+    if (threadIdx.x < 32) {
+      // digits 255..0 in lane order: lane l covers 255 - 8l .. 248 - 8l
+      uint32_t c[8], sum = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        c[j] = hist[255 - (threadIdx.x * 8 + j)];
+        sum += c[j];
+      }
+      const uint32_t incl = warp_inclusive_scan<uint32_t>(sum);
+      uint32_t run = incl - sum;
+      int found = -1;
+      uint32_t above = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (found < 0 && run + c[j] >= need) {
+          found = 255 - (threadIdx.x * 8 + j);
+          above = run;
+        }
+        run += c[j];
+      }
+      const uint32_t hits = __ballot_sync(0xFFFFFFFFu, found >= 0);
+      const int src = hits ? __ffs(hits) - 1 : 0;
+      if (threadIdx.x == src) {
+        bcast[0] = uint32_t(found < 0 ? 0 : found);
+        bcast[1] = above;
+      }
+    }
+    cta_sync();
+    prefix = (prefix << 8) | bcast[0];
+    need -= bcast[1];
+    cta_sync();
+  }
+  return prefix;
+}
+
+// The k-th largest of vals[0..n) (1 <= k <= n), exactly, as a float (two
+// levels for bf16 values, four for binary32).
+template <typename T>
+__device__ float kth_largest_list(const float* vals, int n, int k, uint32_t* hist, uint32_t* bcast) {
+  constexpr int kLevels = KeyTraits<T>::kBits == 16 ? 2 : 4;
+  const uint32_t prefix = kth_largest_key<kLevels>(
+      n, uint32_t(k), [&](int i) { return key_of_bits(__float_as_uint(vals[i])); }, hist, bcast);
+  return value_of_key(kLevels == 2 ? (prefix << 16) | ((prefix & 0x8000u) ? 0u : 0xFFFFu) : prefix);
+}
+
 // ------------------------------------------------------------------ the kept set
 
 // The kept set S of one row: token i with order key k_i is in S when
@@ -537,4 +606,287 @@ __device__ KeptSet gen_kept_set(const T* row, int V, GenShared& gs, const FloatP
     ks.z_kept = zk;
   }
   return ks;
+}
+
+// ------------------------------------------------------------------ top-k-bounded kept set
+
+// With top-k set to k <= kTopKMax the kept set holds at most k tokens, so it
+// comes from a short candidate list instead of radix passes over the row.
+// theta, the k-th largest of the threads' maximum keys from the caller's
+// maximum pass, bounds the row's k-th largest key from below (k threads each
+// saw a key >= theta); one pass collects every token with key >= theta, and
+// the candidates are ranked exactly by (key desc, id asc).  The first k get
+// their exact fixed-point masses and prefix sums; min-p cuts where the keys
+// fall below its threshold key; top-p compares the prefix sums with
+// top_p * Z, Z bracketed by a binary32 sum of every token's exponential
+// taken in the same pass (topk_z_bracket).  A prefix that falls inside the
+// bracket asks for the exact Z, one more pass.  More than kTopCandMax candidates
+// (long runs of equal keys) and the row takes gen_kept_set.
+constexpr int kTopKMax = 128;
+constexpr int kTopCandMax = 1024;
+constexpr int kTopU = 4;   // vectors in flight per thread in the light passes (default)
+
+// kU for raw rows; one vector in flight under a logit transform, whose
+// state already fills the registers.
+template <typename Xf, int kU = kTopU>
+constexpr int light_pass_vectors() {
+  return std::is_same<Xf, NoPrep>::value ? kU : 1;
+}
+
+static_assert(sizeof(GenShared::mass) >= sizeof(unsigned long long) * (kTopCandMax + 2 * kTopKMax),
+              "candidate list, ranked list and masses overlay the mass histograms");
+
+__device__ __forceinline__ unsigned long long* topk_cand(GenShared& gs) {
+  return reinterpret_cast<unsigned long long*>(&gs.mass[0][0][0]);
+}
+// the first k candidates by rank, packed (key << 32) | ~id
+__device__ __forceinline__ unsigned long long* topk_list(GenShared& gs) { return topk_cand(gs) + kTopCandMax; }
+// their fixed-point masses
+__device__ __forceinline__ unsigned long long* topk_mass(GenShared& gs) {
+  return topk_cand(gs) + kTopCandMax + kTopKMax;
+}
+
+__device__ __forceinline__ bool topk_bounded(const smp_row_params& prm, int V) {
+  return prm.top_k > 0 && prm.top_k <= kTopKMax && prm.top_k < V;
+}
+
+// The candidate pass of gen_kept_set_topk.  Every token whose key is at
+// least theta is appended to cand (a count past kTopCandMax is an overflow):
+// raw rows compare the logit with theta's value (theta finite), transformed
+// rows compare keys.  With top-p, each thread also sums e' = 2^y',
+// y' = fl(fl(z - m) * c_hi), pairwise within each 16-byte vector and then one
+// add per vector, and A = sum e' |y'|.  The bracket on Z follows from them
+// (topk_z_bracket).
+struct ZSums {
+  float z;    // sum of e'
+  float a;    // sum of e' |y'|
+};
+
+template <typename T, int kU, bool kRaw, typename Xf>
+__device__ __forceinline__ ZSums topk_candidate_pass(const T* row, int V, uint32_t theta, float theta_v, bool topp,
+                                                     const RowScale& rs, unsigned long long* cand, uint32_t* count,
+                                                     const Xf& xf) {
+  using Vo = VecOps<T>;
+  constexpr int kPer = Vo::kPer;
+  const uintptr_t r0 = reinterpret_cast<uintptr_t>(row);
+  const uintptr_t a0 = (r0 + 15) & ~uintptr_t(15), a1 = (r0 + size_t(V) * sizeof(T)) & ~uintptr_t(15);
+  const bool mid = a1 > a0;
+  const int head = mid ? int((a0 - r0) / sizeof(T)) : V;
+  const int tail0 = mid ? int((a1 - r0) / sizeof(T)) : V;
+  const int nvec = mid ? int((a1 - a0) / 16) : 0;
+  const uint4* vp = reinterpret_cast<const uint4*>(a0);
+  ZSums acc{0.0f, 0.0f};
+  auto visit = [&](int id, float z) -> float {
+    const bool c = kRaw ? (z >= theta_v) : (order_key<T>(z) >= theta);
+    if (c) {
+      const uint32_t s = atomicAdd(count, 1u);
+      if (s < uint32_t(kTopCandMax)) cand[s] = pack_key_id(order_key<T>(z), uint32_t(id));
+    }
+    if (!topp) return 0.0f;
+    const float y = __fmul_rn(__fsub_rn(z, rs.m), rs.c_hi);
+    const bool live = y > -126.0f;   // false for -inf and NaN
+    const float e = live ? ex2_approx(y) : 0.0f;
+    acc.a = __fmaf_rn(e, live ? -y : 0.0f, acc.a);
+    return e;
+  };
+  for (int base = 0; base < nvec; base += kThreads * kU) {
+    uint4 x[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int v = base + u * kThreads + int(threadIdx.x);
+      if (v < nvec) x[u] = __ldg(vp + v);
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int v = base + u * kThreads + int(threadIdx.x);
+      if (v < nvec) {
+        float ev[kPer];
+#pragma unroll
+        for (int q = 0; q < kPer; ++q) {
+          const int id = head + v * kPer + q;
+          ev[q] = visit(id, xf(id, Vo::elem(x[u], q)));
+        }
+#pragma unroll
+        for (int w = 1; w < kPer; w <<= 1)
+#pragma unroll
+          for (int q = 0; q + w < kPer; q += 2 * w) ev[q] = __fadd_rn(ev[q], ev[q + w]);
+        acc.z = __fadd_rn(acc.z, ev[0]);
+      }
+    }
+  }
+  for (int i = threadIdx.x; i < head; i += kThreads) acc.z = __fadd_rn(acc.z, visit(i, xf(i, Elem<T>::widen(row[i]))));
+  for (int i = tail0 + threadIdx.x; i < V; i += kThreads)
+    acc.z = __fadd_rn(acc.z, visit(i, xf(i, Elem<T>::widen(row[i]))));
+  return acc;
+}
+
+// The bracket [z_lo, z_hi] on the exact fixed-point Z from the threads'
+// ZSums (every thread gets it).  Errors, relative to each e = 2^y:
+//  * y' against y: fl(z - m), log2(e) rounded to binary32, its quotient by
+//    T rounded to c_hi, and the product: 4 units of 2^-24 of |y| in all, so
+//    e' is off by at most ln 2 * 4.01 * 2^-24 |y| e, bounded through A
+//    (2.8 * 2^-24 A);
+//  * ex2.approx: relative error below 2^-21 (the instruction's is about 2^-22);
+//  * the sums: a thread adds at most log2(elements per vector) + its vectors
+//    + 2 terms in sequence, each add within 2^-24 of its running sum;
+//  * the fixed-point masses: 3/4 of a unit per token (rounding, and values
+//    below 2^-47 dropped); tokens below 2^-126, dropped here, weigh less.
+// Margins of 2^-10 cover the second-order terms and the double arithmetic.
+template <typename T>
+__device__ __forceinline__ void topk_z_bracket(ZSums acc, int V, GenShared& gs, uint64_t* z_lo, uint64_t* z_hi) {
+  constexpr int kLogPer = VecOps<T>::kPer == 8 ? 3 : VecOps<T>::kPer == 4 ? 2 : 1;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  double zt = double(acc.z), at = double(acc.a);
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    zt += __shfl_xor_sync(0xFFFFFFFFu, zt, o);
+    at += __shfl_xor_sync(0xFFFFFFFFu, at, o);
+  }
+  if (lane == 0) {
+    gs.scan64[warp] = (unsigned long long)__double_as_longlong(zt);
+    gs.red64[warp] = (uint64_t)__double_as_longlong(at);
+  }
+  cta_sync();
+  double zf = 0.0, af = 0.0;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    zf += __longlong_as_double((long long)gs.scan64[w]);
+    af += __longlong_as_double((long long)gs.red64[w]);
+  }
+  cta_sync();
+  const int nvec = V * int(sizeof(T)) / 16 + 1;
+  const double adds = double(kLogPer + (nvec + kThreads - 1) / kThreads + 2);
+  const double u = 0x1p-24;
+  const double rel = (0x1p-21 + adds * u) * (1.0 + 0x1p-10);
+  const double zd = zf * double(kFixedOne);
+  const double ad = af * double(kFixedOne) * (1.0 + 0x1p-10);
+  const double w = rel * zd + 2.8 * u * ad + 0.75 * double(V) + 2.0;
+  *z_lo = zd - w > 0.0 ? __double2ull_rd(zd - w) : 0ull;
+  *z_hi = __double2ull_ru(zd + w);
+}
+
+// S and Z_S of a row as gen_kept_set gives them, for a row with
+// topk_bounded(prm, V), valid sampling knobs (not greedy) and a finite
+// maximum key.  thread_key_max is this thread's maximum key in a pass over
+// every element (any split of the row over the threads); kU is the number
+// of vectors each thread keeps in flight in the candidate pass.  Returns
+// false, with every thread agreeing, when the candidates overflow or fewer
+// than k threads saw a finite maximum (raw rows).  On success the first
+// ks.len entries of topk_list and topk_mass hold S in rank order.
+template <typename T, int kU = kTopU, typename Xf = NoPrep>
+__device__ bool gen_kept_set_topk(const T* row, int V, GenShared& gs, const FloatPair* table,
+                                  const smp_row_params& prm, uint32_t key_max, uint32_t thread_key_max,
+                                  KeptSet* out, const Xf& xf = Xf()) {
+  constexpr int kKeyLevels = KeyTraits<T>::kBits == 32 ? 4 : 2;
+  constexpr int kKeyUp = 32 - KeyTraits<T>::kBits;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t k = uint32_t(prm.top_k);
+  const bool topp = prm.top_p < 1.0f;
+  const bool minp = prm.min_p > 0.0f && prm.min_p < 1.0f;
+  KeptSet ks;
+  ks.rs = make_row_scale(key_value<T>(key_max), prm.temperature);
+
+  // theta: the k-th largest of the threads' maximum keys (k <= kThreads).
+  uint32_t* tkeys = &gs.cnt[0][0];
+  cta_sync();   // earlier readers of the overlaid state are done
+  tkeys[tid] = thread_key_max;
+  const uint32_t theta = kth_largest_key<kKeyLevels>(
+      kThreads, k, [&](int i) { return tkeys[i] << kKeyUp; }, gs.tot_cnt, gs.bc32);
+  const uint32_t key_min_p =
+      minp ? minp_threshold_key<T>(gs.bc32, table, ks.rs, prm.temperature, prm.min_p, key_max) : 0u;
+
+  // One pass: the candidates, and the sums of the bracket on Z.
+  constexpr bool kRaw = std::is_same<Xf, NoPrep>::value;
+  if (kRaw && !key_finite<T>(theta)) return false;   // fewer than k finite thread maxima
+  unsigned long long* cand = topk_cand(gs);
+  if (tid == 0) gs.bc32[5] = 0;
+  cta_sync();
+  const ZSums acc = topk_candidate_pass<T, light_pass_vectors<Xf, kU>(), kRaw>(
+      row, V, theta, key_value<T>(theta), topp, ks.rs, cand, &gs.bc32[5], xf);
+  cta_sync();
+  const uint32_t n = gs.bc32[5];
+  if (n > uint32_t(kTopCandMax) || n < k) {   // (n >= k whenever thread_key_max is as stated)
+    cta_sync();
+    return false;
+  }
+  uint64_t z_lo = 0, z_hi = 0;
+  if (topp) topk_z_bracket<T>(acc, V, gs, &z_lo, &z_hi);
+
+  // Rank every candidate; the first k by rank, in rank order.
+  unsigned long long* list = topk_list(gs);
+  unsigned long long* lmass = topk_mass(gs);
+  for (int c = tid; c < int(n); c += kThreads) {
+    const unsigned long long pc = cand[c];
+    uint32_t r = 0;
+    for (int j = 0; j < int(n); ++j) r += cand[j] > pc;
+    if (r < k) list[r] = pc;
+  }
+  if (tid == 0) {
+    gs.bc32[2] = k - 1;   // first rank whose prefix may reach the top-p target
+    gs.bc32[3] = k - 1;   // first rank whose prefix surely reaches it
+  }
+  cta_sync();
+  // Exact masses of the first k (their logits read again), the min-p cut.
+  uint64_t e = 0;
+  bool below_min_p = false;
+  if (uint32_t(tid) < k) {
+    const unsigned long long pc = list[tid];
+    const uint32_t id = ~uint32_t(pc);
+    e = mass_fixed(xf(int(id), Elem<T>::widen(row[id])), ks.rs, table);
+    lmass[tid] = e;
+    below_min_p = minp && uint32_t(pc >> 32) < key_min_p;
+  }
+  // Keys fall along the ranks, so the tokens at or above the min-p key are
+  // the ranks below the first that is not (the maximum always is).
+  const uint32_t len_m = k - uint32_t(cta_sync_count(below_min_p));
+  uint64_t total;
+  const uint64_t cum =   // prefix mass through this rank
+      gen_scan<uint64_t>(e, reinterpret_cast<uint64_t*>(gs.scan64), &total) + e;
+
+  // Top-p: the first rank r whose prefix reaches top_p * Z (only r < k - 1 matters).
+  uint32_t len_p = k;
+  if (topp) {
+    const MassTarget t_lo = make_mass_target(prm.top_p, z_lo);   // reached first
+    const MassTarget t_hi = make_mass_target(prm.top_p, z_hi);
+    if (t_lo.trivial) {
+      len_p = 1;
+    } else {
+      if (uint32_t(tid) + 1 < k) {
+        if (mass_reaches(cum, t_lo)) atomicMin(&gs.bc32[2], uint32_t(tid));
+        if (mass_reaches(cum, t_hi)) atomicMin(&gs.bc32[3], uint32_t(tid));
+      }
+      cta_sync();
+      uint32_t first = gs.bc32[2];
+      if (first != gs.bc32[3]) {
+        // The bracket does not decide: the exact Z.
+        uint64_t zz = 0;
+        gen_sweep<T>(row, V, [&](int, float z) { zz += mass_fixed(z, ks.rs, table); }, xf);
+        zz = warp_sum<uint64_t>(zz);
+        cta_sync();
+        if (lane == 0) gs.scan64[warp] = zz;
+        if (tid == 0) gs.bc32[2] = k - 1;
+        cta_sync();
+        uint64_t z_exact = 0;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) z_exact += gs.scan64[w];
+        const MassTarget tx = make_mass_target(prm.top_p, z_exact);
+        if (uint32_t(tid) + 1 < k && mass_reaches(cum, tx)) atomicMin(&gs.bc32[2], uint32_t(tid));
+        cta_sync();
+        first = gs.bc32[2];
+      }
+      len_p = first + 1;
+    }
+  }
+  uint32_t len = k < len_p ? k : len_p;
+  len = len < len_m ? len : len_m;
+  if (uint32_t(tid) == len - 1) gs.bc64[0] = cum;
+  cta_sync();
+  const unsigned long long last = list[len - 1];
+  ks.len = len;
+  ks.key = uint32_t(last >> 32);
+  ks.id_cut = ~uint32_t(last);
+  ks.z_kept = gs.bc64[0];
+  cta_sync();
+  *out = ks;
+  return true;
 }

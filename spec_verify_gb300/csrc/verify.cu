@@ -176,6 +176,8 @@ __device__ __forceinline__ void greedy_row_argmax(const T* row, int Vn, int head
 // The statistic of one logit row of a filtered batch row: the row maximum,
 // the kept set S of eq. 39.2 under the row's knobs (the sampler's exact
 // selection over global memory), Z_S and the draft token's mass if it is in S.
+constexpr int kVerifyTopU = 8;   // vectors in flight per thread in the light passes
+
 template <typename T>
 __device__ __forceinline__ void filtered_pos_stat(const VerifyArgs& a, const T* row, int pr, int b, int ipos,
                                                   const FloatPair* table) {
@@ -183,9 +185,11 @@ __device__ __forceinline__ void filtered_pos_stat(const VerifyArgs& a, const T* 
   const int tid = threadIdx.x;
   const int Vn = a.vocab;
   const smp_row_params prm = a.params[b];
-  uint32_t kmax = 0;
-  gen_sweep<T>(row, Vn, [&](int, float z) { kmax = max(kmax, order_key<T>(z)); });
-  kmax = uint32_t(block_max_u64(uint64_t(kmax), gs.red64));
+  // fmaxf skips NaN, which orders with -inf; -0 and +0 share a key
+  float tmax = -INFINITY;
+  gen_sweep<T, kVerifyTopU>(row, Vn, [&](int, float z) { tmax = fmaxf(tmax, z); });
+  const uint32_t tkmax = order_key<T>(tmax);
+  const uint32_t kmax = uint32_t(block_max_u64(uint64_t(tkmax), gs.red64));
   int flags = key_finite<T>(kmax) ? 0 : kRowNonFinite;
   int xd = -1;
   if (ipos < a.k) {
@@ -199,7 +203,9 @@ __device__ __forceinline__ void filtered_pos_stat(const VerifyArgs& a, const T* 
   s.kkey = 0;
   s.kid = 0xFFFFFFFFu;
   if (!flags) {
-    const KeptSet ks = gen_kept_set<T>(row, Vn, gs, table, prm, kmax);
+    KeptSet ks;
+    if (!topk_bounded(prm, Vn) || !gen_kept_set_topk<T, kVerifyTopU>(row, Vn, gs, table, prm, kmax, tkmax, &ks))
+      ks = gen_kept_set<T>(row, Vn, gs, table, prm, kmax);
     s.z = ks.z_kept;
     s.kkey = ks.key;
     s.kid = ks.id_cut;

@@ -262,6 +262,21 @@ __device__ __forceinline__ float exp_fast(float z, const RowScale& rs) {
   return y > -126.0f ? ex2_approx(y) : 0.0f;
 }
 
+// (hi + lo) * 2^n >= x for an exponential in parts and 0 < x < 1, exactly,
+// in binary32: hi * 2^n and lo * 2^n are exact for n >= -100, and within a
+// factor of two of x the difference hi * 2^n - x is exact (Sterbenz), so its
+// sum with lo * 2^n has the sign of the comparison.
+__device__ __forceinline__ bool parts_at_least(const ExpParts& e, float x) {
+  if (e.kind == 1) return true;
+  if (e.kind == 2) return false;
+  if (e.n < -100) return double_from_parts(e) >= double(x);
+  const float sc = pow2f(e.n);
+  const float vh = __fmul_rn(e.hi, sc), vl = __fmul_rn(e.lo, sc);
+  if (vh >= __fmul_rn(2.0f, x)) return true;
+  if (__fmul_rn(2.0f, vh) < x) return false;
+  return __fsub_rn(vh, x) >= -vl;
+}
+
 // exp((z - m) / T) as a double (head + tail, scaled); 0 below 2^-1000.
 __device__ __forceinline__ double mass_double(float z, const RowScale& rs, const FloatPair* table) {
   return double_from_parts(exp_parts(z, rs, table, -1000.0f));

@@ -45,16 +45,11 @@ __device__ void general_row(GenShared& gs, const FloatPair* table, const SampleA
   const int V = a.vocab;
   const T* row = reinterpret_cast<const T*>(a.logits) + size_t(b) * V;
 
-  // The maximum and the lowest id holding it.
-  uint64_t best = 0;
-  gen_sweep<T, light_pass_vectors<Xf>()>(row, V, [&](int i, float z) {
-    const uint64_t p = pack_key_id(order_key<T>(z), uint32_t(i));
-    best = p > best ? p : best;
-  }, xf);
-  const uint32_t thread_key_max = uint32_t(best >> 32);
-  best = block_max_u64(best, gs.red64);
-  const uint32_t key_max = uint32_t(best >> 32);
-  const uint32_t argmax = ~uint32_t(best);
+  // The maximum (fmaxf skips NaN, which orders with -inf; -0 and +0 share a key).
+  float tmax = -INFINITY;
+  gen_sweep<T, light_pass_vectors<Xf>()>(row, V, [&](int, float z) { tmax = fmaxf(tmax, z); }, xf);
+  const uint32_t thread_key_max = order_key<T>(tmax);
+  const uint32_t key_max = uint32_t(block_max_u64(uint64_t(thread_key_max), gs.red64));
   const bool greedy = row_is_greedy(prm);
   int flags = 0;
   if (!key_finite<T>(key_max)) flags |= kRowNonFinite;
@@ -66,7 +61,12 @@ __device__ void general_row(GenShared& gs, const FloatPair* table, const SampleA
     cta_sync();
     return;
   }
-  if (greedy) {
+  if (greedy) {   // the lowest id holding the maximum
+    uint32_t lo = 0xFFFFFFFFu;
+    gen_sweep<T>(row, V, [&](int i, float z) {
+      if (order_key<T>(z) == key_max) lo = min(lo, uint32_t(i));
+    }, xf);
+    const uint32_t argmax = ~uint32_t(block_max_u64(uint64_t(~lo), gs.red64));
     if (tid == 0) {
       a.out_ids[b] = int32_t(argmax);
       if (a.out_probs) a.out_probs[b] = 1.0f;
@@ -79,8 +79,11 @@ __device__ void general_row(GenShared& gs, const FloatPair* table, const SampleA
   }
 
   KeptSet ks;
+  // vectors in flight in the candidate pass: three binary32 vectors keep the
+  // sampler kernel within its registers
+  constexpr int kListU = sizeof(T) == 4 ? 3 : kTopU;
   const bool listed = topk_bounded(prm, V) &&
-                      gen_kept_set_topk<T>(row, V, gs, table, prm, key_max, thread_key_max, &ks, xf);
+                      gen_kept_set_topk<T, kListU>(row, V, gs, table, prm, key_max, thread_key_max, &ks, xf);
   if (!listed) ks = gen_kept_set<T>(row, V, gs, table, prm, key_max, xf);
   auto mass_of = [&](int i, float z) -> uint64_t { return kept_mass<T>(ks, table, i, z); };
   const uint64_t z_kept = ks.z_kept;

@@ -462,21 +462,6 @@ __device__ __forceinline__ void push_unit(StreamShared& ss, CandShared& cs, cons
   }
 }
 
-// (hi + lo) * 2^n >= x for an exponential in parts and 0 < x < 1, exactly,
-// in binary32: hi * 2^n and lo * 2^n are exact for n >= -100, and within a
-// factor of two of x the difference hi * 2^n - x is exact (Sterbenz), so its
-// sum with lo * 2^n has the sign of the comparison.
-__device__ __forceinline__ bool parts_at_least(const ExpParts& e, float x) {
-  if (e.kind == 1) return true;
-  if (e.kind == 2) return false;
-  if (e.n < -100) return double_from_parts(e) >= double(x);
-  const float sc = pow2f(e.n);
-  const float vh = __fmul_rn(e.hi, sc), vl = __fmul_rn(e.lo, sc);
-  if (vh >= __fmul_rn(2.0f, x)) return true;
-  if (__fmul_rn(2.0f, vh) < x) return false;
-  return __fsub_rn(vh, x) >= -vl;
-}
-
 // Exact selection and draw of a min-p / top-k candidate-path row.  The
 // candidates hold every element at or above a lower bound of the kept set's
 // boundary; row_max is the row's largest logit.  Returns false if the row

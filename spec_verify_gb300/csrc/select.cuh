@@ -613,11 +613,11 @@ __device__ KeptSet gen_kept_set(const T* row, int V, GenShared& gs, const FloatP
 // With top-k set to k <= kTopKMax the kept set holds at most k tokens, so it
 // comes from a short candidate list instead of radix passes over the row.
 // theta, the k-th largest of the threads' maximum keys from the caller's
-// maximum pass, bounds the row's k-th largest key from below (k threads each
-// saw a key >= theta); one pass collects every token with key >= theta, and
+// maximum pass (to 16 bits), bounds the row's k-th largest key from below
+// (k threads each saw a key >= theta); one pass collects every token with key >= theta, and
 // the candidates are ranked exactly by (key desc, id asc).  The first k get
-// their exact fixed-point masses and prefix sums; min-p cuts where the keys
-// fall below its threshold key; top-p compares the prefix sums with
+// their exact fixed-point masses and prefix sums; min-p cuts at the first
+// whose exponential falls below min_p; top-p compares the prefix sums with
 // top_p * Z, Z bracketed by a binary32 sum of every token's exponential
 // taken in the same pass (topk_z_bracket).  A prefix that falls inside the
 // bracket asks for the exact Z, one more pass.  More than kTopCandMax candidates
@@ -659,11 +659,11 @@ __device__ __forceinline__ bool topk_bounded(const smp_row_params& prm, int V) {
 // (topk_z_bracket).
 struct ZSums {
   float z;    // sum of e'
-  float a;    // sum of e' |y'|
+  float a;    // -(sum of e' |y'|)
 };
 
-template <typename T, int kU, bool kRaw, typename Xf>
-__device__ __forceinline__ ZSums topk_candidate_pass(const T* row, int V, uint32_t theta, float theta_v, bool topp,
+template <typename T, int kU, bool kRaw, bool kTopp, typename Xf>
+__device__ __forceinline__ ZSums topk_candidate_pass(const T* row, int V, uint32_t theta, float theta_v,
                                                      const RowScale& rs, unsigned long long* cand, uint32_t* count,
                                                      const Xf& xf) {
   using Vo = VecOps<T>;
@@ -676,17 +676,17 @@ __device__ __forceinline__ ZSums topk_candidate_pass(const T* row, int V, uint32
   const int nvec = mid ? int((a1 - a0) / 16) : 0;
   const uint4* vp = reinterpret_cast<const uint4*>(a0);
   ZSums acc{0.0f, 0.0f};
-  auto visit = [&](int id, float z) -> float {
-    const bool c = kRaw ? (z >= theta_v) : (order_key<T>(z) >= theta);
-    if (c) {
-      const uint32_t s = atomicAdd(count, 1u);
-      if (s < uint32_t(kTopCandMax)) cand[s] = pack_key_id(order_key<T>(z), uint32_t(id));
-    }
-    if (!topp) return 0.0f;
-    const float y = __fmul_rn(__fsub_rn(z, rs.m), rs.c_hi);
-    const bool live = y > -126.0f;   // false for -inf and NaN
+  auto is_cand = [&](float z) -> bool { return kRaw ? (z >= theta_v) : (order_key<T>(z) >= theta); };
+  auto append = [&](int id, float z) {
+    const uint32_t s = atomicAdd(count, 1u);
+    if (s < uint32_t(kTopCandMax)) cand[s] = pack_key_id(order_key<T>(z), uint32_t(id));
+  };
+  // e' of one logit (0 unless live); y clamped at -127 (also -inf and NaN),
+  // where the flushed result is 0; acc.a gathers -sum e' |y'| (y <= 0)
+  auto expo = [&](float z, bool live) -> float {
+    const float y = fmaxf(__fmul_rn(__fsub_rn(z, rs.m), rs.c_hi), -127.0f);
     const float e = live ? ex2_approx(y) : 0.0f;
-    acc.a = __fmaf_rn(e, live ? -y : 0.0f, acc.a);
+    acc.a = __fmaf_rn(e, y, acc.a);
     return e;
   };
   for (int base = 0; base < nvec; base += kThreads * kU) {
@@ -694,18 +694,23 @@ __device__ __forceinline__ ZSums topk_candidate_pass(const T* row, int V, uint32
 #pragma unroll
     for (int u = 0; u < kU; ++u) {
       const int v = base + u * kThreads + int(threadIdx.x);
-      if (v < nvec) x[u] = __ldg(vp + v);
+      x[u] = v < nvec ? __ldg(vp + v) : make_uint4(0u, 0u, 0u, 0u);
     }
+    // Every exponential first, free of branches, with a bit per candidate;
+    // the candidates (rare) after, their logits read again one by one.
+    static_assert(kU * kPer <= 64, "one bit per element of a round");
+    unsigned long long bits = 0;
 #pragma unroll
     for (int u = 0; u < kU; ++u) {
       const int v = base + u * kThreads + int(threadIdx.x);
-      if (v < nvec) {
-        float ev[kPer];
+      float ev[kPer];
 #pragma unroll
-        for (int q = 0; q < kPer; ++q) {
-          const int id = head + v * kPer + q;
-          ev[q] = visit(id, xf(id, Vo::elem(x[u], q)));
-        }
+      for (int q = 0; q < kPer; ++q) {
+        const float z = xf(head + v * kPer + q, Vo::elem(x[u], q));
+        if (v < nvec && is_cand(z)) bits |= 1ull << (u * kPer + q);
+        if (kTopp) ev[q] = expo(z, v < nvec);
+      }
+      if (kTopp) {
 #pragma unroll
         for (int w = 1; w < kPer; w <<= 1)
 #pragma unroll
@@ -713,10 +718,31 @@ __device__ __forceinline__ ZSums topk_candidate_pass(const T* row, int V, uint32
         acc.z = __fadd_rn(acc.z, ev[0]);
       }
     }
+    if (__any_sync(0xFFFFFFFFu, bits != 0)) {
+      // One atomic per warp: each lane's count, an exclusive scan over the
+      // lanes, lane 31 reserves the warp's slots.
+      const uint32_t mine = uint32_t(__popcll(bits));
+      const uint32_t incl = warp_inclusive_scan<uint32_t>(mine);
+      uint32_t slot = 0;
+      if ((threadIdx.x & 31) == 31) slot = atomicAdd(count, incl);
+      slot = __shfl_sync(0xFFFFFFFFu, slot, 31) + incl - mine;
+      while (bits) {
+        const int j = __ffsll((long long)bits) - 1;
+        bits &= bits - 1;
+        const int id = head + (base + (j / kPer) * kThreads + int(threadIdx.x)) * kPer + j % kPer;
+        const float z = xf(id, Elem<T>::widen(row[id]));
+        if (slot < uint32_t(kTopCandMax)) cand[slot] = pack_key_id(order_key<T>(z), uint32_t(id));
+        ++slot;
+      }
+    }
   }
-  for (int i = threadIdx.x; i < head; i += kThreads) acc.z = __fadd_rn(acc.z, visit(i, xf(i, Elem<T>::widen(row[i]))));
-  for (int i = tail0 + threadIdx.x; i < V; i += kThreads)
-    acc.z = __fadd_rn(acc.z, visit(i, xf(i, Elem<T>::widen(row[i]))));
+  auto one = [&](int i) {
+    const float z = xf(i, Elem<T>::widen(row[i]));
+    if (is_cand(z)) append(i, z);
+    if (kTopp) acc.z = __fadd_rn(acc.z, expo(z, true));
+  };
+  for (int i = threadIdx.x; i < head; i += kThreads) one(i);
+  for (int i = tail0 + threadIdx.x; i < V; i += kThreads) one(i);
   return acc;
 }
 
@@ -728,41 +754,50 @@ __device__ __forceinline__ ZSums topk_candidate_pass(const T* row, int V, uint32
 //    (2.8 * 2^-24 A);
 //  * ex2.approx: relative error below 2^-21 (the instruction's is about 2^-22);
 //  * the sums: a thread adds at most log2(elements per vector) + its vectors
-//    + 2 terms in sequence, each add within 2^-24 of its running sum;
+//    + 2 terms in sequence, a warp's lanes meet in a tree of depth 5 and
+//    thread 0 adds the warps' sums in sequence, each add within 2^-24 of its
+//    running sum;
 //  * the fixed-point masses: 3/4 of a unit per token (rounding, and values
 //    below 2^-47 dropped); tokens below 2^-126, dropped here, weigh less.
-// Margins of 2^-10 cover the second-order terms and the double arithmetic.
+// Margins of 2^-9 cover the second-order terms; the bound itself is
+// evaluated with upward rounding.
 template <typename T>
 __device__ __forceinline__ void topk_z_bracket(ZSums acc, int V, GenShared& gs, uint64_t* z_lo, uint64_t* z_hi) {
   constexpr int kLogPer = VecOps<T>::kPer == 8 ? 3 : VecOps<T>::kPer == 4 ? 2 : 1;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  double zt = double(acc.z), at = double(acc.a);
+  float zt = acc.z, at = -acc.a;
 #pragma unroll
-  for (int o = 16; o; o >>= 1) {
-    zt += __shfl_xor_sync(0xFFFFFFFFu, zt, o);
-    at += __shfl_xor_sync(0xFFFFFFFFu, at, o);
+  for (int o = 16; o; o >>= 1) {   // a tree of depth 5 over the lanes
+    zt = __fadd_rn(zt, __shfl_xor_sync(0xFFFFFFFFu, zt, o));
+    at = __fadd_rn(at, __shfl_xor_sync(0xFFFFFFFFu, at, o));
   }
-  if (lane == 0) {
-    gs.scan64[warp] = (unsigned long long)__double_as_longlong(zt);
-    gs.red64[warp] = (uint64_t)__double_as_longlong(at);
+  float2* part = reinterpret_cast<float2*>(gs.scan64);
+  if (lane == 0) part[warp] = make_float2(zt, at);
+  cta_sync();
+  if (threadIdx.x == 0) {
+    // binary32 throughout (thread 0 alone), every rounding inside the margins
+    float zf = 0.0f, af = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      zf = __fadd_rn(zf, part[w].x);
+      af = __fadd_rn(af, part[w].y);
+    }
+    const int nvec = V * int(sizeof(T)) / 16 + 1;
+    const float adds = float(kLogPer + (nvec + kThreads - 1) / kThreads + 2 + 5 + kWarps);
+    const float u = 0x1p-24f;
+    const float zd = __fmul_rn(zf, float(kFixedOne));   // exact
+    const float rel = __fmul_ru(__fmaf_ru(adds, u, 0x1p-21f), 1.0f + 0x1p-9f);
+    const float w = __fmul_ru(__fadd_ru(__fadd_ru(__fmul_ru(rel, zd),
+                                                  __fmul_ru(__fmul_ru(2.8f * u, af), float(kFixedOne))),
+                                        __fmaf_ru(0.75f, float(V), 2.0f)),
+                              1.0f + 0x1p-9f);
+    const float lo = __fsub_rd(zd, w);
+    gs.bc64[1] = lo > 0.0f ? __float2ull_rd(lo) : 0ull;
+    gs.bc64[2] = __float2ull_ru(__fadd_ru(zd, w));
   }
   cta_sync();
-  double zf = 0.0, af = 0.0;
-#pragma unroll
-  for (int w = 0; w < kWarps; ++w) {
-    zf += __longlong_as_double((long long)gs.scan64[w]);
-    af += __longlong_as_double((long long)gs.red64[w]);
-  }
-  cta_sync();
-  const int nvec = V * int(sizeof(T)) / 16 + 1;
-  const double adds = double(kLogPer + (nvec + kThreads - 1) / kThreads + 2);
-  const double u = 0x1p-24;
-  const double rel = (0x1p-21 + adds * u) * (1.0 + 0x1p-10);
-  const double zd = zf * double(kFixedOne);
-  const double ad = af * double(kFixedOne) * (1.0 + 0x1p-10);
-  const double w = rel * zd + 2.8 * u * ad + 0.75 * double(V) + 2.0;
-  *z_lo = zd - w > 0.0 ? __double2ull_rd(zd - w) : 0ull;
-  *z_hi = __double2ull_ru(zd + w);
+  *z_lo = gs.bc64[1];
+  *z_hi = gs.bc64[2];
 }
 
 // S and Z_S of a row as gen_kept_set gives them, for a row with
@@ -777,7 +812,6 @@ template <typename T, int kU = kTopU, typename Xf = NoPrep>
 __device__ bool gen_kept_set_topk(const T* row, int V, GenShared& gs, const FloatPair* table,
                                   const smp_row_params& prm, uint32_t key_max, uint32_t thread_key_max,
                                   KeptSet* out, const Xf& xf = Xf()) {
-  constexpr int kKeyLevels = KeyTraits<T>::kBits == 32 ? 4 : 2;
   constexpr int kKeyUp = 32 - KeyTraits<T>::kBits;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t k = uint32_t(prm.top_k);
@@ -786,14 +820,14 @@ __device__ bool gen_kept_set_topk(const T* row, int V, GenShared& gs, const Floa
   KeptSet ks;
   ks.rs = make_row_scale(key_value<T>(key_max), prm.temperature);
 
-  // theta: the k-th largest of the threads' maximum keys (k <= kThreads).
+  // theta: the top 16 bits of the k-th largest of the threads' maximum keys
+  // (k <= kThreads), the rest zero: exact for bf16 keys, a lower bound one
+  // bf16 step wide for binary32 keys, which only adds a few candidates.
   uint32_t* tkeys = &gs.cnt[0][0];
   cta_sync();   // earlier readers of the overlaid state are done
   tkeys[tid] = thread_key_max;
-  const uint32_t theta = kth_largest_key<kKeyLevels>(
-      kThreads, k, [&](int i) { return tkeys[i] << kKeyUp; }, gs.tot_cnt, gs.bc32);
-  const uint32_t key_min_p =
-      minp ? minp_threshold_key<T>(gs.bc32, table, ks.rs, prm.temperature, prm.min_p, key_max) : 0u;
+  const uint32_t theta = kth_largest_key<2>(kThreads, k, [&](int i) { return tkeys[i] << kKeyUp; },
+                                             gs.tot_cnt, gs.bc32) << (16 - kKeyUp);
 
   // One pass: the candidates, and the sums of the bracket on Z.
   constexpr bool kRaw = std::is_same<Xf, NoPrep>::value;
@@ -801,8 +835,10 @@ __device__ bool gen_kept_set_topk(const T* row, int V, GenShared& gs, const Floa
   unsigned long long* cand = topk_cand(gs);
   if (tid == 0) gs.bc32[5] = 0;
   cta_sync();
-  const ZSums acc = topk_candidate_pass<T, light_pass_vectors<Xf, kU>(), kRaw>(
-      row, V, theta, key_value<T>(theta), topp, ks.rs, cand, &gs.bc32[5], xf);
+  constexpr int kPassU = light_pass_vectors<Xf, kU>();
+  const ZSums acc =
+      topp ? topk_candidate_pass<T, kPassU, kRaw, true>(row, V, theta, key_value<T>(theta), ks.rs, cand, &gs.bc32[5], xf)
+           : topk_candidate_pass<T, kPassU, kRaw, false>(row, V, theta, key_value<T>(theta), ks.rs, cand, &gs.bc32[5], xf);
   cta_sync();
   const uint32_t n = gs.bc32[5];
   if (n > uint32_t(kTopCandMax) || n < k) {   // (n >= k whenever thread_key_max is as stated)
@@ -826,18 +862,19 @@ __device__ bool gen_kept_set_topk(const T* row, int V, GenShared& gs, const Floa
     gs.bc32[3] = k - 1;   // first rank whose prefix surely reaches it
   }
   cta_sync();
-  // Exact masses of the first k (their logits read again), the min-p cut.
+  // Exact masses of the first k (their logits read again), and the min-p
+  // test exp((z - m) / T) >= min_p on each (parts_at_least, exact).
   uint64_t e = 0;
   bool below_min_p = false;
   if (uint32_t(tid) < k) {
-    const unsigned long long pc = list[tid];
-    const uint32_t id = ~uint32_t(pc);
-    e = mass_fixed(xf(int(id), Elem<T>::widen(row[id])), ks.rs, table);
+    const uint32_t id = ~uint32_t(list[tid]);
+    const ExpParts ep = exp_parts(xf(int(id), Elem<T>::widen(row[id])), ks.rs, table, -1000.0f);
+    e = fixed_from_parts(ep);
     lmass[tid] = e;
-    below_min_p = minp && uint32_t(pc >> 32) < key_min_p;
+    below_min_p = minp && !parts_at_least(ep, prm.min_p);
   }
-  // Keys fall along the ranks, so the tokens at or above the min-p key are
-  // the ranks below the first that is not (the maximum always is).
+  // Masses fall along the ranks, so the tokens that pass min-p are the ranks
+  // below the first that does not (the maximum always passes).
   const uint32_t len_m = k - uint32_t(cta_sync_count(below_min_p));
   uint64_t total;
   const uint64_t cum =   // prefix mass through this rank

@@ -1,6 +1,7 @@
 """The kept set of rows with top-k up to 128 and top-p (or min-p) from a ranked
-candidate list, on the sampler's general path and the verifier's filtered
-rows, against the fp64 oracle: candidates above the k-th largest thread
+candidate list, on the sampler's general path (binary32 rows; bf16 rows there
+take the count table and are compared alike) and the verifier's filtered
+rows of both types, against the fp64 oracle: candidates above the k-th largest thread
 maximum, exact ranks by (logit desc, id asc), top-p decided from a bracket on
 Z or, when a prefix lands inside it, from the exact Z; the draw read from the
 list.  Rows with long runs of equal logits overflow the list and take the
@@ -181,3 +182,24 @@ def test_verifier_rows_with_top_k(dtype):
     assert int(status.cpu()[0]) == 0
     want = over.spec_verify(vb.values("p"), vb.values("q"), drafts, 21, 4, params=prm)
     compare_verify(want, acc.cpu().numpy(), ids.cpu().numpy()).check()
+
+
+def test_top_p_within_a_few_millionths_of_a_prefix():
+    # top_p placed 1.05e-6 to 1.3e-6 (of Z) from the mass of a prefix that
+    # holds 70 to 97 % of it: outside the parity band, inside the binary32
+    # bracket on Z (about 2e-6 of top_p * Z here), so these rows decide top-p
+    # with the exact Z
+    rng = np.random.default_rng(77)
+    n, V = 48, 5003
+    rows = rng.normal(0.0, 4.0, size=(n, V)).astype(np.float32)
+    prm = knobs(n, np.int32(100), np.float32(0.9))
+    deltas = np.array([-1.3e-6, -1.15e-6, -1.05e-6, 1.05e-6, 1.15e-6, 1.3e-6])
+    for b in range(n):
+        z = rows[b].astype(np.float64)
+        order = np.lexsort((np.arange(V), -z))
+        w = np.exp(z[order] - z.max())
+        cum = np.cumsum(w) / w.sum()
+        r = min(int(np.searchsorted(cum, rng.uniform(0.7, 0.97))) + 1, 99)
+        prm["top_p"][b] = np.float32(cum[r - 1] + deltas[b % len(deltas)])
+    prm["min_p"][::7] = 1e-4
+    check(batch_of(rows, prm, "f32"))

@@ -752,7 +752,8 @@ __device__ __forceinline__ ZSums topk_candidate_pass(const T* row, int V, uint32
 //    T rounded to c_hi, and the product: 4 units of 2^-24 of |y| in all, so
 //    e' is off by at most ln 2 * 4.01 * 2^-24 |y| e, bounded through A
 //    (2.8 * 2^-24 A);
-//  * ex2.approx: relative error below 2^-21 (the instruction's is about 2^-22);
+//  * ex2.approx: taken within 2^-21 relative (its largest relative error over
+//    every binary32 argument in [-126, 1], measured on GB300, is 1.46e-7);
 //  * the sums: a thread adds at most log2(elements per vector) + its vectors
 //    + 2 terms in sequence, a warp's lanes meet in a tree of depth 5 and
 //    thread 0 adds the warps' sums in sequence, each add within 2^-24 of its

@@ -287,6 +287,8 @@ __global__ void __launch_bounds__(kThreads) beam_merge_kernel(BeamArgs a) {
   __shared__ double cs[kBeamMaxCand];
   __shared__ int32_t cf[kBeamMaxCand];   // flat index, or -1 for an empty slot
   __shared__ double beam_c[SMP_MAX_BEAM_WIDTH];
+  __shared__ double beam_m[SMP_MAX_BEAM_WIDTH];
+  __shared__ int beam_f[SMP_MAX_BEAM_WIDTH];
   __shared__ int bad;
   const int g = int(blockIdx.x);
   const int W = a.beams, width = a.width, V = a.vocab, S = a.slices;
@@ -308,6 +310,7 @@ __global__ void __launch_bounds__(kThreads) beam_merge_kernel(BeamArgs a) {
     cf[c] = h->flags;
   }
   __syncthreads();
+  // Per beam (thread b): the flags and the slices' maximum m.
   if (tid < W) {
     const int b = tid;
     int f = isnan(a.scores[size_t(g) * W + b]) ? kRowBadParams : 0;
@@ -322,12 +325,25 @@ __global__ void __launch_bounds__(kThreads) beam_merge_kernel(BeamArgs a) {
       }
     }
     if (!any) f |= kRowNonFinite;
-    double z = 0.0;
-    if (!f)
-      for (int s = 0; s < S; ++s)
-        if (!cf[b * S + s]) z += cs[b * S + s] * exp(cs[kHalf + b * S + s] - m);
-    beam_c[b] = f ? 0.0 : -m - log(z);
+    beam_m[b] = m;
+    beam_f[b] = f;
     if (f) atomicOr(&bad, f);
+  }
+  __syncthreads();
+  // Each slice's Z_s exp(m_s - m), one fp64 exponential per thread (they
+  // are long on this part's fp64 pipe, so not one beam's after another).
+  for (int c = tid; c < W * S; c += kThreads) {
+    const int b = c / S;
+    cs[c] = (beam_f[b] || cf[c]) ? 0.0 : cs[c] * exp(cs[kHalf + c] - beam_m[b]);
+  }
+  __syncthreads();
+  if (tid < W) {   // Z in slice order, then the beam's constant -m - ln Z
+    const int b = tid;
+    double z = 0.0;
+    if (!beam_f[b])
+      for (int s = 0; s < S; ++s)
+        if (!cf[b * S + s]) z += cs[b * S + s];
+    beam_c[b] = beam_f[b] ? 0.0 : -beam_m[b] - log(z);
   }
   // ranks nobody fills (fewer candidates than width, or an error group) stay -1 / NaN
   for (int r = tid; r < width; r += kThreads) {

@@ -710,7 +710,10 @@ __global__ void __launch_bounds__(kResolveThreads, 2) verify_resolve_kernel(Veri
   // when read_q is false): all its vectors requested first, then a rolled
   // loop over the groups (this code runs once per CTA, cold in the
   // instruction cache, so it is kept short).
+  // w returns a 52-bit fixed-point weight, summed as is, or a binary32 value,
+  // summed in binary32 over each group of 16 ids and then converted once.
   auto pair_sum = [&](const T* pr_, const T* qr_, bool read_q, auto&& w) -> uint64_t {
+    using Acc = decltype(w(0, 0.0f, 0.0f));
     const bool vok = ((reinterpret_cast<uintptr_t>(pr_) | reinterpret_cast<uintptr_t>(qr_)) & 15) == 0;
     uint64_t sum = 0;
     const uint32_t ninf = VecOps<T>::neg_inf();
@@ -726,6 +729,7 @@ __global__ void __launch_bounds__(kResolveThreads, 2) verify_resolve_kernel(Veri
           xq[gi] = read_q ? __ldg(reinterpret_cast<const uint4*>(qr_ + gg)) : xp[gi];
         }
       }
+      Acc gsum = 0;
 #pragma unroll 1
       for (int gi = 0; gi < kGroups; ++gi) {
         const int gg = g0 + gi * kPer;
@@ -745,9 +749,11 @@ __global__ void __launch_bounds__(kResolveThreads, 2) verify_resolve_kernel(Veri
             zp = gg + e < c1 ? Elem<T>::widen(pr_[gg + e]) : -INFINITY;
             zq = gg + e < c1 ? Elem<T>::widen(qr_[gg + e]) : -INFINITY;
           }
-          sum += w(gg + e, zp, zq);
+          gsum += w(gg + e, zp, zq);
         }
       }
+      if constexpr (std::is_same<Acc, float>::value) sum += fixed52(gsum);
+      else sum += gsum;
     }
     return sum;
   };
@@ -803,9 +809,11 @@ __global__ void __launch_bounds__(kResolveThreads, 2) verify_resolve_kernel(Veri
 
   // Acceptance rates alpha_i = sum_x min(p_i(x), q_i(x)) for every draft
   // position ("Decoding & Speculative Sampling", section 39.4, Listing 39.5),
-  // on the compared distributions (binary32 p and q, 52-bit fixed-point sums
-  // over the same id chunks as the draw).  The p_i and q_i rows were read by
-  // the position kernel just before and are normally served by L2.
+  // on the compared distributions (binary32 p and q; binary32 sums over
+  // groups of 16 ids, within 16 units of 2^-24 of each group's sum, then
+  // 52-bit fixed-point sums over the same id chunks as the draw).  The p_i
+  // and q_i rows were read by the position kernel just before and are
+  // normally served by L2.
   if constexpr (kParams) {
     if (a.alpha) {
       AlphaShared& as = alpha_shared();
@@ -819,14 +827,14 @@ __global__ void __launch_bounds__(kResolveThreads, 2) verify_resolve_kernel(Veri
         kqi.key = as.kept[2][i];
         kqi.id_cut = as.kept[3][i];
         uint64_t sum = pair_sum(logit_row<T>(a, b, i), logit_row<T>(a, b, K + 1 + i), true,
-                                [&](int id, float zp, float zq) -> uint64_t {
+                                [&](int id, float zp, float zq) -> float {
                                   float p = __fmul_rn(exp_fast(zp, sp), izp);
                                   float q = __fmul_rn(exp_fast(zq, sq), izq);
                                   if (filt) {
                                     if (!in_kept_set(kpi, order_key<T>(zp), uint32_t(id))) p = 0.0f;
                                     if (!in_kept_set(kqi, order_key<T>(zq), uint32_t(id))) q = 0.0f;
                                   }
-                                  return fixed52(fminf(p, q));
+                                  return fminf(p, q);
                                 });
         sum = warp_sum<uint64_t>(sum);
         if ((tid & 31) == 0 && sum) atomicAdd(&as.cta[i], (unsigned long long)sum);

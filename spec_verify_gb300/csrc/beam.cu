@@ -227,16 +227,26 @@ __global__ void __launch_bounds__(kThreads, 2) beam_row_kernel(BeamArgs a) {
   constexpr int kBeamList = int(sizeof(gs.mass) / sizeof(unsigned long long));
   if (tid == 0) n_members = 0;
   cta_sync();
-  gen_sweep<T, kBeamU>(row, len, [&](int i, float z) {
-    const uint32_t k = order_key<T>(isnan(z) ? -INFINITY : z);   // NaN counts as -inf
-    if (k >= theta) {
-      const int slot = atomicAdd(&n_members, 1);
-      if (slot < kBeamList) list[slot] = pack_key_id(k, uint32_t(i));
-    }
-  });
+  // A finite theta: the sampler's candidate pass (a bit per element, one
+  // atomic per warp, the marked logits read again), up to kTopCandMax
+  // entries; else (NaN counts as -inf, and -inf may be listed) one atomic
+  // per listed element, up to kBeamList.
+  const bool finite_theta = key_finite<T>(theta);
+  if (finite_theta) {
+    topk_candidate_pass<T, kBeamU, true, false>(row, len, theta, key_value<T>(theta), RowScale{}, list,
+                                                reinterpret_cast<uint32_t*>(&n_members), NoPrep());
+  } else {
+    gen_sweep<T, kBeamU>(row, len, [&](int i, float z) {
+      const uint32_t k = order_key<T>(z);   // NaN has the key of -inf
+      if (k >= theta) {
+        const int slot = atomicAdd(&n_members, 1);
+        if (slot < kBeamList) list[slot] = pack_key_id(k, uint32_t(i));
+      }
+    });
+  }
   cta_sync();
   int nl = n_members;
-  if (nl > kBeamList) {   // too many at or above theta: exact radix selection of the boundary
+  if (nl > (finite_theta ? kTopCandMax : kBeamList)) {   // too many at or above theta: exact radix selection of the boundary
     smp_row_params prm;
     prm.temperature = 1.0f;
     prm.top_k = a.width;

@@ -416,11 +416,11 @@ static smp_status launch_beam(const BeamArgs& args, cudaStream_t stream) {
   BeamArgs a = args;
   const int dev = current_device();
   if (dev < 0) return fail_cuda(cudaGetLastError());
-  // Slices: enough CTAs for about two per SM, at most kBeamMaxSlices, at
-  // least 2048 ids each, and no more candidates per group than one merge CTA
-  // ranks.
+  // Slices: as many CTAs as fit in one wave at two per SM (rounded down, so
+  // that no slice waits for a second wave), at most kBeamMaxSlices, at least
+  // 2048 ids each, and no more candidates per group than one merge CTA ranks.
   const int64_t rows = int64_t(a.groups) * a.beams;
-  int S = int((2 * int64_t(device_sms(dev)) + rows - 1) / rows);
+  int S = int(2 * int64_t(device_sms(dev)) / rows);
   S = std::min(S, kBeamMaxSlices);
   S = std::min(S, kBeamMaxCand / (a.beams * a.width));
   S = std::min(S, (a.vocab + 2047) / 2048);

@@ -1,15 +1,18 @@
 // Exact selection of a row's kept set, shared by the sampler's general path
 // and the verifier's filtered rows ("Decoding & Speculative Sampling",
 // section 39.2 and eq. 39.2): knob rules, the min-p threshold key, passes over
-// a row in global memory, MSB-first radix selection over order keys, and the
-// kept set S = the shortest of the enabled prefixes of the order (logit
-// descending, id ascending) with its exact fixed-point mass Z_S.
+// a row in global memory, MSB-first radix selection over order keys, the
+// ranked candidate list for top-k up to kTopKMax, and the kept set S = the
+// shortest of the enabled prefixes of the order (logit descending, id
+// ascending) with its exact fixed-point mass Z_S.
 //
-// Every pass reads the row as 16-byte vectors, kGenU per thread in flight, in
-// rounds of kThreads * kGenU vectors; inside a round thread t owns kGenU
-// consecutive vectors, so (round, thread, vector, element) is token-id order.
-// Histograms are private per warp (count histograms for top-k, count and
-// exact fixed-point mass histograms for top-p).
+// Every pass reads the row as 16-byte vectors.  A sweep (no order) keeps kU
+// per thread in flight, vector base + u * kThreads + t for thread t, so each
+// load instruction is coalesced.  A walk (id order) reads rounds of
+// kThreads * kGenU vectors, thread t owning kGenU consecutive ones, so that
+// (round, thread, vector, element) is token-id order.  Histograms are
+// private per warp (count histograms for top-k, count and exact fixed-point
+// mass histograms for top-p).
 //
 // Included inside namespace smp after row_ops.cuh.
 #pragma once
@@ -650,7 +653,8 @@ __device__ __forceinline__ bool topk_bounded(const smp_row_params& prm, int V) {
   return prm.top_k > 0 && prm.top_k <= kTopKMax && prm.top_k < V;
 }
 
-// The candidate pass of gen_kept_set_topk.  Every token whose key is at
+// The candidate pass of gen_kept_set_topk (also the beam step's slices, which
+// ask for no sums).  Every token whose key is at
 // least theta is appended to cand (a count past kTopCandMax is an overflow):
 // raw rows compare the logit with theta's value (theta finite), transformed
 // rows compare keys.  With top-p, each thread also sums e' = 2^y',

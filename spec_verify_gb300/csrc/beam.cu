@@ -14,9 +14,9 @@
 //                      radix selection when too many tie there);
 //   beam_merge_kernel  one CTA per group: each beam's m and Z from its
 //                      slices, the scores s_b + (z - m_b - ln Z_b) in fp64 of
-//                      the listed tokens, and each candidate's rank in the
-//                      group by comparison with all the others; the first
-//                      `width` are written.
+//                      the listed tokens, and the group's best `width` of
+//                      them, picked in rounds of reductions, written in rank
+//                      order.
 // Only a row's best `width` tokens can be among its group's best `width`
 // candidates, because within a beam the score order is the logit order.
 #include <cuda_runtime.h>
@@ -288,16 +288,27 @@ __global__ void __launch_bounds__(kThreads, 2) beam_row_kernel(BeamArgs a) {
   }
 }
 
+// ln z for z >= 1: the binary32 logarithm (logf) of z's mantissa in [1, 2),
+// plus its exponent times ln 2 in fp64.  The mantissa's rounding to binary32
+// and logf each add at most about 6e-8 (absolute; ln of the mantissa < 0.7).
+__device__ __forceinline__ double ln_of_sum(double z) {
+  const long long bits = __double_as_longlong(z);
+  const int e = int((bits >> 52) & 0x7FF) - 1023;
+  const double mant = __longlong_as_double((bits & 0x000FFFFFFFFFFFFFll) | 0x3FF0000000000000ll);
+  return double(logf(float(mant))) + double(e) * 0.6931471805599453;
+}
+
 // One CTA per group.  Per beam: m = the slices' maximum, Z = sum over slices
-// of Z_s exp(m_s - m) in fp64, c = -m - ln Z.  Every listed candidate gets its
-// score s_b + (z + c_b) and its flat index b * V + id; its rank is the number
-// of listed candidates before it in the order (score desc, flat asc), a
-// strict total order, so the first `width` ranks are filled exactly once.
+// of Z_s exp(m_s - m) (binary32 exponentials, fp64 products and sums),
+// c = -m - ln Z.  Every listed candidate gets its score s_b + (z + c_b) and
+// its flat index b * V + id; in the order (score desc, flat asc), a strict
+// total order, the first `width` are picked one per round and written at
+// their ranks.
 __global__ void __launch_bounds__(kThreads) beam_merge_kernel(BeamArgs a) {
   __shared__ double cs[kBeamMaxCand];
   __shared__ int32_t cf[kBeamMaxCand];   // flat index, or -1 for an empty slot
   __shared__ double beam_c[SMP_MAX_BEAM_WIDTH];
-  __shared__ double beam_m[SMP_MAX_BEAM_WIDTH];
+  __shared__ float beam_m[SMP_MAX_BEAM_WIDTH];
   __shared__ int beam_f[SMP_MAX_BEAM_WIDTH];
   __shared__ unsigned long long rk_key[kWarps];   // a ranking round's best per warp
   __shared__ int rk_f[kWarps], rk_c[kWarps];
@@ -313,12 +324,12 @@ __global__ void __launch_bounds__(kThreads) beam_merge_kernel(BeamArgs a) {
   if (tid == 0) bad = 0;
   // The slice headers, one load per thread and all in flight at once, staged
   // in the candidate arrays (free until the candidates are built): Z_s in
-  // cs[c], m_s in cs[half + c], the flags in cf[c] (W * S <= half).
+  // cs[c], the flags in cf[c], the bits of m_s in cf[half + c] (W * S <= half).
   constexpr int kHalf = kBeamMaxCand / 2;
   for (int c = tid; c < W * S; c += kThreads) {
     const BeamSliceHead* h = head_of(c / S, c % S);
     cs[c] = double(h->z) * (1.0 / double(kFixedOne));
-    cs[kHalf + c] = double(h->m);
+    cf[kHalf + c] = __float_as_int(h->m);
     cf[c] = h->flags;
   }
   __syncthreads();
@@ -326,14 +337,14 @@ __global__ void __launch_bounds__(kThreads) beam_merge_kernel(BeamArgs a) {
   if (tid < W) {
     const int b = tid;
     int f = isnan(a.scores[size_t(g) * W + b]) ? kRowBadParams : 0;
-    double m = -INFINITY;
+    float m = -INFINITY;   // the slices' maxima are binary32 logits: fp32 operations, exact
     bool any = false;
     for (int s = 0; s < S; ++s) {
       const int fl = cf[b * S + s];
       f |= fl & kRowNonFinite;
       if (!fl) {
         any = true;
-        m = fmax(m, cs[kHalf + b * S + s]);
+        m = fmaxf(m, __int_as_float(cf[kHalf + b * S + s]));
       }
     }
     if (!any) f |= kRowNonFinite;
@@ -342,11 +353,12 @@ __global__ void __launch_bounds__(kThreads) beam_merge_kernel(BeamArgs a) {
     if (f) atomicOr(&bad, f);
   }
   __syncthreads();
-  // Each slice's Z_s exp(m_s - m), one fp64 exponential per thread (they
-  // are long on this part's fp64 pipe, so not one beam's after another).
+  // Each slice's Z_s exp(m_s - m), one per thread: the binary32 exponential
+  // (expf) of the binary32 difference, times Z_s in fp64.  The fp64 pipe of
+  // this part is narrow, so the merge keeps fp64 to sums and products.
   for (int c = tid; c < W * S; c += kThreads) {
     const int b = c / S;
-    cs[c] = (beam_f[b] || cf[c]) ? 0.0 : cs[c] * exp(cs[kHalf + c] - beam_m[b]);
+    cs[c] = (beam_f[b] || cf[c]) ? 0.0 : cs[c] * double(expf(__fsub_rn(__int_as_float(cf[kHalf + c]), beam_m[b])));
   }
   __syncthreads();
   if (tid < W) {   // Z in slice order, then the beam's constant -m - ln Z
@@ -355,7 +367,7 @@ __global__ void __launch_bounds__(kThreads) beam_merge_kernel(BeamArgs a) {
     if (!beam_f[b])
       for (int s = 0; s < S; ++s)
         if (!cf[b * S + s]) z += cs[b * S + s];
-    beam_c[b] = beam_f[b] ? 0.0 : -beam_m[b] - log(z);
+    beam_c[b] = beam_f[b] ? 0.0 : -double(beam_m[b]) - ln_of_sum(z);
   }
   // ranks nobody fills (fewer candidates than width, or an error group) stay -1 / NaN
   for (int r = tid; r < width; r += kThreads) {

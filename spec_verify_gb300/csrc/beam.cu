@@ -15,8 +15,8 @@
 //   beam_merge_kernel  one CTA per group: each beam's m and Z from its
 //                      slices, the scores s_b + (z - m_b - ln Z_b) in fp64 of
 //                      the listed tokens, and the group's best `width` of
-//                      them, picked in rounds of reductions, written in rank
-//                      order.
+//                      them, picked by warp 0 in rounds of reductions,
+//                      written in rank order.
 // Only a row's best `width` tokens can be among its group's best `width`
 // candidates, because within a beam the score order is the logit order.
 #include <cuda_runtime.h>
@@ -310,8 +310,6 @@ __global__ void __launch_bounds__(kThreads) beam_merge_kernel(BeamArgs a) {
   __shared__ double beam_c[SMP_MAX_BEAM_WIDTH];
   __shared__ float beam_m[SMP_MAX_BEAM_WIDTH];
   __shared__ int beam_f[SMP_MAX_BEAM_WIDTH];
-  __shared__ unsigned long long rk_key[kWarps];   // a ranking round's best per warp
-  __shared__ int rk_f[kWarps], rk_c[kWarps];
   __shared__ int bad;
   const int g = int(blockIdx.x);
   const int W = a.beams, width = a.width, V = a.vocab, S = a.slices;
@@ -407,59 +405,47 @@ __global__ void __launch_bounds__(kThreads) beam_merge_kernel(BeamArgs a) {
   __syncthreads();
   for (int c = tid; c < n; c += kThreads) ck[c] = to_key(cs[c]);
   __syncthreads();
-  // The best `width` in rounds: each round every thread offers its best
-  // candidate not yet taken (score key desc, flat asc), a warp reduction and
-  // thread 0 over the warps pick the round's winner, which is written at that
-  // rank and taken.  (Ranking every candidate against all others ran one
-  // shared load after another, 8-11 us for 144 candidates.)
-  const int lane = tid & 31, warp = tid >> 5;
-  for (int r = 0; r < width; ++r) {
-    unsigned long long bk = 0;
-    int bf = INT_MAX, bc = -1;
-    for (int c = tid; c < n; c += kThreads) {
-      const int f = cf[c];
-      if (f < 0) continue;
-      const unsigned long long k = ck[c];
-      if (bc < 0 || k > bk || (k == bk && f < bf)) {
-        bk = k;
-        bf = f;
-        bc = c;
-      }
-    }
-#pragma unroll
-    for (int o = 16; o; o >>= 1) {
-      const unsigned long long ok = shfl_xor_u64(bk, o);
-      const int of = __shfl_xor_sync(0xFFFFFFFFu, bf, o);
-      const int oc = __shfl_xor_sync(0xFFFFFFFFu, bc, o);
-      if (oc >= 0 && (bc < 0 || ok > bk || (ok == bk && of < bf))) {
-        bk = ok;
-        bf = of;
-        bc = oc;
-      }
-    }
-    if (lane == 0) {
-      rk_key[warp] = bk;
-      rk_f[warp] = bf;
-      rk_c[warp] = bc;
-    }
-    __syncthreads();
-    if (tid == 0) {
-      int wc = -1, wf = INT_MAX;
-      unsigned long long wk = 0;
-      for (int w = 0; w < kWarps; ++w)
-        if (rk_c[w] >= 0 && (wc < 0 || rk_key[w] > wk || (rk_key[w] == wk && rk_f[w] < wf))) {
-          wk = rk_key[w];
-          wf = rk_f[w];
-          wc = rk_c[w];
+  // The best `width` in rounds, by warp 0 alone: each round every lane
+  // offers its best candidate not yet taken (score key desc, flat asc), a
+  // warp reduction picks the round's winner, written at that rank and taken.
+  // (A rank per candidate by comparison with all others ran one shared load
+  // after another, 8-11 us for 144 candidates; rounds with CTA barriers
+  // took about 3 us.)
+  if (tid < 32) {
+    const int lane = tid;
+    for (int r = 0; r < width; ++r) {
+      unsigned long long bk = 0;
+      int bf = INT_MAX, bc = -1;
+      for (int c = lane; c < n; c += 32) {
+        const int f = cf[c];
+        if (f < 0) continue;
+        const unsigned long long k = ck[c];
+        if (bc < 0 || k > bk || (k == bk && f < bf)) {
+          bk = k;
+          bf = f;
+          bc = c;
         }
-      if (wc >= 0) {   // (none left: the remaining ranks keep -1 / NaN)
-        a.out_parent[size_t(g) * width + r] = wf / V;
-        a.out_token[size_t(g) * width + r] = wf % V;
-        a.out_score[size_t(g) * width + r] = from_key(wk);
-        cf[wc] = -1;
       }
+#pragma unroll
+      for (int o = 16; o; o >>= 1) {
+        const unsigned long long ok = shfl_xor_u64(bk, o);
+        const int of = __shfl_xor_sync(0xFFFFFFFFu, bf, o);
+        const int oc = __shfl_xor_sync(0xFFFFFFFFu, bc, o);
+        if (oc >= 0 && (bc < 0 || ok > bk || (ok == bk && of < bf))) {
+          bk = ok;
+          bf = of;
+          bc = oc;
+        }
+      }
+      if (bc < 0) break;   // none left (every lane agrees): the remaining ranks keep -1 / NaN
+      if (lane == 0) {
+        a.out_parent[size_t(g) * width + r] = bf / V;
+        a.out_token[size_t(g) * width + r] = bf % V;
+        a.out_score[size_t(g) * width + r] = from_key(bk);
+        cf[bc] = -1;
+      }
+      __syncwarp();
     }
-    __syncthreads();
   }
 }
 
